@@ -1,0 +1,341 @@
+"""Oracle for the one-pass block-diffusion draft step (DFlash, DFlow relay, DFlash 2).
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` import this module; the product path (the CUDA library and its
+binding) never does, and shares no code with it.
+
+What it is: a plain, slow CPU statement of what the draft step computes, written out
+per sequence and per head with numpy in float64 (``dtype`` may be set to float32 for
+the timed CPU baseline). It consumes the same bf16 values the GPU consumes, widened
+exactly, and rounds nothing in between. Library primitives used as steps: matrix
+products, exp/sqrt/sin/cos, and ``np.lexsort`` for ordering.
+
+Sources (page title, section):
+  [DFlash]  "DFlash 投机解码：块扩散草稿与 KV 注入" (caijizhuo.github.io):
+            符号约定 table; 二、块扩散草稿 -- attention equations; 三、KV 注入 -- the H_c
+            equation and the W_c size; 四、推理流程 -- draft_forward and dflash_cycle.
+  [DFlow]   "DFlow 完全拆解" (pinghaoyang.com.cn/aigc/posts/dflow): 第一步 -- the h_i
+            projection; 第二步 -- the one-position shift; 推理循环可以怎么实现 -- relay
+            placement by absolute position; 问题不在拒绝 -- the accept / bonus split.
+  [DFlash2] "DFlash 2：正确 token 已在候选里" (bowenzhou.top/papers/2026/DFlash2):
+            洞察一 -- the S_t(a,b) selector score and the greedy walk; 洞察二 -- the
+            two-tap dynamic convolution.
+
+Readings where the pages are silent or disagree (each is listed in the design doc):
+  * block layout [anchor, mask x (B-1)] at absolute positions C..C+B-1, C = context
+    rows after the append; offset 0 yields no candidate ([DFlash] 符号约定, dflash_cycle);
+  * pre-norm residual layer x += Attn(RMSNorm(x)); x += FFN(RMSNorm(x)); final RMSNorm;
+    no QK-norm; RMSNorm eps 1e-6; RoPE rotate-half with theta_d = base^(-2d/hd) on q,
+    k_b and k_c at absolute positions; q-head h reads kv-head h // (Hq/Hkv);
+  * tau counts the bonus token (1 <= tau <= B); T[j] verifies candidate c_{j+1};
+  * relay rows k in [a+2, B-1] of the previous verify go to new offset j = k - a
+    (plain add onto the mask embedding); top-k ties and selector ties go to the lower id;
+  * four convs per layer acting on the residual stream (before/after each sublayer),
+    correction linear in the conv input, x_{-1} = 0 at offset 0;
+  * selector A = W_A E[a], B = W_B E[b], G = sigmoid(W_G z_t), U_t = raw logit.
+
+Parity status: every function here is pinned by tests/test_oracle.py (closed forms,
+invariants, brute force on tiny inputs, the pages' worked examples under tests/golden/).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from dflash_inputs import bf16_bits_to_f32
+
+FLAG_RELAY = 1
+FLAG_CONV = 2
+FLAG_SELECT = 4
+
+
+def widen(bits, dtype=np.float64) -> np.ndarray:
+    """bf16 bit patterns -> float array (exact)."""
+    return bf16_bits_to_f32(bits).astype(dtype)
+
+
+def widen_all(bits: dict, dtype=np.float64) -> dict:
+    return {k: widen(v, dtype) for k, v in bits.items()}
+
+
+# ----------------------------------------------------------------------------- pieces
+
+def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis: g * x / sqrt(mean(x^2) + eps).
+
+    [DFlash] 三、KV 注入, the H_c equation (RMSNorm after W_c); eps is not given on
+    the pages, 1e-6 is used.
+    """
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return g * x / np.sqrt(ms + eps)
+
+
+def rope(x: np.ndarray, pos, base: float) -> np.ndarray:
+    """Rotary position embedding, rotate-half pairing (d, d + hd/2).
+
+    x: [..., hd] with leading axis matching ``pos`` (scalar or [rows]); any axes in
+    between (heads) are broadcast. Angle for pair d at position p: p * base^(-2d/hd).
+    """
+    hd = x.shape[-1]
+    h = hd // 2
+    d = np.arange(h, dtype=np.float64)
+    inv = np.power(float(base), -2.0 * d / hd)
+    p = np.asarray(pos, dtype=np.float64)
+    ang = p.reshape(p.shape + (1,) * (x.ndim - 1 - p.ndim) + (1,)) * inv
+    c = np.cos(ang).astype(x.dtype)
+    s = np.sin(ang).astype(x.dtype)
+    x1 = x[..., :h]
+    x2 = x[..., h:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def softmax_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """softmax(q K^T / sqrt(hd)) V with no mask. q [nq, hd], K/V [nk, hd].
+
+    [DFlash] 二、块扩散草稿: Q from the block only, K = [K_c; K_b], V = [V_c; V_b],
+    bidirectional inside the block (no causal mask).
+    """
+    s = (q @ K.T) / math.sqrt(q.shape[-1])
+    s = s - s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    p = p / p.sum(axis=1, keepdims=True)
+    return p @ V
+
+
+def silu(x):
+    return x / (1.0 + np.exp(-x))
+
+
+def sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def dyn_conv(x: np.ndarray, W0: np.ndarray, W1: np.ndarray, base: np.ndarray,
+             group: int = 16) -> np.ndarray:
+    """Two-tap dynamic depthwise convolution over one block's rows.
+
+    [DFlash2] 洞察二: x'_t = k_{t,0} * x_t + k_{t,1} * x_{t-1}, each tap k_{t,j} =
+    base_j + a correction computed from the current hidden state, one correction value
+    shared by every 16 channels. x: [B, D] (block offsets in order); x_{-1} = 0.
+    """
+    c0 = x @ W0.T                      # [B, D/group]
+    c1 = x @ W1.T
+    k0 = base[0][None, :] + np.repeat(c0, group, axis=1)
+    k1 = base[1][None, :] + np.repeat(c1, group, axis=1)
+    prev = np.zeros_like(x)
+    prev[1:] = x[:-1]
+    return k0 * x + k1 * prev
+
+
+# ----------------------------------------------------------------------------- cache
+
+class KVCache:
+    """Drafter context cache holding projected K_c (RoPE applied) and V_c.
+
+    [DFlash] 四、推理流程, the engineering note: the projected K/V of H_c are what the
+    drafter's cache stores, not the raw H_c. Layout per (layer, sequence):
+    [Hkv, Cmax, hd]; rows at or beyond the sequence's ctx_len are ignored.
+    """
+
+    def __init__(self, N: int, nb: int, Hkv: int, Cmax: int, hd: int, dtype=np.float64):
+        self.K = [[np.zeros((Hkv, Cmax, hd), dtype) for _ in range(nb)] for _ in range(N)]
+        self.V = [[np.zeros((Hkv, Cmax, hd), dtype) for _ in range(nb)] for _ in range(N)]
+
+
+# ----------------------------------------------------------------------------- step
+
+def fuse_context(cfg, W: dict, hv_rows: np.ndarray) -> np.ndarray:
+    """h = RMSNorm(W_c [H^{l1}; ...; H^{lL}]) per row.
+
+    [DFlash] 三、KV 注入 (H_c equation); [DFlow] 第一步 (the same projection for the
+    rejected-suffix rows). hv_rows: [R, L*Dt] with the L layers concatenated.
+    """
+    return rmsnorm(hv_rows @ W["W_c"].T, W["g_ctx"], cfg.eps)
+
+
+def ctx_project(cfg, W: dict, hv: np.ndarray, n_commit, ctx_len, cache: KVCache,
+                relay_a=None):
+    """Append committed verifier rows to the context cache; build the relay input.
+
+    hv: [nb, R, L*Dt]. Rows 0..n_commit[i]-1 of sequence i become context rows at
+    absolute positions ctx_len[i] + j: K_c = RoPE(Wk_c h), V_c = Wv_c h for every layer.
+    With ``relay_a`` (the previous round's accepted count a per sequence), rows
+    k in [a+2, B-1] move to new block offset j = k - a ([DFlow] 第二步: the verifier
+    row at position p serves draft position p+1; 推理循环: rejected suffix after the
+    first rejection), giving x0_relay[i, j] = h_k (plain add form).
+
+    Returns (new_ctx_len [nb], x0_relay [nb, B, D] or None). ``cache`` is updated.
+    """
+    nb, R, _ = hv.shape
+    B, D, Hkv, hd = cfg.B, cfg.D, cfg.Hkv, cfg.hd
+    new_len = np.array(ctx_len, dtype=np.int64).copy()
+    x0r = None if relay_a is None else np.zeros((nb, B, D), dtype=hv.dtype)
+    for i in range(nb):
+        h = fuse_context(cfg, W, hv[i])                      # [R, D]
+        c0 = int(ctx_len[i])
+        nc = int(n_commit[i])
+        for j in range(nc):
+            pos = c0 + j
+            for n in range(cfg.N):
+                k = (W[f"layer{n}.Wk_c"] @ h[j]).reshape(Hkv, hd)
+                v = (W[f"layer{n}.Wv_c"] @ h[j]).reshape(Hkv, hd)
+                cache.K[n][i][:, pos, :] = rope(k[None], pos, cfg.rope_base)[0]
+                cache.V[n][i][:, pos, :] = v
+        new_len[i] = c0 + nc
+        if x0r is not None:
+            a = int(relay_a[i])
+            for j in range(2, B - a):
+                k = j + a
+                if k < R:
+                    x0r[i, j] = h[k]
+    return new_len, x0r
+
+
+def block_input(cfg, W: dict, block_ids: np.ndarray, x0_relay=None) -> np.ndarray:
+    """x0 = E[block ids] (+ relay rows): [anchor, m_1..m_{B-1}] ([DFlash] 二, the block)."""
+    x = W["E"][np.asarray(block_ids)]
+    if x0_relay is not None:
+        x = x + x0_relay
+    return x
+
+
+def drafter_layer(cfg, W: dict, n: int, x: np.ndarray, Kc: np.ndarray, Vc: np.ndarray,
+                  C: int) -> np.ndarray:
+    """One drafter layer for one sequence. x: [B, D]; Kc/Vc: [Hkv, >=C, hd].
+
+    [DFlash] 二 attention equations and 四 draft_forward: Q = W_Q H_b from the block only,
+    K = [K_c; K_b], V = [V_c; V_b], no mask; SwiGLU FFN. Pre-norm residual form.
+    """
+    p = f"layer{n}."
+    B = x.shape[0]
+    Hq, Hkv, hd = cfg.Hq, cfg.Hkv, cfg.hd
+    conv = bool(cfg.flags & FLAG_CONV)
+    pos = C + np.arange(B)
+    if conv:
+        x = dyn_conv(x, W[p + "conv0.W0"], W[p + "conv0.W1"], W[p + "conv0.base"], cfg.conv_group)
+    u = rmsnorm(x, W[p + "g_attn"], cfg.eps)
+    qkv = u @ W[p + "W_qkv"].T
+    q = qkv[:, : Hq * hd].reshape(B, Hq, hd)
+    kb = qkv[:, Hq * hd: (Hq + Hkv) * hd].reshape(B, Hkv, hd)
+    vb = qkv[:, (Hq + Hkv) * hd:].reshape(B, Hkv, hd)
+    q = rope(q, pos, cfg.rope_base)
+    kb = rope(kb, pos, cfg.rope_base)
+    o = np.zeros((B, Hq, hd), dtype=x.dtype)
+    grp = Hq // Hkv
+    for h in range(Hq):
+        g = h // grp
+        K = np.concatenate([Kc[g, :C], kb[:, g]], axis=0)
+        V = np.concatenate([Vc[g, :C], vb[:, g]], axis=0)
+        o[:, h] = softmax_attention(q[:, h], K, V)
+    x = x + o.reshape(B, Hq * hd) @ W[p + "W_o"].T
+    if conv:
+        x = dyn_conv(x, W[p + "conv1.W0"], W[p + "conv1.W1"], W[p + "conv1.base"], cfg.conv_group)
+        x = dyn_conv(x, W[p + "conv2.W0"], W[p + "conv2.W1"], W[p + "conv2.base"], cfg.conv_group)
+    u = rmsnorm(x, W[p + "g_ffn"], cfg.eps)
+    x = x + (silu(u @ W[p + "W_gate"].T) * (u @ W[p + "W_up"].T)) @ W[p + "W_down"].T
+    if conv:
+        x = dyn_conv(x, W[p + "conv3.W0"], W[p + "conv3.W1"], W[p + "conv3.base"], cfg.conv_group)
+    return x
+
+
+def draft_block(cfg, W: dict, block_ids: np.ndarray, ctx_len, cache: KVCache,
+                x0_relay=None, seqs=None) -> np.ndarray:
+    """One-pass draft of every block: returns the final-normed hidden [nb, B, D].
+
+    ``seqs`` restricts the computation to a subset of sequences (the others stay zero);
+    sequences are independent.
+    """
+    nb = block_ids.shape[0]
+    out = np.zeros((nb, cfg.B, cfg.D), dtype=W["E"].dtype)
+    for i in (range(nb) if seqs is None else seqs):
+        x = block_input(cfg, W, block_ids[i], None if x0_relay is None else x0_relay[i])
+        C = int(ctx_len[i])
+        for n in range(cfg.N):
+            x = drafter_layer(cfg, W, n, x, cache.K[n][i], cache.V[n][i], C)
+        out[i] = rmsnorm(x, W["g_final"], cfg.eps)
+    return out
+
+
+def lm_logits(W: dict, hidden: np.ndarray) -> np.ndarray:
+    """Shared LM head on mask offsets 1..B-1: [nb, B-1, V] ([DFlash] dflash_cycle, [1:])."""
+    return hidden[:, 1:, :] @ W["W_lm"].T
+
+
+def topk(values: np.ndarray, k: int):
+    """Top-k per row, sorted by value descending, ties to the lower id."""
+    rows = values.reshape(-1, values.shape[-1])
+    ids = np.zeros((rows.shape[0], k), dtype=np.int32)
+    vals = np.zeros((rows.shape[0], k), dtype=values.dtype)
+    col = np.arange(rows.shape[1])
+    for r in range(rows.shape[0]):
+        order = np.lexsort((col, -rows[r]))[:k]
+        ids[r] = order
+        vals[r] = rows[r, order]
+    return ids.reshape(values.shape[:-1] + (k,)), vals.reshape(values.shape[:-1] + (k,))
+
+
+def accept(draft: np.ndarray, target: np.ndarray):
+    """Greedy exact-match accept.
+
+    draft [nb, B-1] = candidates c_1..c_{B-1}; target [nb, B] = the verifier's greedy
+    tokens, T[j] predicted from block offset j, so T[j] verifies c_{j+1}. n = number of
+    leading matches; tau = n + 1 (accepted plus the bonus token, 1 <= tau <= B);
+    bonus = T[n]. ([DFlash] 符号约定 and dflash_cycle step ④; [DFlow] 问题不在拒绝.)
+    """
+    nb, bm1 = draft.shape
+    tau = np.zeros(nb, dtype=np.int32)
+    bonus = np.zeros(nb, dtype=np.int32)
+    for i in range(nb):
+        n = 0
+        while n < bm1 and int(draft[i, n]) == int(target[i, n]):
+            n += 1
+        tau[i] = n + 1
+        bonus[i] = target[i, n]
+    return tau, bonus
+
+
+def select_path(cfg, W: dict, cand_ids: np.ndarray, cand_vals: np.ndarray,
+                hidden: np.ndarray, anchor: np.ndarray) -> np.ndarray:
+    """DFlash 2 path selector, greedy walk ([DFlash2] 洞察一).
+
+    cand_ids/cand_vals: [nb, B-1, k] top-k candidates and their logits U_t(b) for
+    offsets t = 1..B-1; hidden: [nb, B, D] final-normed drafter states z_t.
+    S_t(a, b) = U_t(b) + sum_d A(a)_d G_t,d B(b)_d with A(a) = W_A E[a],
+    B(b) = W_B E[b], G_t = sigmoid(W_G z_t). Walk: a_0 = anchor,
+    a_t = argmax_b S_t(a_{t-1}, b) over the candidates of offset t, ties to the lower id.
+    """
+    nb, bm1, k = cand_ids.shape
+    path = np.zeros((nb, bm1), dtype=np.int32)
+    for i in range(nb):
+        a = int(anchor[i])
+        for t in range(1, bm1 + 1):
+            G = sigmoid(W["W_G"] @ hidden[i, t])
+            Aa = W["W_A"] @ W["E"][a]
+            best_b, best_s = None, None
+            for c in range(k):
+                b = int(cand_ids[i, t - 1, c])
+                s = cand_vals[i, t - 1, c] + np.sum(Aa * G * (W["W_B"] @ W["E"][b]))
+                if best_s is None or s > best_s or (s == best_s and b < best_b):
+                    best_b, best_s = b, s
+            path[i, t - 1] = best_b
+            a = best_b
+    return path
+
+
+def draft_step(cfg, W: dict, hv, n_commit, ctx_len, cache: KVCache, block_ids, target,
+               relay_a=None, seqs=None):
+    """One whole draft step: ctx_project -> draft_block -> LM head + top-k ->
+    (selector) -> accept. Returns a dict of every stage's output."""
+    new_len, x0r = ctx_project(cfg, W, hv, n_commit, ctx_len, cache, relay_a)
+    hidden = draft_block(cfg, W, block_ids, new_len, cache, x0r, seqs)
+    logits = lm_logits(W, hidden)
+    ids, vals = topk(logits, cfg.k_top)
+    draft = ids[..., 0]
+    path = None
+    if cfg.flags & FLAG_SELECT:
+        path = select_path(cfg, W, ids, vals, hidden, np.asarray(block_ids)[:, 0])
+        draft = path
+    tau, bonus = accept(draft, target)
+    return dict(ctx_len=new_len, x0_relay=x0r, hidden=hidden, logits=logits, ids=ids,
+                vals=vals, path=path, draft=draft, tau=tau, bonus=bonus)

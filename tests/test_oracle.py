@@ -1,0 +1,415 @@
+"""Pins for the CPU oracle, independent of the oracle's own code paths.
+
+Each test checks the oracle against something the pages or mathematics fix: closed
+forms, invariants, brute force on tiny inputs, and the pages' worked examples stored
+under tests/golden/ (each with its citation).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import dflash_inputs as di
+from oracle import dflash_oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def small_cfg(**kw):
+    base = dict(name="pin", D=32, Dt=16, L=3, N=2, Hq=4, Hkv=2, hd=8, F=24, V=64, B=6, nb=3,
+                C=10)
+    base.update(kw)
+    return di.Workload(**base)
+
+
+def rand_weights(cfg, seed=0, std=0.3):
+    rng = np.random.default_rng(seed)
+    W = {}
+    for k, shp in di.weight_shapes(cfg).items():
+        base = k.rsplit(".", 1)[-1]
+        if base.startswith("g_"):
+            W[k] = 1.0 + 0.1 * rng.standard_normal(shp)
+        elif base == "base":
+            b = 0.1 * rng.standard_normal(shp)
+            b[0] += 1.0
+            W[k] = b
+        else:
+            W[k] = std * rng.standard_normal(shp)
+    return W
+
+
+def fill_cache(cfg, cache, C, rng):
+    for n in range(cfg.N):
+        for i in range(len(cache.K[n])):
+            cache.K[n][i][:, :C] = rng.standard_normal(cache.K[n][i][:, :C].shape)
+            cache.V[n][i][:, :C] = rng.standard_normal(cache.V[n][i][:, :C].shape)
+
+
+# ----------------------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_closed_form_constant_vector():
+    rng = np.random.default_rng(1)
+    g = rng.standard_normal(17)
+    for c in (0.5, -3.0, 1e-3):
+        y = orc.rmsnorm(np.full(17, c), g, 1e-6)
+        np.testing.assert_allclose(y, g * c / math.sqrt(c * c + 1e-6), rtol=1e-14)
+
+
+def test_rmsnorm_hand_value_and_scale_invariance():
+    y = orc.rmsnorm(np.array([3.0, 4.0]), np.ones(2), 0.0)
+    np.testing.assert_allclose(y, [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rtol=1e-15)
+    x = np.random.default_rng(2).standard_normal((3, 9))
+    np.testing.assert_allclose(orc.rmsnorm(7.5 * x, np.ones(9), 0.0), orc.rmsnorm(x, np.ones(9), 0.0),
+                               rtol=1e-13)
+
+
+# ----------------------------------------------------------------------------- RoPE
+
+def test_rope_hand_value_hd4():
+    # hd = 4: pairs (0, 2) and (1, 3); angles p * base^0 and p * base^(-1/2).
+    x = np.array([1.0, 2.0, 3.0, 4.0])
+    p, base = 3, 100.0
+    t0, t1 = 3.0, 3.0 / 10.0
+    want = [1 * math.cos(t0) - 3 * math.sin(t0), 2 * math.cos(t1) - 4 * math.sin(t1),
+            3 * math.cos(t0) + 1 * math.sin(t0), 4 * math.cos(t1) + 2 * math.sin(t1)]
+    np.testing.assert_allclose(orc.rope(x, p, base), want, rtol=1e-14)
+
+
+def test_rope_identity_at_zero_and_pair_norms():
+    x = np.random.default_rng(3).standard_normal((5, 3, 16))
+    np.testing.assert_array_equal(orc.rope(x, np.zeros(5, int), 1e4), x)
+    y = orc.rope(x, np.arange(5) * 1000 + 7, 1e4)
+    np.testing.assert_allclose(x[..., :8] ** 2 + x[..., 8:] ** 2, y[..., :8] ** 2 + y[..., 8:] ** 2,
+                               rtol=1e-12)
+
+
+def test_rope_scores_depend_only_on_offset():
+    rng = np.random.default_rng(4)
+    q, k = rng.standard_normal(32), rng.standard_normal(32)
+    s1 = orc.rope(q, 50, 1e4) @ orc.rope(k, 20, 1e4)
+    s2 = orc.rope(q, 1050, 1e4) @ orc.rope(k, 1020, 1e4)
+    assert abs(s1 - s2) < 1e-9
+
+
+# ----------------------------------------------------------------------------- attention
+
+def scalar_rope(vec, pos, base):
+    """Rotate pairs (d, d + hd/2) by pos * base^(-2d/hd), one scalar at a time."""
+    hd = len(vec)
+    half = hd // 2
+    out = np.array(vec, dtype=float)
+    for d in range(half):
+        th = pos * base ** (-2.0 * d / hd)
+        out[d] = vec[d] * math.cos(th) - vec[d + half] * math.sin(th)
+        out[d + half] = vec[d + half] * math.cos(th) + vec[d] * math.sin(th)
+    return out
+
+
+def brute_attention(q, K, V):
+    nq, hd = q.shape
+    out = np.zeros((nq, V.shape[1]))
+    for a in range(nq):
+        sc = [sum(q[a, d] * K[b, d] for d in range(hd)) / math.sqrt(hd) for b in range(K.shape[0])]
+        m = max(sc)
+        w = [math.exp(s - m) for s in sc]
+        tot = sum(w)
+        for b in range(K.shape[0]):
+            for d in range(V.shape[1]):
+                out[a, d] += w[b] / tot * V[b, d]
+    return out
+
+
+def test_attention_brute_force():
+    rng = np.random.default_rng(5)
+    q, K, V = rng.standard_normal((3, 4)), rng.standard_normal((7, 4)), rng.standard_normal((7, 4))
+    np.testing.assert_allclose(orc.softmax_attention(q, K, V), brute_attention(q, K, V), rtol=1e-12)
+
+
+def test_attention_equal_keys_gives_mean_and_single_key_gives_row():
+    rng = np.random.default_rng(6)
+    q, V = rng.standard_normal((5, 8)), rng.standard_normal((9, 8))
+    K = np.tile(rng.standard_normal(8), (9, 1))
+    np.testing.assert_allclose(orc.softmax_attention(q, K, V), np.tile(V.mean(0), (5, 1)), rtol=1e-12)
+    np.testing.assert_allclose(orc.softmax_attention(q, K[:1], V[:1]), np.tile(V[0], (5, 1)), rtol=1e-14)
+
+
+def layer_once(cfg, W, x, Kc, Vc, C):
+    return orc.drafter_layer(cfg, W, 0, x, Kc, Vc, C)
+
+
+def test_layer_context_permutation_invariance():
+    cfg = small_cfg()
+    W = rand_weights(cfg)
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((cfg.B, cfg.D))
+    Kc = rng.standard_normal((cfg.Hkv, 12, cfg.hd))
+    Vc = rng.standard_normal((cfg.Hkv, 12, cfg.hd))
+    perm = rng.permutation(12)
+    a = layer_once(cfg, W, x, Kc, Vc, 12)
+    b = layer_once(cfg, W, x, Kc[:, perm], Vc[:, perm], 12)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_empty_context_is_block_self_attention():
+    cfg = small_cfg()
+    W = rand_weights(cfg)
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((cfg.B, cfg.D))
+    garbage = rng.standard_normal((cfg.Hkv, 5, cfg.hd))
+    got = layer_once(cfg, W, x, garbage, garbage, 0)
+    # brute force: the same layer written with scalar loops over the block keys only
+    p = "layer0."
+    u = x / np.sqrt((x * x).mean(1, keepdims=True) + cfg.eps) * W[p + "g_attn"]
+    qkv = u @ W[p + "W_qkv"].T
+    Hq, Hkv, hd = cfg.Hq, cfg.Hkv, cfg.hd
+    q = qkv[:, :Hq * hd].reshape(cfg.B, Hq, hd)
+    k = qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(cfg.B, Hkv, hd)
+    v = qkv[:, (Hq + Hkv) * hd:].reshape(cfg.B, Hkv, hd)
+    def rot(vec, pos):
+        return scalar_rope(vec, pos, cfg.rope_base)
+
+    o = np.zeros((cfg.B, Hq * hd))
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        qs = np.array([rot(q[j, h], j) for j in range(cfg.B)])
+        ks = np.array([rot(k[j, g], j) for j in range(cfg.B)])
+        o[:, h * hd:(h + 1) * hd] = brute_attention(qs, ks, v[:, g])
+    x1 = x + o @ W[p + "W_o"].T
+    u = x1 / np.sqrt((x1 * x1).mean(1, keepdims=True) + cfg.eps) * W[p + "g_ffn"]
+    gt, up = u @ W[p + "W_gate"].T, u @ W[p + "W_up"].T
+    want = x1 + (gt / (1 + np.exp(-gt)) * up) @ W[p + "W_down"].T
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-10)
+
+
+def test_zero_output_projections_make_identity_layers():
+    cfg = small_cfg()
+    W = rand_weights(cfg)
+    for n in range(cfg.N):
+        W[f"layer{n}.W_o"][:] = 0
+        W[f"layer{n}.W_down"][:] = 0
+    rng = np.random.default_rng(9)
+    cache = orc.KVCache(cfg.N, cfg.nb, cfg.Hkv, 16, cfg.hd)
+    fill_cache(cfg, cache, 10, rng)
+    ids = rng.integers(0, cfg.V, (cfg.nb, cfg.B))
+    out = orc.draft_block(cfg, W, ids, np.full(cfg.nb, 10), cache)
+    x = W["E"][ids]
+    np.testing.assert_allclose(out, x / np.sqrt((x * x).mean(-1, keepdims=True) + cfg.eps) * W["g_final"],
+                               rtol=1e-12)
+
+
+def test_batch_independence():
+    cfg = small_cfg()
+    W = rand_weights(cfg)
+    rng = np.random.default_rng(10)
+    cache = orc.KVCache(cfg.N, cfg.nb, cfg.Hkv, 16, cfg.hd)
+    fill_cache(cfg, cache, 16, rng)
+    ids = rng.integers(0, cfg.V, (cfg.nb, cfg.B))
+    lens = np.array([3, 10, 16])
+    a = orc.draft_block(cfg, W, ids, lens, cache)
+    ids2 = ids.copy()
+    ids2[1:] = rng.integers(0, cfg.V, (cfg.nb - 1, cfg.B))
+    for n in range(cfg.N):
+        cache.K[n][2][:] = 0
+    b = orc.draft_block(cfg, W, ids2, np.array([3, 7, 9]), cache)
+    np.testing.assert_array_equal(a[0], b[0])
+
+
+# ----------------------------------------------------------------------------- conv
+
+def test_conv_identity_and_shift():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((6, 32))
+    Z = np.zeros((2, 32))
+    base = np.zeros((2, 32))
+    base[0] = 1
+    np.testing.assert_array_equal(orc.dyn_conv(x, Z, Z, base), x)
+    base = np.zeros((2, 32))
+    base[1] = 1
+    want = np.vstack([np.zeros(32), x[:-1]])
+    np.testing.assert_array_equal(orc.dyn_conv(x, Z, Z, base), want)
+
+
+def test_conv_correction_shared_per_16_channels():
+    # one correction value per 16 channels: a W0 row that picks channel 0 scales the
+    # first 16 channels by (1 + x_t[0]) and leaves the next 16 at base 1.
+    x = np.random.default_rng(12).standard_normal((3, 32))
+    W0 = np.zeros((2, 32))
+    W0[0, 0] = 1.0
+    base = np.zeros((2, 32))
+    base[0] = 1
+    y = orc.dyn_conv(x, W0, np.zeros((2, 32)), base)
+    for t in range(3):
+        np.testing.assert_allclose(y[t, :16], (1 + x[t, 0]) * x[t, :16], rtol=1e-15)
+        np.testing.assert_array_equal(y[t, 16:], x[t, 16:])
+
+
+# ----------------------------------------------------------------------------- top-k / accept
+
+def test_topk_matches_python_sort_with_ties():
+    rng = np.random.default_rng(13)
+    vals = rng.integers(0, 6, (4, 40)).astype(float)  # many exact ties
+    ids, v = orc.topk(vals, 7)
+    for r in range(4):
+        order = sorted(range(40), key=lambda c: (-vals[r, c], c))[:7]
+        assert list(ids[r]) == order
+        assert list(v[r]) == [vals[r, c] for c in order]
+
+
+def test_accept_golden_cases():
+    g = json.load(open(os.path.join(GOLDEN, "accept_cases.json")))
+    for c in g["cases"]:
+        tau, bonus = orc.accept(np.array([c["draft"]]), np.array([c["target"]]))
+        assert (int(tau[0]), int(bonus[0])) == (c["tau"], c["bonus"]), c["why"]
+
+
+def test_accept_tau_range_and_bonus():
+    rng = np.random.default_rng(14)
+    B = 16
+    d = rng.integers(0, 3, (500, B - 1))
+    t = rng.integers(0, 3, (500, B))
+    tau, bonus = orc.accept(d, t)
+    assert tau.min() >= 1 and tau.max() <= B
+    for i in range(500):
+        m = int(tau[i]) - 1
+        assert np.array_equal(d[i, :m], t[i, :m])
+        assert m == B - 1 or d[i, m] != t[i, m]
+        assert bonus[i] == t[i, m]
+
+
+# ----------------------------------------------------------------------------- relay
+
+def test_relay_placement_matches_dflow_example():
+    g = json.load(open(os.path.join(GOLDEN, "relay_positions.json")))
+    cfg = small_cfg(B=g["B"], nb=1)
+    W = rand_weights(cfg)
+    rng = np.random.default_rng(15)
+    hv = rng.standard_normal((1, cfg.B, cfg.L * cfg.Dt))
+    a = g["accepted"]
+    cache = orc.KVCache(cfg.N, 1, cfg.Hkv, 32, cfg.hd)
+    start = g["prev_block_start"]
+    new_len, x0r = orc.ctx_project(cfg, W, hv, [a + 1], [start], cache, relay_a=[a])
+    assert int(new_len[0]) == g["next_block_start"]
+    h = orc.fuse_context(cfg, W, hv[0])
+    placed = {}
+    for e in g["relayed"]:
+        assert e["new_pos"] == e["prev_pos"] + 1
+        assert e["new_pos"] == g["next_block_start"] + e["new_offset"]
+        np.testing.assert_array_equal(x0r[0, e["new_offset"]], h[e["prev_row"]])
+        placed[e["new_offset"]] = True
+    for j in range(cfg.B):
+        if j not in placed:
+            assert not x0r[0, j].any()
+
+
+def test_relay_inactive_when_nearly_all_accepted():
+    cfg = small_cfg(nb=2)
+    W = rand_weights(cfg)
+    rng = np.random.default_rng(16)
+    hv = rng.standard_normal((2, cfg.B, cfg.L * cfg.Dt))
+    cache = orc.KVCache(cfg.N, 2, cfg.Hkv, 32, cfg.hd)
+    _, x0r = orc.ctx_project(cfg, W, hv, [cfg.B - 1, cfg.B], [0, 0], cache,
+                             relay_a=[cfg.B - 2, cfg.B - 1])
+    assert not x0r.any()
+
+
+def test_ctx_project_cache_rows():
+    cfg = small_cfg(nb=1)
+    W = rand_weights(cfg)
+    rng = np.random.default_rng(17)
+    hv = rng.standard_normal((1, 4, cfg.L * cfg.Dt))
+    cache = orc.KVCache(cfg.N, 1, cfg.Hkv, 16, cfg.hd)
+    new_len, _ = orc.ctx_project(cfg, W, hv, [3], [5], cache)
+    assert int(new_len[0]) == 8
+    # h by block decomposition of W_c over the L concatenated layers
+    Wc = W["W_c"]
+    pre = sum(Wc[:, l * cfg.Dt:(l + 1) * cfg.Dt] @ hv[0, :, l * cfg.Dt:(l + 1) * cfg.Dt].T
+              for l in range(cfg.L)).T
+    h = pre / np.sqrt((pre * pre).mean(-1, keepdims=True) + cfg.eps) * W["g_ctx"]
+    for n in range(cfg.N):
+        for j in range(3):
+            v = (W[f"layer{n}.Wv_c"] @ h[j]).reshape(cfg.Hkv, cfg.hd)
+            np.testing.assert_allclose(cache.V[n][0][:, 5 + j], v, rtol=1e-12)
+            k = (W[f"layer{n}.Wk_c"] @ h[j]).reshape(cfg.Hkv, cfg.hd)
+            kc = cache.K[n][0][:, 5 + j]
+            for g in range(cfg.Hkv):
+                np.testing.assert_allclose(kc[g], scalar_rope(k[g], 5 + j, cfg.rope_base),
+                                           rtol=1e-10, atol=1e-12)
+        assert not cache.K[n][0][:, 8:].any() and not cache.K[n][0][:, :5].any()
+
+
+# ----------------------------------------------------------------------------- selector
+
+def test_selector_without_pair_term_is_per_position_argmax():
+    cfg = small_cfg(flags=di.FLAG_SELECT, sel_dim=8)
+    W = rand_weights(cfg)
+    W["W_A"][:] = 0
+    rng = np.random.default_rng(18)
+    ids = np.stack([rng.permutation(cfg.V)[:5] for _ in range(cfg.nb * (cfg.B - 1))])
+    ids = ids.reshape(cfg.nb, cfg.B - 1, 5)
+    vals = rng.integers(0, 3, ids.shape).astype(float)
+    hid = rng.standard_normal((cfg.nb, cfg.B, cfg.D))
+    path = orc.select_path(cfg, W, ids, vals, hid, np.zeros(cfg.nb, int))
+    for i in range(cfg.nb):
+        for t in range(cfg.B - 1):
+            best = sorted(range(5), key=lambda c: (-vals[i, t, c], ids[i, t, c]))[0]
+            assert path[i, t] == ids[i, t, best]
+
+
+def test_selector_pair_term_prefers_coherent_successor():
+    # E rows one-hot, W_A = W_B = 4*I, W_G = 0 (gate 1/2): the pair term adds 8 when
+    # b == a and 0 otherwise, so the walk repeats the anchor whenever it is a candidate
+    # unless some other logit leads by more than 8.
+    cfg = small_cfg(D=8, V=8, B=4, nb=1, flags=di.FLAG_SELECT, sel_dim=8)
+    W = rand_weights(cfg)
+    W["E"] = np.eye(8)
+    W["W_A"] = 4 * np.eye(8)
+    W["W_B"] = 4 * np.eye(8)
+    W["W_G"] = np.zeros((8, 8))
+    ids = np.array([[[1, 3], [3, 5], [5, 6]]])
+    vals = np.array([[[1.0, 0.0], [0.5, 0.0], [0.0, 9.0]]])
+    path = orc.select_path(cfg, W, ids, vals, np.zeros((1, 4, 8)), np.array([3]))
+    # t=1: S(3,1)=1, S(3,3)=0+8 -> 3; t=2: S(3,3)=0.5+8, S(3,5)=0 -> 3;
+    # t=3: S(3,5)=0, S(3,6)=9 -> 6
+    assert path.tolist() == [[3, 3, 6]]
+
+
+# ----------------------------------------------------------------------------- shapes
+
+def test_shape_pins_from_pages():
+    g = json.load(open(os.path.join(GOLDEN, "shape_pins.json")))
+    p = g["W_c_bytes"]
+    w = di.Workload("p", D=p["D"], Dt=p["D"], L=p["L"], N=1, Hq=16, Hkv=8, hd=128, F=8, V=8, B=16,
+                    nb=1, C=1)
+    shp = di.weight_shapes(w)["W_c"]
+    mb = shp[0] * shp[1] * p["bytes_per_param"] / 1e6
+    assert abs(mb - p["quoted_MB"]) / p["quoted_MB"] < p["rel_tol"]
+
+    q = g["conv_params"]
+    w = di.QWEN3_4B.with_(flags=di.FLAG_CONV)
+    assert w.D == q["D"] and w.N == q["N"]
+    n = sum(int(np.prod(s)) for k, s in di.weight_shapes(w).items() if ".conv" in k)
+    assert abs(n / 1e6 - q["quoted_M"]) < q["abs_tol_M"]
+
+    s = g["selector_params"]
+    w = di.QWEN3_4B.with_(flags=di.FLAG_SELECT)
+    n = sum(int(np.prod(v)) for k, v in di.weight_shapes(w).items() if k in ("W_A", "W_B", "W_G"))
+    assert abs(n / 1e6 - s["quoted_M"]) < s["abs_tol_M"]
+
+
+# ----------------------------------------------------------------------------- whole step
+
+def test_tiny_step_runs_and_is_deterministic():
+    cfg = di.TINY
+    bits = di.make_weights(cfg)
+    W = orc.widen_all(bits)
+    cache = orc.KVCache(cfg.N, cfg.nb, cfg.Hkv, 80, cfg.hd)
+    hv = orc.widen(di.verifier_rows(cfg, cfg.C))
+    lens, _ = orc.ctx_project(cfg, W, hv[:, :cfg.C - 3], [cfg.C - 3], [0], cache)
+    ids = di.block_ids(cfg, di.anchors(cfg))
+    out1 = orc.draft_step(cfg, W, hv[:, cfg.C - 3:], [3], lens,
+                          cache, ids, np.zeros((1, cfg.B), np.int32))
+    assert int(out1["ctx_len"][0]) == cfg.C
+    assert 1 <= int(out1["tau"][0]) <= cfg.B
+    assert np.isfinite(out1["hidden"]).all()
