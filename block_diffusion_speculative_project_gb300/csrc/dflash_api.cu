@@ -1,0 +1,760 @@
+// C ABI of libdflash (declared in include/dflash.h): argument validation, TMA
+// descriptor encoding, workspace layout and the launch sequence of each step call.
+// All compute runs in the kernels of gemm_tc.cu, attention.cu and small_ops.cu.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/dflash.h"
+#include "kernels.h"
+
+using namespace df;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+#define DF_CUDA(call)                                                                          \
+  do {                                                                                         \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess)                                                                     \
+      return fail(DFLASH_ERR_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_),     \
+                  __FILE__, __LINE__);                                                         \
+  } while (0)
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D bf16 map over a row-major [rows, cols] matrix (row stride in elements), box
+// {64 columns, box_rows rows}, 128-byte swizzle.
+int encode_2d(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint64_t stride,
+              uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  if (reinterpret_cast<uintptr_t>(ptr) % 16 || (stride * 2) % 16)
+    return fail(DFLASH_ERR_INVALID_ARG, "tensor %p (row stride %llu) is not 16-byte aligned", ptr,
+                (unsigned long long)stride);
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {stride * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled (2D) failed: %d", (int)r);
+  return DFLASH_OK;
+}
+
+// 3D bf16 map {cols, R, G}: row r of group g at ptr + g*gstride + r*rstride (elements).
+int encode_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t R, uint64_t G, uint64_t rstride,
+              uint64_t gstride, uint32_t box_r, uint32_t box_g) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  if (reinterpret_cast<uintptr_t>(ptr) % 16 || (rstride * 2) % 16 || (gstride * 2) % 16)
+    return fail(DFLASH_ERR_INVALID_ARG, "activation tensor %p is not 16-byte aligned", ptr);
+  cuuint64_t dims[3] = {cols, R, G};
+  cuuint64_t strides[2] = {rstride * 2, gstride * 2};
+  cuuint32_t box[3] = {64, box_r, box_g};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled (3D) failed: %d", (int)r);
+  return DFLASH_OK;
+}
+
+// A plain activation matrix [rows, cols] (row stride = cols) as a 3D map with G = 1.
+int encode_act(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols) {
+  return encode_3d(m, ptr, cols, rows, 1, cols, rows * cols, 128, 1);
+}
+
+constexpr int kBN = 128;       // tile width of the generic GEMMs
+constexpr int kBNTopk = 256;   // tile width of the LM head
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct WsLayout {
+  size_t status = 0, counters = 0, partial = 0;
+  size_t pre = 0, h = 0;                       // ctx_project
+  size_t x = 0, u = 0, qkv = 0, o = 0, act = 0, xb = 0, corr = 0;  // draft_block
+  size_t apart = 0, aml = 0;                   // attention partials
+  size_t tk_vals = 0, tk_ids = 0;              // LM head top-k partial lists
+  size_t sel_e = 0, sel_ab = 0, sel_g = 0;     // selector
+  size_t total = 0;
+  size_t counters_bytes = 0, partial_bytes = 0, apart_bytes = 0, apart_ctas = 0;
+};
+
+}  // namespace
+
+struct dflash_handle_s {
+  dflash_config cfg{};
+  int device = 0;
+  int num_sms = kNumSMsDefault;
+  bool have_weights = false;
+  dflash_weights w{};
+  std::vector<dflash_layer_weights> layers;
+  CUtensorMap tm_Wc, tm_lm, tm_A, tm_B, tm_G;
+  std::vector<CUtensorMap> tm_qkv, tm_kc, tm_vc, tm_o, tm_gate, tm_up, tm_down;
+  std::vector<CUtensorMap> tm_c0, tm_c1;  // [layer*4 + which]
+  float inv_freq[64];
+  WsLayout ws;
+  int max_attn_ctas = 2048;
+};
+
+namespace {
+
+int attn_chunk(const dflash_handle_s *h, int nb, int max_ctx, int *splits_out) {
+  const auto &c = h->cfg;
+  const int pairs = std::max(1, nb * c.Hkv);
+  const int want = std::max(1, (2 * 2 * h->num_sms + pairs - 1) / pairs);
+  int chunk = (std::max(1, max_ctx) + want - 1) / want;
+  chunk = std::max(64, (chunk + 63) / 64 * 64);
+  int splits = std::max(1, (max_ctx + chunk - 1) / chunk);
+  while ((long long)splits * pairs > h->max_attn_ctas && splits > 1) {
+    chunk += 64;
+    splits = std::max(1, (max_ctx + chunk - 1) / chunk);
+  }
+  *splits_out = splits;
+  return chunk;
+}
+
+// Largest split-K scratch (bytes) and tile count of one GEMM shape over every row
+// count up to max_rows (the plan depends on the number of m-tiles only).
+size_t gemm_partial_max(const dflash_handle_s *h, int max_rows, int N, int K, int groups, int dual,
+                        int epi, int *max_tiles, int tile_rows = 128) {
+  size_t best = 0;
+  const int max_m_tiles = (max_rows + tile_rows - 1) / tile_rows;
+  for (int mt = 1; mt <= max_m_tiles; ++mt) {
+    const int M = std::min(max_rows, mt * tile_rows);
+    best = std::max(best, gemm_partial_bytes(M, tile_rows, N, K, groups, dual, kBN, h->num_sms, epi));
+    *max_tiles = std::max(*max_tiles, gemm_tiles(M, tile_rows, N, groups, dual, kBN));
+  }
+  return best;
+}
+
+void plan_workspace(dflash_handle_s *h) {
+  const auto &c = h->cfg;
+  WsLayout &L = h->ws;
+  const int Mb = c.max_batch * c.B;                     // draft rows
+  const int Mp = c.max_batch * c.max_proj_rows;         // projection rows
+  const int Ml = c.max_batch * (c.B - 1);               // LM-head rows
+  const int qkv_n = (c.Hq + 2 * c.Hkv) * c.hd;
+  int max_tiles = 0;
+  size_t part = 0;
+  part = std::max(part, gemm_partial_max(h, Mp, c.D, c.L * c.Dt, 1, 0, EPI_F32, &max_tiles));
+  part = std::max(part, gemm_partial_max(h, Mp, c.Hkv * c.hd, c.D, 2 * c.N, 0, EPI_KV, &max_tiles));
+  part = std::max(part, gemm_partial_max(h, Mb, qkv_n, c.D, 1, 0, EPI_ROPE, &max_tiles));
+  part = std::max(part, gemm_partial_max(h, Mb, c.D, c.Hq * c.hd, 1, 0, EPI_RESID, &max_tiles));
+  part = std::max(part, gemm_partial_max(h, Mb, c.F, c.D, 1, 1, EPI_SWIGLU, &max_tiles));
+  part = std::max(part, gemm_partial_max(h, Mb, c.D, c.F, 1, 0, EPI_RESID, &max_tiles));
+  if (c.flags & DFLASH_FLAG_CONV)
+    part = std::max(part, gemm_partial_max(h, Mb, c.D / c.conv_group, c.D, 1, 1, EPI_DUAL_F32, &max_tiles));
+  const int sel_rows = c.max_batch * (1 + (c.B - 1) * c.k_top);
+  if (c.flags & DFLASH_FLAG_SELECT) {
+    part = std::max(part, gemm_partial_max(h, sel_rows, c.sel_dim, c.D, 1, 1, EPI_DUAL_F32, &max_tiles));
+    const int R = c.B - 1;
+    part = std::max(part, gemm_partial_max(h, Ml, c.sel_dim, c.D, 1, 0, EPI_F32, &max_tiles,
+                                           (128 / R) * R));
+  }
+  const size_t apart_max = (size_t)h->max_attn_ctas + (size_t)c.max_batch * c.Hkv;  // CTA bound
+  const size_t rows_attn = (size_t)(c.Hq / c.Hkv) * c.B;
+
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + std::max<size_t>(bytes, 1));
+    return o;
+  };
+  L.status = take(256);
+  L.counters_bytes = (size_t)std::max(max_tiles, 1) * sizeof(int);
+  L.counters = take(L.counters_bytes);
+  L.partial_bytes = part;
+  L.partial = take(part);
+  L.pre = take((size_t)Mp * c.D * 4);
+  L.h = take((size_t)Mp * c.D * 2);
+  L.x = take((size_t)Mb * c.D * 4);
+  L.u = take((size_t)Mb * c.D * 2);
+  L.qkv = take((size_t)Mb * qkv_n * 2);
+  L.o = take((size_t)Mb * c.Hq * c.hd * 2);
+  L.act = take((size_t)Mb * c.F * 2);
+  L.xb = take((size_t)Mb * c.D * 2);
+  L.corr = take((c.flags & DFLASH_FLAG_CONV) ? (size_t)Mb * 2 * (c.D / c.conv_group) * 4 : 0);
+  L.apart_ctas = apart_max;
+  L.apart_bytes = apart_max * rows_attn * c.hd * 4;
+  L.apart = take(L.apart_bytes);
+  L.aml = take(apart_max * rows_attn * 2 * 4);
+  const int ranges = h->num_sms;
+  L.tk_vals = take((size_t)ranges * Ml * c.k_top * 4);
+  L.tk_ids = take((size_t)ranges * Ml * c.k_top * 4);
+  if (c.flags & DFLASH_FLAG_SELECT) {
+    L.sel_e = take((size_t)sel_rows * c.D * 2);
+    L.sel_ab = take((size_t)sel_rows * 2 * c.sel_dim * 4);
+    L.sel_g = take((size_t)Ml * c.sel_dim * 4);
+  }
+  L.total = off;
+}
+
+struct Ws {
+  uint8_t *base;
+  const WsLayout &L;
+  template <class T>
+  T *at(size_t off) const {
+    return reinterpret_cast<T *>(base + off);
+  }
+  int *status() const { return at<int>(L.status); }
+};
+
+int check_ws(const dflash_handle_s *h, void *ws, size_t ws_bytes) {
+  if (!ws) return fail(DFLASH_ERR_INVALID_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign)
+    return fail(DFLASH_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < h->ws.total)
+    return fail(DFLASH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, h->ws.total);
+  return DFLASH_OK;
+}
+
+GemmParams base_params(const dflash_handle_s *h, const Ws &w) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.groups = 1;
+  p.status = w.status();
+  p.max_spin = h->cfg.max_spin;
+  p.stall = (h->cfg.flags & DFLASH_FLAG_TEST_STALL) ? 1 : 0;
+  p.partial = w.at<float>(w.L.partial);
+  p.counters = w.at<int>(w.L.counters);
+  p.hd = h->cfg.hd;
+  std::memcpy(p.inv_freq, h->inv_freq, sizeof(p.inv_freq));
+  return p;
+}
+
+int run_gemm(const dflash_handle_s *h, GemmParams &p, int BN, cudaStream_t s) {
+  const int tile_rows = p.a_grouped ? p.tile_rows : 128;
+  const int tiles = gemm_tiles(p.M, tile_rows, p.N, p.groups, p.dual, BN);
+  if (p.epi != EPI_TOPK) {
+    int splits, kps, items, grid;
+    gemm_plan(p.M, tile_rows, p.N, p.K, p.groups, p.dual, BN, h->num_sms, p.epi, &splits, &kps, &items, &grid);
+    if (splits > 1 && (size_t)tiles * splits * 128 * BN * 4 > h->ws.partial_bytes)
+      return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "split-K scratch exceeds the workspace plan");
+    if ((size_t)tiles * sizeof(int) > h->ws.counters_bytes)
+      return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "tile count exceeds the workspace plan");
+  }
+  DF_CUDA(gemm_launch(p, BN, h->num_sms, s));
+  return DFLASH_OK;
+}
+
+#define DF_TRY(expr)              \
+  do {                            \
+    int rc_ = (expr);             \
+    if (rc_ != DFLASH_OK) return rc_; \
+  } while (0)
+
+const uint16_t *bf(const void *p) { return static_cast<const uint16_t *>(p); }
+
+size_t cache_layer_elems(const dflash_config &c) {
+  return (size_t)c.max_batch * c.Hkv * c.Cmax * c.hd;
+}
+
+// One DFlash 2 conv on the fp32 residual rows x [M, D].
+int run_conv(const dflash_handle_s *h, const Ws &w, int layer, int which, int M, float *x,
+             cudaStream_t s) {
+  const auto &c = h->cfg;
+  const int ng = c.D / c.conv_group;
+  uint16_t *xb = w.at<uint16_t>(w.L.xb);
+  float *corr = w.at<float>(w.L.corr);
+  DF_CUDA(launch_f32_to_bf16(x, xb, (long long)M * c.D, s));
+  GemmParams p = base_params(h, w);
+  DF_TRY(encode_act(&p.tmA, xb, M, c.D));
+  p.tmB[0] = h->tm_c0[layer * 4 + which];
+  p.tmB[1] = h->tm_c1[layer * 4 + which];
+  p.M = M;
+  p.N = ng;
+  p.K = c.D;
+  p.dual = 1;
+  p.epi = EPI_DUAL_F32;
+  p.out = corr;
+  p.ldo = 2 * ng;
+  DF_TRY(run_gemm(h, p, kBN, s));
+  DF_CUDA(launch_conv_apply(x, corr, bf(h->layers[layer].conv_base[which]), M, c.D, c.B,
+                            c.conv_group, s));
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char *dflash_last_error(void) { return g_last_error.c_str(); }
+
+int dflash_create(const dflash_config *cfg, dflash_handle_t *out) {
+  if (!cfg || !out) return fail(DFLASH_ERR_INVALID_ARG, "cfg and out must be non-NULL");
+  *out = nullptr;
+  const dflash_config &c = *cfg;
+  if (c.D <= 0 || c.Dt <= 0 || c.L <= 0 || c.N <= 0 || c.Hq <= 0 || c.Hkv <= 0 || c.F <= 0 ||
+      c.V <= 1 || c.Cmax <= 0 || c.max_batch <= 0 || c.max_proj_rows <= 0)
+    return fail(DFLASH_ERR_INVALID_ARG, "every size in dflash_config must be positive");
+  if (c.N > 16) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "N must be <= 16");
+  if (c.hd != 64 && c.hd != 128) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "hd must be 64 or 128");
+  if (c.Hq % c.Hkv) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "Hq must be a multiple of Hkv");
+  if (c.B < 2 || c.B > 16) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "B must be in 2..16");
+  if ((c.Hq / c.Hkv) * c.B > 64)
+    return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "(Hq/Hkv)*B must be <= 64 (query rows per kv head)");
+  if (c.k_top < 1 || c.k_top > kTopkMax) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "k_top must be in 1..16");
+  if (c.D % 64 || (c.L * c.Dt) % 64 || (c.Hq * c.hd) % 64 || c.F % 8)
+    return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "D, L*Dt, Hq*hd must be multiples of 64 and F of 8");
+  if (c.mask_id < 0 || c.mask_id >= c.V) return fail(DFLASH_ERR_INVALID_ARG, "mask_id outside [0, V)");
+  if (!(c.eps > 0.f) || !(c.rope_base > 1.f)) return fail(DFLASH_ERR_INVALID_ARG, "eps and rope_base");
+  if (c.flags & DFLASH_FLAG_CONV) {
+    if (c.conv_group <= 0 || c.D % c.conv_group || (c.D / c.conv_group) % 8)
+      return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "conv_group must divide D into a multiple of 8 groups");
+  }
+  if (c.flags & DFLASH_FLAG_SELECT) {
+    if (c.sel_dim <= 0 || c.sel_dim % 32) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "sel_dim must be a multiple of 32");
+  }
+  if (2LL * c.N > kMaxBMaps) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "2*N must be <= 12 (grouped K/V projection)");
+  auto *h = new (std::nothrow) dflash_handle_s();
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "out of host memory");
+  h->cfg = c;
+  if (h->cfg.max_spin <= 0) h->cfg.max_spin = 1 << 24;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    delete h;
+    return fail(DFLASH_ERR_CUDA, "no CUDA device");
+  }
+  for (int d = 0; d < 64; ++d)
+    h->inv_freq[d] = d < c.hd / 2 ? (float)std::pow((double)c.rope_base, -2.0 * d / c.hd) : 0.f;
+  plan_workspace(h);
+  *out = h;
+  return DFLASH_OK;
+}
+
+int dflash_destroy(dflash_handle_t h) {
+  delete h;
+  return DFLASH_OK;
+}
+
+int dflash_workspace_size(dflash_handle_t h, size_t *bytes) {
+  if (!h || !bytes) return fail(DFLASH_ERR_INVALID_ARG, "handle and bytes must be non-NULL");
+  *bytes = h->ws.total;
+  return DFLASH_OK;
+}
+
+int dflash_set_weights(dflash_handle_t h, const dflash_weights *w) {
+  if (!h || !w) return fail(DFLASH_ERR_INVALID_ARG, "handle and weights must be non-NULL");
+  const auto &c = h->cfg;
+  if (!w->W_c || !w->g_ctx || !w->E || !w->W_lm || !w->g_final || !w->layers)
+    return fail(DFLASH_ERR_INVALID_ARG, "a required weight pointer is NULL");
+  h->w = *w;
+  h->layers.assign(w->layers, w->layers + c.N);
+  h->w.layers = h->layers.data();
+  const int qkv_n = (c.Hq + 2 * c.Hkv) * c.hd;
+  DF_TRY(encode_2d(&h->tm_Wc, w->W_c, c.D, (uint64_t)c.L * c.Dt, (uint64_t)c.L * c.Dt, kBN));
+  DF_TRY(encode_2d(&h->tm_lm, w->W_lm, c.V, c.D, c.D, kBNTopk));
+  h->tm_qkv.resize(c.N);
+  h->tm_kc.resize(c.N);
+  h->tm_vc.resize(c.N);
+  h->tm_o.resize(c.N);
+  h->tm_gate.resize(c.N);
+  h->tm_up.resize(c.N);
+  h->tm_down.resize(c.N);
+  h->tm_c0.resize(4 * c.N);
+  h->tm_c1.resize(4 * c.N);
+  for (int n = 0; n < c.N; ++n) {
+    const dflash_layer_weights &L = h->layers[n];
+    if (!L.W_qkv || !L.Wk_c || !L.Wv_c || !L.W_o || !L.W_gate || !L.W_up || !L.W_down || !L.g_attn ||
+        !L.g_ffn)
+      return fail(DFLASH_ERR_INVALID_ARG, "layer %d: a weight pointer is NULL", n);
+    DF_TRY(encode_2d(&h->tm_qkv[n], L.W_qkv, qkv_n, c.D, c.D, kBN));
+    DF_TRY(encode_2d(&h->tm_kc[n], L.Wk_c, (uint64_t)c.Hkv * c.hd, c.D, c.D, kBN));
+    DF_TRY(encode_2d(&h->tm_vc[n], L.Wv_c, (uint64_t)c.Hkv * c.hd, c.D, c.D, kBN));
+    DF_TRY(encode_2d(&h->tm_o[n], L.W_o, c.D, (uint64_t)c.Hq * c.hd, (uint64_t)c.Hq * c.hd, kBN));
+    DF_TRY(encode_2d(&h->tm_gate[n], L.W_gate, c.F, c.D, c.D, kBN / 2));
+    DF_TRY(encode_2d(&h->tm_up[n], L.W_up, c.F, c.D, c.D, kBN / 2));
+    DF_TRY(encode_2d(&h->tm_down[n], L.W_down, c.D, c.F, c.F, kBN));
+    if (c.flags & DFLASH_FLAG_CONV) {
+      for (int q = 0; q < 4; ++q) {
+        if (!L.conv_W0[q] || !L.conv_W1[q] || !L.conv_base[q])
+          return fail(DFLASH_ERR_INVALID_ARG, "layer %d conv %d: a weight pointer is NULL", n, q);
+        DF_TRY(encode_2d(&h->tm_c0[4 * n + q], L.conv_W0[q], c.D / c.conv_group, c.D, c.D, kBN / 2));
+        DF_TRY(encode_2d(&h->tm_c1[4 * n + q], L.conv_W1[q], c.D / c.conv_group, c.D, c.D, kBN / 2));
+      }
+    }
+  }
+  if (c.flags & DFLASH_FLAG_SELECT) {
+    if (!w->W_A || !w->W_B || !w->W_G) return fail(DFLASH_ERR_INVALID_ARG, "selector weights are NULL");
+    DF_TRY(encode_2d(&h->tm_A, w->W_A, c.sel_dim, c.D, c.D, kBN / 2));
+    DF_TRY(encode_2d(&h->tm_B, w->W_B, c.sel_dim, c.D, c.D, kBN / 2));
+    DF_TRY(encode_2d(&h->tm_G, w->W_G, c.sel_dim, c.D, c.D, kBN));
+  }
+  h->have_weights = true;
+  return DFLASH_OK;
+}
+
+int dflash_status(dflash_handle_t h, void *ws, dflash_stream_t stream, int *code) {
+  if (!h || !ws || !code) return fail(DFLASH_ERR_INVALID_ARG, "handle, ws and code must be non-NULL");
+  int v = 0;
+  DF_CUDA(cudaStreamSynchronize(stream));
+  DF_CUDA(cudaMemcpy(&v, static_cast<uint8_t *>(ws) + h->ws.status, sizeof(int), cudaMemcpyDeviceToHost));
+  DF_CUDA(cudaMemset(static_cast<uint8_t *>(ws) + h->ws.status, 0, sizeof(int)));
+  *code = (v & kStatusTimeout) ? DFLASH_ERR_TIMEOUT : (v & kStatusCheck) ? DFLASH_ERR_DEVICE_CHECK : DFLASH_OK;
+  return DFLASH_OK;
+}
+
+int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *hv, const int32_t *n_commit,
+                       const int32_t *relay_a, int32_t *ctx_len, void *kcache, void *vcache,
+                       void *x0_relay, void *ws, size_t ws_bytes, dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  const auto &c = h->cfg;
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (R < 0 || R > c.max_proj_rows) return fail(DFLASH_ERR_INVALID_ARG, "R=%d outside [0, max_proj_rows]", R);
+  if (nb == 0 || R == 0) return DFLASH_OK;
+  if (!hv || !n_commit || !ctx_len || !kcache || !vcache)
+    return fail(DFLASH_ERR_INVALID_ARG, "hv, n_commit, ctx_len and the caches must be non-NULL");
+  if (relay_a && !(c.flags & DFLASH_FLAG_RELAY))
+    return fail(DFLASH_ERR_INVALID_ARG, "relay_a given but DFLASH_FLAG_RELAY is not set");
+  DF_TRY(check_ws(h, ws, ws_bytes));
+  Ws w{static_cast<uint8_t *>(ws), h->ws};
+  cudaStream_t s = stream;
+  DF_CUDA(cudaMemsetAsync(w.at<int>(h->ws.counters), 0, h->ws.counters_bytes, s));
+  const int rows = nb * R;
+  float *pre = w.at<float>(h->ws.pre);
+  uint16_t *hh = w.at<uint16_t>(h->ws.h);
+  {  // pre = hv * W_c^T
+    GemmParams p = base_params(h, w);
+    DF_TRY(encode_act(&p.tmA, hv, rows, (uint64_t)c.L * c.Dt));
+    p.tmB[0] = h->tm_Wc;
+    p.M = rows;
+    p.N = c.D;
+    p.K = c.L * c.Dt;
+    p.epi = EPI_F32;
+    p.out = pre;
+    p.ldo = c.D;
+    DF_TRY(run_gemm(h, p, kBN, s));
+  }
+  DF_CUDA(launch_rmsnorm(pre, rows, c.D, bf(h->w.g_ctx), c.eps, hh, s));
+  {  // K_c / V_c of every layer, scattered into the caches (committed rows only)
+    GemmParams p = base_params(h, w);
+    DF_TRY(encode_act(&p.tmA, hh, rows, c.D));
+    for (int n = 0; n < c.N; ++n) {
+      p.tmB[2 * n] = h->tm_kc[n];
+      p.tmB[2 * n + 1] = h->tm_vc[n];
+    }
+    p.groups = 2 * c.N;
+    p.M = rows;
+    p.N = c.Hkv * c.hd;
+    p.K = c.D;
+    p.epi = EPI_KV;
+    p.ctx_len = ctx_len;
+    p.rows_per_seq = R;
+    p.kc = kcache;
+    p.vc = vcache;
+    p.n_commit = n_commit;
+    p.Hkv = c.Hkv;
+    p.Cmax = c.Cmax;
+    p.max_batch = c.max_batch;
+    DF_TRY(run_gemm(h, p, kBN, s));
+  }
+  DF_CUDA(launch_relay_and_len(hh, nb, R, c.B, c.D, relay_a, n_commit, ctx_len,
+                               static_cast<uint16_t *>(x0_relay), c.Cmax, w.status(), s));
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, const void *x0_relay,
+                       const void *kcache, const void *vcache, const int32_t *ctx_len,
+                       int max_ctx_hint, void *out_hidden, void *ws, size_t ws_bytes,
+                       dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  const auto &c = h->cfg;
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (nb == 0) return DFLASH_OK;
+  if (!block_ids || !kcache || !vcache || !ctx_len || !out_hidden)
+    return fail(DFLASH_ERR_INVALID_ARG, "block_ids, caches, ctx_len and out_hidden must be non-NULL");
+  if (x0_relay && !(c.flags & DFLASH_FLAG_RELAY))
+    return fail(DFLASH_ERR_INVALID_ARG, "x0_relay given but DFLASH_FLAG_RELAY is not set");
+  if (max_ctx_hint < 0 || max_ctx_hint > c.Cmax)
+    return fail(DFLASH_ERR_INVALID_ARG, "max_ctx_hint=%d outside [0, Cmax]", max_ctx_hint);
+  DF_TRY(check_ws(h, ws, ws_bytes));
+  Ws w{static_cast<uint8_t *>(ws), h->ws};
+  cudaStream_t s = stream;
+  const bool conv = (c.flags & DFLASH_FLAG_CONV) != 0;
+  const int M = nb * c.B;
+  const int qkv_n = (c.Hq + 2 * c.Hkv) * c.hd;
+  const int max_ctx = max_ctx_hint > 0 ? max_ctx_hint : c.Cmax;
+  float *x = w.at<float>(h->ws.x);
+  uint16_t *u = w.at<uint16_t>(h->ws.u);
+  uint16_t *qkv = w.at<uint16_t>(h->ws.qkv);
+  uint16_t *o = w.at<uint16_t>(h->ws.o);
+  uint16_t *act = w.at<uint16_t>(h->ws.act);
+  DF_CUDA(cudaMemsetAsync(w.at<int>(h->ws.counters), 0, h->ws.counters_bytes, s));
+
+  CUtensorMap tm_u, tm_o, tm_act;
+  DF_TRY(encode_act(&tm_u, u, M, c.D));
+  DF_TRY(encode_act(&tm_o, o, M, (uint64_t)c.Hq * c.hd));
+  DF_TRY(encode_act(&tm_act, act, M, c.F));
+
+  DF_CUDA(launch_embed_rmsnorm(block_ids, bf(h->w.E), static_cast<const uint16_t *>(x0_relay), M, c.D,
+                               c.V, x, conv ? nullptr : bf(h->layers[0].g_attn), c.eps, u, w.status(), s));
+  AttnParams ap{};
+  ap.qkv = qkv;
+  ap.ctx_len = ctx_len;
+  ap.o = o;
+  ap.part_o = w.at<float>(h->ws.apart);
+  ap.part_ml = w.at<float>(h->ws.aml);
+  ap.nb = nb;
+  ap.B = c.B;
+  ap.Hq = c.Hq;
+  ap.Hkv = c.Hkv;
+  ap.hd = c.hd;
+  ap.Cmax = c.Cmax;
+  ap.max_batch = c.max_batch;
+  ap.max_ctx = max_ctx;
+  ap.status = w.status();
+  ap.chunk = attn_chunk(h, nb, max_ctx, &ap.splits);
+  if ((size_t)nb * c.Hkv * ap.splits > h->ws.apart_ctas)
+    return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "attention partials exceed the workspace plan");
+
+  for (int n = 0; n < c.N; ++n) {
+    const dflash_layer_weights &Lw = h->layers[n];
+    if (conv) {
+      DF_TRY(run_conv(h, w, n, 0, M, x, s));
+      DF_CUDA(launch_rmsnorm(x, M, c.D, bf(Lw.g_attn), c.eps, u, s));
+    } else if (n > 0) {
+      DF_CUDA(launch_rmsnorm(x, M, c.D, bf(Lw.g_attn), c.eps, u, s));
+    }
+    {  // q | k_b | v_b with RoPE on q and k_b at positions ctx_len + j
+      GemmParams p = base_params(h, w);
+      p.tmA = tm_u;
+      p.tmB[0] = h->tm_qkv[n];
+      p.M = M;
+      p.N = qkv_n;
+      p.K = c.D;
+      p.epi = EPI_ROPE;
+      p.out = qkv;
+      p.ldo = qkv_n;
+      p.ctx_len = ctx_len;
+      p.rows_per_seq = c.B;
+      p.rope_cols = (c.Hq + c.Hkv) * c.hd;
+      DF_TRY(run_gemm(h, p, kBN, s));
+    }
+    ap.kc = static_cast<const uint16_t *>(kcache) + n * cache_layer_elems(c);
+    ap.vc = static_cast<const uint16_t *>(vcache) + n * cache_layer_elems(c);
+    DF_CUDA(launch_attention(ap, s));
+    {  // x += o W_O^T
+      GemmParams p = base_params(h, w);
+      p.tmA = tm_o;
+      p.tmB[0] = h->tm_o[n];
+      p.M = M;
+      p.N = c.D;
+      p.K = c.Hq * c.hd;
+      p.epi = EPI_RESID;
+      p.xres = x;
+      p.ldo = c.D;
+      DF_TRY(run_gemm(h, p, kBN, s));
+    }
+    if (conv) {
+      DF_TRY(run_conv(h, w, n, 1, M, x, s));
+      DF_TRY(run_conv(h, w, n, 2, M, x, s));
+    }
+    DF_CUDA(launch_rmsnorm(x, M, c.D, bf(Lw.g_ffn), c.eps, u, s));
+    {  // act = silu(u W_gate^T) * (u W_up^T)
+      GemmParams p = base_params(h, w);
+      p.tmA = tm_u;
+      p.tmB[0] = h->tm_gate[n];
+      p.tmB[1] = h->tm_up[n];
+      p.dual = 1;
+      p.M = M;
+      p.N = c.F;
+      p.K = c.D;
+      p.epi = EPI_SWIGLU;
+      p.out = act;
+      p.ldo = c.F;
+      DF_TRY(run_gemm(h, p, kBN, s));
+    }
+    {  // x += act W_down^T
+      GemmParams p = base_params(h, w);
+      p.tmA = tm_act;
+      p.tmB[0] = h->tm_down[n];
+      p.M = M;
+      p.N = c.D;
+      p.K = c.F;
+      p.epi = EPI_RESID;
+      p.xres = x;
+      p.ldo = c.D;
+      DF_TRY(run_gemm(h, p, kBN, s));
+    }
+    if (conv) DF_TRY(run_conv(h, w, n, 3, M, x, s));
+  }
+  DF_CUDA(launch_rmsnorm(x, M, c.D, bf(h->w.g_final), c.eps, static_cast<uint16_t *>(out_hidden), s));
+  return DFLASH_OK;
+}
+
+int dflash_lm_head_topk(dflash_handle_t h, int nb, const void *hidden, int k, int32_t *out_ids,
+                        float *out_vals, float *out_logits, void *ws, size_t ws_bytes,
+                        dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  const auto &c = h->cfg;
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (k < 1 || k > c.k_top) return fail(DFLASH_ERR_INVALID_ARG, "k=%d outside [1, k_top]", k);
+  if (nb == 0) return DFLASH_OK;
+  if (!hidden || !out_ids || !out_vals) return fail(DFLASH_ERR_INVALID_ARG, "hidden and outputs must be non-NULL");
+  DF_TRY(check_ws(h, ws, ws_bytes));
+  Ws w{static_cast<uint8_t *>(ws), h->ws};
+  cudaStream_t s = stream;
+  const int R = c.B - 1;
+  const int S = 128 / R;
+  const int Ml = nb * R;
+  GemmParams p = base_params(h, w);
+  // rows 1..B-1 of every block: 3D map {D, B-1, nb} starting at row 1
+  DF_TRY(encode_3d(&p.tmA, static_cast<const uint16_t *>(hidden) + c.D, c.D, R, nb, c.D,
+                   (uint64_t)c.B * c.D, R, S));
+  p.tmB[0] = h->tm_lm;
+  p.a_grouped = 1;
+  p.a_S = S;
+  p.tile_rows = S * R;
+  p.M = Ml;
+  p.N = c.V;
+  p.K = c.D;
+  p.epi = EPI_TOPK;
+  p.topk_k = k;
+  p.part_vals = w.at<float>(h->ws.tk_vals);
+  p.part_ids = w.at<int>(h->ws.tk_ids);
+  p.logits_out = out_logits;
+  DF_TRY(run_gemm(h, p, kBNTopk, s));
+  const int ranges = p.items / p.m_tiles;
+  if (ranges > h->num_sms) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "top-k ranges exceed the plan");
+  DF_CUDA(launch_topk_merge(p.part_vals, p.part_ids, Ml, k, k, (long long)Ml * k, ranges, k, out_ids,
+                            out_vals, s));
+  return DFLASH_OK;
+}
+
+int dflash_topk(dflash_handle_t h, int rows, int cols, const float *logits, int k, int32_t *out_ids,
+                float *out_vals, void *ws, size_t ws_bytes, dflash_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+  if (rows < 0 || cols < 1 || k < 1 || k > kTopkMax || k > cols)
+    return fail(DFLASH_ERR_INVALID_ARG, "rows=%d cols=%d k=%d", rows, cols, k);
+  if (rows == 0) return DFLASH_OK;
+  if (!logits || !out_ids || !out_vals) return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor");
+  DF_CUDA(launch_topk_merge(logits, nullptr, rows, cols, cols, 0, 1, k, out_ids, out_vals, stream));
+  return DFLASH_OK;
+}
+
+int dflash_accept(dflash_handle_t h, int nb, const int32_t *draft, const int32_t *target,
+                  int32_t *out_tau, int32_t *out_bonus, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+  if (nb < 0) return fail(DFLASH_ERR_INVALID_ARG, "nb < 0");
+  if (nb == 0) return DFLASH_OK;
+  if (!draft || !target || !out_tau || !out_bonus) return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor");
+  DF_CUDA(launch_accept(draft, target, nb, h->cfg.B, out_tau, out_bonus, stream));
+  return DFLASH_OK;
+}
+
+int dflash2_conv(dflash_handle_t h, int layer, int which, int nb, float *x, void *ws, size_t ws_bytes,
+                 dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  const auto &c = h->cfg;
+  if (!(c.flags & DFLASH_FLAG_CONV)) return fail(DFLASH_ERR_INVALID_ARG, "DFLASH_FLAG_CONV is not set");
+  if (layer < 0 || layer >= c.N || which < 0 || which > 3)
+    return fail(DFLASH_ERR_INVALID_ARG, "layer=%d which=%d", layer, which);
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (nb == 0) return DFLASH_OK;
+  if (!x) return fail(DFLASH_ERR_INVALID_ARG, "x is NULL");
+  DF_TRY(check_ws(h, ws, ws_bytes));
+  Ws w{static_cast<uint8_t *>(ws), h->ws};
+  DF_CUDA(cudaMemsetAsync(w.at<int>(h->ws.counters), 0, h->ws.counters_bytes, stream));
+  return run_conv(h, w, layer, which, nb * c.B, x, stream);
+}
+
+int dflash2_select(dflash_handle_t h, int nb, int k, const int32_t *topk_ids, const float *topk_vals,
+                   const void *hidden, const int32_t *block_ids, int32_t *out_path, void *ws,
+                   size_t ws_bytes, dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  const auto &c = h->cfg;
+  if (!(c.flags & DFLASH_FLAG_SELECT)) return fail(DFLASH_ERR_INVALID_ARG, "DFLASH_FLAG_SELECT is not set");
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (k < 1 || k > c.k_top) return fail(DFLASH_ERR_INVALID_ARG, "k=%d outside [1, k_top]", k);
+  if (nb == 0) return DFLASH_OK;
+  if (!topk_ids || !topk_vals || !hidden || !block_ids || !out_path)
+    return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor");
+  DF_TRY(check_ws(h, ws, ws_bytes));
+  Ws w{static_cast<uint8_t *>(ws), h->ws};
+  cudaStream_t s = stream;
+  DF_CUDA(cudaMemsetAsync(w.at<int>(h->ws.counters), 0, h->ws.counters_bytes, s));
+  const int per = 1 + (c.B - 1) * k;
+  const int rows = nb * per;
+  uint16_t *eg = w.at<uint16_t>(h->ws.sel_e);
+  float *ab = w.at<float>(h->ws.sel_ab);
+  float *gp = w.at<float>(h->ws.sel_g);
+  DF_CUDA(launch_gather_select(block_ids, topk_ids, nb, c.B, k, bf(h->w.E), c.D, c.V, eg, w.status(), s));
+  {  // A | B projections of the gathered embeddings
+    GemmParams p = base_params(h, w);
+    DF_TRY(encode_act(&p.tmA, eg, rows, c.D));
+    p.tmB[0] = h->tm_A;
+    p.tmB[1] = h->tm_B;
+    p.dual = 1;
+    p.M = rows;
+    p.N = c.sel_dim;
+    p.K = c.D;
+    p.epi = EPI_DUAL_F32;
+    p.out = ab;
+    p.ldo = 2 * c.sel_dim;
+    DF_TRY(run_gemm(h, p, kBN, s));
+  }
+  {  // G pre-activation from the hidden rows of offsets 1..B-1
+    const int R = c.B - 1;
+    const int S = 128 / R;
+    GemmParams p = base_params(h, w);
+    DF_TRY(encode_3d(&p.tmA, static_cast<const uint16_t *>(hidden) + c.D, c.D, R, nb, c.D,
+                     (uint64_t)c.B * c.D, R, S));
+    p.tmB[0] = h->tm_G;
+    p.a_grouped = 1;
+    p.a_S = S;
+    p.tile_rows = S * R;
+    p.M = nb * R;
+    p.N = c.sel_dim;
+    p.K = c.D;
+    p.epi = EPI_F32;
+    p.out = gp;
+    p.ldo = c.sel_dim;
+    DF_TRY(run_gemm(h, p, kBN, s));
+  }
+  DF_CUDA(launch_select_walk(topk_ids, topk_vals, ab, gp, block_ids, nb, c.B, k, c.sel_dim, out_path, s));
+  return DFLASH_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,600 @@
+// tcgen05 tensor-core GEMM for the draft step's dense contractions:
+//   D[M, N] = A[M, K] * B[N, K]^T,  A = activations (bf16), B = weights (bf16),
+//   fp32 accumulation in TMEM, fused epilogues.
+//
+// Hardware mapping (sm_103a):
+//   * one CTA = 6 warps: warp 0 issues TMA tile loads (128B swizzle, K-major),
+//     warp 1 allocates TMEM and one thread issues tcgen05.mma (M=128, N=BN, K=16),
+//     warps 2..5 drain the fp32 accumulator with tcgen05.ld (32x32b) and run the
+//     epilogue; each epilogue warp owns the TMEM lane quarter (warp % 4).
+//   * an mbarrier ring of STAGES smem slots couples TMA and MMA; tcgen05.commit
+//     frees a slot when the MMAs that read it complete.
+//   * two TMEM accumulators (2*BN columns) let the epilogue of one work item run
+//     under the MMAs of the next; CTAs are persistent over work items.
+//   * split-K: every split writes its fp32 partial tile; the last split to arrive
+//     (atomic counter, no waiting) sums the partials in split order and runs the
+//     epilogue, so results do not depend on arrival order.
+//   * weights are streamed with an L2 evict-first policy, activations evict-last.
+#include <algorithm>
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace df {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kGemmThreads = 192;
+// Bound of the teardown waits for this CTA's own TMA copies and MMAs, which finish
+// without help from any other thread; independent of the caller's max_spin.
+constexpr int kDrainSpin = 1 << 22;
+
+template <int BN>
+struct TileCfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (200 * 1024 / STAGE) > 8 ? 8 : (200 * 1024 / STAGE);
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE + 256;
+};
+
+struct Item {
+  int m, n, g, s;
+};
+
+__device__ __forceinline__ int item_count(const GemmParams &p) {
+  if (p.epi == EPI_TOPK) {
+    const int range = blockIdx.x / p.m_tiles;
+    const int n0 = range * p.tiles_per_cta;
+    const int n1 = min(p.n_tiles, n0 + p.tiles_per_cta);
+    return max(0, n1 - n0);
+  }
+  if (static_cast<int>(blockIdx.x) >= p.items) return 0;
+  return (p.items - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1;
+}
+
+__device__ __forceinline__ Item item_at(const GemmParams &p, int j) {
+  Item r;
+  if (p.epi == EPI_TOPK) {
+    r.m = blockIdx.x % p.m_tiles;
+    r.n = (blockIdx.x / p.m_tiles) * p.tiles_per_cta + j;
+    r.g = 0;
+    r.s = 0;
+    return r;
+  }
+  int it = blockIdx.x + j * gridDim.x;
+  r.m = it % p.m_tiles;
+  it /= p.m_tiles;
+  r.n = it % p.n_tiles;
+  it /= p.n_tiles;
+  r.g = it % p.groups;
+  r.s = it / p.groups;
+  return r;
+}
+
+// ------------------------------------------------------------------ epilogue helpers
+
+__device__ __forceinline__ void store_bf16_32(uint16_t *dst, const float (&v)[32], int nvalid) {
+  if (nvalid >= 32) {
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+      d4[q] = w;
+    }
+  } else {
+    for (int i = 0; i < nvalid; ++i) {
+      __nv_bfloat16 b = __float2bfloat16_rn(v[i]);
+      dst[i] = *reinterpret_cast<uint16_t *>(&b);
+    }
+  }
+}
+
+__device__ __forceinline__ void store_f32_32(float *dst, const float (&v)[32], int nvalid) {
+  if (nvalid >= 32) {
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  } else {
+    for (int i = 0; i < nvalid; ++i) dst[i] = v[i];
+  }
+}
+
+__device__ __forceinline__ void add_f32_32(float *dst, const float (&v)[32], int nvalid) {
+  if (nvalid >= 32) {
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float4 x = d4[q];
+      x.x += v[4 * q];
+      x.y += v[4 * q + 1];
+      x.z += v[4 * q + 2];
+      x.w += v[4 * q + 3];
+      d4[q] = x;
+    }
+  } else {
+    for (int i = 0; i < nvalid; ++i) dst[i] += v[i];
+  }
+}
+
+__device__ __forceinline__ void rope_pair(const GemmParams &p, int pos, int d0, float (&a)[32],
+                                          float (&b)[32]) {
+  const float fpos = static_cast<float>(pos);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float sn, cs;
+    sincosf(fpos * p.inv_freq[d0 + i], &sn, &cs);
+    const float x1 = a[i], x2 = b[i];
+    a[i] = x1 * cs - x2 * sn;
+    b[i] = x2 * cs + x1 * sn;
+  }
+}
+
+__device__ __forceinline__ void topk_insert(float (&kv)[kTopkMax], int (&ki)[kTopkMax], float v,
+                                            int id) {
+  if (!topk_before(v, id, kv[kTopkMax - 1], ki[kTopkMax - 1])) return;
+  float cv = v;
+  int ci = id;
+#pragma unroll
+  for (int s = 0; s < kTopkMax; ++s) {
+    if (topk_before(cv, ci, kv[s], ki[s])) {
+      const float tv = kv[s];
+      const int ti = ki[s];
+      kv[s] = cv;
+      ki[s] = ci;
+      cv = tv;
+      ci = ti;
+    }
+  }
+}
+
+// Runs the epilogue of one output tile. `fetch(c, v)` returns the 32 fp32 values of
+// accumulator columns [32c, 32c+32) of this thread's row; it is called by every lane
+// (tcgen05.ld is warp-collective); only the stores depend on row validity.
+template <int BN, int EPI, class Fetch>
+__device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t, int row,
+                                              bool row_ok, Fetch &&fetch, float (&kv)[kTopkMax],
+                                              int (&ki)[kTopkMax]) {
+  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_RESID) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      fetch(c, v);
+      const int col0 = t.n * BN + c * 32;
+      const int nval = min(32, p.N - col0);
+      if (row_ok && nval > 0) {
+        if constexpr (EPI == EPI_BF16)
+          store_bf16_32(static_cast<uint16_t *>(p.out) + row * p.ldo + col0, v, nval);
+        else if constexpr (EPI == EPI_F32)
+          store_f32_32(static_cast<float *>(p.out) + row * p.ldo + col0, v, nval);
+        else
+          add_f32_32(p.xres + row * p.ldo + col0, v, nval);
+      }
+    }
+  } else if constexpr (EPI == EPI_ROPE) {
+    const int half = p.hd >> 1;
+    int pos = 0;
+    if (row_ok) pos = p.ctx_len[row / p.rows_per_seq] + row % p.rows_per_seq;
+#pragma unroll 1
+    for (int h0 = 0; h0 < BN; h0 += p.hd) {
+      const int gcol = t.n * BN + h0;
+      const bool rot = gcol < p.rope_cols;
+#pragma unroll 1
+      for (int cc = 0; cc < half; cc += 32) {
+        float a[32], b[32];
+        fetch((h0 + cc) >> 5, a);
+        fetch((h0 + half + cc) >> 5, b);
+        if (row_ok && gcol < p.N) {
+          if (rot) rope_pair(p, pos, cc, a, b);
+          uint16_t *o = static_cast<uint16_t *>(p.out) + row * p.ldo + gcol;
+          store_bf16_32(o + cc, a, 32);
+          store_bf16_32(o + half + cc, b, 32);
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      float g[32], u[32];
+      fetch(c, g);
+      fetch(c + BN / 64, u);
+      const int col0 = t.n * (BN / 2) + c * 32;
+      const int nval = min(32, p.N - col0);
+      if (row_ok && nval > 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + expf(-g[i])) * u[i];
+        store_bf16_32(static_cast<uint16_t *>(p.out) + row * p.ldo + col0, g, nval);
+      }
+    }
+  } else if constexpr (EPI == EPI_DUAL_F32) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      fetch(c, v);
+      const int which = c >= BN / 64 ? 1 : 0;
+      const int col0 = t.n * (BN / 2) + (c - which * (BN / 64)) * 32;
+      const int nval = min(32, p.N - col0);
+      if (row_ok && nval > 0)
+        store_f32_32(static_cast<float *>(p.out) + row * p.ldo + which * p.N + col0, v, nval);
+    }
+  } else if constexpr (EPI == EPI_KV) {
+    const int layer = t.g >> 1;
+    const bool isk = (t.g & 1) == 0;
+    const int half = p.hd >> 1;
+    int seq = 0, pos = 0;
+    bool live = false;
+    if (row_ok) {
+      seq = row / p.rows_per_seq;
+      const int j = row % p.rows_per_seq;
+      live = j < p.n_commit[seq];
+      pos = p.ctx_len[seq] + j;
+      if (live && (pos < 0 || pos >= p.Cmax)) {
+        flag_status(p.status, kStatusCheck);
+        live = false;
+      }
+    }
+    uint16_t *cache = static_cast<uint16_t *>(isk ? p.kc : p.vc);
+#pragma unroll 1
+    for (int h0 = 0; h0 < BN; h0 += p.hd) {
+      const int head = (t.n * BN + h0) / p.hd;
+#pragma unroll 1
+      for (int cc = 0; cc < half; cc += 32) {
+        float a[32], b[32];
+        fetch((h0 + cc) >> 5, a);
+        fetch((h0 + half + cc) >> 5, b);
+        if (live && head < p.Hkv) {
+          if (isk) rope_pair(p, pos, cc, a, b);
+          uint16_t *o = cache + ((((size_t)layer * p.max_batch + seq) * p.Hkv + head) * p.Cmax + pos) *
+                                    (size_t)p.hd;
+          store_bf16_32(o + cc, a, 32);
+          store_bf16_32(o + half + cc, b, 32);
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_TOPK) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      fetch(c, v);
+      const int col0 = t.n * BN + c * 32;
+      if (row_ok) {
+        if (p.logits_out) {
+          const int nval = min(32, p.N - col0);
+          if (nval > 0) store_f32_32(p.logits_out + (size_t)row * p.N + col0, v, nval);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i < p.N) topk_insert(kv, ki, v[i], col0 + i);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+  using C = TileCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE);
+  uint64_t *empty = full + C::STAGES;
+  uint64_t *acc_full = empty + C::STAGES;
+  uint64_t *acc_empty = acc_full + 2;
+  uint64_t *mma_done = acc_empty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+  volatile int *s_last = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nitems = item_count(p);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0 && nitems > 0 && !p.stall) {
+      // ---------------- TMA producer
+      tma_prefetch_desc(&p.tmA);
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; j < nitems && ok; ++j) {
+        const Item t = item_at(p, j);
+        const int kt0 = t.s * p.kt_per_split;
+        const int kt1 = min(p.kt_total, kt0 + p.kt_per_split);
+        for (int kt = kt0; kt < kt1; ++kt, ++it) {
+          const int st = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!mbar_wait(&empty[st], ph ^ 1, p.max_spin)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[st], p.stage_tx_bytes);
+          uint8_t *a = sA + st * C::A_BYTES;
+          uint8_t *b = sB + st * C::B_BYTES;
+          if (p.a_grouped)
+            tma_load_3d(a, &p.tmA, &full[st], kt * BK, 0, t.m * p.a_S, pol_a);
+          else
+            tma_load_3d(a, &p.tmA, &full[st], kt * BK, t.m * BM, 0, pol_a);
+          if (p.dual) {
+            tma_load_2d(b, &p.tmB[0], &full[st], kt * BK, t.n * (BN / 2), pol_w);
+            tma_load_2d(b + (BN / 2) * 128, &p.tmB[1], &full[st], kt * BK, t.n * (BN / 2), pol_w);
+          } else {
+            tma_load_2d(b, &p.tmB[t.g], &full[st], kt * BK, t.n * BN, pol_w);
+          }
+        }
+      }
+      if (!ok) flag_status(p.status, kStatusTimeout);
+      // Every issued load must land before the CTA may exit (bounded).
+      for (int k = max(0, it - C::STAGES); k < it; ++k)
+        mbar_wait(&full[k % C::STAGES], (k / C::STAGES) & 1, kDrainSpin);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && nitems > 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; j < nitems && ok; ++j) {
+        const Item t = item_at(p, j);
+        const int buf = j & 1;
+        const uint32_t use = j >> 1;
+        if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, p.max_spin)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * BN;
+        const int kt0 = t.s * p.kt_per_split;
+        const int kt1 = min(p.kt_total, kt0 + p.kt_per_split);
+        for (int kt = kt0; kt < kt1; ++kt, ++it) {
+          const int st = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!mbar_wait(&full[st], ph, p.max_spin)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + st * C::A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + st * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma_bf16(d, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32),
+                        idesc, (kt > kt0 || k > 0) ? 1u : 0u);
+          tc_commit(&empty[st]);
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[buf]);
+      }
+      if (!ok) flag_status(p.status, kStatusTimeout);
+      // Every issued MMA must complete before TMEM is freed (bounded).
+      tc_commit(mma_done);
+      mbar_wait(mma_done, 0, kDrainSpin);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    float kv[kTopkMax];
+    int ki[kTopkMax];
+#pragma unroll
+    for (int s = 0; s < kTopkMax; ++s) {
+      kv[s] = -FLT_MAX;
+      ki[s] = INT_MAX;
+    }
+    bool ok = true;
+    for (int j = 0; j < nitems; ++j) {
+      const Item t = item_at(p, j);
+      const int buf = j & 1;
+      const uint32_t use = j >> 1;
+      if (!mbar_wait(&acc_full[buf], use & 1, p.max_spin)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+      const int row = t.m * p.tile_rows + r;
+      const bool row_ok = (r < p.tile_rows) && (row < p.M);
+      if (p.splits > 1) {
+        const int tile = (t.g * p.n_tiles + t.n) * p.m_tiles + t.m;
+        float *mine = p.partial + ((size_t)(tile * p.splits + t.s) * BM + r) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          float4 *d4 = reinterpret_cast<float4 *>(mine + c * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            __stcg(d4 + k, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 64) {
+          const int old = atomicAdd(&p.counters[tile], 1);
+          *s_last = (old == p.splits - 1) ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        if (!*s_last) continue;
+        __threadfence();
+        const float *base = p.partial + ((size_t)tile * p.splits * BM + r) * BN;
+        auto fetch = [&](int c, float (&v)[32]) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          for (int s = 0; s < p.splits; ++s) {
+            const float4 *src = reinterpret_cast<const float4 *>(base + (size_t)s * BM * BN + c * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float4 x = __ldcg(src + k);
+              v[4 * k] += x.x;
+              v[4 * k + 1] += x.y;
+              v[4 * k + 2] += x.z;
+              v[4 * k + 3] += x.w;
+            }
+          }
+        };
+        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, kv, ki);
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 64) p.counters[tile] = 0;
+      } else {
+        auto fetch = [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); };
+        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, kv, ki);
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+      }
+    }
+    if (!ok) flag_status(p.status, kStatusTimeout);
+    if constexpr (EPI == EPI_TOPK) {
+      if (ok && nitems > 0) {
+        const int m = blockIdx.x % p.m_tiles;
+        const int range = blockIdx.x / p.m_tiles;
+        const int row = m * p.tile_rows + r;
+        if (r < p.tile_rows && row < p.M) {
+          float *pv = p.part_vals + ((size_t)range * p.M + row) * p.topk_k;
+          int *pi = p.part_ids + ((size_t)range * p.M + row) * p.topk_k;
+#pragma unroll
+          for (int s = 0; s < kTopkMax; ++s)
+            if (s < p.topk_k) {
+              pv[s] = kv[s];
+              pi[s] = ki[s];
+            }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN) {
+  const int m_tiles = (M + tile_rows - 1) / tile_rows;
+  const int ncols = dual ? BN / 2 : BN;
+  const int n_tiles = (N + ncols - 1) / ncols;
+  return m_tiles * n_tiles * groups;
+}
+
+void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN, int num_sms,
+               int epi, int *splits_out, int *kps_out, int *items_out, int *grid_out) {
+  const int base = gemm_tiles(M, tile_rows, N, groups, dual, BN);
+  const int kt = (K + BK - 1) / BK;
+  int best_kps = kt, best_splits = 1;
+  if (epi != EPI_TOPK) {
+    double best_score = -1e30;
+    for (int kps = kt; kps >= 1; --kps) {
+      const int splits = (kt + kps - 1) / kps;
+      if (kps < 4 && splits > 1) break;
+      if (splits > 32) break;
+      const long long items = (long long)base * splits;
+      const long long waves = (items + num_sms - 1) / num_sms;
+      const double eff = double(items) / double(waves * num_sms);
+      const double score = eff - 0.01 * splits;
+      if (score > best_score + 1e-9) {
+        best_score = score;
+        best_kps = kps;
+        best_splits = splits;
+      }
+    }
+  }
+  *splits_out = best_splits;
+  *kps_out = best_kps;
+  *items_out = base * best_splits;
+  *grid_out = std::max(1, std::min(base * best_splits, num_sms));
+}
+
+size_t gemm_partial_bytes(int M, int tile_rows, int N, int K, int groups, int dual, int BN,
+                          int num_sms, int epi) {
+  int splits, kps, items, grid;
+  gemm_plan(M, tile_rows, N, K, groups, dual, BN, num_sms, epi, &splits, &kps, &items, &grid);
+  if (splits <= 1) return 0;
+  const int tiles = gemm_tiles(M, tile_rows, N, groups, dual, BN);
+  return (size_t)tiles * splits * BM * BN * sizeof(float);
+}
+
+template <int BN, int EPI>
+static cudaError_t launch_one(const GemmParams &p, int grid, cudaStream_t s) {
+  using C = TileCfg<BN>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  gemm_tc_kernel<BN, EPI><<<grid, kGemmThreads, C::SMEM, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s) {
+  if (p.a_grouped == 0) p.tile_rows = BM;
+  p.m_tiles = (p.M + p.tile_rows - 1) / p.tile_rows;
+  const int ncols = p.dual ? BN / 2 : BN;
+  p.n_tiles = (p.N + ncols - 1) / ncols;
+  p.kt_total = (p.K + BK - 1) / BK;
+  int grid;
+  if (p.epi == EPI_TOPK) {
+    p.splits = 1;
+    p.kt_per_split = p.kt_total;
+    const int ranges0 = std::max(1, num_sms / p.m_tiles);
+    p.tiles_per_cta = (p.n_tiles + ranges0 - 1) / ranges0;
+    const int ranges = (p.n_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
+    grid = ranges * p.m_tiles;
+    p.items = grid;
+  } else {
+    gemm_plan(p.M, p.tile_rows, p.N, p.K, p.groups, p.dual, BN, num_sms, p.epi, &p.splits,
+              &p.kt_per_split, &p.items, &grid);
+  }
+  // expect-tx bytes of one stage: the A box plus the B box(es)
+  const uint32_t a_rows = p.a_grouped ? (uint32_t)p.tile_rows : (uint32_t)BM;
+  p.stage_tx_bytes = a_rows * BK * 2 + (uint32_t)BN * BK * 2;
+  switch (BN * 16 + p.epi) {
+    case 128 * 16 + EPI_BF16: return launch_one<128, EPI_BF16>(p, grid, s);
+    case 128 * 16 + EPI_F32: return launch_one<128, EPI_F32>(p, grid, s);
+    case 128 * 16 + EPI_RESID: return launch_one<128, EPI_RESID>(p, grid, s);
+    case 128 * 16 + EPI_ROPE: return launch_one<128, EPI_ROPE>(p, grid, s);
+    case 128 * 16 + EPI_SWIGLU: return launch_one<128, EPI_SWIGLU>(p, grid, s);
+    case 128 * 16 + EPI_DUAL_F32: return launch_one<128, EPI_DUAL_F32>(p, grid, s);
+    case 128 * 16 + EPI_KV: return launch_one<128, EPI_KV>(p, grid, s);
+    case 256 * 16 + EPI_TOPK: return launch_one<256, EPI_TOPK>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace df

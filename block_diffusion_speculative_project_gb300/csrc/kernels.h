@@ -1,0 +1,140 @@
+// Internal interface between the C-ABI layer (dflash_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace df {
+
+// Bits of the device status word (first word of the workspace).
+constexpr int kStatusTimeout = 1;  // a bounded wait ran out
+constexpr int kStatusCheck = 2;    // a bounds check failed (index skipped)
+
+constexpr int kNumSMsDefault = 152;
+
+// ---------------------------------------------------------------- GEMM engine
+
+enum GemmEpi : int {
+  EPI_BF16 = 0,   // out bf16 [M, ldo] = acc
+  EPI_F32 = 1,    // out f32  [M, ldo] = acc
+  EPI_RESID = 2,  // xres f32 [M, ldo] += acc
+  EPI_ROPE = 3,   // out bf16 = RoPE(acc) on columns < rope_cols (per hd-wide head)
+  EPI_SWIGLU = 4, // dual: out bf16 [M, ldo] = silu(acc_gate) * acc_up
+  EPI_DUAL_F32 = 5, // dual: out f32 [M, ldo]: cols [0,N) from B0, [N,2N) from B1
+  EPI_KV = 6,     // grouped: scatter rows into the K/V caches (RoPE on K groups)
+  EPI_TOPK = 7,   // per-row running top-k over the CTA's vocab range
+};
+
+constexpr int kMaxBMaps = 12;
+constexpr int kTopkMax = 16;
+
+// Kernel parameters of the tcgen05 GEMM  D[M, N] = A[M, K] * B[N, K]^T.
+// A: bf16 rows, read through a 3D tensor map {K, R, G} (plain matrices use G = 1).
+// B: bf16 weights [N, K], one 2D tensor map per group (or two for dual).
+struct GemmParams {
+  CUtensorMap tmA;
+  CUtensorMap tmB[kMaxBMaps];
+  int M;           // logical rows
+  int tile_rows;   // logical rows per m-tile (<= 128)
+  int a_grouped;   // 0: tile m loads rows [128m, 128m+128) of dim1; 1: groups [m*S, m*S+S)
+  int a_S;         // groups per tile when a_grouped
+  int N;           // output columns per group (per weight when dual)
+  int K;
+  int m_tiles, n_tiles, groups, dual, splits;
+  int kt_total, kt_per_split;
+  int items;       // m_tiles * n_tiles * groups * splits
+  uint32_t stage_tx_bytes;
+  int epi;
+  void *out;
+  long long ldo;
+  float *xres;
+  // RoPE (EPI_ROPE, EPI_KV)
+  const int *ctx_len;
+  int rows_per_seq;
+  int rope_cols;
+  int hd;
+  float inv_freq[64];
+  // K/V scatter (EPI_KV): group g -> layer g/2, g%2 == 0 keys (rotated), 1 values
+  void *kc;
+  void *vc;
+  const int *n_commit;
+  int Hkv, Cmax, max_batch;
+  // top-k (EPI_TOPK)
+  int topk_k;
+  int tiles_per_cta;
+  float *part_vals;  // [ranges][M][topk_k]
+  int *part_ids;
+  float *logits_out; // [M][N] or null
+  // split-K
+  float *partial;    // [tile][split][128][BN] f32
+  int *counters;     // [tile]
+  int *status;
+  int max_spin;
+  int stall;         // test hook: issue no loads so the waits run out
+};
+
+struct GemmLaunch {
+  int BN;
+  int grid;
+  size_t smem;
+};
+
+// Chooses BN/splits/grid, fills the derived fields of p and launches.
+// partial/counters must be sized by gemm_scratch_bytes for the same shape.
+cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s);
+// Bytes of split-K partials and counters the launch with these shapes needs.
+void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN, int num_sms,
+               int epi, int *splits, int *kt_per_split, int *items, int *grid);
+size_t gemm_partial_bytes(int M, int tile_rows, int N, int K, int groups, int dual, int BN,
+                          int num_sms, int epi);
+int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN);
+
+// ---------------------------------------------------------------- small kernels
+
+cudaError_t launch_embed_rmsnorm(const int *ids, const uint16_t *E, const uint16_t *relay, int M,
+                                 int D, int V, float *x, const uint16_t *g, float eps, uint16_t *u,
+                                 int *status, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float *x, int M, int D, const uint16_t *g, float eps, uint16_t *u,
+                           cudaStream_t s);
+cudaError_t launch_rmsnorm_rows(const float *x, int M, int D, const uint16_t *g, float eps,
+                                uint16_t *u, int B, int skip_first, cudaStream_t s);
+cudaError_t launch_relay_and_len(const uint16_t *h, int nb, int R, int B, int D,
+                                 const int *relay_a, const int *n_commit, int *ctx_len,
+                                 uint16_t *x0_relay, int Cmax, int *status, cudaStream_t s);
+cudaError_t launch_accept(const int *draft, const int *target, int nb, int B, int *tau, int *bonus,
+                          cudaStream_t s);
+cudaError_t launch_topk_merge(const float *vals, const int *ids, int rows, int ncand_per_row,
+                              long long row_stride, long long part_stride, int parts, int k,
+                              int *out_ids, float *out_vals, cudaStream_t s);
+cudaError_t launch_f32_to_bf16(const float *x, uint16_t *y, long long n, cudaStream_t s);
+cudaError_t launch_conv_apply(float *x, const float *corr, const uint16_t *base, int M, int D,
+                              int B, int group, cudaStream_t s);
+cudaError_t launch_gather_select(const int *block_ids, const int *cand_ids, int nb, int B, int k,
+                                 const uint16_t *E, int D, int V, uint16_t *out, int *status,
+                                 cudaStream_t s);
+cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, const float *AB,
+                               const float *G, const int *block_ids, int nb, int B, int k,
+                               int sel_dim, int *path, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+
+struct AttnParams {
+  const uint16_t *qkv;  // [nb*B, (Hq+2Hkv)*hd] bf16, q and k_b already rotated
+  const uint16_t *kc;   // cache base of this layer: [max_batch][Hkv][Cmax][hd]
+  const uint16_t *vc;
+  const int *ctx_len;   // [nb]
+  uint16_t *o;          // [nb*B, Hq*hd] bf16
+  float *part_o;        // [nb][Hkv][splits][rows][hd]
+  float *part_ml;       // [nb][Hkv][splits][rows][2]
+  int nb, B, Hq, Hkv, hd, Cmax, max_batch;
+  int chunk;            // context keys per split (multiple of 64)
+  int splits;           // grid.x
+  int max_ctx;          // bound used for the grid
+  int *status;
+};
+
+cudaError_t launch_attention(const AttnParams &p, cudaStream_t s);
+size_t attention_partial_bytes(int nb, int Hq, int Hkv, int hd, int B, int splits);
+
+}  // namespace df

@@ -1,0 +1,396 @@
+// CUDA-core kernels of the draft step: embedding gather, RMSNorm, relay placement,
+// greedy accept, top-k merge, DFlash 2 conv application and selector walk.
+// All are memory- or latency-bound row operations; each reads its inputs once with
+// 16-byte vector accesses where the row layout allows.
+#include <algorithm>
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace df {
+
+__device__ __forceinline__ float bits_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bits(float x) {
+  __nv_bfloat16 b = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t *>(&b);
+}
+
+// Sum over a CTA of 256 threads.
+__device__ __forceinline__ float block_sum_256(float v, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) t += red[k];
+  __syncthreads();
+  return t;
+}
+
+// ---------------------------------------------------------------- RMSNorm
+// y = g * x / sqrt(mean(x^2) + eps), fp32 statistics, bf16 output.
+// Mode 0: x given (f32). Mode 1: x = E[ids[r]] (+ relay[r]) is built, stored to x,
+// and normalised when g != nullptr.
+template <int MODE>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float *xin, const int *ids,
+                                                      const uint16_t *E, const uint16_t *relay,
+                                                      float *xout, int D, const uint16_t *g,
+                                                      float eps, uint16_t *u, int B, int skip,
+                                                      int rows_out_per_seq, int V, int *status) {
+  __shared__ float red[8];
+  const int r = blockIdx.x;
+  extern __shared__ float row[];  // D floats
+  float ss = 0.f;
+  for (int c = threadIdx.x * 4; c < D; c += 256 * 4) {
+    float4 v;
+    if (MODE == 0) {
+      v = *reinterpret_cast<const float4 *>(xin + (size_t)r * D + c);
+    } else {
+      int id = ids[r];
+      if (id < 0 || id >= V) {
+        if (c == threadIdx.x * 4 && threadIdx.x == 0) flag_status(status, kStatusCheck);
+        id = 0;
+      }
+      const uint2 e = *reinterpret_cast<const uint2 *>(E + (size_t)id * D + c);
+      v = make_float4(bits_to_f32(e.x & 0xFFFF), bits_to_f32(e.x >> 16), bits_to_f32(e.y & 0xFFFF),
+                      bits_to_f32(e.y >> 16));
+      if (relay) {
+        const uint2 q = *reinterpret_cast<const uint2 *>(relay + (size_t)r * D + c);
+        v.x += bits_to_f32(q.x & 0xFFFF);
+        v.y += bits_to_f32(q.x >> 16);
+        v.z += bits_to_f32(q.y & 0xFFFF);
+        v.w += bits_to_f32(q.y >> 16);
+      }
+      *reinterpret_cast<float4 *>(xout + (size_t)r * D + c) = v;
+    }
+    *reinterpret_cast<float4 *>(row + c) = v;
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  if (g == nullptr) return;
+  const float tot = block_sum_256(ss, red);
+  const float inv = rsqrtf(tot / static_cast<float>(D) + eps);
+  // optional row remap: skip the first `skip` rows of every block of B rows
+  int orow = r;
+  if (skip) {
+    const int j = r % B;
+    if (j < skip) return;
+    orow = (r / B) * rows_out_per_seq + (j - skip);
+  }
+  for (int c = threadIdx.x * 4; c < D; c += 256 * 4) {
+    const float4 v = *reinterpret_cast<const float4 *>(row + c);
+    const uint2 gg = *reinterpret_cast<const uint2 *>(g + c);
+    uint2 o;
+    o.x = static_cast<uint32_t>(f32_to_bits(v.x * inv * bits_to_f32(gg.x & 0xFFFF))) |
+          (static_cast<uint32_t>(f32_to_bits(v.y * inv * bits_to_f32(gg.x >> 16))) << 16);
+    o.y = static_cast<uint32_t>(f32_to_bits(v.z * inv * bits_to_f32(gg.y & 0xFFFF))) |
+          (static_cast<uint32_t>(f32_to_bits(v.w * inv * bits_to_f32(gg.y >> 16))) << 16);
+    *reinterpret_cast<uint2 *>(u + (size_t)orow * D + c) = o;
+  }
+}
+
+cudaError_t launch_embed_rmsnorm(const int *ids, const uint16_t *E, const uint16_t *relay, int M,
+                                 int D, int V, float *x, const uint16_t *g, float eps, uint16_t *u,
+                                 int *status, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  rmsnorm_kernel<1><<<M, 256, D * sizeof(float), s>>>(nullptr, ids, E, relay, x, D, g, eps, u, 1, 0, 0,
+                                                      V, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const float *x, int M, int D, const uint16_t *g, float eps, uint16_t *u,
+                           cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  rmsnorm_kernel<0><<<M, 256, D * sizeof(float), s>>>(x, nullptr, nullptr, nullptr, nullptr, D, g,
+                                                      eps, u, 1, 0, 0, 0, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_rows(const float *x, int M, int D, const uint16_t *g, float eps,
+                                uint16_t *u, int B, int skip_first, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  rmsnorm_kernel<0><<<M, 256, D * sizeof(float), s>>>(x, nullptr, nullptr, nullptr, nullptr, D, g,
+                                                      eps, u, B, skip_first, B - skip_first, 0,
+                                                      nullptr);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- relay placement
+// x0_relay[i, j] = h[i*R + j + a] for j in [2, B-1-a] (j + a < R), else 0;
+// then ctx_len[i] += n_commit[i].
+__global__ void __launch_bounds__(256) relay_len_kernel(const uint16_t *h, int R, int B, int D,
+                                                        const int *relay_a, const int *n_commit,
+                                                        int *ctx_len, uint16_t *x0, int Cmax,
+                                                        int *status) {
+  const int i = blockIdx.x;
+  if (x0) {
+    const int a = relay_a ? relay_a[i] : INT_MAX / 2;
+    for (int j = 0; j < B; ++j) {
+      const int k = j + a;
+      const bool take = relay_a && j >= 2 && j <= B - 1 - a && k < R && a >= 0;
+      uint4 *dst = reinterpret_cast<uint4 *>(x0 + ((size_t)i * B + j) * D);
+      const uint4 *src = take ? reinterpret_cast<const uint4 *>(h + ((size_t)i * R + k) * D) : nullptr;
+      for (int c = threadIdx.x; c < D / 8; c += 256) dst[c] = take ? src[c] : make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (threadIdx.x == 0 && n_commit) {
+    const int nl = ctx_len[i] + n_commit[i];
+    if (nl > Cmax || n_commit[i] < 0 || n_commit[i] > R) flag_status(status, kStatusCheck);
+    ctx_len[i] = min(nl, Cmax);
+  }
+}
+
+cudaError_t launch_relay_and_len(const uint16_t *h, int nb, int R, int B, int D,
+                                 const int *relay_a, const int *n_commit, int *ctx_len,
+                                 uint16_t *x0_relay, int Cmax, int *status, cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  relay_len_kernel<<<nb, 256, 0, s>>>(h, R, B, D, relay_a, n_commit, ctx_len, x0_relay, Cmax, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- accept
+__global__ void accept_kernel(const int *draft, const int *target, int nb, int B, int *tau,
+                              int *bonus) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= nb) return;
+  const int *d = draft + (size_t)i * (B - 1);
+  const int *t = target + (size_t)i * B;
+  int n = 0;
+  while (n < B - 1 && d[n] == t[n]) ++n;
+  tau[i] = n + 1;
+  bonus[i] = t[n];
+}
+
+cudaError_t launch_accept(const int *draft, const int *target, int nb, int B, int *tau, int *bonus,
+                          cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  accept_kernel<<<(nb + 127) / 128, 128, 0, s>>>(draft, target, nb, B, tau, bonus);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- top-k merge
+// One CTA per row. Candidate c of part q of row r: vals[q*part_stride + r*row_stride + c]
+// (ids from `ids` at the same index, or c itself when ids == nullptr).
+// Each thread keeps a sorted top-16 of its strided candidates; then k rounds of a
+// CTA-wide arg-best (value descending, ties to the lower id) pop the winners.
+__global__ void __launch_bounds__(256) topk_merge_kernel(const float *vals, const int *ids,
+                                                         int ncand, long long row_stride,
+                                                         long long part_stride, int parts, int k,
+                                                         int *out_ids, float *out_vals) {
+  __shared__ float sv[256 * kTopkMax];
+  __shared__ int si[256 * kTopkMax];
+  __shared__ float wv[8];
+  __shared__ int wi[8], wt[8];
+  const int r = blockIdx.x;
+  float kv[kTopkMax];
+  int ki[kTopkMax];
+#pragma unroll
+  for (int s = 0; s < kTopkMax; ++s) {
+    kv[s] = -FLT_MAX;
+    ki[s] = INT_MAX;
+  }
+  const long long total = (long long)parts * ncand;
+  for (long long e = threadIdx.x; e < total; e += 256) {
+    const int q = static_cast<int>(e / ncand), c = static_cast<int>(e % ncand);
+    const long long idx = (long long)q * part_stride + (long long)r * row_stride + c;
+    const float v = vals[idx];
+    const int id = ids ? ids[idx] : c;
+    if (!topk_before(v, id, kv[kTopkMax - 1], ki[kTopkMax - 1])) continue;
+    float cv = v;
+    int ci = id;
+#pragma unroll
+    for (int s = 0; s < kTopkMax; ++s) {
+      if (topk_before(cv, ci, kv[s], ki[s])) {
+        const float tv = kv[s];
+        const int ti = ki[s];
+        kv[s] = cv;
+        ki[s] = ci;
+        cv = tv;
+        ci = ti;
+      }
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < kTopkMax; ++s) {
+    sv[threadIdx.x * kTopkMax + s] = kv[s];
+    si[threadIdx.x * kTopkMax + s] = ki[s];
+  }
+  int head = 0;
+  __syncthreads();
+  for (int round = 0; round < k; ++round) {
+    float bv = head < kTopkMax ? sv[threadIdx.x * kTopkMax + head] : -FLT_MAX;
+    int bi = head < kTopkMax ? si[threadIdx.x * kTopkMax + head] : INT_MAX;
+    int bt = threadIdx.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const int ot = __shfl_xor_sync(0xffffffffu, bt, o);
+      if (topk_before(ov, oi, bv, bi) || (ov == bv && oi == bi && ot < bt)) {
+        bv = ov;
+        bi = oi;
+        bt = ot;
+      }
+    }
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+      wv[w] = bv;
+      wi[w] = bi;
+      wt[w] = bt;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float fv = wv[0];
+      int fi = wi[0], ft = wt[0];
+      for (int q = 1; q < 8; ++q)
+        if (topk_before(wv[q], wi[q], fv, fi) || (wv[q] == fv && wi[q] == fi && wt[q] < ft)) {
+          fv = wv[q];
+          fi = wi[q];
+          ft = wt[q];
+        }
+      out_vals[(size_t)r * k + round] = fv;
+      out_ids[(size_t)r * k + round] = fi;
+      wt[0] = ft;
+    }
+    __syncthreads();
+    if (threadIdx.x == wt[0]) ++head;
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_topk_merge(const float *vals, const int *ids, int rows, int ncand_per_row,
+                              long long row_stride, long long part_stride, int parts, int k,
+                              int *out_ids, float *out_vals, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  topk_merge_kernel<<<rows, 256, 0, s>>>(vals, ids, ncand_per_row, row_stride, part_stride, parts, k,
+                                         out_ids, out_vals);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- misc
+__global__ void f32_to_bf16_kernel(const float *x, uint16_t *y, long long n) {
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (long long)gridDim.x * blockDim.x)
+    y[e] = f32_to_bits(x[e]);
+}
+
+cudaError_t launch_f32_to_bf16(const float *x, uint16_t *y, long long n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 152 * 16));
+  f32_to_bf16_kernel<<<blocks, 256, 0, s>>>(x, y, n);
+  return cudaGetLastError();
+}
+
+// Two-tap conv apply, in place on x [M, D] (blocks of B rows):
+// x'[t] = (b0 + c0[t][ch/group]) * x[t] + (b1 + c1[t][ch/group]) * x[t-1], x[-1] = 0.
+// corr [M, 2*D/group] holds c0 in columns [0, D/group) and c1 after them.
+// Rows are visited from last to first so x[t-1] is read before it is overwritten.
+__global__ void conv_apply_kernel(float *x, const float *corr, const uint16_t *base, int D, int B,
+                                  int group) {
+  const int i = blockIdx.x;
+  const int ch = blockIdx.y * blockDim.x + threadIdx.x;
+  if (ch >= D) return;
+  const int ng = D / group;
+  const float b0 = bits_to_f32(base[ch]), b1 = bits_to_f32(base[D + ch]);
+  float *xb = x + (size_t)i * B * D;
+  const float *cb = corr + (size_t)i * B * 2 * ng;
+  float prev = xb[(size_t)(B - 1) * D + ch];
+  for (int t = B - 1; t >= 0; --t) {
+    const float cur = prev;
+    prev = t > 0 ? xb[(size_t)(t - 1) * D + ch] : 0.f;
+    const float k0 = b0 + cb[(size_t)t * 2 * ng + ch / group];
+    const float k1 = b1 + cb[(size_t)t * 2 * ng + ng + ch / group];
+    xb[(size_t)t * D + ch] = k0 * cur + k1 * prev;
+  }
+}
+
+cudaError_t launch_conv_apply(float *x, const float *corr, const uint16_t *base, int M, int D,
+                              int B, int group, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  dim3 grid(M / B, (D + 255) / 256);
+  conv_apply_kernel<<<grid, 256, 0, s>>>(x, corr, base, D, B, group);
+  return cudaGetLastError();
+}
+
+// Row r of sequence i = r / per, e = r % per: the anchor (e == 0) or candidate e-1.
+__global__ void gather_select_kernel(const int *block_ids, const int *cand_ids, int B, int k,
+                                     const uint16_t *E, int D, int V, uint16_t *out, int *status) {
+  const int r = blockIdx.x;
+  const int per = 1 + (B - 1) * k;
+  const int i = r / per, e = r % per;
+  int id = e == 0 ? block_ids[(size_t)i * B] : cand_ids[(size_t)i * (B - 1) * k + (e - 1)];
+  if (id < 0 || id >= V) {
+    if (threadIdx.x == 0) flag_status(status, kStatusCheck);
+    id = 0;
+  }
+  const uint4 *src = reinterpret_cast<const uint4 *>(E + (size_t)id * D);
+  uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)r * D);
+  for (int c = threadIdx.x; c < D / 8; c += blockDim.x) dst[c] = src[c];
+}
+
+cudaError_t launch_gather_select(const int *block_ids, const int *cand_ids, int nb, int B, int k,
+                                 const uint16_t *E, int D, int V, uint16_t *out, int *status,
+                                 cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  gather_select_kernel<<<nb * (1 + (B - 1) * k), 128, 0, s>>>(block_ids, cand_ids, B, k, E, D, V, out,
+                                                              status);
+  return cudaGetLastError();
+}
+
+// Selector walk, one CTA per sequence. AB [rows, 2*sel]: A | B projections of the
+// gathered tokens; per sequence the rows are [anchor, then candidate (t, c) for
+// t = 1..B-1, c = 0..k-1]. G [nb*(B-1), sel]: W_G z_t before the sigmoid.
+__global__ void __launch_bounds__(256) select_walk_kernel(const int *cand_ids,
+                                                          const float *cand_vals, const float *AB,
+                                                          const float *G, const int *block_ids,
+                                                          int B, int k, int sel, int *path) {
+  __shared__ float score[kTopkMax];
+  __shared__ int s_arow;
+  const int i = blockIdx.x;
+  const int per = 1 + (B - 1) * k;
+  const float *ABi = AB + (size_t)i * per * 2 * sel;
+  if (threadIdx.x == 0) s_arow = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = 1; t < B; ++t) {
+    const int arow = s_arow;
+    const float *Ga = G + ((size_t)i * (B - 1) + (t - 1)) * sel;
+    for (int c = warp; c < k; c += 8) {
+      const int brow = 1 + (t - 1) * k + c;
+      float acc = 0.f;
+      for (int d = lane; d < sel; d += 32) {
+        const float gate = 1.0f / (1.0f + expf(-Ga[d]));
+        acc += ABi[(size_t)arow * 2 * sel + d] * gate * ABi[(size_t)brow * 2 * sel + sel + d];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) score[c] = cand_vals[((size_t)i * (B - 1) + (t - 1)) * k + c] + acc;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int *ids = cand_ids + ((size_t)i * (B - 1) + (t - 1)) * k;
+      int best = 0;
+      for (int c = 1; c < k; ++c)
+        if (topk_before(score[c], ids[c], score[best], ids[best])) best = c;
+      path[(size_t)i * (B - 1) + (t - 1)] = ids[best];
+      s_arow = 1 + (t - 1) * k + best;
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, const float *AB,
+                               const float *G, const int *block_ids, int nb, int B, int k,
+                               int sel_dim, int *path, cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  select_walk_kernel<<<nb, 256, 0, s>>>(cand_ids, cand_vals, AB, G, block_ids, B, k, sel_dim, path);
+  return cudaGetLastError();
+}
+
+}  // namespace df

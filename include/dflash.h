@@ -1,0 +1,240 @@
+/*
+ * dflash.h -- C ABI of libdflash: the one-pass block-diffusion draft step
+ * (DFlash drafter with KV injection, DFlow relay, DFlash 2 selector and conv)
+ * on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Sources (page title, section):
+ *   [DFlash]  "DFlash 投机解码：块扩散草稿与 KV 注入" (caijizhuo.github.io)
+ *   [DFlow]   "DFlow 完全拆解" (pinghaoyang.com.cn/aigc/posts/dflow)
+ *   [DFlash2] "DFlash 2：正确 token 已在候选里" (bowenzhou.top/papers/2026/DFlash2)
+ *
+ * Conventions shared by every call
+ *   - Every tensor argument is a DEVICE pointer owned by the caller: weights, KV
+ *     caches, inputs, outputs and the workspace. The library allocates no device
+ *     memory. Weights are borrowed by dflash_set_weights and must outlive the handle.
+ *   - Matrices are row-major. Weight matrices are [out_features, in_features] bf16.
+ *     "bf16" tensors hold IEEE bfloat16 bit patterns; "f32" tensors hold float.
+ *   - Every step call is asynchronous on the given stream and performs no host
+ *     synchronisation; a handle and its workspace serve one stream at a time.
+ *   - Every call returns DFLASH_OK (0) or a negative DFLASH_ERR_* code; on error
+ *     dflash_last_error() returns a thread-local message. Argument errors are
+ *     detected on the host before any launch. Errors found on the device (a bounded
+ *     wait that ran out, a context length beyond the hint or capacity) are recorded
+ *     in a status word inside the workspace and read back by dflash_status().
+ *   - No C++ exception crosses the ABI.
+ *
+ * KV cache layout (both K and V): bf16 [N][max_batch][Hkv][Cmax][hd]; sequence i of
+ * a call uses slot i. K rows hold RoPE-rotated keys.
+ *
+ * Block layout (reading of [DFlash] 符号约定 and 四、推理流程): block i is
+ * [anchor, mask_id x (B-1)] at absolute positions ctx_len[i] .. ctx_len[i]+B-1,
+ * where ctx_len counts the context rows in the cache; offsets 1..B-1 carry the
+ * B-1 draft candidates.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *dflash_stream_t;
+
+enum dflash_status_code {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = -1,       /* null pointer, negative size, bad index */
+  DFLASH_ERR_UNSUPPORTED_SHAPE = -2, /* a shape outside what the kernels support */
+  DFLASH_ERR_CUDA = -3,              /* a CUDA runtime or driver call failed */
+  DFLASH_ERR_TIMEOUT = -4,           /* a bounded device-side wait ran out */
+  DFLASH_ERR_DEVICE_CHECK = -5       /* a device-side bounds check failed */
+};
+
+enum dflash_flags {
+  DFLASH_FLAG_RELAY = 1,  /* DFlow relay rows are accepted by ctx_project / draft_block */
+  DFLASH_FLAG_CONV = 2,   /* DFlash 2 two-tap dynamic conv, 4 per layer */
+  DFLASH_FLAG_SELECT = 4, /* DFlash 2 path selector weights are registered */
+  /* Test hook for the failure path: the GEMM producers issue no loads, so every
+   * wait on them runs out after max_spin polls, DFLASH_ERR_TIMEOUT is recorded and
+   * the kernels return with the context intact. Never set in production. */
+  DFLASH_FLAG_TEST_STALL = 1 << 30
+};
+
+typedef struct dflash_config {
+  int D;        /* drafter hidden size, multiple of 64 */
+  int Dt;       /* target hidden size of each of the L selected layers */
+  int L;        /* number of target layers concatenated into the W_c input */
+  int N;        /* drafter layers, 1..16 */
+  int Hq;       /* query heads */
+  int Hkv;      /* key/value heads; Hq % Hkv == 0; query head h reads kv head h/(Hq/Hkv) */
+  int hd;       /* head dim: 64 or 128 */
+  int F;        /* SwiGLU FFN width, multiple of 8 */
+  int V;        /* vocabulary size */
+  int B;        /* block size: anchor + B-1 masks, 2..16 */
+  int k_top;    /* candidates kept per position by dflash_lm_head_topk, 1..16 */
+  float rope_base; /* RoPE base (theta_d = base^(-2d/hd), rotate-half pairing) */
+  float eps;    /* RMSNorm epsilon */
+  int mask_id;  /* token id of the mask embedding row in E */
+  int Cmax;     /* context capacity per sequence (cache rows) */
+  int max_batch;      /* sequences the cache and workspace are sized for */
+  int max_proj_rows;  /* largest R (rows per sequence) passed to dflash_ctx_project */
+  int conv_group;     /* channels sharing one conv correction (16); used with CONV */
+  int sel_dim;        /* selector embedding width (256); used with SELECT */
+  unsigned flags;     /* DFLASH_FLAG_* */
+  int max_spin;       /* iteration bound of every device-side wait; 0 = default */
+} dflash_config;
+
+typedef struct dflash_layer_weights {
+  const void *W_qkv;  /* bf16 [(Hq+2*Hkv)*hd, D]: rows q heads, then k_b heads, then v_b heads */
+  const void *Wk_c;   /* bf16 [Hkv*hd, D]: context-key projection W_c^K of this layer */
+  const void *Wv_c;   /* bf16 [Hkv*hd, D]: context-value projection W_c^V of this layer */
+  const void *W_o;    /* bf16 [D, Hq*hd] */
+  const void *W_gate; /* bf16 [F, D] */
+  const void *W_up;   /* bf16 [F, D] */
+  const void *W_down; /* bf16 [D, F] */
+  const void *g_attn; /* bf16 [D] RMSNorm gain before attention */
+  const void *g_ffn;  /* bf16 [D] RMSNorm gain before the FFN */
+  const void *conv_W0[4];   /* CONV: bf16 [D/conv_group, D], correction of tap 0 */
+  const void *conv_W1[4];   /* CONV: bf16 [D/conv_group, D], correction of tap 1 */
+  const void *conv_base[4]; /* CONV: bf16 [2, D], base kernel (tap 0, tap 1) */
+} dflash_layer_weights;
+
+typedef struct dflash_weights {
+  const void *W_c;     /* bf16 [D, L*Dt]: fused target-context projection */
+  const void *g_ctx;   /* bf16 [D]: RMSNorm gain after W_c */
+  const void *E;       /* bf16 [V, D]: shared token embedding */
+  const void *W_lm;    /* bf16 [V, D]: shared LM head */
+  const void *g_final; /* bf16 [D]: final RMSNorm gain */
+  const void *W_A;     /* SELECT: bf16 [sel_dim, D] */
+  const void *W_B;     /* SELECT: bf16 [sel_dim, D] */
+  const void *W_G;     /* SELECT: bf16 [sel_dim, D] */
+  const dflash_layer_weights *layers; /* N entries; copied by dflash_set_weights */
+} dflash_weights;
+
+typedef struct dflash_handle_s *dflash_handle_t;
+
+/* ------------------------------------------------------------------ lifecycle */
+
+/* Validate cfg and create a handle bound to the current CUDA device.
+ * Unsupported: hd not in {64,128}, Hq % Hkv != 0, B outside 2..16, k_top outside
+ * 1..16, D or L*Dt or Hq*hd not a multiple of 64, F not a multiple of 8. */
+DFLASH_API int dflash_create(const dflash_config *cfg, dflash_handle_t *out);
+
+/* Destroy a handle. Safe on NULL. Does not touch borrowed weights. */
+DFLASH_API int dflash_destroy(dflash_handle_t h);
+
+/* Register weight pointers (borrowed). Builds the TMA descriptors of every weight
+ * matrix. All pointers must be 16-byte aligned; optional groups (conv, selector)
+ * must be non-NULL when their flag is set. */
+DFLASH_API int dflash_set_weights(dflash_handle_t h, const dflash_weights *w);
+
+/* Bytes of workspace every step call of this handle needs (sized for max_batch,
+ * max_proj_rows and Cmax). The caller allocates it (256-byte aligned). */
+DFLASH_API int dflash_workspace_size(dflash_handle_t h, size_t *bytes);
+
+/* Synchronise `stream`, read and clear the device status word in `ws`.
+ * *code = DFLASH_OK, DFLASH_ERR_TIMEOUT or DFLASH_ERR_DEVICE_CHECK. */
+DFLASH_API int dflash_status(dflash_handle_t h, void *ws, dflash_stream_t stream, int *code);
+
+/* Thread-local message for the last error returned on this thread. */
+DFLASH_API const char *dflash_last_error(void);
+
+/* ------------------------------------------------------------------ step calls */
+
+/* Fused target-context projection and context-KV append, plus the DFlow relay
+ * input ([DFlash] 三、KV 注入 H_c equation and the engineering note that the
+ * projected K/V, not H_c, are cached; [DFlow] 第一步 / 第二步).
+ *   hv        bf16 [nb, R, L*Dt]: verifier hidden states of R consecutive rows per
+ *             sequence, the L selected layers concatenated along features.
+ *   n_commit  int32 [nb]: rows 0..n_commit[i]-1 of sequence i become context rows at
+ *             positions ctx_len[i]+j: h = RMSNorm(W_c hv), K_c = RoPE(Wk_c h),
+ *             V_c = Wv_c h are written into every layer's cache. 0 <= n_commit <= R.
+ *   relay_a   int32 [nb] or NULL (requires DFLASH_FLAG_RELAY when non-NULL): the
+ *             previous round's accepted count a; rows k in [a+2, B-1] (k < R) are
+ *             relayed to block offset j = k - a of the next block.
+ *   ctx_len   int32 [nb], device, updated in place to ctx_len + n_commit.
+ *   kcache, vcache  the caches (layout above); ctx_len + n_commit must stay <= Cmax.
+ *   x0_relay  bf16 [nb, B, D] output or NULL: h_k at the relayed offsets, 0 elsewhere.
+ * Prefill is the same call with R = the prompt length (R <= max_proj_rows). */
+DFLASH_API int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *hv,
+                       const int32_t *n_commit, const int32_t *relay_a, int32_t *ctx_len,
+                       void *kcache, void *vcache, void *x0_relay, void *ws, size_t ws_bytes,
+                       dflash_stream_t stream);
+
+/* One-pass draft of nb blocks through the N drafter layers ([DFlash] 二、块扩散草稿
+ * attention equations and 四、推理流程 draft_forward): x = E[block_ids] (+ x0_relay);
+ * per layer x += Attn(RMSNorm(x)) with Q from the block only, K = [K_c; K_b],
+ * V = [V_c; V_b] and no mask; x += W_down(silu(W_gate u) * W_up u), u = RMSNorm(x);
+ * with CONV a two-tap dynamic conv before and after each sublayer ([DFlash2] 洞察二).
+ *   block_ids    int32 [nb, B] token ids (anchor, then mask ids)
+ *   x0_relay     bf16 [nb, B, D] or NULL: added to the embeddings (DFlow relay)
+ *   ctx_len      int32 [nb]: context rows per sequence (after this round's append)
+ *   max_ctx_hint host int: an upper bound on every ctx_len[i] used to size the
+ *                attention grid (0 = Cmax). A larger ctx_len is reported as
+ *                DFLASH_ERR_DEVICE_CHECK by dflash_status.
+ *   out_hidden   bf16 [nb, B, D]: final RMSNorm output (input of the LM head). */
+DFLASH_API int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, const void *x0_relay,
+                       const void *kcache, const void *vcache, const int32_t *ctx_len,
+                       int max_ctx_hint, void *out_hidden, void *ws, size_t ws_bytes,
+                       dflash_stream_t stream);
+
+/* Shared LM head on offsets 1..B-1 with a fused per-position top-k ([DFlash]
+ * dflash_cycle argmax(...)[1:]; [DFlash2] 洞察一 top-16 candidates).
+ *   hidden     bf16 [nb, B, D] (dflash_draft_block output)
+ *   k          1..k_top
+ *   out_ids    int32 [nb, B-1, k]: ids sorted by logit descending, ties to the lower id
+ *   out_vals   f32   [nb, B-1, k]: their fp32 logits
+ *   out_logits f32   [nb, B-1, V] or NULL: every logit (for parity checks). */
+DFLASH_API int dflash_lm_head_topk(dflash_handle_t h, int nb, const void *hidden, int k, int32_t *out_ids,
+                        float *out_vals, float *out_logits, void *ws, size_t ws_bytes,
+                        dflash_stream_t stream);
+
+/* Top-k of each row of an fp32 matrix with the same ordering rule as
+ * dflash_lm_head_topk (value descending, ties to the lower column).
+ *   logits f32 [rows, cols]; out_ids int32 [rows, k]; out_vals f32 [rows, k]; k 1..16. */
+DFLASH_API int dflash_topk(dflash_handle_t h, int rows, int cols, const float *logits, int k,
+                int32_t *out_ids, float *out_vals, void *ws, size_t ws_bytes,
+                dflash_stream_t stream);
+
+/* Greedy exact-match accept ([DFlash] 符号约定: 1 <= tau <= B; dflash_cycle step ④;
+ * [DFlow] 问题不在拒绝).
+ *   draft   int32 [nb, B-1]: candidates c_1..c_{B-1}
+ *   target  int32 [nb, B]: verifier greedy tokens; T[j] verifies c_{j+1}
+ *   out_tau int32 [nb]: n + 1 with n the number of leading matches
+ *   out_bonus int32 [nb]: T[n] */
+DFLASH_API int dflash_accept(dflash_handle_t h, int nb, const int32_t *draft, const int32_t *target,
+                  int32_t *out_tau, int32_t *out_bonus, dflash_stream_t stream);
+
+/* DFlash 2 two-tap dynamic depthwise conv ([DFlash2] 洞察二), in place:
+ * x'_t = k_{t,0} * x_t + k_{t,1} * x_{t-1}, k_{t,j} = base_j + expand(W_j x_t),
+ * one correction per conv_group channels, x_{-1} = 0 at block offset 0.
+ *   layer 0..N-1, which 0..3 (before attention, after attention, before FFN, after FFN)
+ *   x  f32 [nb*B, D]: residual stream rows, blocks of B consecutive rows. */
+DFLASH_API int dflash2_conv(dflash_handle_t h, int layer, int which, int nb, float *x, void *ws,
+                 size_t ws_bytes, dflash_stream_t stream);
+
+/* DFlash 2 path selector, greedy walk ([DFlash2] 洞察一):
+ * S_t(a,b) = U_t(b) + <A(a) * G(z_t), B(b)>, A = W_A E[a], B = W_B E[b],
+ * G = sigmoid(W_G z_t); a_0 = anchor, a_t = argmax over the candidates of offset t
+ * (ties to the lower id).
+ *   topk_ids int32 [nb, B-1, k], topk_vals f32 [nb, B-1, k] (dflash_lm_head_topk output)
+ *   hidden bf16 [nb, B, D]; block_ids int32 [nb, B] (column 0 is the anchor)
+ *   out_path int32 [nb, B-1]: the selected draft. */
+DFLASH_API int dflash2_select(dflash_handle_t h, int nb, int k, const int32_t *topk_ids,
+                   const float *topk_vals, const void *hidden, const int32_t *block_ids,
+                   int32_t *out_path, void *ws, size_t ws_bytes, dflash_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H */

@@ -296,7 +296,7 @@ def accept(draft: np.ndarray, target: np.ndarray):
 
 
 def select_path(cfg, W: dict, cand_ids: np.ndarray, cand_vals: np.ndarray,
-                hidden: np.ndarray, anchor: np.ndarray) -> np.ndarray:
+                hidden: np.ndarray, anchor: np.ndarray, return_margins: bool = False):
     """DFlash 2 path selector, greedy walk ([DFlash2] 洞察一).
 
     cand_ids/cand_vals: [nb, B-1, k] top-k candidates and their logits U_t(b) for
@@ -304,23 +304,29 @@ def select_path(cfg, W: dict, cand_ids: np.ndarray, cand_vals: np.ndarray,
     S_t(a, b) = U_t(b) + sum_d A(a)_d G_t,d B(b)_d with A(a) = W_A E[a],
     B(b) = W_B E[b], G_t = sigmoid(W_G z_t). Walk: a_0 = anchor,
     a_t = argmax_b S_t(a_{t-1}, b) over the candidates of offset t, ties to the lower id.
+    With ``return_margins`` also returns, per step, the best score minus the runner-up.
     """
     nb, bm1, k = cand_ids.shape
     path = np.zeros((nb, bm1), dtype=np.int32)
+    margins = np.full((nb, bm1), np.inf)
     for i in range(nb):
         a = int(anchor[i])
         for t in range(1, bm1 + 1):
             G = sigmoid(W["W_G"] @ hidden[i, t])
             Aa = W["W_A"] @ W["E"][a]
             best_b, best_s = None, None
+            scores = []
             for c in range(k):
                 b = int(cand_ids[i, t - 1, c])
                 s = cand_vals[i, t - 1, c] + np.sum(Aa * G * (W["W_B"] @ W["E"][b]))
+                scores.append(s)
                 if best_s is None or s > best_s or (s == best_s and b < best_b):
                     best_b, best_s = b, s
             path[i, t - 1] = best_b
+            if k > 1:
+                margins[i, t - 1] = best_s - sorted(scores)[-2]
             a = best_b
-    return path
+    return (path, margins) if return_margins else path
 
 
 def draft_step(cfg, W: dict, hv, n_commit, ctx_len, cache: KVCache, block_ids, target,

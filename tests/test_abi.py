@@ -1,0 +1,40 @@
+"""The C-ABI library builds, loads, and exports every symbol include/dflash.h declares
+(no compute calls: these run without a GPU)."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared():
+    src = open(os.path.join(ROOT, "include", "dflash.h")).read()
+    return sorted(set(re.findall(r"DFLASH_API\s+[\w\s\*]*?\b(dflash\w*)\s*\(", src)))
+
+
+def test_header_declares_the_step_calls():
+    names = declared()
+    for n in ("dflash_ctx_project", "dflash_draft_block", "dflash_lm_head_topk", "dflash_accept",
+              "dflash2_conv", "dflash2_select", "dflash_create", "dflash_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    from block_diffusion_speculative_project_gb300 import build
+    path = build.build()
+    lib = ctypes.CDLL(path)
+    for n in declared():
+        assert hasattr(lib, n), f"{n} declared in dflash.h but not exported"
+
+
+def test_binding_wraps_every_symbol_and_validates_without_gpu():
+    from block_diffusion_speculative_project_gb300 import dflash
+    assert set(dflash.EXPORTED) == set(declared())
+    cfg = dflash.dflash_config(D=256, Dt=256, L=5, N=2, Hq=4, Hkv=4, hd=96, F=688, V=4096, B=8,
+                               k_top=16, rope_base=1e4, eps=1e-6, mask_id=4095, Cmax=80,
+                               max_batch=1, max_proj_rows=64, conv_group=16, sel_dim=256)
+    try:
+        dflash.dflash_create(cfg)
+        raise AssertionError("hd=96 must be rejected")
+    except dflash.DflashError as e:
+        assert e.code == dflash.DFLASH_ERR_UNSUPPORTED_SHAPE

@@ -1,0 +1,346 @@
+"""GPU parity of every step call against the CPU oracle, on seeded synthetic inputs.
+
+Each test calls libdflash through its C ABI (ctypes binding) and the oracle on the
+same bf16 values. Sizes span several GEMM tiles, ragged tails (F, V and L*Dt not
+multiples of the tile), ragged and empty contexts, and the small tiny workload.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dflash_inputs as di
+from _parity import assert_close, check_topk
+from oracle import dflash_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+MEDIUM = di.Workload("medium_d512_hd128_gqa4", D=512, Dt=192, L=5, N=2, Hq=8, Hkv=2, hd=128,
+                     F=1000, V=5003, B=16, nb=3, C=300)
+MEDIUM_B8 = MEDIUM.with_(name="medium_b8", B=8, nb=5)
+MEDIUM_ALL = MEDIUM.with_(name="medium_relay_conv_select",
+                          flags=di.FLAG_RELAY | di.FLAG_CONV | di.FLAG_SELECT)
+
+
+def lib():
+    from block_diffusion_speculative_project_gb300 import dflash, drafter
+    return dflash, drafter
+
+
+def make(w, Cmax, max_proj_rows, seed=0, max_batch=None, max_spin=0, flags_extra=0, bits=None):
+    _, drafter = lib()
+    bits = di.make_weights(w, seed) if bits is None else bits
+    dev = {k: drafter.to_device_bf16(v) for k, v in bits.items()}
+    shape = w.with_(flags=w.flags | flags_extra) if flags_extra else w
+    dr = drafter.Drafter(shape, dev, max_batch or w.nb, Cmax, max_proj_rows, max_spin=max_spin)
+    return dr, orc.widen_all(bits), bits
+
+
+def i32(a):
+    return torch.tensor(np.asarray(a, dtype=np.int32), device="cuda")
+
+
+def bf16(bits):
+    _, drafter = lib()
+    return drafter.to_device_bf16(bits)
+
+
+def f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def random_cache(w, nb, Cmax, seed=0):
+    shp = (w.N, nb, w.Hkv, Cmax, w.hd)
+    return di.normal_bf16("kcache", shp, 1.0, seed=seed), di.normal_bf16("vcache", shp, 1.0, seed=seed)
+
+
+def oracle_cache(w, kb, vb, Cmax):
+    c = orc.KVCache(w.N, kb.shape[1], w.Hkv, Cmax, w.hd)
+    K, V = orc.widen(kb), orc.widen(vb)
+    for n in range(w.N):
+        for i in range(kb.shape[1]):
+            c.K[n][i][:] = K[n, i]
+            c.V[n][i][:] = V[n, i]
+    return c
+
+
+# ----------------------------------------------------------------------------- accept / top-k
+
+def test_accept_matches_oracle_exactly():
+    import json, os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "accept_cases.json")))
+    dr, _, _ = make(di.TINY, 80, 8)
+    B = g["B"]
+    d = np.array([c["draft"] for c in g["cases"]], np.int32)
+    t = np.array([c["target"] for c in g["cases"]], np.int32)
+    rng = np.random.default_rng(1)
+    d = np.vstack([d, rng.integers(0, 3, (300, B - 1))]).astype(np.int32)
+    t = np.vstack([t, rng.integers(0, 3, (300, B))]).astype(np.int32)
+    tau, bonus = torch.empty(len(d), dtype=torch.int32, device="cuda"), torch.empty(len(d), dtype=torch.int32, device="cuda")
+    dr.accept(len(d), i32(d), i32(t), tau, bonus)
+    ot, ob = orc.accept(d, t)
+    assert np.array_equal(tau.cpu().numpy(), ot)
+    assert np.array_equal(bonus.cpu().numpy(), ob)
+    for c, tt, bb in zip(g["cases"], tau.cpu().numpy(), bonus.cpu().numpy()):
+        assert (tt, bb) == (c["tau"], c["bonus"])
+
+
+@pytest.mark.parametrize("rows,cols,k", [(7, 5000, 16), (1, 151936, 16), (3, 17, 16), (5, 300, 1)])
+def test_topk_exact_with_ties(rows, cols, k):
+    dr, _, _ = make(di.TINY, 80, 8)
+    rng = np.random.default_rng(cols)
+    logits = rng.integers(-3, 4, (rows, cols)).astype(np.float32)  # dense exact ties
+    ids = torch.empty(rows, k, dtype=torch.int32, device="cuda")
+    vals = torch.empty(rows, k, dtype=torch.float32, device="cuda")
+    dr.topk(rows, cols, torch.tensor(logits, device="cuda"), k, ids, vals)
+    oi, ov = orc.topk(logits.astype(np.float64), k)
+    assert np.array_equal(ids.cpu().numpy(), oi)
+    assert np.array_equal(vals.cpu().numpy(), ov.astype(np.float32))
+
+
+# ----------------------------------------------------------------------------- LM head
+
+@pytest.mark.parametrize("w", [di.TINY, MEDIUM, MEDIUM_B8], ids=lambda w: w.name)
+def test_lm_head_topk_stage(w):
+    bits = di.make_weights(w)
+    # duplicate LM-head rows: exact logit ties that must resolve to the lower id
+    bits["W_lm"][w.V - 2] = bits["W_lm"][5]
+    bits["W_lm"][w.V - 3] = bits["W_lm"][5]
+    dr, W, _ = make(w, 64, w.B, bits=bits)
+    hid_bits = di.normal_bf16("hidden", (w.nb, w.B, w.D), 1.0)
+    hid = bf16(hid_bits)
+    k = w.k_top
+    ids = torch.empty(w.nb, w.B - 1, k, dtype=torch.int32, device="cuda")
+    vals = torch.empty(w.nb, w.B - 1, k, dtype=torch.float32, device="cuda")
+    logits = torch.empty(w.nb, w.B - 1, w.V, dtype=torch.float32, device="cuda")
+    dr.lm_head_topk(w.nb, hid, k, ids, vals, logits)
+    ol = orc.lm_logits(W, orc.widen(hid_bits))
+    err = assert_close(logits.cpu().numpy(), ol, "logits")
+    assert err < 1e-3, f"fp32-accumulated logits drift {err}"
+    check_topk(ids.cpu().numpy(), vals.cpu().numpy(), ol, k, "lm_head top-k")
+    gi = ids.cpu().numpy().reshape(-1, k)
+    gl = logits.cpu().numpy().reshape(-1, w.V)
+    for r in range(gi.shape[0]):
+        assert np.array_equal(gl[r, 5], gl[r, w.V - 2]), "duplicate rows must tie exactly"
+        row = gi[r].tolist()
+        for dup in (w.V - 2, w.V - 3):
+            if dup in row:
+                assert 5 in row and row.index(5) < row.index(dup)
+
+
+# ----------------------------------------------------------------------------- ctx_project
+
+@pytest.mark.parametrize("w", [di.TINY, MEDIUM, MEDIUM_ALL], ids=lambda w: w.name)
+def test_ctx_project_stage(w):
+    Cmax, R = 96, w.B
+    dr, W, _ = make(w, Cmax, R)
+    rng = np.random.default_rng(2)
+    nb = w.nb
+    hv_bits = di.verifier_rows(w, R, name="hv_stage")
+    n_commit = rng.integers(0, R + 1, nb).astype(np.int32)
+    n_commit[0] = R
+    if nb > 1:
+        n_commit[1] = 0
+    c0 = rng.integers(0, Cmax - R, nb).astype(np.int32)
+    relay = (w.flags & di.FLAG_RELAY) != 0
+    a = rng.integers(0, w.B, nb).astype(np.int32) if relay else None
+    ctx = i32(c0)
+    x0 = torch.full((nb, w.B, w.D), float("nan"), dtype=torch.bfloat16, device="cuda") if relay else None
+    dr.ctx_project(nb, R, bf16(hv_bits), i32(n_commit), ctx, relay_a=None if a is None else i32(a),
+                   x0_relay=x0)
+    assert dr.status() == 0
+    cache = orc.KVCache(w.N, nb, w.Hkv, Cmax, w.hd)
+    new_len, x0r = orc.ctx_project(w, W, orc.widen(hv_bits), n_commit, c0, cache, relay_a=a)
+    assert np.array_equal(ctx.cpu().numpy(), new_len)
+    K, V = f64(dr.kcache), f64(dr.vcache)
+    for n in range(w.N):
+        for i in range(nb):
+            lo, hi = c0[i], c0[i] + n_commit[i]
+            assert_close(K[n, i][:, lo:hi], cache.K[n][i][:, lo:hi], f"K_c layer {n} seq {i}")
+            assert_close(V[n, i][:, lo:hi], cache.V[n][i][:, lo:hi], f"V_c layer {n} seq {i}")
+            assert not K[n, i][:, :lo].any() and not K[n, i][:, hi:].any(), "rows outside the append"
+    if relay:
+        g = f64(x0)
+        assert_close(g, x0r, "x0_relay")
+        assert np.array_equal(g == 0, x0r == 0), "relay placement"
+
+
+# ----------------------------------------------------------------------------- draft_block
+
+@pytest.mark.parametrize("w", [di.TINY, MEDIUM, MEDIUM_B8, MEDIUM_ALL], ids=lambda w: w.name)
+def test_draft_block_stage(w):
+    Cmax = 320
+    dr, W, _ = make(w, Cmax, w.B)
+    kb, vb = random_cache(w, w.nb, Cmax)
+    dr.kcache.copy_(bf16(kb))
+    dr.vcache.copy_(bf16(vb))
+    lens = np.array([Cmax, 0, 65, 300, 64, 1, 63][: w.nb], dtype=np.int32)
+    ids = di.block_ids(w, di.anchors(w))
+    x0_bits = None
+    if w.flags & di.FLAG_RELAY:
+        x0_bits = di.normal_bf16("x0_relay", (w.nb, w.B, w.D), 1.0)
+    out = torch.empty(w.nb, w.B, w.D, dtype=torch.bfloat16, device="cuda")
+    dr.draft_block(w.nb, i32(ids), i32(lens), out, x0_relay=None if x0_bits is None else bf16(x0_bits),
+                   max_ctx_hint=Cmax)
+    assert dr.status() == 0
+    oc = oracle_cache(w, kb, vb, Cmax)
+    want = orc.draft_block(w, W, ids, lens, oc, None if x0_bits is None else orc.widen(x0_bits))
+    assert_close(f64(out), want, f"hidden {w.name}")
+
+
+def test_draft_block_batch_independent_bitwise():
+    w = MEDIUM
+    Cmax = 320
+    dr, W, _ = make(w, Cmax, w.B)
+    kb, vb = random_cache(w, w.nb, Cmax)
+    dr.kcache.copy_(bf16(kb))
+    dr.vcache.copy_(bf16(vb))
+    ids = di.block_ids(w, di.anchors(w))
+    lens = np.array([200, 17, 300], np.int32)
+    out1 = torch.empty(w.nb, w.B, w.D, dtype=torch.bfloat16, device="cuda")
+    dr.draft_block(w.nb, i32(ids), i32(lens), out1, max_ctx_hint=Cmax)
+    ids2 = ids.copy()
+    ids2[1:, 0] = (ids2[1:, 0] + 7) % (w.V - 1)
+    dr.kcache[:, 1:].normal_()
+    out2 = torch.empty_like(out1)
+    dr.draft_block(w.nb, i32(ids2), i32(np.array([200, 40, 90], np.int32)), out2, max_ctx_hint=Cmax)
+    assert torch.equal(out1[0], out2[0])
+
+
+# ----------------------------------------------------------------------------- conv / select
+
+def test_conv_stage():
+    w = MEDIUM_ALL
+    dr, W, _ = make(w, 64, w.B)
+    M = w.nb * w.B
+    x0 = np.random.default_rng(3).standard_normal((M, w.D)).astype(np.float32)
+    x = torch.tensor(x0, device="cuda")
+    dr.conv(1, 2, w.nb, x)
+    assert dr.status() == 0
+    p = "layer1.conv2."
+    xf = x0.astype(np.float64).reshape(w.nb, w.B, w.D)
+    got = x.cpu().numpy().reshape(w.nb, w.B, w.D)
+    for i in range(w.nb):
+        want = orc.dyn_conv(xf[i], W[p + "W0"], W[p + "W1"], W[p + "base"], w.conv_group)
+        assert_close(got[i], want, f"conv seq {i}")
+
+
+def test_select_stage():
+    w = MEDIUM_ALL
+    dr, W, _ = make(w, 64, w.B)
+    rng = np.random.default_rng(4)
+    k = w.k_top
+    cand = np.stack([rng.permutation(w.V)[:k] for _ in range(w.nb * (w.B - 1))]).reshape(w.nb, w.B - 1, k)
+    vals = rng.standard_normal((w.nb, w.B - 1, k)).astype(np.float32)
+    hid_bits = di.normal_bf16("sel_hidden", (w.nb, w.B, w.D), 1.0)
+    ids = di.block_ids(w, di.anchors(w))
+    path = torch.empty(w.nb, w.B - 1, dtype=torch.int32, device="cuda")
+    dr.select(w.nb, k, i32(cand), torch.tensor(vals, device="cuda"), bf16(hid_bits), i32(ids), path)
+    assert dr.status() == 0
+    want, margin = orc.select_path(w, W, cand, vals.astype(np.float64), orc.widen(hid_bits),
+                                   ids[:, 0], return_margins=True)
+    got = path.cpu().numpy()
+    decided = 0
+    for i in range(w.nb):
+        for t in range(w.B - 1):
+            if margin[i, t] <= 1e-2 * max(1.0, abs(vals[i, t]).max()):
+                assert got[i, t] in cand[i, t]
+                break
+            assert got[i, t] == want[i, t], f"seq {i} offset {t + 1}"
+            decided += 1
+    assert decided > 0
+
+
+# ----------------------------------------------------------------------------- whole step
+
+@pytest.mark.parametrize("w", [di.TINY, MEDIUM_ALL], ids=lambda w: w.name)
+def test_full_step(w):
+    """Prefill through ctx_project, then one draft step (append, draft, LM head, accept)."""
+    Cmax, C = 96, 70
+    dr, W, _ = make(w, Cmax, C)
+    nb = w.nb
+    hv_pre = di.verifier_rows(w, C, name="hv_prefill")
+    tp = np.minimum(di.tau_prev(w), w.B).astype(np.int32)
+    ctx = i32(np.zeros(nb, np.int32))
+    dr.ctx_project(nb, C, bf16(hv_pre), i32(C - tp), ctx)
+    cache = orc.KVCache(w.N, nb, w.Hkv, Cmax, w.hd)
+    lens, _ = orc.ctx_project(w, W, orc.widen(hv_pre), C - tp, np.zeros(nb), cache)
+    relay = (w.flags & di.FLAG_RELAY) != 0
+    hv = di.verifier_rows(w, w.B, name="hv_step")
+    a = (tp - 1).astype(np.int32)
+    x0 = torch.empty(nb, w.B, w.D, dtype=torch.bfloat16, device="cuda") if relay else None
+    dr.ctx_project(nb, w.B, bf16(hv), i32(tp), ctx, relay_a=i32(a) if relay else None, x0_relay=x0)
+    ids = di.block_ids(w, di.anchors(w))
+    out = torch.empty(nb, w.B, w.D, dtype=torch.bfloat16, device="cuda")
+    dr.draft_block(nb, i32(ids), ctx, out, x0_relay=x0, max_ctx_hint=C)
+    k = w.k_top
+    tid = torch.empty(nb, w.B - 1, k, dtype=torch.int32, device="cuda")
+    tv = torch.empty(nb, w.B - 1, k, dtype=torch.float32, device="cuda")
+    tl = torch.empty(nb, w.B - 1, w.V, dtype=torch.float32, device="cuda")
+    dr.lm_head_topk(nb, out, k, tid, tv, tl)
+    assert dr.status() == 0
+    o = orc.draft_step(w, W, orc.widen(hv), tp, lens, cache, ids, np.zeros((nb, w.B), np.int32),
+                       relay_a=a if relay else None)
+    assert np.array_equal(ctx.cpu().numpy(), o["ctx_len"])
+    assert int(o["ctx_len"].max()) <= C
+    if relay:
+        assert_close(f64(x0), o["x0_relay"], "x0_relay")
+    assert_close(f64(out), o["hidden"], "hidden")
+    assert_close(tl.cpu().numpy(), o["logits"], "logits")
+    und = check_topk(tid.cpu().numpy(), tv.cpu().numpy(), o["logits"], k, "top-k")
+    draft = tid[..., 0].contiguous()
+    if w.flags & di.FLAG_SELECT:
+        path = torch.empty(nb, w.B - 1, dtype=torch.int32, device="cuda")
+        dr.select(nb, k, tid, tv, out, i32(ids), path)
+        draft = path
+    target = di.target_row_from_draft(draft.cpu().numpy(), w.V)
+    tau = torch.empty(nb, dtype=torch.int32, device="cuda")
+    bonus = torch.empty(nb, dtype=torch.int32, device="cuda")
+    dr.accept(nb, draft, i32(target), tau, bonus)
+    ot, ob = orc.accept(draft.cpu().numpy(), target)
+    assert np.array_equal(tau.cpu().numpy(), ot) and np.array_equal(bonus.cpu().numpy(), ob)
+    assert und <= 0.2 * nb * (w.B - 1) * k
+
+
+# ----------------------------------------------------------------------------- failure paths
+
+def test_argument_errors():
+    dflash, drafter = lib()
+    dr, _, _ = make(di.TINY, 80, 8)
+    with pytest.raises(dflash.DflashError) as e:
+        dr.ctx_project(5, 8, torch.empty(1, device="cuda"), i32([1]), i32([0]))
+    assert e.value.code == dflash.DFLASH_ERR_INVALID_ARG
+    with pytest.raises(dflash.DflashError) as e:
+        dr.lm_head_topk(1, torch.empty(8, 256, dtype=torch.bfloat16, device="cuda"), 17,
+                        i32([0]), i32([0]))
+    assert e.value.code == dflash.DFLASH_ERR_INVALID_ARG
+    bad = dflash.dflash_config.from_buffer_copy(dr.cfg)
+    bad.B = 17
+    with pytest.raises(dflash.DflashError) as e:
+        dflash.dflash_create(bad)
+    assert e.value.code == dflash.DFLASH_ERR_UNSUPPORTED_SHAPE
+
+
+def test_context_beyond_hint_is_reported():
+    dflash, _ = lib()
+    w = di.TINY
+    dr, _, _ = make(w, 80, 8)
+    out = torch.empty(1, w.B, w.D, dtype=torch.bfloat16, device="cuda")
+    dr.draft_block(1, i32(di.block_ids(w, [3])), i32([50]), out, max_ctx_hint=40)
+    assert dr.status() == dflash.DFLASH_ERR_DEVICE_CHECK
+    assert dr.status() == dflash.DFLASH_OK  # status clears on read
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A wait that nothing signals runs out, reports TIMEOUT, and the GPU stays usable."""
+    dflash, _ = lib()
+    w = di.TINY
+    dr, W, bits = make(w, 80, 8, max_spin=2000, flags_extra=dflash.FLAG_TEST_STALL)
+    out = torch.empty(1, w.B, w.D, dtype=torch.bfloat16, device="cuda")
+    dr.draft_block(1, i32(di.block_ids(w, [3])), i32([0]), out, max_ctx_hint=16)
+    assert dr.status() == dflash.DFLASH_ERR_TIMEOUT
+    del dr
+    dr2, W, _ = make(w, 80, 8, bits=bits)
+    dr2.draft_block(1, i32(di.block_ids(w, [3])), i32([0]), out, max_ctx_hint=16)
+    assert dr2.status() == dflash.DFLASH_OK
+    want = orc.draft_block(w, W, di.block_ids(w, [3]), [0], orc.KVCache(w.N, 1, w.Hkv, 80, w.hd))
+    assert_close(f64(out), want, "hidden after a timed-out call")
