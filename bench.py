@@ -1,0 +1,467 @@
+"""Benchmark of the one-pass block-diffusion draft step on GB300.
+
+One step = rewind ctx_len, dflash_ctx_project (append the previous round's committed
+verifier rows; relay rows with the relay workload), dflash_draft_block,
+dflash_lm_head_topk (+ dflash2_select with the DFlash 2 workload), dflash_accept,
+over one batch of seeded synthetic inputs already resident in HBM. The step is
+captured in a CUDA graph and replayed; K timed replays are bracketed by a barrier and
+a device synchronize, timed with CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+N > 1 (torchrun, one process per GPU) runs N independent replicas (the step shards
+by sequence with no exchange); value = sequences of all ranks / the slowest rank's
+time. --impl reference times the CPU oracle (the only reference this method has) on
+the host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dflash_inputs as di  # noqa: E402
+
+DEFAULT_WORKLOAD = di.QWEN3_8B.name
+METRIC = "draft blocks/sec (Qwen3-8B-shaped, B=16)"
+PROJ_CHUNK = 512
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def step_bytes_flops(w: di.Workload, ctx: np.ndarray, tp: np.ndarray):
+    """Algorithmic bytes and FLOPs of one step (each weight read once, each context
+    K/V row read once per layer, inputs and outputs once)."""
+    qkv_n = (w.Hq + 2 * w.Hkv) * w.hd
+    per_layer_w = (qkv_n * w.D + w.D * w.Hq * w.hd + 3 * w.F * w.D + 2 * w.Hkv * w.hd * w.D)
+    if w.flags & di.FLAG_CONV:
+        per_layer_w += 4 * (2 * (w.D // w.conv_group) * w.D + 2 * w.D)
+    wbytes = 2 * (w.N * per_layer_w + w.D * w.L * w.Dt + w.V * w.D + 2 * w.D * w.N + 2 * w.D)
+    if w.flags & di.FLAG_SELECT:
+        wbytes += 2 * 3 * w.sel_dim * w.D
+    kv_bytes = int(ctx.sum()) * w.N * 2 * w.Hkv * w.hd * 2
+    M = w.nb * w.B
+    rows_proj = w.nb * w.B
+    io = rows_proj * w.L * w.Dt * 2 + w.nb * w.B * w.D * 2 + int(tp.sum()) * w.N * 2 * w.Hkv * w.hd * 2
+    flops = 2 * rows_proj * w.D * w.L * w.Dt + 2 * rows_proj * w.N * 2 * w.Hkv * w.hd * w.D
+    flops += 2 * M * w.N * (qkv_n * w.D + w.D * w.Hq * w.hd + 3 * w.F * w.D)
+    flops += 2 * 2 * w.N * (w.Hq * w.B) * w.hd * int((ctx + w.B).sum())
+    flops += 2 * w.nb * (w.B - 1) * w.V * w.D
+    return wbytes + kv_bytes + io, flops, wbytes, kv_bytes
+
+
+def kernels_per_step(w: di.Workload) -> int:
+    """Launches of libdflash kernels in one step (see dflash_api.cu)."""
+    n = 4                                 # ctx_project: W_c GEMM, RMSNorm, K/V GEMM, relay/len
+    conv = bool(w.flags & di.FLAG_CONV)
+    n += 1                                # embedding (+ first RMSNorm)
+    per_layer = 7 + (1 if False else 0)   # QKV, attn split, attn merge, O, RMSNorm, gate|up, down
+    n += w.N * per_layer + (w.N - 1)      # RMSNorm before attention for layers 1..N-1
+    if conv:
+        n += 1                            # layer 0 attention RMSNorm is separate when CONV
+        n += w.N * 4 * 3                  # each conv: cast, GEMM, apply
+    n += 1                                # final RMSNorm
+    n += 2                                # LM head GEMM + merge
+    if w.flags & di.FLAG_SELECT:
+        n += 4                            # gather, A|B GEMM, G GEMM, walk
+    n += 1                                # accept
+    return n
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        sm = [r[0] for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[2][k].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def traffic_from_profile(kernel_src: str):
+    """dram bytes per launch of the LM-head GEMM from the committed ncu summary, or
+    None when the kernel source changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "lm_head_topk_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = dict(line.split("=", 1) for line in open(p).read().split() if "=" in line)
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    if kv.get("gemm_source_sha") != sha:
+        return None
+    try:
+        return float(kv["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world):
+    import torch
+    from block_diffusion_speculative_project_gb300.drafter import Drafter, to_device_bf16
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = di.WORKLOADS[args.workload]
+    seed = 0  # every replica runs the same workload
+    ctx = di.context_lengths(w, seed).astype(np.int32)
+    tp = di.tau_prev(w, seed).astype(np.int32)
+    relay = bool(w.flags & di.FLAG_RELAY)
+    if relay:
+        a = di.accepted_prev(w, seed).astype(np.int32)
+        tp = (a + 1).astype(np.int32)
+    base = (ctx - tp).astype(np.int32)
+    Cmax = int(ctx.max()) + w.B
+    t0 = time.time()
+    bits = di.make_weights(w, seed)
+    weights = {k: to_device_bf16(v, dev) for k, v in bits.items()}
+    t_gen = time.time() - t0
+    dr = Drafter(w, weights, w.nb, Cmax, max(PROJ_CHUNK, w.B))
+    i32 = lambda x: torch.tensor(np.asarray(x, np.int32), device=dev)
+
+    # prefill C_i - tau_prev_i context rows per sequence (outside every timed region)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    ctx_len = i32(np.zeros(w.nb))
+    done = np.zeros(w.nb, np.int64)
+    while (done < base).any():
+        R = PROJ_CHUNK
+        ncommit = np.minimum(R, base - done).astype(np.int32)
+        hv = torch.randn(w.nb, R, w.L * w.Dt, device=dev, generator=g).to(torch.bfloat16)
+        dr.ctx_project(w.nb, R, hv, i32(ncommit), ctx_len)
+        done += ncommit
+    del hv
+    ctx_base = ctx_len.clone()
+    assert np.array_equal(ctx_base.cpu().numpy(), base)
+
+    # step inputs, resident in HBM
+    hv_step = to_device_bf16(di.verifier_rows(w, w.B, seed, name="hv_step"), dev)
+    n_commit = i32(tp)
+    relay_a = i32(a) if relay else None
+    x0 = torch.empty(w.nb, w.B, w.D, dtype=torch.bfloat16, device=dev) if relay else None
+    block = i32(di.block_ids(w, di.anchors(w, seed)))
+    hidden = torch.empty(w.nb, w.B, w.D, dtype=torch.bfloat16, device=dev)
+    k = w.k_top
+    tid = torch.empty(w.nb, w.B - 1, k, dtype=torch.int32, device=dev)
+    tv = torch.empty(w.nb, w.B - 1, k, dtype=torch.float32, device=dev)
+    path = torch.empty(w.nb, w.B - 1, dtype=torch.int32, device=dev)
+    target = i32(np.zeros((w.nb, w.B)))
+    tau = i32(np.zeros(w.nb))
+    bonus = i32(np.zeros(w.nb))
+    select = bool(w.flags & di.FLAG_SELECT)
+    draft = path if select else tid[..., 0]
+    draft_c = torch.empty(w.nb, w.B - 1, dtype=torch.int32, device=dev)
+    max_ctx = int(ctx.max())
+    stream = torch.cuda.Stream(device=dev)
+    try:  # event-record nodes inside the captured step (torch >= 2.7)
+        ev_lm = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+        lm_in_graph = True
+    except TypeError:
+        ev_lm = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        lm_in_graph = False
+
+    def step(s, lm_events=None):
+        ctx_len.copy_(ctx_base)
+        dr.ctx_project(w.nb, w.B, hv_step, n_commit, ctx_len, relay_a=relay_a, x0_relay=x0, stream=s)
+        dr.draft_block(w.nb, block, ctx_len, hidden, x0_relay=x0, max_ctx_hint=max_ctx, stream=s)
+        if lm_events:
+            lm_events[0].record(s)
+        dr.lm_head_topk(w.nb, hidden, k, tid, tv, stream=s)
+        if lm_events:
+            lm_events[1].record(s)
+        if select:
+            dr.select(w.nb, k, tid, tv, hidden, block, path, stream=s)
+        draft_c.copy_(draft)
+        dr.accept(w.nb, draft_c, target, tau, bonus, stream=s)
+
+    with torch.cuda.stream(stream):
+        step(stream)
+    stream.synchronize()
+    if dr.status(stream) != 0:
+        raise RuntimeError("device status reports an error after the first step")
+    target.copy_(i32(di.target_row_from_draft(draft_c.cpu().numpy(), w.V, seed)))
+
+    # capture one step in a CUDA graph (warm-up launches above configured every kernel)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        step(stream)  # one more eager step before capture
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            step(stream)
+    lm_graph = None
+    if lm_in_graph:
+        lm_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(lm_graph, stream=stream):
+                step(stream, ev_lm)
+
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            graph.replay()
+    stream.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # timed region
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index)
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    ms_total = e0.elapsed_time(e1)
+
+    # dominant kernel (LM head GEMM + top-k): events on its stream inside the replayed
+    # graph, averaged over replays of the same step
+    lm_ms = []
+    for _ in range(max(5, min(50, args.steps // 10))):
+        with torch.cuda.stream(stream):
+            if lm_graph is not None:
+                lm_graph.replay()
+            else:
+                step(stream, ev_lm)
+        stream.synchronize()
+        lm_ms.append(ev_lm[0].elapsed_time(ev_lm[1]))
+    if dr.status(stream) != 0:
+        raise RuntimeError("device status reports an error after the timed steps")
+    tau_h = tau.cpu().numpy()
+
+    # e2e through the public API with host buffers: H2D of the step's inputs from pinned
+    # memory and D2H of its results, every step, inside the timed region
+    host_hv = hv_step.cpu().pin_memory()
+    host_in = torch.cat([n_commit, block.flatten(), target.flatten()]).cpu().pin_memory()
+    dev_in = torch.empty_like(host_in, device=dev)
+    host_out = torch.empty(w.nb * (2 + (w.B - 1) * k), dtype=torch.int32).pin_memory()
+    e2e_steps = max(10, min(args.steps, 200))
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_e2e = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            hv_step.copy_(host_hv, non_blocking=True)
+            dev_in.copy_(host_in, non_blocking=True)
+            graph.replay()
+            out = torch.cat([tau, bonus, tid.flatten()])
+            host_out.copy_(out, non_blocking=True)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t_e2e
+    barrier()
+    h2d = host_hv.numel() * 2 + host_in.numel() * 4
+    d2h = host_out.numel() * 4
+
+    # max over ranks
+    ms_step = ms_total / args.steps
+    vals = np.array([ms_step, e2e_s], dtype=np.float64)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor(vals, device=dev if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        vals = t.cpu().numpy()
+    ms_step, e2e_s = float(vals[0]), float(vals[1])
+
+    if rank != 0:
+        return None
+    hbm, tf_burst, tf_sus, src = load_peaks()
+    total_bytes, flops, wbytes, kvbytes = step_bytes_flops(w, ctx, tp)
+    lm_bytes = 2 * w.V * w.D + 2 * w.nb * (w.B - 1) * w.D + 8 * w.nb * (w.B - 1) * k
+    lm_avg = float(np.mean(lm_ms))
+    achieved = lm_bytes / (lm_avg * 1e-3) / 1e9
+    traffic = traffic_from_profile(os.path.join(ROOT, "block_diffusion_speculative_project_gb300",
+                                                "csrc", "gemm_tc.cu"))
+    blocks = w.nb * world
+    value = blocks / (ms_step * 1e-3)
+    step_t_roof = max(total_bytes / (hbm * 1e9), flops / (tf_sus * 1e12 if tf_sus else tf_burst * 1e12))
+    line = {
+        "metric": METRIC if args.workload == DEFAULT_WORKLOAD else f"draft blocks/sec ({args.workload})",
+        "value": round(value, 2),
+        "unit": "blocks/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded: weights N(0,0.02), verifier states N(0,1))",
+        "config": {"workload": w.name, "nb_per_gpu": w.nb, "B": w.B, "context": int(ctx.mean()),
+                   "context_range": [int(ctx.min()), int(ctx.max())], "parallelism": f"replicas{world}",
+                   "l2": f"inputs larger than L2 ({total_bytes / 1e9:.2f} GB read per step)",
+                   "cuda_graph": True},
+        "draft_tokens_per_s": round(value * (w.B - 1), 1),
+        "step_roofline": {"bytes": total_bytes, "flops": flops, "t_roofline_ms": round(step_t_roof * 1e3, 4),
+                          "frac": round(step_t_roof * 1e3 / ms_step, 4),
+                          "hbm_frac_at_8TBps": round(total_bytes / 8e12 * 1e3 / ms_step, 4)},
+        "roofline": {"kernel": "gemm_tc_kernel<256,EPI_TOPK> (LM head + fused top-k) + top-k merge",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
+                     "avg_launch_ms": round(lm_avg, 4), "bytes_per_launch": lm_bytes},
+        "e2e": {"value": round(blocks * e2e_steps / e2e_s, 2), "unit": "blocks/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": kernels_per_step(w) * args.steps,
+        "clocks": clk,
+        "tau_mean": round(float(tau_h.mean()), 3),
+        "setup_s": {"weights": round(t_gen, 1)},
+    }
+    if not args.no_cpu_baseline and rank == 0:
+        line["cpu_baseline"] = cpu_baseline(w, bits, args.cpu_seconds)
+    return line
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+
+def cpu_baseline(w: di.Workload, bits=None, budget_s: float = 15.0):
+    """The oracle, as it stands, in float32 on this host's cores over a bounded sample:
+    whole draft steps of single sequences of the workload (context filled with seeded
+    values, the step's own append, draft, LM head, top-k and accept)."""
+    from oracle import dflash_oracle as orc
+    cores = len(os.sched_getaffinity(0))
+    if bits is None:
+        bits = di.make_weights(w)
+    W = orc.widen_all(bits, np.float32)
+    ctx = di.context_lengths(w).astype(np.int64)
+    tp = di.tau_prev(w).astype(np.int64)
+    a = None
+    if w.flags & di.FLAG_RELAY:
+        a = di.accepted_prev(w).astype(np.int64)
+        tp = a + 1
+    ids = di.block_ids(w, di.anchors(w))
+    rng = np.random.default_rng(7)
+    done, t_used = 0, 0.0
+    while t_used < budget_s and done < w.nb:
+        i = done
+        Cmax = int(ctx[i]) + w.B
+        cache = orc.KVCache(w.N, 1, w.Hkv, Cmax, w.hd, np.float32)
+        base = int(ctx[i] - tp[i])
+        for n in range(w.N):
+            cache.K[n][0][:, :base] = rng.standard_normal((w.Hkv, base, w.hd), dtype=np.float32)
+            cache.V[n][0][:, :base] = rng.standard_normal((w.Hkv, base, w.hd), dtype=np.float32)
+        hv = orc.widen(di.verifier_rows(w.with_(nb=1), w.B, name=f"hv_cpu{i}"), np.float32)
+        t0 = time.perf_counter()
+        orc.draft_step(w, W, hv, tp[i:i + 1], [base], cache, ids[i:i + 1],
+                       np.zeros((1, w.B), np.int32), relay_a=None if a is None else a[i:i + 1])
+        t_used += time.perf_counter() - t0
+        done += 1
+    per_seq = t_used / done
+    return {"value": round(1.0 / per_seq, 4), "unit": "blocks/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} whole-step sequence(s) of {w.name} (fp32 numpy oracle), {t_used:.1f} s",
+            "seconds_per_block": round(per_seq, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = di.WORKLOADS[args.workload]
+    t0 = time.time()
+    bits = di.make_weights(w)
+    gen = time.time() - t0
+    budget = max(5.0, min(60.0, args.cpu_seconds))
+    per_step = []
+    for _ in range(args.warmup + args.steps):
+        per_step.append(cpu_baseline(w, bits, budget / max(1, args.steps + args.warmup)))
+    timed = per_step[args.warmup:]
+    spb = float(np.mean([t["seconds_per_block"] for t in timed]))
+    value = 1.0 / spb
+    cb = dict(timed[-1])
+    cb["value"] = round(value, 4)
+    return {"impl": "reference", "metric": METRIC if args.workload == DEFAULT_WORKLOAD else
+            f"draft blocks/sec ({args.workload})", "value": round(value, 4), "unit": "blocks/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(spb * w.nb * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "nb_per_gpu": w.nb, "B": w.B},
+            "cpu_baseline": cb, "e2e": {"value": round(value, 4), "unit": "blocks/s",
+                                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "setup_s": {"weights": round(gen, 1)}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(di.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group(backend)
+    line = run_reference(args, rank, world) if args.impl == "reference" else run_gpu(args, rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

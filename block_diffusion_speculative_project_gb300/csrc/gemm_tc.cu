@@ -77,8 +77,14 @@ __device__ __forceinline__ Item item_at(const GemmParams &p, int j) {
 
 // ------------------------------------------------------------------ epilogue helpers
 
+// Vector stores need 16-byte alignment; rows of odd width (e.g. the logits of a
+// vocabulary that is not a multiple of 4) fall back to scalar stores.
+__device__ __forceinline__ bool aligned16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+}
+
 __device__ __forceinline__ void store_bf16_32(uint16_t *dst, const float (&v)[32], int nvalid) {
-  if (nvalid >= 32) {
+  if (nvalid >= 32 && aligned16(dst)) {
     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -90,7 +96,7 @@ __device__ __forceinline__ void store_bf16_32(uint16_t *dst, const float (&v)[32
       d4[q] = w;
     }
   } else {
-    for (int i = 0; i < nvalid; ++i) {
+    for (int i = 0; i < min(nvalid, 32); ++i) {
       __nv_bfloat16 b = __float2bfloat16_rn(v[i]);
       dst[i] = *reinterpret_cast<uint16_t *>(&b);
     }
@@ -98,17 +104,17 @@ __device__ __forceinline__ void store_bf16_32(uint16_t *dst, const float (&v)[32
 }
 
 __device__ __forceinline__ void store_f32_32(float *dst, const float (&v)[32], int nvalid) {
-  if (nvalid >= 32) {
+  if (nvalid >= 32 && aligned16(dst)) {
     float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
     for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
   } else {
-    for (int i = 0; i < nvalid; ++i) dst[i] = v[i];
+    for (int i = 0; i < min(nvalid, 32); ++i) dst[i] = v[i];
   }
 }
 
 __device__ __forceinline__ void add_f32_32(float *dst, const float (&v)[32], int nvalid) {
-  if (nvalid >= 32) {
+  if (nvalid >= 32 && aligned16(dst)) {
     float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -120,7 +126,7 @@ __device__ __forceinline__ void add_f32_32(float *dst, const float (&v)[32], int
       d4[q] = x;
     }
   } else {
-    for (int i = 0; i < nvalid; ++i) dst[i] += v[i];
+    for (int i = 0; i < min(nvalid, 32); ++i) dst[i] += v[i];
   }
 }
 

@@ -14,6 +14,10 @@ Value recipe (the pages give no trained weights; these stand in for them):
   * weights                  ~ N(0, 0.02)
   * RMSNorm gains            ~ 1 + N(0, 0.02)
   * conv base kernel (2, D)  ~ (1, 0) + N(0, 0.02)
+  * conv correction W_j      ~ N(0, (0.02 / sqrt(D))^2): the correction is small next
+                               to the base kernel, as the DFlash 2 page describes it; at
+                               N(0, 0.02) the two-tap conv is quadratic in x and the
+                               residual stream diverges within two layers
   * verifier hidden states   ~ N(0, 1)
   * anchors                  ~ U{0 .. V-2};  mask id = V-1
 """
@@ -193,6 +197,8 @@ def make_weight(name: str, shape, seed: int = 0) -> np.ndarray:
     base = name.rsplit(".", 1)[-1]
     if base.startswith("g_"):
         return normal_bf16(name, shape, 0.02, mean=1.0, seed=seed)
+    if ".conv" in name and base in ("W0", "W1"):
+        return normal_bf16(name, shape, 0.02 / float(np.sqrt(shape[1])), seed=seed)
     if base == "base":
         x = _fill_normal(name, int(np.prod(shape)), seed).reshape(shape) * np.float32(0.02)
         x[0] += np.float32(1.0)
