@@ -258,12 +258,14 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(dev.index)
     time.sleep(0.3)
+    torch.cuda.nvtx.range_push("timed")
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(args.steps):
             graph.replay()
         e1.record(stream)
     stream.synchronize()
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     barrier()
     clk = clocks.stop()

@@ -77,6 +77,8 @@ template <int HD>
 __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const AttnParams p) {
   using C = AttnCfg<HD>;
   extern __shared__ __align__(128) uint8_t smem[];
+  griddep_wait();
+  griddep_launch();
   const int s = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
   const int grp = p.Hq / p.Hkv;
   const int nrows = grp * p.B;
@@ -290,30 +292,57 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const AttnPara
 }
 
 // Combine the splits of one (sequence, kv head) in split order and write o (bf16).
+// One warp per query row; each lane owns HD/32 consecutive output elements, so the
+// partial rows are read with vector loads and the split weights are computed once
+// per row.
+constexpr int kMergeWarps = 8;
+
 template <int HD>
-__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
-  const int g = blockIdx.x % p.Hkv, i = blockIdx.x / p.Hkv;
+__global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const AttnParams p) {
+  constexpr int E = HD / 32;
+  griddep_wait();
+  griddep_launch();
+  const int g = blockIdx.y, i = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = p.Hq / p.Hkv;
   const int nrows = grp * p.B;
+  const int t = blockIdx.x * kMergeWarps + warp;
+  if (t >= nrows) return;
   const int ctx_used = max(0, min(p.ctx_len[i], min(p.max_ctx, p.Cmax)));
   const int nsplit = max(1, (ctx_used + p.chunk - 1) / p.chunk);
   const float sl2 = rsqrtf(static_cast<float>(HD)) * 1.4426950408889634f;
-  const size_t pbase = ((size_t)i * p.Hkv + g) * p.splits * nrows;
-  for (int e = threadIdx.x; e < nrows * HD; e += blockDim.x) {
-    const int t = e / HD, d = e % HD;
-    float M = -FLT_MAX;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.part_ml[(pbase + (size_t)s * nrows + t) * 2]);
-    float L = 0.f, acc = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const size_t r = pbase + (size_t)s * nrows + t;
-      const float w = exp2f((p.part_ml[r * 2] - M) * sl2);
-      L += p.part_ml[r * 2 + 1] * w;
-      acc += p.part_o[r * HD + d] * w;
+  const size_t pbase = ((size_t)i * p.Hkv + g) * p.splits * nrows + t;
+  float M = -FLT_MAX;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.part_ml[(pbase + (size_t)s * nrows) * 2]);
+  float L = 0.f, acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const size_t r = pbase + (size_t)s * nrows;
+    const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + r * 2);
+    const float wgt = exp2f((ml.x - M) * sl2);
+    L += ml.y * wgt;
+    const float *src = p.part_o + r * HD + lane * E;
+    if constexpr (E == 4) {
+      const float4 v = *reinterpret_cast<const float4 *>(src);
+      acc[0] += v.x * wgt;
+      acc[1] += v.y * wgt;
+      acc[2] += v.z * wgt;
+      acc[3] += v.w * wgt;
+    } else {
+      const float2 v = *reinterpret_cast<const float2 *>(src);
+      acc[0] += v.x * wgt;
+      acc[1] += v.y * wgt;
     }
-    const int hh = t / p.B, j = t % p.B;
-    __nv_bfloat16 b = __float2bfloat16_rn(acc / L);
-    p.o[((size_t)i * p.B + j) * (p.Hq * HD) + (size_t)(g * grp + hh) * HD + d] =
-        *reinterpret_cast<uint16_t *>(&b);
+  }
+  const float inv = 1.0f / L;
+  const int hh = t / p.B, j = t % p.B;
+  uint16_t *dst = p.o + ((size_t)i * p.B + j) * (p.Hq * HD) + (size_t)(g * grp + hh) * HD + lane * E;
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                 pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   }
 }
 
@@ -333,11 +362,11 @@ static cudaError_t launch_attn_hd(const AttnParams &p, cudaStream_t s) {
     configured = true;
   }
   dim3 grid(p.splits, p.Hkv, p.nb);
-  attn_split_kernel<HD><<<grid, kAttnThreads, C::SMEM, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(attn_split_kernel<HD>, grid, dim3(kAttnThreads), C::SMEM, s, p);
   if (e != cudaSuccess) return e;
-  attn_merge_kernel<HD><<<p.nb * p.Hkv, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  const int nrows = (p.Hq / p.Hkv) * p.B;
+  dim3 mgrid((nrows + kMergeWarps - 1) / kMergeWarps, p.Hkv, p.nb);
+  return launch_pdl(attn_merge_kernel<HD>, mgrid, dim3(kMergeWarps * 32), 0, s, p);
 }
 
 cudaError_t launch_attention(const AttnParams &p, cudaStream_t s) {

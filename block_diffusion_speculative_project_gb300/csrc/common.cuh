@@ -184,6 +184,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ------------------------------------------------------------------ programmatic launch
+
+// Wait until the preceding kernel in the stream has completed and its memory is
+// visible (no-op when the launch was not programmatic).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel in the stream to start launching; it still waits for this
+// grid's completion before it reads what this grid writes.
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ misc
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

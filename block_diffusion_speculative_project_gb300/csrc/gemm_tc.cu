@@ -41,6 +41,15 @@ struct TileCfg {
   static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE + 256;
 };
 
+// Top-k epilogue: a per-thread stash of one 32-value chunk (stride 33 floats, so the
+// 32 threads of a warp hit distinct banks).
+constexpr size_t kTopkStashBytes = 128 * 33 * sizeof(float);
+
+template <int BN, int EPI>
+constexpr size_t gemm_smem_bytes() {
+  return TileCfg<BN>::SMEM + (EPI == EPI_TOPK ? kTopkStashBytes : 0);
+}
+
 struct Item {
   int m, n, g, s;
 };
@@ -96,9 +105,12 @@ __device__ __forceinline__ void store_bf16_32(uint16_t *dst, const float (&v)[32
       d4[q] = w;
     }
   } else {
-    for (int i = 0; i < min(nvalid, 32); ++i) {
-      __nv_bfloat16 b = __float2bfloat16_rn(v[i]);
-      dst[i] = *reinterpret_cast<uint16_t *>(&b);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < nvalid) {
+        __nv_bfloat16 b = __float2bfloat16_rn(v[i]);
+        dst[i] = *reinterpret_cast<uint16_t *>(&b);
+      }
     }
   }
 }
@@ -109,7 +121,9 @@ __device__ __forceinline__ void store_f32_32(float *dst, const float (&v)[32], i
 #pragma unroll
     for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
   } else {
-    for (int i = 0; i < min(nvalid, 32); ++i) dst[i] = v[i];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nvalid) dst[i] = v[i];
   }
 }
 
@@ -126,8 +140,20 @@ __device__ __forceinline__ void add_f32_32(float *dst, const float (&v)[32], int
       d4[q] = x;
     }
   } else {
-    for (int i = 0; i < min(nvalid, 32); ++i) dst[i] += v[i];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nvalid) dst[i] += v[i];
   }
+}
+
+// Rotation angle pos * inv_freq reduced to [-pi, pi] with a two-constant split of
+// 2*pi (Cody and Waite's method): 6.28125 has 8 significant bits, so k * 6.28125 is
+// exact for the k that occur here (|k| < 2^15) and only the small second constant
+// rounds. The reduced angle then goes to the fast sine/cosine intrinsic.
+__device__ __forceinline__ void rope_sincos(float angle, float *sn, float *cs) {
+  const float k = rintf(angle * 0.15915494309189535f);
+  const float r = fmaf(-k, 1.9353071795864769e-3f, fmaf(-k, 6.28125f, angle));
+  __sincosf(r, sn, cs);
 }
 
 __device__ __forceinline__ void rope_pair(const GemmParams &p, int pos, int d0, float (&a)[32],
@@ -136,29 +162,54 @@ __device__ __forceinline__ void rope_pair(const GemmParams &p, int pos, int d0, 
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     float sn, cs;
-    sincosf(fpos * p.inv_freq[d0 + i], &sn, &cs);
+    rope_sincos(fpos * p.inv_freq[d0 + i], &sn, &cs);
     const float x1 = a[i], x2 = b[i];
     a[i] = x1 * cs - x2 * sn;
     b[i] = x2 * cs + x1 * sn;
   }
 }
 
-__device__ __forceinline__ void topk_insert(float (&kv)[kTopkMax], int (&ki)[kTopkMax], float v,
-                                            int id) {
-  if (!topk_before(v, id, kv[kTopkMax - 1], ki[kTopkMax - 1])) return;
-  float cv = v;
-  int ci = id;
+// Per-thread top-k state of the LM-head epilogue: an unsorted set of kTopkMax
+// (value, id) pairs in registers plus the position and value of its worst member,
+// which is the threshold a new value has to beat (value descending, ties to the
+// lower id). Replacing the worst member and rescanning for the new worst costs a
+// fixed, branch-free 2*kTopkMax steps, and the code stays small.
+struct TopkState {
+  float v[kTopkMax];
+  int id[kTopkMax];
+  float worst_v;
+  int worst_id;
+  int worst_slot;
+};
+
+__device__ __forceinline__ void topk_init(TopkState &tk) {
 #pragma unroll
   for (int s = 0; s < kTopkMax; ++s) {
-    if (topk_before(cv, ci, kv[s], ki[s])) {
-      const float tv = kv[s];
-      const int ti = ki[s];
-      kv[s] = cv;
-      ki[s] = ci;
-      cv = tv;
-      ci = ti;
-    }
+    tk.v[s] = -FLT_MAX;
+    tk.id[s] = INT_MAX - s;  // distinct sentinels: the highest id is the worst
   }
+  tk.worst_v = -FLT_MAX;
+  tk.worst_id = INT_MAX;
+  tk.worst_slot = 0;
+}
+
+__device__ __forceinline__ void topk_replace_worst(TopkState &tk, float v, int id) {
+#pragma unroll
+  for (int s = 0; s < kTopkMax; ++s)
+    if (s == tk.worst_slot) {
+      tk.v[s] = v;
+      tk.id[s] = id;
+    }
+  tk.worst_v = tk.v[0];
+  tk.worst_id = tk.id[0];
+  tk.worst_slot = 0;
+#pragma unroll
+  for (int s = 1; s < kTopkMax; ++s)
+    if (topk_before(tk.worst_v, tk.worst_id, tk.v[s], tk.id[s])) {
+      tk.worst_v = tk.v[s];
+      tk.worst_id = tk.id[s];
+      tk.worst_slot = s;
+    }
 }
 
 // Runs the epilogue of one output tile. `fetch(c, v)` returns the 32 fp32 values of
@@ -166,8 +217,8 @@ __device__ __forceinline__ void topk_insert(float (&kv)[kTopkMax], int (&ki)[kTo
 // (tcgen05.ld is warp-collective); only the stores depend on row validity.
 template <int BN, int EPI, class Fetch>
 __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t, int row,
-                                              bool row_ok, Fetch &&fetch, float (&kv)[kTopkMax],
-                                              int (&ki)[kTopkMax]) {
+                                              bool row_ok, Fetch &&fetch, TopkState &tk,
+                                              float *stash) {
   if constexpr (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_RESID) {
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -270,14 +321,23 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
       float v[32];
       fetch(c, v);
       const int col0 = t.n * BN + c * 32;
-      if (row_ok) {
-        if (p.logits_out) {
-          const int nval = min(32, p.N - col0);
-          if (nval > 0) store_f32_32(p.logits_out + (size_t)row * p.N + col0, v, nval);
-        }
+      const int nval = row_ok ? min(32, p.N - col0) : 0;
+      if (p.logits_out && nval > 0) store_f32_32(p.logits_out + (size_t)row * p.N + col0, v, nval);
+      // branch-free filter: which of the 32 values beat the current worst member
+      uint32_t mask = 0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (col0 + i < p.N) topk_insert(kv, ki, v[i], col0 + i);
+      for (int i = 0; i < 32; ++i)
+        mask |= static_cast<uint32_t>(i < nval && topk_before(v[i], col0 + i, tk.worst_v, tk.worst_id)) << i;
+      if (mask) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) stash[i] = v[i];
+#pragma unroll 1
+        while (mask) {
+          const int i = __ffs(mask) - 1;
+          mask &= mask - 1;
+          const float x = stash[i];
+          if (topk_before(x, col0 + i, tk.worst_v, tk.worst_id)) topk_replace_worst(tk, x, col0 + i);
+        }
       }
     }
   }
@@ -300,6 +360,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   uint64_t *mma_done = acc_empty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
   volatile int *s_last = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  float *stash_base = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE + 256);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -326,39 +387,84 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  if (threadIdx.x == 0) griddep_launch();
+
   if (warp == 0) {
     if (lane == 0 && nitems > 0 && !p.stall) {
       // ---------------- TMA producer
       tma_prefetch_desc(&p.tmA);
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
-      int it = 0;
-      bool ok = true;
-      for (int j = 0; j < nitems && ok; ++j) {
-        const Item t = item_at(p, j);
-        const int kt0 = t.s * p.kt_per_split;
-        const int kt1 = min(p.kt_total, kt0 + p.kt_per_split);
-        for (int kt = kt0; kt < kt1; ++kt, ++it) {
-          const int st = it % C::STAGES;
-          const uint32_t ph = (it / C::STAGES) & 1;
-          if (!mbar_wait(&empty[st], ph ^ 1, p.max_spin)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[st], p.stage_tx_bytes);
-          uint8_t *a = sA + st * C::A_BYTES;
-          uint8_t *b = sB + st * C::B_BYTES;
-          if (p.a_grouped)
-            tma_load_3d(a, &p.tmA, &full[st], kt * BK, 0, t.m * p.a_S, pol_a);
-          else
-            tma_load_3d(a, &p.tmA, &full[st], kt * BK, t.m * BM, 0, pol_a);
-          if (p.dual) {
-            tma_load_2d(b, &p.tmB[0], &full[st], kt * BK, t.n * (BN / 2), pol_w);
-            tma_load_2d(b + (BN / 2) * 128, &p.tmB[1], &full[st], kt * BK, t.n * (BN / 2), pol_w);
-          } else {
-            tma_load_2d(b, &p.tmB[t.g], &full[st], kt * BK, t.n * BN, pol_w);
-          }
+      // Iteration cursor over (work item, k-tile) in this CTA's order.
+      struct Cursor {
+        int j, kt, kt1;
+        Item t;
+      };
+      auto begin = [&](Cursor &c) {
+        c.j = 0;
+        c.t = item_at(p, 0);
+        c.kt = c.t.s * p.kt_per_split;
+        c.kt1 = min(p.kt_total, c.kt + p.kt_per_split);
+      };
+      auto advance = [&](Cursor &c) -> bool {
+        if (++c.kt < c.kt1) return true;
+        if (++c.j >= nitems) return false;
+        c.t = item_at(p, c.j);
+        c.kt = c.t.s * p.kt_per_split;
+        c.kt1 = min(p.kt_total, c.kt + p.kt_per_split);
+        return true;
+      };
+      auto load_a = [&](const Cursor &c, int st) {
+        uint8_t *a = sA + st * C::A_BYTES;
+        if (p.a_grouped)
+          tma_load_3d(a, &p.tmA, &full[st], c.kt * BK, 0, c.t.m * p.a_S, pol_a);
+        else
+          tma_load_3d(a, &p.tmA, &full[st], c.kt * BK, c.t.m * BM, 0, pol_a);
+      };
+      auto load_b = [&](const Cursor &c, int st) {
+        uint8_t *b = sB + st * C::B_BYTES;
+        if (p.dual) {
+          tma_load_2d(b, &p.tmB[0], &full[st], c.kt * BK, c.t.n * (BN / 2), pol_w);
+          tma_load_2d(b + (BN / 2) * 128, &p.tmB[1], &full[st], c.kt * BK, c.t.n * (BN / 2), pol_w);
+        } else {
+          tma_load_2d(b, &p.tmB[c.t.g], &full[st], c.kt * BK, c.t.n * BN, pol_w);
         }
+      };
+      // Weights do not depend on earlier kernels: fill every stage's weight tile
+      // before waiting for the producer of the activations.
+      Cursor c;
+      begin(c);
+      int pre = 0;
+      bool more = true;
+      while (more && pre < C::STAGES) {
+        mbar_arrive_expect_tx(&full[pre], p.stage_tx_bytes);
+        load_b(c, pre);
+        ++pre;
+        more = advance(c);
+      }
+      griddep_wait();
+      {
+        Cursor ca;
+        begin(ca);
+        for (int k = 0; k < pre; ++k) {
+          load_a(ca, k);
+          advance(ca);
+        }
+      }
+      int it = pre;
+      bool ok = true;
+      while (more) {
+        const int st = it % C::STAGES;
+        const uint32_t ph = (it / C::STAGES) & 1;
+        if (!mbar_wait(&empty[st], ph ^ 1, p.max_spin)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[st], p.stage_tx_bytes);
+        load_a(c, st);
+        load_b(c, st);
+        ++it;
+        more = advance(c);
       }
       if (!ok) flag_status(p.status, kStatusTimeout);
       // Every issued load must land before the CTA may exit (bounded).
@@ -409,15 +515,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     }
   } else {
     // ---------------- epilogue warps 2..5
+    griddep_wait();
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    float kv[kTopkMax];
-    int ki[kTopkMax];
-#pragma unroll
-    for (int s = 0; s < kTopkMax; ++s) {
-      kv[s] = -FLT_MAX;
-      ki[s] = INT_MAX;
-    }
+    float *stash = stash_base + r * 33;
+    TopkState tk;
+    if constexpr (EPI == EPI_TOPK) topk_init(tk);
     bool ok = true;
     for (int j = 0; j < nitems; ++j) {
       const Item t = item_at(p, j);
@@ -431,7 +534,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
       const int row = t.m * p.tile_rows + r;
       const bool row_ok = (r < p.tile_rows) && (row < p.M);
-      if (p.splits > 1) {
+      if (EPI != EPI_TOPK && p.splits > 1) {
         const int tile = (t.g * p.n_tiles + t.n) * p.m_tiles + t.m;
         float *mine = p.partial + ((size_t)(tile * p.splits + t.s) * BM + r) * BN;
 #pragma unroll 1
@@ -470,12 +573,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
             }
           }
         };
-        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, kv, ki);
+        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, tk, stash);
         named_bar_sync(1, 128);
         if (threadIdx.x == 64) p.counters[tile] = 0;
       } else {
         auto fetch = [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); };
-        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, kv, ki);
+        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, tk, stash);
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
       }
@@ -487,14 +590,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
         const int range = blockIdx.x / p.m_tiles;
         const int row = m * p.tile_rows + r;
         if (r < p.tile_rows && row < p.M) {
+          // order the members (value descending, ties to the lower id) by rank
           float *pv = p.part_vals + ((size_t)range * p.M + row) * p.topk_k;
           int *pi = p.part_ids + ((size_t)range * p.M + row) * p.topk_k;
+#pragma unroll 1
+          for (int a = 0; a < kTopkMax; ++a) {
+            float va = -FLT_MAX;
+            int ia = INT_MAX;
 #pragma unroll
-          for (int s = 0; s < kTopkMax; ++s)
-            if (s < p.topk_k) {
-              pv[s] = kv[s];
-              pi[s] = ki[s];
+            for (int s = 0; s < kTopkMax; ++s)
+              if (s == a) {
+                va = tk.v[s];
+                ia = tk.id[s];
+              }
+            int rank = 0;
+#pragma unroll
+            for (int s = 0; s < kTopkMax; ++s) rank += topk_before(tk.v[s], tk.id[s], va, ia) ? 1 : 0;
+            if (rank < p.topk_k) {
+              pv[rank] = va;
+              pi[rank] = ia;
             }
+          }
         }
       }
     }
@@ -556,16 +672,15 @@ size_t gemm_partial_bytes(int M, int tile_rows, int N, int K, int groups, int du
 
 template <int BN, int EPI>
 static cudaError_t launch_one(const GemmParams &p, int grid, cudaStream_t s) {
-  using C = TileCfg<BN>;
+  constexpr size_t smem = gemm_smem_bytes<BN, EPI>();
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  gemm_tc_kernel<BN, EPI><<<grid, kGemmThreads, C::SMEM, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), smem, s, p);
 }
 
 cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s) {

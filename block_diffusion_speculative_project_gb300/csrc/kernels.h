@@ -7,6 +7,25 @@
 
 namespace df {
 
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel in the stream drains; every libdflash kernel calls
+// griddepcontrol.wait before it touches data produced upstream.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Bits of the device status word (first word of the workspace).
 constexpr int kStatusTimeout = 1;  // a bounded wait ran out
 constexpr int kStatusCheck = 2;    // a bounds check failed (index skipped)

@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float *xin, const in
                                                       float *xout, int D, const uint16_t *g,
                                                       float eps, uint16_t *u, int B, int skip,
                                                       int rows_out_per_seq, int V, int *status) {
+  griddep_wait();
+  griddep_launch();
   __shared__ float red[8];
   const int r = blockIdx.x;
   extern __shared__ float row[];  // D floats
@@ -99,25 +101,28 @@ cudaError_t launch_embed_rmsnorm(const int *ids, const uint16_t *E, const uint16
                                  int D, int V, float *x, const uint16_t *g, float eps, uint16_t *u,
                                  int *status, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  rmsnorm_kernel<1><<<M, 256, D * sizeof(float), s>>>(nullptr, ids, E, relay, x, D, g, eps, u, 1, 0, 0,
-                                                      V, status);
+  cudaError_t e = launch_pdl(rmsnorm_kernel<1>, dim3(M), dim3(256), D * sizeof(float), s, nullptr, ids, E,
+                             relay, x, D, g, eps, u, 1, 0, 0, V, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(const float *x, int M, int D, const uint16_t *g, float eps, uint16_t *u,
                            cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  rmsnorm_kernel<0><<<M, 256, D * sizeof(float), s>>>(x, nullptr, nullptr, nullptr, nullptr, D, g,
-                                                      eps, u, 1, 0, 0, 0, nullptr);
+  cudaError_t e = launch_pdl(rmsnorm_kernel<0>, dim3(M), dim3(256), D * sizeof(float), s, x, nullptr,
+                             nullptr, nullptr, nullptr, D, g, eps, u, 1, 0, 0, 0, nullptr);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm_rows(const float *x, int M, int D, const uint16_t *g, float eps,
                                 uint16_t *u, int B, int skip_first, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  rmsnorm_kernel<0><<<M, 256, D * sizeof(float), s>>>(x, nullptr, nullptr, nullptr, nullptr, D, g,
-                                                      eps, u, B, skip_first, B - skip_first, 0,
-                                                      nullptr);
+  cudaError_t e = launch_pdl(rmsnorm_kernel<0>, dim3(M), dim3(256), D * sizeof(float), s, x, nullptr,
+                             nullptr, nullptr, nullptr, D, g, eps, u, B, skip_first, B - skip_first, 0,
+                             nullptr);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -128,6 +133,8 @@ __global__ void __launch_bounds__(256) relay_len_kernel(const uint16_t *h, int R
                                                         const int *relay_a, const int *n_commit,
                                                         int *ctx_len, uint16_t *x0, int Cmax,
                                                         int *status) {
+  griddep_wait();
+  griddep_launch();
   const int i = blockIdx.x;
   if (x0) {
     const int a = relay_a ? relay_a[i] : INT_MAX / 2;
@@ -150,13 +157,17 @@ cudaError_t launch_relay_and_len(const uint16_t *h, int nb, int R, int B, int D,
                                  const int *relay_a, const int *n_commit, int *ctx_len,
                                  uint16_t *x0_relay, int Cmax, int *status, cudaStream_t s) {
   if (nb <= 0) return cudaSuccess;
-  relay_len_kernel<<<nb, 256, 0, s>>>(h, R, B, D, relay_a, n_commit, ctx_len, x0_relay, Cmax, status);
+  cudaError_t e = launch_pdl(relay_len_kernel, dim3(nb), dim3(256), 0, s, h, R, B, D, relay_a, n_commit,
+                             ctx_len, x0_relay, Cmax, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- accept
 __global__ void accept_kernel(const int *draft, const int *target, int nb, int B, int *tau,
                               int *bonus) {
+  griddep_wait();
+  griddep_launch();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= nb) return;
   const int *d = draft + (size_t)i * (B - 1);
@@ -170,7 +181,9 @@ __global__ void accept_kernel(const int *draft, const int *target, int nb, int B
 cudaError_t launch_accept(const int *draft, const int *target, int nb, int B, int *tau, int *bonus,
                           cudaStream_t s) {
   if (nb <= 0) return cudaSuccess;
-  accept_kernel<<<(nb + 127) / 128, 128, 0, s>>>(draft, target, nb, B, tau, bonus);
+  cudaError_t e = launch_pdl(accept_kernel, dim3((nb + 127) / 128), dim3(128), 0, s, draft, target, nb, B,
+                             tau, bonus);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -183,6 +196,8 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float *vals, cons
                                                          int ncand, long long row_stride,
                                                          long long part_stride, int parts, int k,
                                                          int *out_ids, float *out_vals) {
+  griddep_wait();
+  griddep_launch();
   __shared__ float sv[256 * kTopkMax];
   __shared__ int si[256 * kTopkMax];
   __shared__ float wv[8];
@@ -268,13 +283,16 @@ cudaError_t launch_topk_merge(const float *vals, const int *ids, int rows, int n
                               long long row_stride, long long part_stride, int parts, int k,
                               int *out_ids, float *out_vals, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  topk_merge_kernel<<<rows, 256, 0, s>>>(vals, ids, ncand_per_row, row_stride, part_stride, parts, k,
-                                         out_ids, out_vals);
+  cudaError_t e = launch_pdl(topk_merge_kernel, dim3(rows), dim3(256), 0, s, vals, ids, ncand_per_row,
+                             row_stride, part_stride, parts, k, out_ids, out_vals);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- misc
 __global__ void f32_to_bf16_kernel(const float *x, uint16_t *y, long long n) {
+  griddep_wait();
+  griddep_launch();
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (long long)gridDim.x * blockDim.x)
     y[e] = f32_to_bits(x[e]);
@@ -283,7 +301,8 @@ __global__ void f32_to_bf16_kernel(const float *x, uint16_t *y, long long n) {
 cudaError_t launch_f32_to_bf16(const float *x, uint16_t *y, long long n, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 152 * 16));
-  f32_to_bf16_kernel<<<blocks, 256, 0, s>>>(x, y, n);
+  cudaError_t e = launch_pdl(f32_to_bf16_kernel, dim3(blocks), dim3(256), 0, s, x, y, n);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -293,6 +312,8 @@ cudaError_t launch_f32_to_bf16(const float *x, uint16_t *y, long long n, cudaStr
 // Rows are visited from last to first so x[t-1] is read before it is overwritten.
 __global__ void conv_apply_kernel(float *x, const float *corr, const uint16_t *base, int D, int B,
                                   int group) {
+  griddep_wait();
+  griddep_launch();
   const int i = blockIdx.x;
   const int ch = blockIdx.y * blockDim.x + threadIdx.x;
   if (ch >= D) return;
@@ -314,13 +335,16 @@ cudaError_t launch_conv_apply(float *x, const float *corr, const uint16_t *base,
                               int B, int group, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   dim3 grid(M / B, (D + 255) / 256);
-  conv_apply_kernel<<<grid, 256, 0, s>>>(x, corr, base, D, B, group);
+  cudaError_t e = launch_pdl(conv_apply_kernel, grid, dim3(256), 0, s, x, corr, base, D, B, group);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 // Row r of sequence i = r / per, e = r % per: the anchor (e == 0) or candidate e-1.
 __global__ void gather_select_kernel(const int *block_ids, const int *cand_ids, int B, int k,
                                      const uint16_t *E, int D, int V, uint16_t *out, int *status) {
+  griddep_wait();
+  griddep_launch();
   const int r = blockIdx.x;
   const int per = 1 + (B - 1) * k;
   const int i = r / per, e = r % per;
@@ -338,8 +362,9 @@ cudaError_t launch_gather_select(const int *block_ids, const int *cand_ids, int 
                                  const uint16_t *E, int D, int V, uint16_t *out, int *status,
                                  cudaStream_t s) {
   if (nb <= 0) return cudaSuccess;
-  gather_select_kernel<<<nb * (1 + (B - 1) * k), 128, 0, s>>>(block_ids, cand_ids, B, k, E, D, V, out,
-                                                              status);
+  cudaError_t e = launch_pdl(gather_select_kernel, dim3(nb * (1 + (B - 1) * k)), dim3(128), 0, s,
+                             block_ids, cand_ids, B, k, E, D, V, out, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -350,6 +375,8 @@ __global__ void __launch_bounds__(256) select_walk_kernel(const int *cand_ids,
                                                           const float *cand_vals, const float *AB,
                                                           const float *G, const int *block_ids,
                                                           int B, int k, int sel, int *path) {
+  griddep_wait();
+  griddep_launch();
   __shared__ float score[kTopkMax];
   __shared__ int s_arow;
   const int i = blockIdx.x;
@@ -389,7 +416,9 @@ cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, cons
                                const float *G, const int *block_ids, int nb, int B, int k,
                                int sel_dim, int *path, cudaStream_t s) {
   if (nb <= 0) return cudaSuccess;
-  select_walk_kernel<<<nb, 256, 0, s>>>(cand_ids, cand_vals, AB, G, block_ids, B, k, sel_dim, path);
+  cudaError_t e = launch_pdl(select_walk_kernel, dim3(nb), dim3(256), 0, s, cand_ids, cand_vals, AB, G,
+                             block_ids, B, k, sel_dim, path);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
