@@ -261,16 +261,6 @@ GemmParams base_params(const dflash_handle_s *h, const Ws &w) {
 }
 
 int run_gemm(const dflash_handle_s *h, GemmParams &p, int BN, cudaStream_t s) {
-  const int tile_rows = p.a_grouped ? p.tile_rows : 128;
-  const int tiles = gemm_tiles(p.M, tile_rows, p.N, p.groups, p.dual, BN);
-  if (p.epi != EPI_TOPK) {
-    int splits, kps, items, grid;
-    gemm_plan(p.M, tile_rows, p.N, p.K, p.groups, p.dual, BN, h->num_sms, p.epi, &splits, &kps, &items, &grid);
-    if (splits > 1 && (size_t)tiles * splits * 128 * BN * 4 > h->ws.partial_bytes)
-      return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "split-K scratch exceeds the workspace plan");
-    if ((size_t)tiles * sizeof(int) > h->ws.counters_bytes)
-      return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "tile count exceeds the workspace plan");
-  }
   DF_CUDA(gemm_launch(p, BN, h->num_sms, s));
   return DFLASH_OK;
 }

@@ -11,9 +11,11 @@
 //     frees a slot when the MMAs that read it complete.
 //   * two TMEM accumulators (2*BN columns) let the epilogue of one work item run
 //     under the MMAs of the next; CTAs are persistent over work items.
-//   * split-K: every split writes its fp32 partial tile; the last split to arrive
-//     (atomic counter, no waiting) sums the partials in split order and runs the
-//     epilogue, so results do not depend on arrival order.
+//   * split-K across a thread-block cluster: the S CTAs of a cluster each reduce a
+//     1/S slice of K for the same output tile, stage their fp32 partial in their own
+//     (now idle) pipeline smem, and after a hardware cluster barrier every CTA sums
+//     a 1/S row slice of the tile over all S partials through distributed shared
+//     memory, in rank order (deterministic), and runs the epilogue on it.
 //   * weights are streamed with an L2 evict-first policy, activations evict-last.
 #include <algorithm>
 #include <cfloat>
@@ -30,6 +32,8 @@ constexpr int kGemmThreads = 192;
 // Bound of the teardown waits for this CTA's own TMA copies and MMAs, which finish
 // without help from any other thread; independent of the caller's max_spin.
 constexpr int kDrainSpin = 1 << 22;
+// Row stride (floats) of the partial tile staged for the cluster reduction.
+constexpr int kRedStride = 128 + 4;
 
 template <int BN>
 struct TileCfg {
@@ -55,6 +59,7 @@ struct Item {
 };
 
 __device__ __forceinline__ int item_count(const GemmParams &p) {
+  if (p.csplit > 1) return 1;
   if (p.epi == EPI_TOPK) {
     const int range = blockIdx.x / p.m_tiles;
     const int n0 = range * p.tiles_per_cta;
@@ -74,7 +79,17 @@ __device__ __forceinline__ Item item_at(const GemmParams &p, int j) {
     r.s = 0;
     return r;
   }
-  int it = blockIdx.x + j * gridDim.x;
+  int it;
+  if (p.csplit > 1) {
+    it = blockIdx.x / p.csplit;
+    r.m = it % p.m_tiles;
+    it /= p.m_tiles;
+    r.n = it % p.n_tiles;
+    r.g = it / p.n_tiles;
+    r.s = static_cast<int>(cluster_ctarank());
+    return r;
+  }
+  it = blockIdx.x + j * gridDim.x;
   r.m = it % p.m_tiles;
   it /= p.m_tiles;
   r.n = it % p.n_tiles;
@@ -534,48 +549,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
       const int row = t.m * p.tile_rows + r;
       const bool row_ok = (r < p.tile_rows) && (row < p.M);
-      if (EPI != EPI_TOPK && p.splits > 1) {
-        const int tile = (t.g * p.n_tiles + t.n) * p.m_tiles + t.m;
-        float *mine = p.partial + ((size_t)(tile * p.splits + t.s) * BM + r) * BN;
+      if (EPI != EPI_TOPK && p.csplit > 1) {
+        // Stage this CTA's partial tile, row r at red[r * kRedStride], in the
+        // pipeline smem (every TMA write has landed and every MMA has completed).
+        float *red = reinterpret_cast<float *>(smem) + r * kRedStride;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(taddr + c * 32, v);
-          float4 *d4 = reinterpret_cast<float4 *>(mine + c * 32);
+          float4 *d4 = reinterpret_cast<float4 *>(red + c * 32);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            __stcg(d4 + k, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
+          for (int k = 0; k < 8; ++k) d4[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         }
-        tc_fence_before();
-        mbar_arrive(&acc_empty[buf]);
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (threadIdx.x == 64) {
-          const int old = atomicAdd(&p.counters[tile], 1);
-          *s_last = (old == p.splits - 1) ? 1 : 0;
-        }
-        named_bar_sync(1, 128);
-        if (!*s_last) continue;
-        __threadfence();
-        const float *base = p.partial + ((size_t)tile * p.splits * BM + r) * BN;
-        auto fetch = [&](int c, float (&v)[32]) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
-          for (int s = 0; s < p.splits; ++s) {
-            const float4 *src = reinterpret_cast<const float4 *>(base + (size_t)s * BM * BN + c * 32);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const float4 x = __ldcg(src + k);
-              v[4 * k] += x.x;
-              v[4 * k + 1] += x.y;
-              v[4 * k + 2] += x.z;
-              v[4 * k + 3] += x.w;
-            }
-          }
-        };
-        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, tk, stash);
-        named_bar_sync(1, 128);
-        if (threadIdx.x == 64) p.counters[tile] = 0;
       } else {
         auto fetch = [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); };
         epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, tk, stash);
@@ -616,6 +601,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     }
   }
 
+  if (EPI != EPI_TOPK && p.csplit > 1) {
+    // Every partial of the cluster is staged; sum this CTA's row slice over the
+    // cluster in rank order and run the epilogue on it.
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= 2 && nitems > 0) {
+      const int q = warp & 3;
+      const int r = q * 32 + lane;
+      const int per = BM / p.csplit;
+      if (r / per == static_cast<int>(cluster_ctarank())) {
+        const Item t = item_at(p, 0);
+        const int row = t.m * p.tile_rows + r;
+        const bool row_ok = (r < p.tile_rows) && (row < p.M);
+        const uint32_t mine = smem_u32(smem) + static_cast<uint32_t>(r * kRedStride) * 4u;
+        auto fetch = [&](int c, float (&v)[32]) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+#pragma unroll 1
+          for (int src = 0; src < p.csplit; ++src) {
+            const uint32_t a = cluster_map(mine + c * 128u, static_cast<uint32_t>(src));
+            float4 x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = ld_cluster_f4(a + 16u * k);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              v[4 * k] += x[k].x;
+              v[4 * k + 1] += x[k].y;
+              v[4 * k + 2] += x[k].z;
+              v[4 * k + 3] += x[k].w;
+            }
+          }
+        };
+        TopkState tk;
+        float *stash = nullptr;
+        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, tk, stash);
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();  // peers may still be reading this CTA's partial
+  }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -633,45 +659,30 @@ int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN) {
   return m_tiles * n_tiles * groups;
 }
 
+// Chooses the cluster split S: the largest power of two <= 8 such that all
+// tiles * S CTAs run in one wave and every split keeps >= 8 k-tiles. Multi-wave
+// cluster launches measured slower than one persistent unsplit wave, so larger
+// tile counts stay unsplit.
 void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN, int num_sms,
-               int epi, int *splits_out, int *kps_out, int *items_out, int *grid_out) {
-  const int base = gemm_tiles(M, tile_rows, N, groups, dual, BN);
+               int epi, int *splits_out, int *kps_out, int *items_out, int *grid_out, int *csplit_out) {
+  const int tiles = gemm_tiles(M, tile_rows, N, groups, dual, BN);
   const int kt = (K + BK - 1) / BK;
-  int best_kps = kt, best_splits = 1;
-  if (epi != EPI_TOPK) {
-    double best_score = -1e30;
-    for (int kps = kt; kps >= 1; --kps) {
-      const int splits = (kt + kps - 1) / kps;
-      if (kps < 4 && splits > 1) break;
-      if (splits > 32) break;
-      const long long items = (long long)base * splits;
-      const long long waves = (items + num_sms - 1) / num_sms;
-      const double eff = double(items) / double(waves * num_sms);
-      const double score = eff - 0.01 * splits;
-      if (score > best_score + 1e-9) {
-        best_score = score;
-        best_kps = kps;
-        best_splits = splits;
-      }
-    }
-  }
-  *splits_out = best_splits;
-  *kps_out = best_kps;
-  *items_out = base * best_splits;
-  *grid_out = std::max(1, std::min(base * best_splits, num_sms));
+  int best_s = 1;
+  if (epi != EPI_TOPK)
+    for (int S = 2; S <= 8; S *= 2)
+      if ((long long)tiles * S <= num_sms && kt >= 8 * S) best_s = S;
+  *splits_out = 1;
+  *csplit_out = best_s;
+  *kps_out = (kt + best_s - 1) / best_s;
+  *items_out = best_s > 1 ? tiles * best_s : tiles;
+  *grid_out = best_s > 1 ? tiles * best_s : std::max(1, std::min(tiles, num_sms));
 }
 
-size_t gemm_partial_bytes(int M, int tile_rows, int N, int K, int groups, int dual, int BN,
-                          int num_sms, int epi) {
-  int splits, kps, items, grid;
-  gemm_plan(M, tile_rows, N, K, groups, dual, BN, num_sms, epi, &splits, &kps, &items, &grid);
-  if (splits <= 1) return 0;
-  const int tiles = gemm_tiles(M, tile_rows, N, groups, dual, BN);
-  return (size_t)tiles * splits * BM * BN * sizeof(float);
-}
+size_t gemm_partial_bytes(int, int, int, int, int, int, int, int, int) { return 0; }
 
 template <int BN, int EPI>
 static cudaError_t launch_one(const GemmParams &p, int grid, cudaStream_t s) {
+  // (cluster launches are chosen by p.csplit)
   constexpr size_t smem = gemm_smem_bytes<BN, EPI>();
   static bool configured = false;
   if (!configured) {
@@ -680,6 +691,9 @@ static cudaError_t launch_one(const GemmParams &p, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  if (p.csplit > 1)
+    return launch_pdl_cluster(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), smem, s, p.csplit,
+                              p);
   return launch_pdl(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), smem, s, p);
 }
 
@@ -690,6 +704,7 @@ cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s) {
   p.n_tiles = (p.N + ncols - 1) / ncols;
   p.kt_total = (p.K + BK - 1) / BK;
   int grid;
+  p.csplit = 1;
   if (p.epi == EPI_TOPK) {
     p.splits = 1;
     p.kt_per_split = p.kt_total;
@@ -700,7 +715,7 @@ cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s) {
     p.items = grid;
   } else {
     gemm_plan(p.M, p.tile_rows, p.N, p.K, p.groups, p.dual, BN, num_sms, p.epi, &p.splits,
-              &p.kt_per_split, &p.items, &grid);
+              &p.kt_per_split, &p.items, &grid, &p.csplit);
   }
   // expect-tx bytes of one stage: the A box plus the B box(es)
   const uint32_t a_rows = p.a_grouped ? (uint32_t)p.tile_rows : (uint32_t)BM;

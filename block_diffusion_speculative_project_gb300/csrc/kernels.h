@@ -26,6 +26,27 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Programmatic launch of a kernel in thread-block clusters of `cluster` CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t s, int cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Bits of the device status word (first word of the workspace).
 constexpr int kStatusTimeout = 1;  // a bounded wait ran out
 constexpr int kStatusCheck = 2;    // a bounds check failed (index skipped)
@@ -91,6 +112,7 @@ struct GemmParams {
   int *status;
   int max_spin;
   int stall;         // test hook: issue no loads so the waits run out
+  int csplit;        // >1: split K across the CTAs of a cluster, reduce through DSMEM
 };
 
 struct GemmLaunch {
@@ -104,7 +126,7 @@ struct GemmLaunch {
 cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s);
 // Bytes of split-K partials and counters the launch with these shapes needs.
 void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN, int num_sms,
-               int epi, int *splits, int *kt_per_split, int *items, int *grid);
+               int epi, int *splits, int *kt_per_split, int *items, int *grid, int *csplit);
 size_t gemm_partial_bytes(int M, int tile_rows, int N, int K, int groups, int dual, int BN,
                           int num_sms, int epi);
 int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN);
