@@ -302,6 +302,37 @@ int run_conv(const dflash_handle_s *h, const Ws &w, int layer, int which, int M,
   return DFLASH_OK;
 }
 
+// ---------------------------------------------------------------- allocation-free LM head
+//
+// Scratch of dflash_lm_head_topk_noalloc: the per-range partial top-k lists (and a
+// fallback status word) live in this file-scope device array instead of a
+// caller-provided workspace. Every GPU that loads the library holds it until the
+// process exits. Host code may not use the symbol as a device address: its device
+// address is looked up once per device with cudaGetSymbolAddress.
+constexpr size_t kNoallocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+uint8_t *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up on the
+// first call for that device, with the device current).
+int noalloc_scratch(int device, uint8_t **out) {
+  if (device < 0 || device >= kMaxDevices) return fail(DFLASH_ERR_CUDA, "device index %d out of range", device);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[device]) {
+    void *ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr)
+      return fail(DFLASH_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed: %s",
+                  cudaGetErrorString(e));
+    g_noalloc_ptr[device] = static_cast<uint8_t *>(ptr);
+  }
+  *out = g_noalloc_ptr[device];
+  return DFLASH_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -646,6 +677,68 @@ int dflash_lm_head_topk(dflash_handle_t h, int nb, const void *hidden, int k, in
   DF_TRY(run_gemm(h, p, kBNTopk, s));
   const int ranges = p.items / p.m_tiles;
   if (ranges > h->num_sms) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "top-k ranges exceed the plan");
+  DF_CUDA(launch_topk_merge(p.part_vals, p.part_ids, Ml, k, k, (long long)Ml * k, ranges, k, out_ids,
+                            out_vals, s));
+  return DFLASH_OK;
+}
+
+int dflash_lm_head_topk_noalloc(dflash_handle_t h, int nb, const void *hidden, int k, int32_t *out_ids,
+                                float *out_vals, int32_t *out_status, dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  const auto &c = h->cfg;
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (k < 1 || k > c.k_top) return fail(DFLASH_ERR_INVALID_ARG, "k=%d outside [1, k_top]", k);
+  if (nb == 0) return DFLASH_OK;
+  if (!hidden || !out_ids || !out_vals) return fail(DFLASH_ERR_INVALID_ARG, "hidden and outputs must be non-NULL");
+  int dev = 0;
+  DF_CUDA(cudaGetDevice(&dev));
+  uint8_t *scratch = nullptr;
+  DF_TRY(noalloc_scratch(dev, &scratch));
+  const int R = c.B - 1;
+  const int S = 128 / R;
+  const int Ml = nb * R;
+  // Same work split as the LM-head launch: vocabulary ranges x row tiles.
+  const int m_tiles = (Ml + S * R - 1) / (S * R);
+  const int n_tiles = (c.V + kBNTopk - 1) / kBNTopk;
+  const int ranges0 = std::max(1, h->num_sms / m_tiles);
+  const int tpc = (n_tiles + ranges0 - 1) / ranges0;
+  const int ranges = (n_tiles + tpc - 1) / tpc;
+  const size_t list_bytes = (size_t)ranges * Ml * k * sizeof(float);
+  const size_t need = 256 + 2 * list_bytes;
+  if (need > kNoallocScratchBytes)
+    return fail(DFLASH_ERR_UNSUPPORTED_SHAPE,
+                "dflash_lm_head_topk_noalloc needs %zu bytes of scratch (%d ranges x %d rows x k=%d); "
+                "its static scratch holds %zu bytes",
+                need, ranges, Ml, k, kNoallocScratchBytes);
+  cudaStream_t s = stream;
+  int *status = reinterpret_cast<int *>(scratch);
+  if (out_status) {
+    status = out_status;
+  } else {
+    DF_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s));  // the array keeps the last call's word
+  }
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.groups = 1;
+  p.status = status;
+  p.max_spin = c.max_spin;
+  p.stall = (c.flags & DFLASH_FLAG_TEST_STALL) ? 1 : 0;
+  p.hd = c.hd;
+  DF_TRY(encode_3d(&p.tmA, static_cast<const uint16_t *>(hidden) + c.D, c.D, R, nb, c.D,
+                   (uint64_t)c.B * c.D, R, S));
+  p.tmB[0] = h->tm_lm;
+  p.a_grouped = 1;
+  p.a_S = S;
+  p.tile_rows = S * R;
+  p.M = Ml;
+  p.N = c.V;
+  p.K = c.D;
+  p.epi = EPI_TOPK;
+  p.topk_k = k;
+  p.part_vals = reinterpret_cast<float *>(scratch + 256);
+  p.part_ids = reinterpret_cast<int *>(scratch + 256 + list_bytes);
+  DF_CUDA(gemm_launch(p, kBNTopk, h->num_sms, s));
+  if (p.items / p.m_tiles != ranges) return fail(DFLASH_ERR_CUDA, "LM-head range plan mismatch");
   DF_CUDA(launch_topk_merge(p.part_vals, p.part_ids, Ml, k, k, (long long)Ml * k, ranges, k, out_ids,
                             out_vals, s));
   return DFLASH_OK;

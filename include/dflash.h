@@ -198,6 +198,28 @@ DFLASH_API int dflash_lm_head_topk(dflash_handle_t h, int nb, const void *hidden
                         float *out_vals, float *out_logits, void *ws, size_t ws_bytes,
                         dflash_stream_t stream);
 
+/* Allocation-free variant of dflash_lm_head_topk, for callers that cannot hand the
+ * library a workspace: code running inside a CUDA-graph capture (a cudaMalloc there
+ * is not allowed), hosts whose device memory is entirely owned by another pool
+ * allocator, and latency-critical threads that must not risk the implicit device
+ * synchronisation an allocation can cause. The pages describe no such call; it
+ * exists only for these callers.
+ *   Same inputs and outputs as dflash_lm_head_topk, minus out_logits and the
+ *   workspace. Scratch (the per-range partial top-k lists) lives in a 4 MiB
+ *   file-scope device array that every GPU loading the library holds until exit;
+ *   any shape whose lists need more is rejected with DFLASH_ERR_UNSUPPORTED_SHAPE.
+ *   out_status: int32 device word or NULL. When given, device-side errors are
+ *   OR-ed into it (value 1: a bounded wait ran out; value 2: a bounds check
+ *   failed); the caller clears it. When NULL they are not reported.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before
+ *   any stream capture. The call allocates nothing. All calls share the one array,
+ *   so calls that overlap on the GPU (different streams, or different handles on
+ *   the same device, not ordered by the caller) race and must not be issued. */
+DFLASH_API int dflash_lm_head_topk_noalloc(dflash_handle_t h, int nb, const void *hidden, int k,
+                                           int32_t *out_ids, float *out_vals, int32_t *out_status,
+                                           dflash_stream_t stream);
+
 /* Top-k of each row of an fp32 matrix with the same ordering rule as
  * dflash_lm_head_topk (value descending, ties to the lower column).
  *   logits f32 [rows, cols]; out_ids int32 [rows, k]; out_vals f32 [rows, k]; k 1..16. */
