@@ -141,6 +141,20 @@ def traffic_from_profile(kernel_src: str):
         return None
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of a list of floats over all ranks (identity when not distributed).
+    The only cross-rank communication in the benchmark: the draft step itself shards by
+    sequence and exchanges nothing."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    dev = device if (device is not None and dist.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu().tolist()]
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args, rank, world):
@@ -310,14 +324,7 @@ def run_gpu(args, rank, world):
     d2h = host_out.numel() * 4
 
     # max over ranks
-    ms_step = ms_total / args.steps
-    vals = np.array([ms_step, e2e_s], dtype=np.float64)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor(vals, device=dev if dist.get_backend() == "nccl" else "cpu")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        vals = t.cpu().numpy()
-    ms_step, e2e_s = float(vals[0]), float(vals[1])
+    ms_step, e2e_s = max_over_ranks([ms_total / args.steps, e2e_s], dev)
 
     if rank != 0:
         return None
