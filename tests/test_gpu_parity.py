@@ -116,7 +116,8 @@ def test_lm_head_topk_stage(w):
     ol = orc.lm_logits(W, orc.widen(hid_bits))
     err = assert_close(logits.cpu().numpy(), ol, "logits")
     assert err < 1e-3, f"fp32-accumulated logits drift {err}"
-    check_topk(ids.cpu().numpy(), vals.cpu().numpy(), ol, k, "lm_head top-k")
+    und = check_topk(ids.cpu().numpy(), vals.cpu().numpy(), ol, k, "lm_head top-k", abs_delta=2e-3)
+    print(f"{w.name}: {und} top-k positions within 2e-3 of the next value")
     gi = ids.cpu().numpy().reshape(-1, k)
     gl = logits.cpu().numpy().reshape(-1, w.V)
     for r in range(gi.shape[0]):
