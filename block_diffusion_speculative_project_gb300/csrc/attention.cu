@@ -12,7 +12,8 @@
 // the splits in split order.
 //
 // Inner loop: 64-key sub-chunks of K and V are staged into shared memory with
-// 16-byte cp.async (3-stage ring, XOR-swizzled rows for conflict-free ldmatrix);
+// 16-byte cp.async (2-stage ring, XOR-swizzled rows for conflict-free ldmatrix; three
+// CTAs share an SM so twelve warps hide the MMA and shared-memory latencies);
 // each warp owns 16 query rows and runs QK^T and PV on tensor cores with
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate), keeping P in registers, with an
 // online softmax in fp32 (exp2 with the 1/sqrt(hd) * log2(e) scale folded in).
@@ -30,7 +31,7 @@ template <int HD>
 struct AttnCfg {
   static constexpr int ROW_BYTES = HD * 2;
   static constexpr int TILE_BYTES = kSub * ROW_BYTES;
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = 2;
   static constexpr size_t SMEM = size_t(STAGES) * 2 * TILE_BYTES;
 };
 
@@ -74,7 +75,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads, 3) attn_split_kernel(const AttnParams p) {
   using C = AttnCfg<HD>;
   extern __shared__ __align__(128) uint8_t smem[];
   griddep_wait();

@@ -610,27 +610,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       const int q = warp & 3;
       const int r = q * 32 + lane;
       const int per = BM / p.csplit;
-      if (r / per == static_cast<int>(cluster_ctarank())) {
+      const int rank = static_cast<int>(cluster_ctarank());
+      // Phase 1: the 128 epilogue threads sum this CTA's row slice over the S staged
+      // partials (float4 units, loads of two ranks in flight) into a local buffer
+      // placed after the staged partial; the sum runs in rank order.
+      float *slice = reinterpret_cast<float *>(smem) + BM * kRedStride;
+      const uint32_t red0 = smem_u32(smem);
+      const int units = per * (BN / 4);
+      for (int e = threadIdx.x - 64; e < units; e += 128) {
+        const int rr = e / (BN / 4), c4 = e % (BN / 4);
+        const uint32_t off = static_cast<uint32_t>(((rank * per + rr) * kRedStride + c4 * 4) * 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int src0 = 0; src0 < p.csplit; src0 += 2) {
+          float4 x0 = ld_cluster_f4(cluster_map(red0 + off, static_cast<uint32_t>(src0)));
+          float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (src0 + 1 < p.csplit) x1 = ld_cluster_f4(cluster_map(red0 + off, static_cast<uint32_t>(src0 + 1)));
+          acc.x += x0.x;
+          acc.y += x0.y;
+          acc.z += x0.z;
+          acc.w += x0.w;
+          acc.x += x1.x;
+          acc.y += x1.y;
+          acc.z += x1.z;
+          acc.w += x1.w;
+        }
+        *reinterpret_cast<float4 *>(slice + rr * kRedStride + c4 * 4) = acc;
+      }
+      named_bar_sync(1, 128);
+      // Phase 2: the owner thread of each row of the slice runs the epilogue.
+      if (r / per == rank) {
         const Item t = item_at(p, 0);
         const int row = t.m * p.tile_rows + r;
         const bool row_ok = (r < p.tile_rows) && (row < p.M);
-        const uint32_t mine = smem_u32(smem) + static_cast<uint32_t>(r * kRedStride) * 4u;
+        const float *mine = slice + (r - rank * per) * kRedStride;
         auto fetch = [&](int c, float (&v)[32]) {
+          const float4 *src = reinterpret_cast<const float4 *>(mine + c * 32);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
-#pragma unroll 1
-          for (int src = 0; src < p.csplit; ++src) {
-            const uint32_t a = cluster_map(mine + c * 128u, static_cast<uint32_t>(src));
-            float4 x[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = ld_cluster_f4(a + 16u * k);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              v[4 * k] += x[k].x;
-              v[4 * k + 1] += x[k].y;
-              v[4 * k + 2] += x[k].z;
-              v[4 * k + 3] += x[k].w;
-            }
+          for (int k = 0; k < 8; ++k) {
+            const float4 x = src[k];
+            v[4 * k] = x.x;
+            v[4 * k + 1] = x.y;
+            v[4 * k + 2] = x.z;
+            v[4 * k + 3] = x.w;
           }
         };
         TopkState tk;

@@ -188,10 +188,29 @@ cudaError_t launch_accept(const int *draft, const int *target, int nb, int B, in
 }
 
 // ---------------------------------------------------------------- top-k merge
-// One CTA per row. Candidate c of part q of row r: vals[q*part_stride + r*row_stride + c]
-// (ids from `ids` at the same index, or c itself when ids == nullptr).
-// Each thread keeps a sorted top-16 of its strided candidates; then k rounds of a
-// CTA-wide arg-best (value descending, ties to the lower id) pop the winners.
+// One CTA (8 warps) per row. Candidate c of part q of row r:
+// vals[q*part_stride + r*row_stride + c] (ids from `ids` at the same index, or c itself
+// when ids == nullptr). Each thread keeps a sorted top-16 of its strided candidates;
+// each warp merges its 32 lists with shuffle-only arg-best rounds; warp 0 merges the
+// 8 warp lists the same way. Order: value descending, ties to the lower id.
+__device__ __forceinline__ void warp_pop_best(float &hv, int &hi, int lane, float &best_v,
+                                              int &best_i, int &best_lane) {
+  best_v = hv;
+  best_i = hi;
+  best_lane = lane;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best_v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+    const int ol = __shfl_xor_sync(0xffffffffu, best_lane, o);
+    if (topk_before(ov, oi, best_v, best_i) || (ov == best_v && oi == best_i && ol < best_lane)) {
+      best_v = ov;
+      best_i = oi;
+      best_lane = ol;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) topk_merge_kernel(const float *vals, const int *ids,
                                                          int ncand, long long row_stride,
                                                          long long part_stride, int parts, int k,
@@ -200,9 +219,10 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float *vals, cons
   griddep_launch();
   __shared__ float sv[256 * kTopkMax];
   __shared__ int si[256 * kTopkMax];
-  __shared__ float wv[8];
-  __shared__ int wi[8], wt[8];
+  __shared__ float wv[8 * kTopkMax];
+  __shared__ int wi[8 * kTopkMax];
   const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float kv[kTopkMax];
   int ki[kTopkMax];
 #pragma unroll
@@ -236,46 +256,39 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float *vals, cons
     sv[threadIdx.x * kTopkMax + s] = kv[s];
     si[threadIdx.x * kTopkMax + s] = ki[s];
   }
-  int head = 0;
-  __syncthreads();
-  for (int round = 0; round < k; ++round) {
-    float bv = head < kTopkMax ? sv[threadIdx.x * kTopkMax + head] : -FLT_MAX;
-    int bi = head < kTopkMax ? si[threadIdx.x * kTopkMax + head] : INT_MAX;
-    int bt = threadIdx.x;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const int ot = __shfl_xor_sync(0xffffffffu, bt, o);
-      if (topk_before(ov, oi, bv, bi) || (ov == bv && oi == bi && ot < bt)) {
-        bv = ov;
-        bi = oi;
-        bt = ot;
+  __syncwarp();
+  // warp level: pop the best head of the 32 lane lists k times
+  {
+    int head = 0;
+    for (int round = 0; round < k; ++round) {
+      float hv = head < kTopkMax ? sv[threadIdx.x * kTopkMax + head] : -FLT_MAX;
+      int hi = head < kTopkMax ? si[threadIdx.x * kTopkMax + head] : INT_MAX;
+      float bv;
+      int bi, bl;
+      warp_pop_best(hv, hi, lane, bv, bi, bl);
+      if (lane == 0) {
+        wv[warp * kTopkMax + round] = bv;
+        wi[warp * kTopkMax + round] = bi;
       }
+      if (lane == bl) ++head;
     }
-    const int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
-      wv[w] = bv;
-      wi[w] = bi;
-      wt[w] = bt;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int head = 0;
+    const int src = lane < 8 ? lane : -1;
+    for (int round = 0; round < k; ++round) {
+      float hv = (src >= 0 && head < k) ? wv[src * kTopkMax + head] : -FLT_MAX;
+      int hi = (src >= 0 && head < k) ? wi[src * kTopkMax + head] : INT_MAX;
+      float bv;
+      int bi, bl;
+      warp_pop_best(hv, hi, lane, bv, bi, bl);
+      if (lane == 0) {
+        out_vals[(size_t)r * k + round] = bv;
+        out_ids[(size_t)r * k + round] = bi;
+      }
+      if (lane == bl) ++head;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float fv = wv[0];
-      int fi = wi[0], ft = wt[0];
-      for (int q = 1; q < 8; ++q)
-        if (topk_before(wv[q], wi[q], fv, fi) || (wv[q] == fv && wi[q] == fi && wt[q] < ft)) {
-          fv = wv[q];
-          fi = wi[q];
-          ft = wt[q];
-        }
-      out_vals[(size_t)r * k + round] = fv;
-      out_ids[(size_t)r * k + round] = fi;
-      wt[0] = ft;
-    }
-    __syncthreads();
-    if (threadIdx.x == wt[0]) ++head;
-    __syncthreads();
   }
 }
 
