@@ -102,19 +102,20 @@ int encode_act(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols) {
 
 constexpr int kBN = 128;       // tile width of the generic GEMMs
 constexpr int kBNTopk = 256;   // tile width of the LM head
+constexpr int kBNGateUp = 192; // gate|up GEMM: 96 gate + 96 up rows per tile (F/96 tiles)
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t status = 0, counters = 0, partial = 0;
+  size_t status = 0;
   size_t pre = 0, h = 0;                       // ctx_project
   size_t x = 0, u = 0, qkv = 0, o = 0, act = 0, xb = 0, corr = 0;  // draft_block
   size_t apart = 0, aml = 0;                   // attention partials
   size_t tk_vals = 0, tk_ids = 0;              // LM head top-k partial lists
   size_t sel_e = 0, sel_ab = 0, sel_g = 0;     // selector
   size_t total = 0;
-  size_t counters_bytes = 0, partial_bytes = 0, apart_bytes = 0, apart_ctas = 0;
+  size_t apart_bytes = 0, apart_ctas = 0;
 };
 
 }  // namespace
@@ -151,20 +152,6 @@ int attn_chunk(const dflash_handle_s *h, int nb, int max_ctx, int *splits_out) {
   return chunk;
 }
 
-// Largest split-K scratch (bytes) and tile count of one GEMM shape over every row
-// count up to max_rows (the plan depends on the number of m-tiles only).
-size_t gemm_partial_max(const dflash_handle_s *h, int max_rows, int N, int K, int groups, int dual,
-                        int epi, int *max_tiles, int tile_rows = 128) {
-  size_t best = 0;
-  const int max_m_tiles = (max_rows + tile_rows - 1) / tile_rows;
-  for (int mt = 1; mt <= max_m_tiles; ++mt) {
-    const int M = std::min(max_rows, mt * tile_rows);
-    best = std::max(best, gemm_partial_bytes(M, tile_rows, N, K, groups, dual, kBN, h->num_sms, epi));
-    *max_tiles = std::max(*max_tiles, gemm_tiles(M, tile_rows, N, groups, dual, kBN));
-  }
-  return best;
-}
-
 void plan_workspace(dflash_handle_s *h) {
   const auto &c = h->cfg;
   WsLayout &L = h->ws;
@@ -172,23 +159,6 @@ void plan_workspace(dflash_handle_s *h) {
   const int Mp = c.max_batch * c.max_proj_rows;         // projection rows
   const int Ml = c.max_batch * (c.B - 1);               // LM-head rows
   const int qkv_n = (c.Hq + 2 * c.Hkv) * c.hd;
-  int max_tiles = 0;
-  size_t part = 0;
-  part = std::max(part, gemm_partial_max(h, Mp, c.D, c.L * c.Dt, 1, 0, EPI_F32, &max_tiles));
-  part = std::max(part, gemm_partial_max(h, Mp, c.Hkv * c.hd, c.D, 2 * c.N, 0, EPI_KV, &max_tiles));
-  part = std::max(part, gemm_partial_max(h, Mb, qkv_n, c.D, 1, 0, EPI_ROPE, &max_tiles));
-  part = std::max(part, gemm_partial_max(h, Mb, c.D, c.Hq * c.hd, 1, 0, EPI_RESID, &max_tiles));
-  part = std::max(part, gemm_partial_max(h, Mb, c.F, c.D, 1, 1, EPI_SWIGLU, &max_tiles));
-  part = std::max(part, gemm_partial_max(h, Mb, c.D, c.F, 1, 0, EPI_RESID, &max_tiles));
-  if (c.flags & DFLASH_FLAG_CONV)
-    part = std::max(part, gemm_partial_max(h, Mb, c.D / c.conv_group, c.D, 1, 1, EPI_DUAL_F32, &max_tiles));
-  const int sel_rows = c.max_batch * (1 + (c.B - 1) * c.k_top);
-  if (c.flags & DFLASH_FLAG_SELECT) {
-    part = std::max(part, gemm_partial_max(h, sel_rows, c.sel_dim, c.D, 1, 1, EPI_DUAL_F32, &max_tiles));
-    const int R = c.B - 1;
-    part = std::max(part, gemm_partial_max(h, Ml, c.sel_dim, c.D, 1, 0, EPI_F32, &max_tiles,
-                                           (128 / R) * R));
-  }
   const size_t apart_max = (size_t)h->max_attn_ctas + (size_t)c.max_batch * c.Hkv;  // CTA bound
   const size_t rows_attn = (size_t)(c.Hq / c.Hkv) * c.B;
 
@@ -199,10 +169,6 @@ void plan_workspace(dflash_handle_s *h) {
     return o;
   };
   L.status = take(256);
-  L.counters_bytes = (size_t)std::max(max_tiles, 1) * sizeof(int);
-  L.counters = take(L.counters_bytes);
-  L.partial_bytes = part;
-  L.partial = take(part);
   L.pre = take((size_t)Mp * c.D * 4);
   L.h = take((size_t)Mp * c.D * 2);
   L.x = take((size_t)Mb * c.D * 4);
@@ -220,6 +186,7 @@ void plan_workspace(dflash_handle_s *h) {
   L.tk_vals = take((size_t)ranges * Ml * c.k_top * 4);
   L.tk_ids = take((size_t)ranges * Ml * c.k_top * 4);
   if (c.flags & DFLASH_FLAG_SELECT) {
+    const int sel_rows = c.max_batch * (1 + (c.B - 1) * c.k_top);
     L.sel_e = take((size_t)sel_rows * c.D * 2);
     L.sel_ab = take((size_t)sel_rows * 2 * c.sel_dim * 4);
     L.sel_g = take((size_t)Ml * c.sel_dim * 4);
@@ -253,8 +220,6 @@ GemmParams base_params(const dflash_handle_s *h, const Ws &w) {
   p.status = w.status();
   p.max_spin = h->cfg.max_spin;
   p.stall = (h->cfg.flags & DFLASH_FLAG_TEST_STALL) ? 1 : 0;
-  p.partial = w.at<float>(w.L.partial);
-  p.counters = w.at<int>(w.L.counters);
   p.hd = h->cfg.hd;
   std::memcpy(p.inv_freq, h->inv_freq, sizeof(p.inv_freq));
   return p;
@@ -423,8 +388,8 @@ int dflash_set_weights(dflash_handle_t h, const dflash_weights *w) {
     DF_TRY(encode_2d(&h->tm_kc[n], L.Wk_c, (uint64_t)c.Hkv * c.hd, c.D, c.D, kBN));
     DF_TRY(encode_2d(&h->tm_vc[n], L.Wv_c, (uint64_t)c.Hkv * c.hd, c.D, c.D, kBN));
     DF_TRY(encode_2d(&h->tm_o[n], L.W_o, c.D, (uint64_t)c.Hq * c.hd, (uint64_t)c.Hq * c.hd, kBN));
-    DF_TRY(encode_2d(&h->tm_gate[n], L.W_gate, c.F, c.D, c.D, kBN / 2));
-    DF_TRY(encode_2d(&h->tm_up[n], L.W_up, c.F, c.D, c.D, kBN / 2));
+    DF_TRY(encode_2d(&h->tm_gate[n], L.W_gate, c.F, c.D, c.D, kBNGateUp / 2));
+    DF_TRY(encode_2d(&h->tm_up[n], L.W_up, c.F, c.D, c.D, kBNGateUp / 2));
     DF_TRY(encode_2d(&h->tm_down[n], L.W_down, c.D, c.F, c.F, kBN));
     if (c.flags & DFLASH_FLAG_CONV) {
       for (int q = 0; q < 4; ++q) {
@@ -470,7 +435,6 @@ int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *hv, const i
   DF_TRY(check_ws(h, ws, ws_bytes));
   Ws w{static_cast<uint8_t *>(ws), h->ws};
   cudaStream_t s = stream;
-  DF_CUDA(cudaMemsetAsync(w.at<int>(h->ws.counters), 0, h->ws.counters_bytes, s));
   const int rows = nb * R;
   float *pre = w.at<float>(h->ws.pre);
   uint16_t *hh = w.at<uint16_t>(h->ws.h);
@@ -540,7 +504,6 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
   uint16_t *qkv = w.at<uint16_t>(h->ws.qkv);
   uint16_t *o = w.at<uint16_t>(h->ws.o);
   uint16_t *act = w.at<uint16_t>(h->ws.act);
-  DF_CUDA(cudaMemsetAsync(w.at<int>(h->ws.counters), 0, h->ws.counters_bytes, s));
 
   CUtensorMap tm_u, tm_o, tm_act;
   DF_TRY(encode_act(&tm_u, u, M, c.D));
@@ -623,7 +586,7 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
       p.epi = EPI_SWIGLU;
       p.out = act;
       p.ldo = c.F;
-      DF_TRY(run_gemm(h, p, kBN, s));
+      DF_TRY(run_gemm(h, p, kBNGateUp, s));
     }
     {  // x += act W_down^T
       GemmParams p = base_params(h, w);
@@ -779,7 +742,6 @@ int dflash2_conv(dflash_handle_t h, int layer, int which, int nb, float *x, void
   if (!x) return fail(DFLASH_ERR_INVALID_ARG, "x is NULL");
   DF_TRY(check_ws(h, ws, ws_bytes));
   Ws w{static_cast<uint8_t *>(ws), h->ws};
-  DF_CUDA(cudaMemsetAsync(w.at<int>(h->ws.counters), 0, h->ws.counters_bytes, stream));
   return run_conv(h, w, layer, which, nb * c.B, x, stream);
 }
 
@@ -797,7 +759,6 @@ int dflash2_select(dflash_handle_t h, int nb, int k, const int32_t *topk_ids, co
   DF_TRY(check_ws(h, ws, ws_bytes));
   Ws w{static_cast<uint8_t *>(ws), h->ws};
   cudaStream_t s = stream;
-  DF_CUDA(cudaMemsetAsync(w.at<int>(h->ws.counters), 0, h->ws.counters_bytes, s));
   const int per = 1 + (c.B - 1) * k;
   const int rows = nb * per;
   uint16_t *eg = w.at<uint16_t>(h->ws.sel_e);

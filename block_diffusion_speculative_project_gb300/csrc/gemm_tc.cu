@@ -32,17 +32,18 @@ constexpr int kGemmThreads = 192;
 // Bound of the teardown waits for this CTA's own TMA copies and MMAs, which finish
 // without help from any other thread; independent of the caller's max_spin.
 constexpr int kDrainSpin = 1 << 22;
-// Row stride (floats) of the partial tile staged for the cluster reduction.
-constexpr int kRedStride = 128 + 4;
-
 template <int BN>
 struct TileCfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = (200 * 1024 / STAGE) > 8 ? 8 : (200 * 1024 / STAGE);
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;  // power of two >= 2*BN
   static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE + 256;
+  // Cluster split-K reuses the pipeline smem: the staged partial tile (BM rows of
+  // RED_STRIDE floats) followed by the reduced row slice (at most BM / 2 rows).
+  static constexpr int RED_STRIDE = BN + 4;
+  static constexpr bool RED_FITS = size_t(BM + BM / 2) * RED_STRIDE * 4 <= size_t(STAGES) * STAGE;
 };
 
 // Top-k epilogue: a per-thread stash of one 32-value chunk (stride 33 floats, so the
@@ -363,6 +364,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
   using C = TileCfg<BN>;
+  static_assert(EPI == EPI_TOPK || C::RED_FITS, "cluster reduction buffers exceed the pipeline smem");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -374,7 +376,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   uint64_t *acc_empty = acc_full + 2;
   uint64_t *mma_done = acc_empty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
-  volatile int *s_last = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *stash_base = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE + 256);
 
   const int warp = threadIdx.x >> 5;
@@ -550,9 +551,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       const int row = t.m * p.tile_rows + r;
       const bool row_ok = (r < p.tile_rows) && (row < p.M);
       if (EPI != EPI_TOPK && p.csplit > 1) {
-        // Stage this CTA's partial tile, row r at red[r * kRedStride], in the
+        // Stage this CTA's partial tile, row r at red[r * RED_STRIDE], in the
         // pipeline smem (every TMA write has landed and every MMA has completed).
-        float *red = reinterpret_cast<float *>(smem) + r * kRedStride;
+        float *red = reinterpret_cast<float *>(smem) + r * C::RED_STRIDE;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
@@ -609,17 +610,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     if (warp >= 2 && nitems > 0) {
       const int q = warp & 3;
       const int r = q * 32 + lane;
-      const int per = BM / p.csplit;
       const int rank = static_cast<int>(cluster_ctarank());
+      const int row0 = rank * BM / p.csplit;               // this CTA's rows [row0, row1)
+      const int per = (rank + 1) * BM / p.csplit - row0;
       // Phase 1: the 128 epilogue threads sum this CTA's row slice over the S staged
       // partials (float4 units, loads of two ranks in flight) into a local buffer
       // placed after the staged partial; the sum runs in rank order.
-      float *slice = reinterpret_cast<float *>(smem) + BM * kRedStride;
+      float *slice = reinterpret_cast<float *>(smem) + BM * C::RED_STRIDE;
       const uint32_t red0 = smem_u32(smem);
       const int units = per * (BN / 4);
       for (int e = threadIdx.x - 64; e < units; e += 128) {
         const int rr = e / (BN / 4), c4 = e % (BN / 4);
-        const uint32_t off = static_cast<uint32_t>(((rank * per + rr) * kRedStride + c4 * 4) * 4);
+        const uint32_t off = static_cast<uint32_t>(((row0 + rr) * C::RED_STRIDE + c4 * 4) * 4);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int src0 = 0; src0 < p.csplit; src0 += 2) {
           float4 x0 = ld_cluster_f4(cluster_map(red0 + off, static_cast<uint32_t>(src0)));
@@ -634,15 +636,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
           acc.z += x1.z;
           acc.w += x1.w;
         }
-        *reinterpret_cast<float4 *>(slice + rr * kRedStride + c4 * 4) = acc;
+        *reinterpret_cast<float4 *>(slice + rr * C::RED_STRIDE + c4 * 4) = acc;
       }
       named_bar_sync(1, 128);
       // Phase 2: the owner thread of each row of the slice runs the epilogue.
-      if (r / per == rank) {
+      if (r >= row0 && r < row0 + per) {
         const Item t = item_at(p, 0);
         const int row = t.m * p.tile_rows + r;
         const bool row_ok = (r < p.tile_rows) && (row < p.M);
-        const float *mine = slice + (r - rank * per) * kRedStride;
+        const float *mine = slice + (r - row0) * C::RED_STRIDE;
         auto fetch = [&](int c, float (&v)[32]) {
           const float4 *src = reinterpret_cast<const float4 *>(mine + c * 32);
 #pragma unroll
@@ -680,18 +682,23 @@ int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN) {
   return m_tiles * n_tiles * groups;
 }
 
-// Chooses the cluster split S: the largest power of two <= 8 such that all
-// tiles * S CTAs run in one wave and every split keeps >= 8 k-tiles. Multi-wave
-// cluster launches measured slower than one persistent unsplit wave, so larger
-// tile counts stay unsplit.
+// Chooses the cluster split S: the largest S <= 8 such that every tile's cluster of
+// S CTAs is resident at once (cluster_cap[S] = clusters of that size the device
+// holds concurrently; 0 = unknown, then tiles * S <= num_sms) and every split keeps
+// >= 8 k-tiles. Multi-wave cluster launches measured slower than one persistent
+// unsplit wave, so larger tile counts stay unsplit.
 void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN, int num_sms,
-               int epi, int *splits_out, int *kps_out, int *items_out, int *grid_out, int *csplit_out) {
+               int epi, const int *cluster_cap, int *splits_out, int *kps_out, int *items_out,
+               int *grid_out, int *csplit_out) {
   const int tiles = gemm_tiles(M, tile_rows, N, groups, dual, BN);
   const int kt = (K + BK - 1) / BK;
   int best_s = 1;
   if (epi != EPI_TOPK)
-    for (int S = 2; S <= 8; S *= 2)
-      if ((long long)tiles * S <= num_sms && kt >= 8 * S) best_s = S;
+    for (int S = 2; S <= 8; ++S) {
+      const bool fits = cluster_cap && cluster_cap[S] > 0 ? tiles <= cluster_cap[S]
+                                                          : (long long)tiles * S <= num_sms;
+      if (fits && kt >= 8 * S) best_s = S;
+    }
   *splits_out = 1;
   *csplit_out = best_s;
   *kps_out = (kt + best_s - 1) / best_s;
@@ -699,19 +706,66 @@ void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN,
   *grid_out = best_s > 1 ? tiles * best_s : std::max(1, std::min(tiles, num_sms));
 }
 
-size_t gemm_partial_bytes(int, int, int, int, int, int, int, int, int) { return 0; }
+// Per-instantiation launch set-up, done once per process: the dynamic shared memory
+// opt-in and, for each cluster size 2..8, how many clusters of this kernel the device
+// keeps resident at once (cluster placement is limited by the GPCs, so tiles * S <=
+// SMs alone does not guarantee a single wave).
+struct KernelSetup {
+  cudaError_t err = cudaSuccess;
+  int cluster_cap[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+};
 
 template <int BN, int EPI>
-static cudaError_t launch_one(const GemmParams &p, int grid, cudaStream_t s) {
-  // (cluster launches are chosen by p.csplit)
-  constexpr size_t smem = gemm_smem_bytes<BN, EPI>();
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
+static const KernelSetup &kernel_setup() {
+  static const KernelSetup setup = [] {
+    KernelSetup k;
+    constexpr size_t smem = gemm_smem_bytes<BN, EPI>();
+    k.err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+    if (k.err != cudaSuccess || EPI == EPI_TOPK) return k;
+    for (int S = 2; S <= 8; ++S) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(S);
+      cfg.blockDim = dim3(kGemmThreads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = S;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      k.cluster_cap[S] = n;
+    }
+    return k;
+  }();
+  return setup;
+}
+
+template <int BN, int EPI>
+static cudaError_t plan_and_launch(GemmParams &p, int num_sms, cudaStream_t s) {
+  const KernelSetup &ks = kernel_setup<BN, EPI>();
+  if (ks.err != cudaSuccess) return ks.err;
+  int grid;
+  p.csplit = 1;
+  if (EPI == EPI_TOPK) {
+    p.splits = 1;
+    p.kt_per_split = p.kt_total;
+    const int ranges0 = std::max(1, num_sms / p.m_tiles);
+    p.tiles_per_cta = (p.n_tiles + ranges0 - 1) / ranges0;
+    const int ranges = (p.n_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
+    grid = ranges * p.m_tiles;
+    p.items = grid;
+  } else {
+    gemm_plan(p.M, p.tile_rows, p.N, p.K, p.groups, p.dual, BN, num_sms, p.epi, ks.cluster_cap,
+              &p.splits, &p.kt_per_split, &p.items, &grid, &p.csplit);
   }
+  constexpr size_t smem = gemm_smem_bytes<BN, EPI>();
   if (p.csplit > 1)
     return launch_pdl_cluster(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), smem, s, p.csplit,
                               p);
@@ -724,32 +778,19 @@ cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s) {
   const int ncols = p.dual ? BN / 2 : BN;
   p.n_tiles = (p.N + ncols - 1) / ncols;
   p.kt_total = (p.K + BK - 1) / BK;
-  int grid;
-  p.csplit = 1;
-  if (p.epi == EPI_TOPK) {
-    p.splits = 1;
-    p.kt_per_split = p.kt_total;
-    const int ranges0 = std::max(1, num_sms / p.m_tiles);
-    p.tiles_per_cta = (p.n_tiles + ranges0 - 1) / ranges0;
-    const int ranges = (p.n_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
-    grid = ranges * p.m_tiles;
-    p.items = grid;
-  } else {
-    gemm_plan(p.M, p.tile_rows, p.N, p.K, p.groups, p.dual, BN, num_sms, p.epi, &p.splits,
-              &p.kt_per_split, &p.items, &grid, &p.csplit);
-  }
   // expect-tx bytes of one stage: the A box plus the B box(es)
   const uint32_t a_rows = p.a_grouped ? (uint32_t)p.tile_rows : (uint32_t)BM;
   p.stage_tx_bytes = a_rows * BK * 2 + (uint32_t)BN * BK * 2;
   switch (BN * 16 + p.epi) {
-    case 128 * 16 + EPI_BF16: return launch_one<128, EPI_BF16>(p, grid, s);
-    case 128 * 16 + EPI_F32: return launch_one<128, EPI_F32>(p, grid, s);
-    case 128 * 16 + EPI_RESID: return launch_one<128, EPI_RESID>(p, grid, s);
-    case 128 * 16 + EPI_ROPE: return launch_one<128, EPI_ROPE>(p, grid, s);
-    case 128 * 16 + EPI_SWIGLU: return launch_one<128, EPI_SWIGLU>(p, grid, s);
-    case 128 * 16 + EPI_DUAL_F32: return launch_one<128, EPI_DUAL_F32>(p, grid, s);
-    case 128 * 16 + EPI_KV: return launch_one<128, EPI_KV>(p, grid, s);
-    case 256 * 16 + EPI_TOPK: return launch_one<256, EPI_TOPK>(p, grid, s);
+    case 128 * 16 + EPI_BF16: return plan_and_launch<128, EPI_BF16>(p, num_sms, s);
+    case 128 * 16 + EPI_F32: return plan_and_launch<128, EPI_F32>(p, num_sms, s);
+    case 128 * 16 + EPI_RESID: return plan_and_launch<128, EPI_RESID>(p, num_sms, s);
+    case 128 * 16 + EPI_ROPE: return plan_and_launch<128, EPI_ROPE>(p, num_sms, s);
+    case 128 * 16 + EPI_SWIGLU: return plan_and_launch<128, EPI_SWIGLU>(p, num_sms, s);
+    case 192 * 16 + EPI_SWIGLU: return plan_and_launch<192, EPI_SWIGLU>(p, num_sms, s);
+    case 128 * 16 + EPI_DUAL_F32: return plan_and_launch<128, EPI_DUAL_F32>(p, num_sms, s);
+    case 128 * 16 + EPI_KV: return plan_and_launch<128, EPI_KV>(p, num_sms, s);
+    case 256 * 16 + EPI_TOPK: return plan_and_launch<256, EPI_TOPK>(p, num_sms, s);
     default: return cudaErrorInvalidValue;
   }
 }

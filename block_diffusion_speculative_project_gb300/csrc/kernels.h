@@ -106,9 +106,6 @@ struct GemmParams {
   float *part_vals;  // [ranges][M][topk_k]
   int *part_ids;
   float *logits_out; // [M][N] or null
-  // split-K
-  float *partial;    // [tile][split][128][BN] f32
-  int *counters;     // [tile]
   int *status;
   int max_spin;
   int stall;         // test hook: issue no loads so the waits run out
@@ -121,14 +118,14 @@ struct GemmLaunch {
   size_t smem;
 };
 
-// Chooses BN/splits/grid, fills the derived fields of p and launches.
-// partial/counters must be sized by gemm_scratch_bytes for the same shape.
+// Fills the derived fields of p (tiles, cluster split, grid) and launches; the
+// GEMM needs no global scratch (a split K is reduced inside its cluster).
 cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s);
-// Bytes of split-K partials and counters the launch with these shapes needs.
+// cluster_cap[S] (S = 2..8): clusters of S CTAs the device keeps resident at once,
+// 0 = unknown; may be null.
 void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN, int num_sms,
-               int epi, int *splits, int *kt_per_split, int *items, int *grid, int *csplit);
-size_t gemm_partial_bytes(int M, int tile_rows, int N, int K, int groups, int dual, int BN,
-                          int num_sms, int epi);
+               int epi, const int *cluster_cap, int *splits, int *kt_per_split, int *items, int *grid,
+               int *csplit);
 int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN);
 
 // ---------------------------------------------------------------- small kernels
