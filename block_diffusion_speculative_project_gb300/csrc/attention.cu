@@ -1,22 +1,38 @@
-// Split-K context attention of the drafter layer with KV injection:
+// Context attention of the drafter layer with KV injection, on the tcgen05 tensor cores:
 //   for each sequence i and query head h (kv head g = h / (Hq/Hkv)):
 //   o = softmax(q K^T / sqrt(hd)) V,  K = [K_c (cached context rows); K_b (block rows)],
 //   V likewise, with no mask (the block is bidirectional).
 // Source: "DFlash 投机解码：块扩散草稿与 KV 注入", 二、块扩散草稿 (attention equations).
 //
-// Work decomposition: one CTA per (context split s, kv head g, sequence i). The
-// Hq/Hkv query heads that share g and the B block offsets form the rows of one
-// query tile (64 rows at B=16, GQA 4:1), so every K/V byte streamed from HBM is
-// used by all of them. Split 0 also owns the B block keys. Each CTA writes an
-// unnormalised partial (o, running max m, running sum l); a merge kernel combines
-// the splits in split order.
+// K_b and V_b were written by the QKV GEMM into cache rows [ctx_len, ctx_len + B), so a
+// (sequence, kv head) pair attends to L = ctx_len + B contiguous cache rows.
 //
-// Inner loop: 64-key sub-chunks of K and V are staged into shared memory with
-// 16-byte cp.async (2-stage ring, XOR-swizzled rows for conflict-free ldmatrix; three
-// CTAs share an SM so twelve warps hide the MMA and shared-memory latencies);
-// each warp owns 16 query rows and runs QK^T and PV on tensor cores with
-// mma.sync m16n8k16 (bf16 in, fp32 accumulate), keeping P in registers, with an
-// online softmax in fp32 (exp2 with the 1/sqrt(hd) * log2(e) scale folded in).
+// Work decomposition (even split of the streamed bytes): the keys of every pair are cut
+// into 64-key units; the units of all pairs, in (sequence, kv head) order, are divided
+// into `grid` contiguous ranges of equal size, one per CTA (one CTA per SM). A CTA walks
+// its range; each maximal run of units of one pair is a segment. A segment that covers
+// its whole pair writes the final output; otherwise it writes an unnormalised partial
+// (o, running max, running sum) to slot pair + cta, and a merge kernel combines the
+// partials of the pair in CTA order. The split points depend on the batch's context
+// lengths only, so results are deterministic for a given batch.
+//
+// One CTA, 320 threads:
+//   warp 0       TMA producer: Q tile of the segment's pair ({64 of hd, Hq/Hkv heads, B
+//                rows} boxes from the qkv buffer) and per unit a K tile and a V tile
+//                (64 cache rows x hd, 128-byte swizzle) into a 4-stage ring.
+//   warp 1       MMA issuer: S = Q K^T (M = 128 query rows, the G*B real ones zero-padded,
+//                N = 64 keys, K = hd) into TMEM S buffer j % 2, then O_{j%2} += P V
+//                (N = hd, K = 64 keys; V read MN-major straight from its TMA tile).
+//   warps 2..9   softmax, two halves of four warps: half h takes the units j with
+//                j % 2 == h and keeps its own running max, running sum and O_h, so the
+//                two halves work on consecutive units at once. Thread r of a half owns
+//                query row r (its TMEM lane): it reads S, masks keys beyond L, updates
+//                its max and sum in fp32 (exp2 with the 1/sqrt(hd) * log2(e) scale
+//                folded in) and writes P (bf16) to shared memory for the PV MMA. O_h is
+//                rescaled in TMEM only when the row's max grows by more than 2^8 in
+//                probability scale, so P stays <= 256 and most units need no O round
+//                trip. At the end of a segment half 0 merges (m, l, O) of both halves
+//                and writes the output or the partial.
 #include <cfloat>
 
 #include "common.cuh"
@@ -24,278 +40,565 @@
 
 namespace df {
 
-constexpr int kAttnThreads = 128;
-constexpr int kSub = 64;  // keys per sub-chunk
+// Warp roles for NQ TMEM lane quarters of real query rows (NQ = 2 when G*B <= 64, else
+// 4): half 0 = warps [0, NQ), half 1 = warps [4, 4 + NQ) (warp w reads TMEM lanes of
+// quarter w % 4), then the producer and the MMA warp.
+template <int NQ>
+struct AttnRoles {
+  static constexpr int PRODUCER = NQ == 4 ? 8 : 2;
+  static constexpr int MMA = PRODUCER + 1;
+  static constexpr int THREADS = (NQ == 4 ? 10 : 6) * 32;
+  static constexpr int HALF_THREADS = NQ * 32;
+};
+constexpr int kKeys = 64;           // keys per unit
+constexpr int kAttnStages = 4;
+constexpr int kQRows = 128;         // MMA M: query rows, zero-padded beyond G*B
+constexpr int kAttnDrainSpin = 1 << 22;
+constexpr float kRescaleLog2 = 8.0f;
 
 template <int HD>
 struct AttnCfg {
-  static constexpr int ROW_BYTES = HD * 2;
-  static constexpr int TILE_BYTES = kSub * ROW_BYTES;
-  static constexpr int STAGES = 2;
-  static constexpr size_t SMEM = size_t(STAGES) * 2 * TILE_BYTES;
+  static constexpr int ATOMS = HD / 64;               // 128-byte swizzle atoms across hd
+  static constexpr int ATOM_Q = kQRows * 128;         // one atom of the Q tile
+  static constexpr int ATOM_KV = kKeys * 128;         // one atom of a K or V tile
+  static constexpr int Q_BYTES = ATOMS * ATOM_Q;
+  static constexpr int KV_TILE = ATOMS * ATOM_KV;
+  static constexpr int STAGE = 2 * KV_TILE;           // K tile then V tile
+  static constexpr int P_BYTES = kQRows * kKeys * 2;  // P of one unit, bf16, K-major
+  static constexpr int OFF_KV = Q_BYTES;
+  static constexpr int OFF_P = OFF_KV + kAttnStages * STAGE;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_ML = OFF_BAR + 256;        // half 1's (max, sum) per row
+  static constexpr size_t SMEM = 1024 + OFF_ML + kQRows * 8;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t S_COL = 0;                // two S buffers of 64 columns
+  static constexpr uint32_t O_COL = 128;              // O_0, O_1: hd columns each
 };
 
-// Byte offset of 16-byte chunk `chunk` inside a staged row: XOR with the row's low
-// three bits so the 8 rows read by one ldmatrix phase hit distinct banks.
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return static_cast<uint32_t>((chunk ^ (row & 7)) * 16);
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
+// Context rows of sequence i used by the attention: ctx_len clamped to the caller's
+// bound and to the cache (the block occupies the B rows after it).
+__device__ __forceinline__ int attn_ctx(const AttnParams &p, int i) {
+  const int hi = min(p.max_ctx, p.Cmax - p.B);
+  return max(0, min(p.ctx_len[i], hi));
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+__device__ __forceinline__ int attn_units(const AttnParams &p, int i) {
+  return (attn_ctx(p, i) + p.B + kKeys - 1) / kKeys;
 }
 
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// Warp-collective: Hkv * (sum of units of sequences [0, n)).
+__device__ long long attn_units_before(const AttnParams &p, int n, int lane) {
+  long long s = 0;
+  for (int i = lane; i < n; i += 32) s += attn_units(p, i);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s * p.Hkv;
 }
 
-template <int HD>
-__global__ void __launch_bounds__(kAttnThreads, 3) attn_split_kernel(const AttnParams p) {
+// First unit of CTA c when T units are split over G CTAs.
+__device__ __forceinline__ long long attn_cta_start(long long T, int G, int c) {
+  return (long long)c * T / G;
+}
+// The CTA whose range holds unit u.
+__device__ __forceinline__ int attn_cta_of(long long T, int G, long long u) {
+  return static_cast<int>(((u + 1) * G + T - 1) / T - 1);
+}
+
+// Position of a CTA in its unit range.
+struct AttnWalk {
+  int pair;   // i * Hkv + g
+  int unit;   // unit index inside the pair
+  int L, U;   // keys and units of the pair
+  int seg;    // segment index inside this CTA
+  int seg_unit0;  // first unit of the current segment inside the pair
+  int left;   // units left in this CTA's range, including the current one
+};
+
+__device__ __forceinline__ void walk_set_pair(AttnWalk &w, const AttnParams &p) {
+  const int i = w.pair / p.Hkv;
+  w.L = attn_ctx(p, i) + p.B;
+  w.U = (w.L + kKeys - 1) / kKeys;
+}
+__device__ __forceinline__ bool walk_first(const AttnWalk &w) { return w.unit == w.seg_unit0; }
+__device__ __forceinline__ bool walk_last(const AttnWalk &w) { return w.left == 1 || w.unit == w.U - 1; }
+__device__ __forceinline__ void walk_next(AttnWalk &w, const AttnParams &p) {
+  --w.left;
+  if (++w.unit == w.U) {
+    ++w.pair;
+    w.unit = 0;
+    w.seg_unit0 = 0;
+    ++w.seg;
+    if (w.left > 0) walk_set_pair(w, p);
+  }
+}
+
+template <int HD, int NQ>
+__global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ AttnParams p) {
   using C = AttnCfg<HD>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  using Ro = AttnRoles<NQ>;
+  constexpr int HT = Ro::HALF_THREADS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint8_t *sQ = smem;
+  uint8_t *sKV = smem + C::OFF_KV;
+  uint8_t *sP = smem + C::OFF_P;
+  uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *kv_empty = kv_full + kAttnStages;
+  uint64_t *s_full = kv_empty + kAttnStages;   // [2]
+  uint64_t *s_empty = s_full + 2;              // [2]
+  uint64_t *p_full = s_empty + 2;              // [2]
+  uint64_t *p_empty = p_full + 2;              // [2]
+  uint64_t *q_full = p_empty + 2;
+  uint64_t *q_empty = q_full + 1;
+  uint64_t *o_done = q_empty + 1;             // [2]: PV into O_h completed
+  uint64_t *o_free = o_done + 2;              // both O read at a segment end
+  uint64_t *ml_ready = o_free + 1;            // half 1's (max, sum) written
+  uint64_t *mma_done = ml_ready + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+  int *sched = reinterpret_cast<int *>(tmem_slot + 1);  // [pair, unit, count]
+  float2 *ml1 = reinterpret_cast<float2 *>(smem + C::OFF_ML);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.Hq / p.Hkv;
+  const int R = G * p.B;  // real query rows
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kAttnStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_empty[b], HT);
+      mbar_init(&p_full[b], HT);
+      mbar_init(&p_empty[b], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(&o_done[0], 1);
+    mbar_init(&o_done[1], 1);
+    mbar_init(o_free, HT);
+    mbar_init(ml_ready, HT);
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == Ro::PRODUCER && lane == 0) {
+    tma_prefetch_desc(&p.tmQ);
+    tma_prefetch_desc(&p.tmK);
+    tma_prefetch_desc(&p.tmV);
+  }
+  if (warp == Ro::MMA) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp < NQ) {
+    // Zero the padding rows of Q (rows >= R are never loaded) and of both P buffers,
+    // so the padded MMA rows compute on zeros.
+    const int t = threadIdx.x;
+    for (int a = 0; a < C::ATOMS; ++a)
+      for (int e = R * 8 + t; e < kQRows * 8; e += HT)
+        *reinterpret_cast<uint4 *>(sQ + a * C::ATOM_Q + e * 16) = make_uint4(0, 0, 0, 0);
+    for (int e = R * 8 + t; e < kQRows * 8; e += HT) {
+      *reinterpret_cast<uint4 *>(sP + e * 16) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4 *>(sP + C::P_BYTES + e * 16) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+
   griddep_wait();
-  griddep_launch();
-  const int s = blockIdx.x, g = blockIdx.y, i = blockIdx.z;
-  const int grp = p.Hq / p.Hkv;
-  const int nrows = grp * p.B;
-  const int ctx = p.ctx_len[i];
-  if (ctx < 0 || ctx > p.max_ctx || ctx > p.Cmax) {
-    if (s == 0 && g == 0 && threadIdx.x == 0) flag_status(p.status, kStatusCheck);
-  }
-  const int ctx_used = max(0, min(ctx, min(p.max_ctx, p.Cmax)));
-  const int nsplit = max(1, (ctx_used + p.chunk - 1) / p.chunk);
-  if (s >= nsplit) return;
-  const int key0 = s * p.chunk;
-  const int key1 = min(ctx_used, key0 + p.chunk);
-  const int nctx = max(0, key1 - key0);
-  const int has_block = (s == 0) ? 1 : 0;
-  const int nsub = has_block + (nctx + kSub - 1) / kSub;
+  if (threadIdx.x == 0) griddep_launch();
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ldq = (p.Hq + 2 * p.Hkv) * HD;
-  const uint16_t *kbase = p.kc + (((size_t)i * p.Hkv + g) * p.Cmax) * HD;
-  const uint16_t *vbase = p.vc + (((size_t)i * p.Hkv + g) * p.Cmax) * HD;
-  const uint32_t sbase = smem_u32(smem);
-
-  // Stage sub-chunk u into ring slot `slot`: K tile then V tile, rows of HD bf16.
-  auto load_sub = [&](int u, int slot) {
-    const uint32_t kdst = sbase + slot * 2 * C::TILE_BYTES;
-    const uint32_t vdst = kdst + C::TILE_BYTES;
-    constexpr int CHUNKS = HD / 8;  // 16-byte chunks per row
-    for (int e = tid; e < kSub * CHUNKS; e += kAttnThreads) {
-      const int row = e / CHUNKS, ch = e % CHUNKS;
-      const uint16_t *ks;
-      const uint16_t *vs;
-      bool valid;
-      if (has_block && u == 0) {
-        valid = row < p.B;
-        const size_t qrow = (size_t)i * p.B + (valid ? row : 0);
-        ks = p.qkv + qrow * ldq + (size_t)(p.Hq + g) * HD + ch * 8;
-        vs = p.qkv + qrow * ldq + (size_t)(p.Hq + p.Hkv + g) * HD + ch * 8;
-      } else {
-        const int key = key0 + (u - has_block) * kSub + row;
-        valid = key < key1;
-        const size_t kr = valid ? (size_t)key : 0;
-        ks = kbase + kr * HD + ch * 8;
-        vs = vbase + kr * HD + ch * 8;
+  if (warp == Ro::PRODUCER) {
+    // Schedule: total units, this CTA's range, and the pair/unit it starts at.
+    const long long T = attn_units_before(p, p.nb, lane);
+    const int Ge = T < p.grid ? static_cast<int>(T) : p.grid;
+    int count = 0, pair0 = 0, unit0 = 0;
+    if (static_cast<int>(blockIdx.x) < Ge) {
+      const long long u0 = attn_cta_start(T, Ge, blockIdx.x);
+      const long long u1 = attn_cta_start(T, Ge, blockIdx.x + 1);
+      count = static_cast<int>(u1 - u0);
+      // find the sequence holding u0: inclusive scan of Hkv * units, 32 sequences at a time
+      long long base = 0;
+      int seq = -1;
+      for (int b = 0; b < p.nb && seq < 0; b += 32) {
+        const int i = b + lane;
+        long long v = i < p.nb ? (long long)p.Hkv * attn_units(p, i) : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long y = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, i < p.nb && base + v > u0);
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          const long long before = base + __shfl_sync(0xffffffffu, v, l) -
+                                   (long long)p.Hkv * attn_units(p, b + l);
+          seq = b + l;
+          const int U = attn_units(p, seq);
+          const long long off = u0 - before;
+          pair0 = seq * p.Hkv + static_cast<int>(off / U);
+          unit0 = static_cast<int>(off % U);
+        }
+        base += __shfl_sync(0xffffffffu, v, 31);
       }
-      const uint32_t off = row * C::ROW_BYTES + swz(row, ch);
-      cp_async16(kdst + off, ks, valid);
-      cp_async16(vdst + off, vs, valid);
+      if (seq < 0) count = 0;  // unreachable when T counts every unit
     }
-  };
-  auto nvalid_of = [&](int u) -> int {
-    if (has_block && u == 0) return p.B;
-    return min(kSub, nctx - (u - has_block) * kSub);
-  };
-
-  // Query fragments (A operand of m16n8k16) for this warp's 16 rows.
-  const int wrow0 = warp * 16;
-  const bool active = wrow0 < nrows;
-  uint32_t qf[HD / 16][4];
-  {
-    const int r0 = wrow0 + (lane >> 2), r1 = r0 + 8;
-    const int c = (lane & 3) * 2;
-    const uint32_t *q32[2] = {nullptr, nullptr};
-    const int rr[2] = {r0, r1};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (rr[h] < nrows) {
-        const int hh = rr[h] / p.B, j = rr[h] % p.B;
-        q32[h] = reinterpret_cast<const uint32_t *>(p.qkv + ((size_t)i * p.B + j) * ldq +
-                                                    (size_t)(g * grp + hh) * HD);
+    if (lane == 0) {
+      sched[0] = pair0;
+      sched[1] = unit0;
+      sched[2] = count;
+    }
+  }
+  if (warp == Ro::MMA && lane == 0) {
+    // Report context lengths outside [0, min(max_ctx, Cmax - B)] once per launch.
+    if (blockIdx.x == 0)
+      for (int i = 0; i < p.nb; ++i) {
+        const int c = p.ctx_len[i];
+        if (c < 0 || c > p.max_ctx || c > p.Cmax - p.B) flag_status(p.status, kStatusCheck);
       }
-    }
-#pragma unroll
-    for (int ks = 0; ks < HD / 16; ++ks) {
-      const int col = ks * 16 + c;
-      qf[ks][0] = q32[0] ? q32[0][col / 2] : 0u;
-      qf[ks][1] = q32[1] ? q32[1][col / 2] : 0u;
-      qf[ks][2] = q32[0] ? q32[0][(col + 8) / 2] : 0u;
-      qf[ks][3] = q32[1] ? q32[1][(col + 8) / 2] : 0u;
-    }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nunits = sched[2];
+  AttnWalk w0;
+  w0.pair = sched[0];
+  w0.unit = sched[1];
+  w0.seg = 0;
+  w0.seg_unit0 = w0.unit;
+  w0.left = nunits;
+  if (nunits > 0) walk_set_pair(w0, p);
 
-  float o[HD / 8][4];
+  if (warp == Ro::PRODUCER) {
+    if (lane == 0 && nunits > 0 && !p.stall) {
+      // ---------------- TMA producer
+      const uint64_t pol_kv = policy_evict_first();
+      const uint64_t pol_q = policy_evict_last();
+      const uint32_t q_bytes = static_cast<uint32_t>(C::ATOMS * R * 128);
+      AttnWalk w = w0;
+      bool ok = true;
+      int j = 0, q_loads = 0;
+      for (; j < nunits; ++j) {
+        const int i = w.pair / p.Hkv, g = w.pair % p.Hkv;
+        if (walk_first(w)) {
+          if (w.seg > 0 && !mbar_wait(q_empty, (w.seg - 1) & 1, p.max_spin)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(q_full, q_bytes);
 #pragma unroll
-  for (int n = 0; n < HD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f;
-  const float sl2 = rsqrtf(static_cast<float>(HD)) * 1.4426950408889634f;
-
-  // prologue: fill STAGES-1 slots
+          for (int a = 0; a < C::ATOMS; ++a)
+            tma_load_3d(sQ + a * C::ATOM_Q, &p.tmQ, q_full, a * 64, g * G, i * p.B, pol_q);
+          ++q_loads;
+        }
+        const int st = j % kAttnStages;
+        if (j >= kAttnStages && !mbar_wait(&kv_empty[st], ((j / kAttnStages) & 1) ^ 1, p.max_spin)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
+        const int row = p.layer_row0 + (i * p.Hkv + g) * p.Cmax + w.unit * kKeys;
+        uint8_t *kt = sKV + st * C::STAGE;
 #pragma unroll
-  for (int u = 0; u < C::STAGES - 1; ++u) {
-    if (u < nsub) load_sub(u, u);
-    cp_async_commit();
-  }
-
-  for (int u = 0; u < nsub; ++u) {
-    {
-      const int un = u + C::STAGES - 1;
-      if (un < nsub) load_sub(un, un % C::STAGES);
-      cp_async_commit();
+        for (int a = 0; a < C::ATOMS; ++a) {
+          tma_load_2d(kt + a * C::ATOM_KV, &p.tmK, &kv_full[st], a * 64, row, pol_kv);
+          tma_load_2d(kt + C::KV_TILE + a * C::ATOM_KV, &p.tmV, &kv_full[st], a * 64, row, pol_kv);
+        }
+        walk_next(w, p);
+      }
+      if (!ok) flag_status(p.status, kStatusTimeout);
+      // Every issued load must land before the CTA may exit (bounded).
+      for (int k = max(0, j - kAttnStages); k < j; ++k)
+        mbar_wait(&kv_full[k % kAttnStages], (k / kAttnStages) & 1, kAttnDrainSpin);
+      if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, kAttnDrainSpin);
     }
-    cp_async_wait<C::STAGES - 1>();
-    __syncthreads();
-    const int slot = u % C::STAGES;
-    const uint32_t ksm = sbase + slot * 2 * C::TILE_BYTES;
-    const uint32_t vsm = ksm + C::TILE_BYTES;
-    const int nv = nvalid_of(u);
-    if (active) {
-      float sc[8][4];
+  } else if (warp == Ro::MMA) {
+    if (lane == 0 && nunits > 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t id_s = idesc_bf16_f32(kQRows, kKeys);
+      constexpr uint32_t id_pv = idesc_bf16_f32(kQRows, HD) | kIdescBMajorMN;
+      const uint32_t q_addr = smem_u32(sQ);
+      AttnWalk w = w0;
+      bool ok = true;
+      int jf = 0;                 // first unit of the current segment
+      int prev_jf = 0, prev_seg = 0;
+      for (int j = 0; j <= nunits && ok; ++j) {
+        if (j < nunits) {
+          const int st = j % kAttnStages, sb = j & 1;
+          if (walk_first(w)) {
+            jf = j;
+            if (!mbar_wait(q_full, w.seg & 1, p.max_spin)) ok = false;
+          }
+          if (ok && !mbar_wait(&kv_full[st], (j / kAttnStages) & 1, p.max_spin)) ok = false;
+          if (ok && j >= 2 && !mbar_wait(&s_empty[sb], ((j >> 1) - 1) & 1, p.max_spin)) ok = false;
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sKV + st * C::STAGE);
 #pragma unroll
-      for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-      const int mi = lane >> 3, rr = lane & 7;
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t qa = q_addr + (kk >> 2) * C::ATOM_Q + (kk & 3) * 32;
+            const uint32_t ka = k_addr + (kk >> 2) * C::ATOM_KV + (kk & 3) * 32;
+            tc_mma_bf16(tmem_base + C::S_COL + sb * kKeys, sw128_kmajor_desc(qa), sw128_kmajor_desc(ka),
+                        id_s, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&s_full[sb]);
+          if (walk_last(w)) tc_commit(q_empty);
+        }
+        if (j > 0) {
+          // PV of the previous unit into O of its half; the first unit of each half in
+          // a segment starts the accumulator (after both O of the last segment were read)
+          const int jp = j - 1, st = jp % kAttnStages, pb = jp & 1;
+          const bool start = jp < prev_jf + 2;
+          if (!mbar_wait(&p_full[pb], (jp >> 1) & 1, p.max_spin)) ok = false;
+          if (ok && start && prev_seg > 0 && !mbar_wait(o_free, (prev_seg - 1) & 1, p.max_spin)) ok = false;
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t p_addr = smem_u32(sP + pb * C::P_BYTES);
+          const uint32_t v_addr = smem_u32(sKV + st * C::STAGE + C::KV_TILE);
 #pragma unroll
-      for (int ks = 0; ks < HD / 16; ++ks) {
-#pragma unroll
-        for (int ntp = 0; ntp < 4; ++ntp) {
-          const int key = ntp * 16 + (mi >> 1) * 8 + rr;
-          const int ch = ks * 2 + (mi & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(ksm + key * C::ROW_BYTES + swz(key, ch), b0, b1, b2, b3);
-          mma_bf16(sc[2 * ntp], qf[ks], b0, b1);
-          mma_bf16(sc[2 * ntp + 1], qf[ks], b2, b3);
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            tc_mma_bf16(tmem_base + C::O_COL + pb * HD, sw128_kmajor_desc(p_addr + kk * 32),
+                        sw128_mnmajor_desc(v_addr + kk * 16 * 128, C::ATOM_KV), id_pv,
+                        (!start || kk > 0) ? 1u : 0u);
+          tc_commit(&o_done[pb]);
+          tc_commit(&p_empty[pb]);
+          tc_commit(&kv_empty[st]);
+        }
+        if (j < nunits) {
+          prev_jf = jf;
+          prev_seg = w.seg;
+          walk_next(w, p);
         }
       }
-      // mask keys beyond the valid count, then online softmax update
-      float mx0 = -FLT_MAX, mx1 = -FLT_MAX;
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const int k0 = n * 8 + (lane & 3) * 2;
-        if (k0 >= nv) sc[n][0] = sc[n][2] = -FLT_MAX;
-        if (k0 + 1 >= nv) sc[n][1] = sc[n][3] = -FLT_MAX;
-        mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
-        mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
+      if (!ok) flag_status(p.status, kStatusTimeout);
+      // Every issued MMA must complete before TMEM is freed (bounded).
+      tc_commit(mma_done);
+      mbar_wait(mma_done, 0, kAttnDrainSpin);
+    }
+  } else if ((warp & 3) < NQ) {
+    // ---------------- softmax warps: half h = warp / 4 takes units j % 2 == h; thread r
+    // of a half owns query row r = TMEM lane r
+    const int half = warp >> 2;
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const bool real = r < R;
+    const bool warp_real = q * 32 < R;
+    const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t o_mine = trow + C::O_COL + half * HD;
+    const float sl2 = rsqrtf(static_cast<float>(HD)) * 1.4426950408889634f;
+    // row r of the Q tile is block position r / G of query head g * G + r % G
+    const int jq = r / G, hq = r % G;
+    AttnWalk w = w0;
+    float m_run = -FLT_MAX, l_run = 0.f;
+    bool ok = true;
+    int jf = 0;
+    for (int j = 0; j < nunits && ok; ++j) {
+      const int st = j % kAttnStages;
+      if (walk_first(w)) {
+        jf = j;
+        m_run = -FLT_MAX;
+        l_run = 0.f;
       }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = exp2f((m0 - mn0) * sl2), al1 = exp2f((m1 - mn1) * sl2);
-      m0 = mn0;
-      m1 = mn1;
-      l0 *= al0;
-      l1 *= al1;
+      if ((j & 1) == half) {
+        const bool first = j < jf + 2;  // first unit of this half in the segment
+        const int nv = min(kKeys, w.L - w.unit * kKeys);
+        ok = mbar_wait(&s_full[half], (j >> 1) & 1, p.max_spin);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sv[kKeys];
+        if (warp_real) {
+          float t0[32], t1[32];
+          tmem_ld32(trow + C::S_COL + half * kKeys, t0);
+          tmem_ld32(trow + C::S_COL + half * kKeys + 32, t1);
 #pragma unroll
-      for (int n = 0; n < HD / 8; ++n) {
-        o[n][0] *= al0;
-        o[n][1] *= al0;
-        o[n][2] *= al1;
-        o[n][3] *= al1;
+          for (int c = 0; c < 32; ++c) {
+            sv[c] = t0[c];
+            sv[c + 32] = t1[c];
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&s_empty[half]);
+
+        bool need = false;
+        float alpha = 1.f;
+        if (warp_real) {
+          if (nv < kKeys) {
+#pragma unroll
+            for (int c = 0; c < kKeys; ++c) sv[c] = c < nv ? sv[c] : -FLT_MAX;
+          }
+          float m8[8];
+#pragma unroll
+          for (int a = 0; a < 8; ++a) m8[a] = fmaxf(sv[a], sv[a + 8]);
+#pragma unroll
+          for (int c = 16; c < kKeys; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
+          const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          need = real && (mx - m_run) * sl2 > kRescaleLog2;
+          if (need) {
+            alpha = ex2_approx((m_run - mx) * sl2);
+            m_run = mx;
+            l_run *= alpha;
+          }
+        }
+        if (!first && __any_sync(0xffffffffu, need)) {
+          // O_h *= alpha once PV of this half's previous unit has completed
+          ok = mbar_wait(&o_done[half], ((j >> 1) - 1) & 1, p.max_spin);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            float ov[32];
+            tmem_ld32(o_mine + cc * 32, ov);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] *= alpha;
+            tmem_st32(o_mine + cc * 32, ov);
+          }
+        }
+        // P buffer `half` is free once PV of this half's previous unit has completed
+        ok = j < 2 || mbar_wait(&p_empty[half], ((j >> 1) - 1) & 1, p.max_spin);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        if (real) {
+          uint32_t pk[kKeys / 2];
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+          const float mb = m_run * sl2;
+#pragma unroll
+          for (int c = 0; c < kKeys; c += 2) {
+            const float p0 = ex2_approx(fmaf(sv[c], sl2, -mb));
+            const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, -mb));
+            ls[(c >> 1) & 3] += p0 + p1;
+            pk[c >> 1] = pack_bf16x2(p0, p1);
+          }
+          l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          uint8_t *prow = sP + half * C::P_BYTES + r * 128;
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16)
+            *reinterpret_cast<uint4 *>(prow + ((c16 ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+        }
+        if (nv < kKeys) {
+          // V rows beyond the last key may hold anything (even NaN): zero them, P is 0 there.
+          ok = mbar_wait(&kv_full[st], (j / kAttnStages) & 1, p.max_spin);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          uint8_t *vt = sKV + st * C::STAGE + C::KV_TILE;
+          const int nz = (kKeys - nv) * 8;  // 16-byte chunks per atom
+          for (int e = r; e < C::ATOMS * nz; e += HT) {
+            const int a = e / nz, x = e % nz;
+            *reinterpret_cast<uint4 *>(vt + a * C::ATOM_KV + nv * 128 + x * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[half]);
       }
-      uint32_t pa[4][4];
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const int k0 = n * 8 + (lane & 3) * 2;
-        const float p0 = (k0 < nv) ? exp2f((sc[n][0] - mn0) * sl2) : 0.f;
-        const float p1 = (k0 + 1 < nv) ? exp2f((sc[n][1] - mn0) * sl2) : 0.f;
-        const float p2 = (k0 < nv) ? exp2f((sc[n][2] - mn1) * sl2) : 0.f;
-        const float p3 = (k0 + 1 < nv) ? exp2f((sc[n][3] - mn1) * sl2) : 0.f;
-        l0 += p0 + p1;
-        l1 += p2 + p3;
-        const int kk = n >> 1;
-        if ((n & 1) == 0) {
-          pa[kk][0] = pack_bf16x2(p0, p1);
-          pa[kk][1] = pack_bf16x2(p2, p3);
+
+      if (walk_last(w)) {
+        // segment [jf, j]: the last unit of each half in it, or -1
+        const int seg = w.seg;
+        const int last_h[2] = {(j & 1) == 0 ? j : (j - 1 >= jf ? j - 1 : -1),
+                               (j & 1) == 1 ? j : (j - 1 >= jf ? j - 1 : -1)};
+        if (half == 1) {
+          // hand (max, sum) to half 0 once O_1 is final; the slot is free once half 0
+          // has read the previous segment's
+          ok = seg == 0 || mbar_wait(o_free, (seg - 1) & 1, p.max_spin);
+          if (ok && last_h[1] >= 0) ok = mbar_wait(&o_done[1], (last_h[1] >> 1) & 1, p.max_spin);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          ml1[r] = last_h[1] >= 0 ? make_float2(m_run, l_run) : make_float2(-FLT_MAX, 0.f);
+          tc_fence_before();
+          mbar_arrive(ml_ready);
         } else {
-          pa[kk][2] = pack_bf16x2(p0, p1);
-          pa[kk][3] = pack_bf16x2(p2, p3);
+          ok = last_h[0] < 0 || mbar_wait(&o_done[0], (last_h[0] >> 1) & 1, p.max_spin);
+          if (ok) ok = mbar_wait(ml_ready, seg & 1, p.max_spin);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float2 o1 = ml1[r];
+          const bool has0 = last_h[0] >= 0, has1 = last_h[1] >= 0;
+          const float m0 = has0 ? m_run : -FLT_MAX;
+          const float M = fmaxf(m0, o1.x);
+          const float a0 = has0 ? ex2_approx((m0 - M) * sl2) : 0.f;
+          const float a1 = has1 ? ex2_approx((o1.x - M) * sl2) : 0.f;
+          const float L = (has0 ? l_run * a0 : 0.f) + o1.y * a1;
+          const bool whole = w.seg_unit0 == 0 && w.unit == w.U - 1;
+          const int i = w.pair / p.Hkv, g = w.pair % p.Hkv;
+          const int slot = w.pair + static_cast<int>(blockIdx.x);
+          const float inv = 1.0f / L;
+          if (warp_real) {
+#pragma unroll 1
+            for (int cc = 0; cc < HD / 32; ++cc) {
+              float ov[32], o1v[32];
+              if (has0) tmem_ld32(trow + C::O_COL + cc * 32, ov);
+              if (has1) tmem_ld32(trow + C::O_COL + HD + cc * 32, o1v);
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                ov[c] = (has0 ? ov[c] * a0 : 0.f) + (has1 ? o1v[c] * a1 : 0.f);
+              if (!real) continue;
+              if (whole) {
+                uint16_t *dst = p.o + ((size_t)i * p.B + jq) * ((size_t)p.Hq * HD) +
+                                (size_t)(g * G + hq) * HD + cc * 32;
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                  reinterpret_cast<uint4 *>(dst)[v] =
+                      make_uint4(pack_bf16x2(ov[8 * v] * inv, ov[8 * v + 1] * inv),
+                                 pack_bf16x2(ov[8 * v + 2] * inv, ov[8 * v + 3] * inv),
+                                 pack_bf16x2(ov[8 * v + 4] * inv, ov[8 * v + 5] * inv),
+                                 pack_bf16x2(ov[8 * v + 6] * inv, ov[8 * v + 7] * inv));
+              } else {
+                float *dst = p.part_o + ((size_t)slot * R + r) * HD + cc * 32;
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                  reinterpret_cast<float4 *>(dst)[v] =
+                      make_float4(ov[4 * v], ov[4 * v + 1], ov[4 * v + 2], ov[4 * v + 3]);
+              }
+            }
+          }
+          if (real && !whole)
+            *reinterpret_cast<float2 *>(p.part_ml + ((size_t)slot * R + r) * 2) = make_float2(M, L);
+          tc_fence_before();
+          mbar_arrive(o_free);
         }
       }
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        if (kk * 16 >= nv) break;
-#pragma unroll
-        for (int ndp = 0; ndp < HD / 16; ++ndp) {
-          const int key = kk * 16 + (mi & 1) * 8 + rr;
-          const int ch = ndp * 2 + (mi >> 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vsm + key * C::ROW_BYTES + swz(key, ch), b0, b1, b2, b3);
-          mma_bf16(o[2 * ndp], pa[kk], b0, b1);
-          mma_bf16(o[2 * ndp + 1], pa[kk], b2, b3);
-        }
-      }
+      walk_next(w, p);
     }
-    __syncthreads();
+    if (!ok) flag_status(p.status, kStatusTimeout);
   }
-  cp_async_wait<0>();
 
-  if (active) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const size_t pbase = (((size_t)i * p.Hkv + g) * p.splits + s) * nrows;
-    const int r0 = wrow0 + (lane >> 2), r1 = r0 + 8;
-    const int c = (lane & 3) * 2;
-    if (r0 < nrows) {
-      float *dst = p.part_o + (pbase + r0) * HD;
-#pragma unroll
-      for (int n = 0; n < HD / 8; ++n)
-        *reinterpret_cast<float2 *>(dst + n * 8 + c) = make_float2(o[n][0], o[n][1]);
-      if ((lane & 3) == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + r0) * 2) = make_float2(m0, l0);
-    }
-    if (r1 < nrows) {
-      float *dst = p.part_o + (pbase + r1) * HD;
-#pragma unroll
-      for (int n = 0; n < HD / 8; ++n)
-        *reinterpret_cast<float2 *>(dst + n * 8 + c) = make_float2(o[n][2], o[n][3]);
-      if ((lane & 3) == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + r1) * 2) = make_float2(m1, l1);
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == Ro::MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
-// Combine the splits of one (sequence, kv head) in split order and write o (bf16).
-// One warp per query row; each lane owns HD/32 consecutive output elements, so the
-// partial rows are read with vector loads and the split weights are computed once
-// per row.
+// Combine the partials of every pair whose units were split over several CTAs, in CTA
+// order, and write o (bf16). One CTA per (pair, 8 query rows); one warp per row; each
+// lane owns hd/32 consecutive output elements.
 constexpr int kMergeWarps = 8;
 
 template <int HD>
@@ -303,77 +606,80 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   constexpr int E = HD / 32;
   griddep_wait();
   griddep_launch();
-  const int g = blockIdx.y, i = blockIdx.z;
+  const int pair = blockIdx.x;
+  const int i = pair / p.Hkv, g = pair % p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = p.Hq / p.Hkv;
-  const int nrows = grp * p.B;
-  const int t = blockIdx.x * kMergeWarps + warp;
-  if (t >= nrows) return;
-  const int ctx_used = max(0, min(p.ctx_len[i], min(p.max_ctx, p.Cmax)));
-  const int nsplit = max(1, (ctx_used + p.chunk - 1) / p.chunk);
+  const int G = p.Hq / p.Hkv;
+  const int R = G * p.B;
+  const int r = blockIdx.y * kMergeWarps + warp;
+  if (r >= R) return;
+  const long long T = attn_units_before(p, p.nb, lane);
+  const int Ge = T < p.grid ? static_cast<int>(T) : p.grid;
+  const int U = attn_units(p, i);
+  const long long A = attn_units_before(p, i, lane) + (long long)g * U;
+  const int c0 = attn_cta_of(T, Ge, A), c1 = attn_cta_of(T, Ge, A + U - 1);
+  if (c0 == c1) return;  // written whole by the attention kernel
   const float sl2 = rsqrtf(static_cast<float>(HD)) * 1.4426950408889634f;
-  const size_t pbase = ((size_t)i * p.Hkv + g) * p.splits * nrows + t;
-  float M = -FLT_MAX;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.part_ml[(pbase + (size_t)s * nrows) * 2]);
-  float L = 0.f, acc[E];
+  {
+    float M = -FLT_MAX;
+    for (int c = c0; c <= c1; ++c) M = fmaxf(M, p.part_ml[((size_t)(pair + c) * R + r) * 2]);
+    float L = 0.f, acc[E];
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
-    const size_t r = pbase + (size_t)s * nrows;
-    const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + r * 2);
-    const float wgt = exp2f((ml.x - M) * sl2);
-    L += ml.y * wgt;
-    const float *src = p.part_o + r * HD + lane * E;
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int c = c0; c <= c1; ++c) {
+      const size_t row = (size_t)(pair + c) * R + r;
+      const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + row * 2);
+      const float wgt = exp2f((ml.x - M) * sl2);
+      L += ml.y * wgt;
+      const float *src = p.part_o + row * HD + lane * E;
+      if constexpr (E == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(src);
+        acc[0] += v.x * wgt;
+        acc[1] += v.y * wgt;
+        acc[2] += v.z * wgt;
+        acc[3] += v.w * wgt;
+      } else {
+        const float2 v = *reinterpret_cast<const float2 *>(src);
+        acc[0] += v.x * wgt;
+        acc[1] += v.y * wgt;
+      }
+    }
+    const float inv = 1.0f / L;
+    const int jq = r / G, hq = r % G;
+    uint16_t *dst = p.o + ((size_t)i * p.B + jq) * ((size_t)p.Hq * HD) + (size_t)(g * G + hq) * HD + lane * E;
     if constexpr (E == 4) {
-      const float4 v = *reinterpret_cast<const float4 *>(src);
-      acc[0] += v.x * wgt;
-      acc[1] += v.y * wgt;
-      acc[2] += v.z * wgt;
-      acc[3] += v.w * wgt;
+      *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                   pack_bf16x2(acc[2] * inv, acc[3] * inv));
     } else {
-      const float2 v = *reinterpret_cast<const float2 *>(src);
-      acc[0] += v.x * wgt;
-      acc[1] += v.y * wgt;
+      *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     }
   }
-  const float inv = 1.0f / L;
-  const int hh = t / p.B, j = t % p.B;
-  uint16_t *dst = p.o + ((size_t)i * p.B + j) * (p.Hq * HD) + (size_t)(g * grp + hh) * HD + lane * E;
-  if constexpr (E == 4) {
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
-                                                 pack_bf16x2(acc[2] * inv, acc[3] * inv));
-  } else {
-    *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  }
 }
 
-size_t attention_partial_bytes(int nb, int Hq, int Hkv, int hd, int B, int splits) {
-  const size_t rows = (size_t)(Hq / Hkv) * B;
-  return (size_t)nb * Hkv * splits * rows * ((size_t)hd + 2) * sizeof(float);
-}
-
-template <int HD>
-static cudaError_t launch_attn_hd(const AttnParams &p, cudaStream_t s) {
+template <int HD, int NQ>
+static cudaError_t launch_attn(const AttnParams &p, cudaStream_t s) {
   using C = AttnCfg<HD>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<HD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  dim3 grid(p.splits, p.Hkv, p.nb);
-  cudaError_t e = launch_pdl(attn_split_kernel<HD>, grid, dim3(kAttnThreads), C::SMEM, s, p);
+  static const cudaError_t configured = cudaFuncSetAttribute(
+      attn_tc_kernel<HD, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (configured != cudaSuccess) return configured;
+  cudaError_t e = launch_pdl(attn_tc_kernel<HD, NQ>, dim3(p.grid), dim3(AttnRoles<NQ>::THREADS), C::SMEM,
+                             s, p);
   if (e != cudaSuccess) return e;
-  const int nrows = (p.Hq / p.Hkv) * p.B;
-  dim3 mgrid((nrows + kMergeWarps - 1) / kMergeWarps, p.Hkv, p.nb);
-  return launch_pdl(attn_merge_kernel<HD>, mgrid, dim3(kMergeWarps * 32), 0, s, p);
+  const int R = (p.Hq / p.Hkv) * p.B;
+  return launch_pdl(attn_merge_kernel<HD>, dim3(p.nb * p.Hkv, (R + kMergeWarps - 1) / kMergeWarps),
+                    dim3(kMergeWarps * 32), 0, s, p);
 }
 
 cudaError_t launch_attention(const AttnParams &p, cudaStream_t s) {
-  if (p.hd == 128) return launch_attn_hd<128>(p, s);
-  if (p.hd == 64) return launch_attn_hd<64>(p, s);
-  return cudaErrorInvalidValue;
+  if (p.Hq % p.Hkv != 0) return cudaErrorInvalidValue;
+  const int R = (p.Hq / p.Hkv) * p.B;
+  if (R > kQRows) return cudaErrorInvalidValue;
+  const bool wide = R > 64;
+  switch (p.hd) {
+    case 64: return wide ? launch_attn<64, 4>(p, s) : launch_attn<64, 2>(p, s);
+    case 128: return wide ? launch_attn<128, 4>(p, s) : launch_attn<128, 2>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace df

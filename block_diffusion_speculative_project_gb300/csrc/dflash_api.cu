@@ -132,25 +132,9 @@ struct dflash_handle_s {
   std::vector<CUtensorMap> tm_c0, tm_c1;  // [layer*4 + which]
   float inv_freq[64];
   WsLayout ws;
-  int max_attn_ctas = 2048;
 };
 
 namespace {
-
-int attn_chunk(const dflash_handle_s *h, int nb, int max_ctx, int *splits_out) {
-  const auto &c = h->cfg;
-  const int pairs = std::max(1, nb * c.Hkv);
-  const int want = std::max(1, (2 * 2 * h->num_sms + pairs - 1) / pairs);
-  int chunk = (std::max(1, max_ctx) + want - 1) / want;
-  chunk = std::max(64, (chunk + 63) / 64 * 64);
-  int splits = std::max(1, (max_ctx + chunk - 1) / chunk);
-  while ((long long)splits * pairs > h->max_attn_ctas && splits > 1) {
-    chunk += 64;
-    splits = std::max(1, (max_ctx + chunk - 1) / chunk);
-  }
-  *splits_out = splits;
-  return chunk;
-}
 
 void plan_workspace(dflash_handle_s *h) {
   const auto &c = h->cfg;
@@ -159,7 +143,7 @@ void plan_workspace(dflash_handle_s *h) {
   const int Mp = c.max_batch * c.max_proj_rows;         // projection rows
   const int Ml = c.max_batch * (c.B - 1);               // LM-head rows
   const int qkv_n = (c.Hq + 2 * c.Hkv) * c.hd;
-  const size_t apart_max = (size_t)h->max_attn_ctas + (size_t)c.max_batch * c.Hkv;  // CTA bound
+  const size_t apart_max = attention_slots(c.max_batch, c.Hkv, h->num_sms);
   const size_t rows_attn = (size_t)(c.Hq / c.Hkv) * c.B;
 
   size_t off = 0;
@@ -242,6 +226,38 @@ size_t cache_layer_elems(const dflash_config &c) {
   return (size_t)c.max_batch * c.Hkv * c.Cmax * c.hd;
 }
 
+// Attention launch parameters for nb sequences: q rows of stride ldq (elements) with
+// the queries in their first Hq*hd columns, caches of every layer, output o.
+int attention_params(const dflash_handle_s *h, const Ws &w, int nb, const void *q, int ldq,
+                     const void *kcache, const void *vcache, const int32_t *ctx_len, int max_ctx,
+                     void *o, AttnParams *out) {
+  const auto &c = h->cfg;
+  AttnParams &ap = *out;
+  DF_TRY(encode_3d(&ap.tmQ, q, c.hd, c.Hq, (uint64_t)nb * c.B, c.hd, ldq, c.Hq / c.Hkv, c.B));
+  const uint64_t cache_rows = (uint64_t)c.N * c.max_batch * c.Hkv * c.Cmax;
+  DF_TRY(encode_2d(&ap.tmK, kcache, cache_rows, c.hd, c.hd, 64));
+  DF_TRY(encode_2d(&ap.tmV, vcache, cache_rows, c.hd, c.hd, 64));
+  ap.ctx_len = ctx_len;
+  ap.o = static_cast<uint16_t *>(o);
+  ap.part_o = w.at<float>(h->ws.apart);
+  ap.part_ml = w.at<float>(h->ws.aml);
+  ap.nb = nb;
+  ap.B = c.B;
+  ap.Hq = c.Hq;
+  ap.Hkv = c.Hkv;
+  ap.hd = c.hd;
+  ap.Cmax = c.Cmax;
+  ap.max_batch = c.max_batch;
+  ap.max_ctx = max_ctx;
+  ap.grid = h->num_sms;
+  ap.status = w.status();
+  ap.max_spin = c.max_spin;
+  ap.stall = (c.flags & DFLASH_FLAG_TEST_STALL) ? 1 : 0;
+  if (attention_slots(nb, c.Hkv, ap.grid) > h->ws.apart_ctas)
+    return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "attention partials exceed the workspace plan");
+  return DFLASH_OK;
+}
+
 // One DFlash 2 conv on the fp32 residual rows x [M, D].
 int run_conv(const dflash_handle_s *h, const Ws &w, int layer, int which, int M, float *x,
              cudaStream_t s) {
@@ -317,8 +333,11 @@ int dflash_create(const dflash_config *cfg, dflash_handle_t *out) {
   if (c.hd != 64 && c.hd != 128) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "hd must be 64 or 128");
   if (c.Hq % c.Hkv) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "Hq must be a multiple of Hkv");
   if (c.B < 2 || c.B > 16) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "B must be in 2..16");
-  if ((c.Hq / c.Hkv) * c.B > 64)
-    return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "(Hq/Hkv)*B must be <= 64 (query rows per kv head)");
+  if ((c.Hq / c.Hkv) * c.B > 128)
+    return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "(Hq/Hkv)*B must be <= 128 (query rows per kv head)");
+  if (c.Cmax <= c.B) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "Cmax must exceed B");
+  if ((long long)c.N * c.max_batch * c.Hkv * c.Cmax >= (1LL << 31))
+    return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "N*max_batch*Hkv*Cmax cache rows must be < 2^31");
   if (c.k_top < 1 || c.k_top > kTopkMax) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "k_top must be in 1..16");
   if (c.D % 64 || (c.L * c.Dt) % 64 || (c.Hq * c.hd) % 64 || c.F % 8)
     return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "D, L*Dt, Hq*hd must be multiples of 64 and F of 8");
@@ -479,7 +498,7 @@ int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *hv, const i
 }
 
 int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, const void *x0_relay,
-                       const void *kcache, const void *vcache, const int32_t *ctx_len,
+                       void *kcache, void *vcache, const int32_t *ctx_len,
                        int max_ctx_hint, void *out_hidden, void *ws, size_t ws_bytes,
                        dflash_stream_t stream) {
   if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
@@ -498,7 +517,7 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
   const bool conv = (c.flags & DFLASH_FLAG_CONV) != 0;
   const int M = nb * c.B;
   const int qkv_n = (c.Hq + 2 * c.Hkv) * c.hd;
-  const int max_ctx = max_ctx_hint > 0 ? max_ctx_hint : c.Cmax;
+  const int max_ctx = max_ctx_hint > 0 ? std::min(max_ctx_hint, c.Cmax - c.B) : c.Cmax - c.B;
   float *x = w.at<float>(h->ws.x);
   uint16_t *u = w.at<uint16_t>(h->ws.u);
   uint16_t *qkv = w.at<uint16_t>(h->ws.qkv);
@@ -513,23 +532,7 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
   DF_CUDA(launch_embed_rmsnorm(block_ids, bf(h->w.E), static_cast<const uint16_t *>(x0_relay), M, c.D,
                                c.V, x, conv ? nullptr : bf(h->layers[0].g_attn), c.eps, u, w.status(), s));
   AttnParams ap{};
-  ap.qkv = qkv;
-  ap.ctx_len = ctx_len;
-  ap.o = o;
-  ap.part_o = w.at<float>(h->ws.apart);
-  ap.part_ml = w.at<float>(h->ws.aml);
-  ap.nb = nb;
-  ap.B = c.B;
-  ap.Hq = c.Hq;
-  ap.Hkv = c.Hkv;
-  ap.hd = c.hd;
-  ap.Cmax = c.Cmax;
-  ap.max_batch = c.max_batch;
-  ap.max_ctx = max_ctx;
-  ap.status = w.status();
-  ap.chunk = attn_chunk(h, nb, max_ctx, &ap.splits);
-  if ((size_t)nb * c.Hkv * ap.splits > h->ws.apart_ctas)
-    return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "attention partials exceed the workspace plan");
+  DF_TRY(attention_params(h, w, nb, qkv, qkv_n, kcache, vcache, ctx_len, max_ctx, o, &ap));
 
   for (int n = 0; n < c.N; ++n) {
     const dflash_layer_weights &Lw = h->layers[n];
@@ -539,7 +542,9 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
     } else if (n > 0) {
       DF_CUDA(launch_rmsnorm(x, M, c.D, bf(Lw.g_attn), c.eps, u, s));
     }
-    {  // q | k_b | v_b with RoPE on q and k_b at positions ctx_len + j
+    uint16_t *kc_n = static_cast<uint16_t *>(kcache) + n * cache_layer_elems(c);
+    uint16_t *vc_n = static_cast<uint16_t *>(vcache) + n * cache_layer_elems(c);
+    {  // q -> qkv buffer; k_b, v_b -> cache rows ctx_len + j; RoPE on q and k_b
       GemmParams p = base_params(h, w);
       p.tmA = tm_u;
       p.tmB[0] = h->tm_qkv[n];
@@ -552,10 +557,14 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
       p.ctx_len = ctx_len;
       p.rows_per_seq = c.B;
       p.rope_cols = (c.Hq + c.Hkv) * c.hd;
+      p.q_cols = c.Hq * c.hd;
+      p.kc = kc_n;
+      p.vc = vc_n;
+      p.Hkv = c.Hkv;
+      p.Cmax = c.Cmax;
       DF_TRY(run_gemm(h, p, kBN, s));
     }
-    ap.kc = static_cast<const uint16_t *>(kcache) + n * cache_layer_elems(c);
-    ap.vc = static_cast<const uint16_t *>(vcache) + n * cache_layer_elems(c);
+    ap.layer_row0 = n * c.max_batch * c.Hkv * c.Cmax;
     DF_CUDA(launch_attention(ap, s));
     {  // x += o W_O^T
       GemmParams p = base_params(h, w);
@@ -704,6 +713,27 @@ int dflash_lm_head_topk_noalloc(dflash_handle_t h, int nb, const void *hidden, i
   if (p.items / p.m_tiles != ranges) return fail(DFLASH_ERR_CUDA, "LM-head range plan mismatch");
   DF_CUDA(launch_topk_merge(p.part_vals, p.part_ids, Ml, k, k, (long long)Ml * k, ranges, k, out_ids,
                             out_vals, s));
+  return DFLASH_OK;
+}
+
+int dflash_attention(dflash_handle_t h, int nb, int layer, const void *q, const void *kcache,
+                     const void *vcache, const int32_t *ctx_len, int max_ctx_hint, void *out_o, void *ws,
+                     size_t ws_bytes, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+  const auto &c = h->cfg;
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (layer < 0 || layer >= c.N) return fail(DFLASH_ERR_INVALID_ARG, "layer=%d outside [0, N)", layer);
+  if (max_ctx_hint < 0 || max_ctx_hint > c.Cmax)
+    return fail(DFLASH_ERR_INVALID_ARG, "max_ctx_hint=%d outside [0, Cmax]", max_ctx_hint);
+  if (nb == 0) return DFLASH_OK;
+  if (!q || !kcache || !vcache || !ctx_len || !out_o) return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor");
+  DF_TRY(check_ws(h, ws, ws_bytes));
+  Ws w{static_cast<uint8_t *>(ws), h->ws};
+  const int max_ctx = max_ctx_hint > 0 ? std::min(max_ctx_hint, c.Cmax - c.B) : c.Cmax - c.B;
+  AttnParams ap{};
+  DF_TRY(attention_params(h, w, nb, q, c.Hq * c.hd, kcache, vcache, ctx_len, max_ctx, out_o, &ap));
+  ap.layer_row0 = layer * c.max_batch * c.Hkv * c.Cmax;
+  DF_CUDA(launch_attention(ap, stream));
   return DFLASH_OK;
 }
 

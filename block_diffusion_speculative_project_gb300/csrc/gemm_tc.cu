@@ -253,20 +253,40 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
     }
   } else if constexpr (EPI == EPI_ROPE) {
     const int half = p.hd >> 1;
-    int pos = 0;
-    if (row_ok) pos = p.ctx_len[row / p.rows_per_seq] + row % p.rows_per_seq;
+    int seq = 0, pos = 0;
+    bool pos_ok = false;
+    if (row_ok) {
+      seq = row / p.rows_per_seq;
+      pos = p.ctx_len[seq] + row % p.rows_per_seq;
+      pos_ok = pos >= 0 && pos < p.Cmax;
+    }
 #pragma unroll 1
     for (int h0 = 0; h0 < BN; h0 += p.hd) {
       const int gcol = t.n * BN + h0;
       const bool rot = gcol < p.rope_cols;
+      // destination row of this head: the q part of the qkv buffer, or the block's
+      // cache row ctx_len + j of a k / v head
+      uint16_t *o = nullptr;
+      if (row_ok && gcol < p.N) {
+        if (gcol < p.q_cols) {
+          o = static_cast<uint16_t *>(p.out) + row * p.ldo + gcol;
+        } else if (pos_ok) {
+          const int kvh = (gcol - p.q_cols) / p.hd;  // 0..2*Hkv-1
+          const bool isv = kvh >= p.Hkv;
+          const int head = isv ? kvh - p.Hkv : kvh;
+          o = static_cast<uint16_t *>(isv ? p.vc : p.kc) +
+              (((size_t)seq * p.Hkv + head) * p.Cmax + pos) * (size_t)p.hd;
+        } else {
+          flag_status(p.status, kStatusCheck);
+        }
+      }
 #pragma unroll 1
       for (int cc = 0; cc < half; cc += 32) {
         float a[32], b[32];
         fetch((h0 + cc) >> 5, a);
         fetch((h0 + half + cc) >> 5, b);
-        if (row_ok && gcol < p.N) {
+        if (o) {
           if (rot) rope_pair(p, pos, cc, a, b);
-          uint16_t *o = static_cast<uint16_t *>(p.out) + row * p.ldo + gcol;
           store_bf16_32(o + cc, a, 32);
           store_bf16_32(o + half + cc, b, 32);
         }

@@ -59,7 +59,9 @@ enum GemmEpi : int {
   EPI_BF16 = 0,   // out bf16 [M, ldo] = acc
   EPI_F32 = 1,    // out f32  [M, ldo] = acc
   EPI_RESID = 2,  // xres f32 [M, ldo] += acc
-  EPI_ROPE = 3,   // out bf16 = RoPE(acc) on columns < rope_cols (per hd-wide head)
+  EPI_ROPE = 3,   // q|k|v of the block: RoPE on columns < rope_cols (per hd-wide head);
+                  // columns < q_cols to out bf16, the k and v heads to the layer's
+                  // caches kc / vc at rows ctx_len + j
   EPI_SWIGLU = 4, // dual: out bf16 [M, ldo] = silu(acc_gate) * acc_up
   EPI_DUAL_F32 = 5, // dual: out f32 [M, ldo]: cols [0,N) from B0, [N,2N) from B1
   EPI_KV = 6,     // grouped: scatter rows into the K/V caches (RoPE on K groups)
@@ -93,9 +95,11 @@ struct GemmParams {
   const int *ctx_len;
   int rows_per_seq;
   int rope_cols;
+  int q_cols;      // EPI_ROPE: columns written to out; the rest are Hkv k then Hkv v heads
   int hd;
   float inv_freq[64];
-  // K/V scatter (EPI_KV): group g -> layer g/2, g%2 == 0 keys (rotated), 1 values
+  // K/V scatter (EPI_KV): group g -> layer g/2, g%2 == 0 keys (rotated), 1 values;
+  // EPI_ROPE: the current layer's caches
   void *kc;
   void *vc;
   const int *n_commit;
@@ -157,22 +161,29 @@ cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, cons
 
 // ---------------------------------------------------------------- attention
 
+// Context attention of one drafter layer (see attention.cu). The block's own K/V rows
+// have already been written to cache rows [ctx_len, ctx_len + B) by the QKV GEMM, so
+// every sequence attends to the ctx_len + B contiguous cache rows of its heads.
 struct AttnParams {
-  const uint16_t *qkv;  // [nb*B, (Hq+2Hkv)*hd] bf16, q and k_b already rotated
-  const uint16_t *kc;   // cache base of this layer: [max_batch][Hkv][Cmax][hd]
-  const uint16_t *vc;
+  CUtensorMap tmQ;      // qkv buffer as {hd, Hq heads, nb*B rows}, box {64, Hq/Hkv, B}
+  CUtensorMap tmK;      // key cache of every layer as rows of hd: {hd, N*max_batch*Hkv*Cmax}, box {64, 64}
+  CUtensorMap tmV;      // value cache, same shape
   const int *ctx_len;   // [nb]
   uint16_t *o;          // [nb*B, Hq*hd] bf16
-  float *part_o;        // [nb][Hkv][splits][rows][hd]
-  float *part_ml;       // [nb][Hkv][splits][rows][2]
+  float *part_o;        // [slots][G*B rows][hd] unnormalised partial outputs
+  float *part_ml;       // [slots][G*B rows][2] (running max, running sum)
   int nb, B, Hq, Hkv, hd, Cmax, max_batch;
-  int chunk;            // context keys per split (multiple of 64)
-  int splits;           // grid.x
-  int max_ctx;          // bound used for the grid
+  int layer_row0;       // first cache row of this layer: layer * max_batch * Hkv * Cmax
+  int max_ctx;          // caller's bound on ctx_len (larger values are reported and clamped)
+  int grid;             // CTAs of the attention launch (work is split evenly over them)
   int *status;
+  int max_spin;
+  int stall;            // test hook: issue no loads so the waits run out
 };
 
+// Slots of partial outputs the attention of nb sequences may write: at most one per
+// (pair, CTA) boundary, i.e. nb * Hkv + grid.
+inline size_t attention_slots(int nb, int Hkv, int grid) { return (size_t)nb * Hkv + grid; }
 cudaError_t launch_attention(const AttnParams &p, cudaStream_t s);
-size_t attention_partial_bytes(int nb, int Hq, int Hkv, int hd, int B, int splits);
 
 }  // namespace df

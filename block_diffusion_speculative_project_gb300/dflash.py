@@ -72,6 +72,7 @@ def _load():
         "dflash_draft_block": (i, [p, i, p, p, p, p, p, i, p, p, sz, p]),
         "dflash_lm_head_topk": (i, [p, i, p, i, p, p, p, p, sz, p]),
         "dflash_lm_head_topk_noalloc": (i, [p, i, p, i, p, p, p, p]),
+        "dflash_attention": (i, [p, i, i, p, p, p, p, i, p, p, sz, p]),
         "dflash_topk": (i, [p, i, i, p, i, p, p, p, sz, p]),
         "dflash_accept": (i, [p, i, p, p, p, p, p]),
         "dflash2_conv": (i, [p, i, i, i, p, p, sz, p]),
@@ -87,7 +88,7 @@ def _load():
 LIB = _load()
 EXPORTED = ("dflash_create", "dflash_destroy", "dflash_set_weights", "dflash_workspace_size",
             "dflash_status", "dflash_last_error", "dflash_ctx_project", "dflash_draft_block",
-            "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_topk", "dflash_accept", "dflash2_conv", "dflash2_select")
+            "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_attention", "dflash_topk", "dflash_accept", "dflash2_conv", "dflash2_select")
 
 
 def _check(rc: int):
@@ -159,6 +160,13 @@ def dflash_lm_head_topk_noalloc(h, nb, hidden, k, out_ids, out_vals, out_status=
                                 stream=None) -> None:
     _check(LIB.dflash_lm_head_topk_noalloc(h, nb, _ptr(hidden), k, _ptr(out_ids), _ptr(out_vals),
                                            _ptr(out_status), _stream(stream)))
+
+
+def dflash_attention(h, nb, layer, q, kcache, vcache, ctx_len, max_ctx_hint, out_o, ws,
+                     stream=None) -> None:
+    _check(LIB.dflash_attention(h, nb, layer, _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(ctx_len),
+                                max_ctx_hint, _ptr(out_o), _ptr(ws), ws.numel() * ws.element_size(),
+                                _stream(stream)))
 
 
 def dflash_topk(h, rows, cols, logits, k, out_ids, out_vals, ws=None, stream=None) -> None:

@@ -93,6 +93,10 @@ class Drafter:
         _d.dflash2_select(self.h, nb, k, topk_ids, topk_vals, hidden, block_ids, out_path, self.ws,
                           stream)
 
+    def attention(self, nb, layer, q, ctx_len, out_o, max_ctx_hint=0, stream=None):
+        _d.dflash_attention(self.h, nb, layer, q, self.kcache, self.vcache, ctx_len, max_ctx_hint,
+                            out_o, self.ws, stream)
+
     def topk(self, rows, cols, logits, k, out_ids, out_vals, stream=None):
         _d.dflash_topk(self.h, rows, cols, logits, k, out_ids, out_vals, None, stream)
 

@@ -177,13 +177,18 @@ DFLASH_API int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *
  * with CONV a two-tap dynamic conv before and after each sublayer ([DFlash2] 洞察二).
  *   block_ids    int32 [nb, B] token ids (anchor, then mask ids)
  *   x0_relay     bf16 [nb, B, D] or NULL: added to the embeddings (DFlow relay)
- *   ctx_len      int32 [nb]: context rows per sequence (after this round's append)
- *   max_ctx_hint host int: an upper bound on every ctx_len[i] used to size the
- *                attention grid (0 = Cmax). A larger ctx_len is reported as
- *                DFLASH_ERR_DEVICE_CHECK by dflash_status.
+ *   kcache, vcache  the caches: every layer's K_b / V_b (K_b rotated) are written to
+ *                rows [ctx_len[i], ctx_len[i] + B) of sequence i, which the attention
+ *                then reads with the context rows; those rows are scratch (the next
+ *                dflash_ctx_project overwrites the committed ones).
+ *   ctx_len      int32 [nb]: context rows per sequence (after this round's append);
+ *                ctx_len[i] + B must be <= Cmax.
+ *   max_ctx_hint host int: an upper bound on every ctx_len[i] (0 = Cmax - B). A
+ *                ctx_len[i] above min(hint, Cmax - B), or negative, is reported as
+ *                DFLASH_ERR_DEVICE_CHECK by dflash_status (and clamped).
  *   out_hidden   bf16 [nb, B, D]: final RMSNorm output (input of the LM head). */
 DFLASH_API int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, const void *x0_relay,
-                       const void *kcache, const void *vcache, const int32_t *ctx_len,
+                       void *kcache, void *vcache, const int32_t *ctx_len,
                        int max_ctx_hint, void *out_hidden, void *ws, size_t ws_bytes,
                        dflash_stream_t stream);
 
@@ -219,6 +224,22 @@ DFLASH_API int dflash_lm_head_topk(dflash_handle_t h, int nb, const void *hidden
 DFLASH_API int dflash_lm_head_topk_noalloc(dflash_handle_t h, int nb, const void *hidden, int k,
                                            int32_t *out_ids, float *out_vals, int32_t *out_status,
                                            dflash_stream_t stream);
+
+/* The drafter layer's context attention alone ([DFlash] 二、块扩散草稿 attention
+ * equations): the stage dflash_draft_block runs between its QKV and O GEMMs, exposed
+ * for stage-wise checks on given q, K and V.
+ *   layer      0..N-1: the layer whose cache rows are read
+ *   q          bf16 [nb, B, Hq, hd]: rotated queries of the block rows
+ *   kcache, vcache  the caches; sequence i attends to rows [0, ctx_len[i] + B) of its
+ *              kv head in layer `layer` (context rows, then the block's own K_b / V_b at
+ *              rows ctx_len[i] + j, where dflash_draft_block writes them); no mask
+ *   ctx_len, max_ctx_hint  as for dflash_draft_block
+ *   out_o      bf16 [nb, B, Hq, hd]: softmax(q K^T / sqrt(hd)) V, query head h reading
+ *              kv head h / (Hq/Hkv) */
+DFLASH_API int dflash_attention(dflash_handle_t h, int nb, int layer, const void *q,
+                                const void *kcache, const void *vcache, const int32_t *ctx_len,
+                                int max_ctx_hint, void *out_o, void *ws, size_t ws_bytes,
+                                dflash_stream_t stream);
 
 /* Top-k of each row of an fp32 matrix with the same ordering rule as
  * dflash_lm_head_topk (value descending, ties to the lower column).

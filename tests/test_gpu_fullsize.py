@@ -7,10 +7,15 @@ Stage-wise checks, where both sides consume the same inputs, use the stated tole
 LM-head logits and the top-k (oracle logits from the GPU's own bf16 hidden), the
 selector (GPU candidates and hidden) and accept (exact). The end-to-end drafter
 hidden after N = 5 layers at D = 2560..4096 carries the bf16 storage error of about
-20 rounding points; an exact bf16-rounding model of the same computation deviates
-from fp64 by up to 0.046 at the 4B shape. That comparison uses the derived bound
-HIDDEN_ATOL + HIDDEN_RTOL|o| and additionally requires the stated tolerance to hold
-for at least 95% of the elements.
+20 rounding points. tests/bf16_storage_model.py rounds the fp64 oracle to bf16 at exactly
+the kernel path's storage points; on the sampled sequences of these workloads it deviates
+from fp64 by max 0.044-0.072, max |err|/(1+|o|) 0.034-0.056, mean 0.0083-0.0098, with
+96.0-98.5% of elements within the stated tolerance. The GPU adds an independent rounding
+noise of the same size (its pre-rounding values are fp32, not fp64, so some bf16 roundings
+land on the other side; RoPE angles in fp32), so its error is expected within sqrt(2) of
+the model's. The end-to-end comparison therefore requires |g - o| <= 0.1 (1 + |o|)
+(sqrt(2) x 0.056 with 25% margin), a mean error <= 0.015 (1.5 x the model's largest
+mean) and >= 93% of the elements within the stated tolerance.
 
 Context caches are seeded random values for the sampled sequences (the same bf16 bits
 on both sides) and device-generated values for the others; the step then appends the
@@ -27,9 +32,10 @@ from oracle import dflash_oracle as orc
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-HIDDEN_ATOL = 6e-2
-HIDDEN_RTOL = 2e-2
-STATED_FRACTION = 0.95
+HIDDEN_ATOL = 0.1
+HIDDEN_RTOL = 0.1
+HIDDEN_MEAN = 0.015
+STATED_FRACTION = 0.93
 
 _W = {}
 
@@ -114,6 +120,8 @@ def run_case(w, sample):
             assert_close(x0[i].float().cpu().numpy(), x0r[si], f"x0_relay seq {i}")
         gh = hid[i].float().cpu().numpy().astype(np.float64)
         assert_close(gh, ohid[si], f"hidden seq {i} (derived bf16 bound)", atol=HIDDEN_ATOL, rtol=HIDDEN_RTOL)
+        mean_err = np.abs(gh - ohid[si]).mean()
+        assert mean_err <= HIDDEN_MEAN, f"hidden seq {i}: mean error {mean_err:.4f}"
         within = (np.abs(gh - ohid[si]) <= 2e-2 + 1e-2 * np.abs(ohid[si])).mean()
         assert within >= STATED_FRACTION, f"hidden seq {i}: only {within:.4f} within the stated tolerance"
         # stage-wise LM head: oracle logits from the GPU's own bf16 hidden
@@ -122,7 +130,8 @@ def run_case(w, sample):
         assert err < 1e-3, f"logits seq {i}: fp32-accumulated logits drift {err}"
         und += check_topk(tid[i].cpu().numpy(), tv[i].cpu().numpy(), slog, k, f"top-k seq {i}",
                           abs_delta=2e-3)
-        print(f"seq {i}: hidden max err {np.abs(gh - ohid[si]).max():.4f}, {within:.4f} within stated")
+        print(f"seq {i}: hidden max err {np.abs(gh - ohid[si]).max():.4f}, mean {mean_err:.5f}, "
+              f"{within:.4f} within stated")
     if select:
         ghid = hid[s].float().cpu().numpy().astype(np.float64)
         opath, margin = orc.select_path(w, W, tid[s].cpu().numpy(), tv[s].cpu().numpy().astype(np.float64),

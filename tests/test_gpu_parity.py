@@ -19,6 +19,7 @@ MEDIUM = di.Workload("medium_d512_hd128_gqa4", D=512, Dt=192, L=5, N=2, Hq=8, Hk
 MEDIUM_B8 = MEDIUM.with_(name="medium_b8", B=8, nb=5)
 MEDIUM_ALL = MEDIUM.with_(name="medium_relay_conv_select",
                           flags=di.FLAG_RELAY | di.FLAG_CONV | di.FLAG_SELECT)
+MEDIUM_G8 = MEDIUM.with_(name="medium_gqa8_128_query_rows", Hq=16)  # (Hq/Hkv)*B = 128
 
 
 def lib():
@@ -174,7 +175,7 @@ def test_draft_block_stage(w):
     kb, vb = random_cache(w, w.nb, Cmax)
     dr.kcache.copy_(bf16(kb))
     dr.vcache.copy_(bf16(vb))
-    lens = np.array([Cmax, 0, 65, 300, 64, 1, 63][: w.nb], dtype=np.int32)
+    lens = np.array([Cmax - w.B, 0, 65, 300, 64, 1, 63][: w.nb], dtype=np.int32)
     ids = di.block_ids(w, di.anchors(w))
     x0_bits = None
     if w.flags & di.FLAG_RELAY:
@@ -188,13 +189,17 @@ def test_draft_block_stage(w):
     assert_close(f64(out), want, f"hidden {w.name}")
 
 
-def test_draft_block_batch_independent_bitwise():
+def test_draft_block_other_sequences_do_not_leak():
+    """A sequence's hidden does not depend on the other sequences' tokens or caches
+    (bitwise, same context lengths); with other lengths only the attention's split
+    points move, so it stays within the stated tolerance of the oracle."""
     w = MEDIUM
     Cmax = 320
     dr, W, _ = make(w, Cmax, w.B)
     kb, vb = random_cache(w, w.nb, Cmax)
     dr.kcache.copy_(bf16(kb))
     dr.vcache.copy_(bf16(vb))
+    oc = oracle_cache(w, kb, vb, Cmax)
     ids = di.block_ids(w, di.anchors(w))
     lens = np.array([200, 17, 300], np.int32)
     out1 = torch.empty(w.nb, w.B, w.D, dtype=torch.bfloat16, device="cuda")
@@ -202,9 +207,71 @@ def test_draft_block_batch_independent_bitwise():
     ids2 = ids.copy()
     ids2[1:, 0] = (ids2[1:, 0] + 7) % (w.V - 1)
     dr.kcache[:, 1:].normal_()
+    dr.vcache[:, 1:].normal_()
     out2 = torch.empty_like(out1)
-    dr.draft_block(w.nb, i32(ids2), i32(np.array([200, 40, 90], np.int32)), out2, max_ctx_hint=Cmax)
+    dr.draft_block(w.nb, i32(ids2), i32(lens), out2, max_ctx_hint=Cmax)
     assert torch.equal(out1[0], out2[0])
+    out3 = torch.empty_like(out1)
+    dr.draft_block(w.nb, i32(ids2), i32(np.array([200, 40, 90], np.int32)), out3, max_ctx_hint=Cmax)
+    want = orc.draft_block(w, W, ids[:1], lens[:1], oc)
+    assert_close(f64(out3[:1]), want, "hidden of sequence 0 with other lengths")
+    assert dr.status() == 0
+
+
+def test_draft_block_long_ragged():
+    """Thousands of context rows per sequence, ragged down to 1 row: many 64-key units
+    per attention CTA and several (sequence, kv head) segments per CTA."""
+    w = MEDIUM.with_(name="medium_long_ragged", nb=6)
+    Cmax = 4200
+    dr, W, _ = make(w, Cmax, w.B)
+    kb, vb = random_cache(w, w.nb, Cmax, seed=3)
+    dr.kcache.copy_(bf16(kb))
+    dr.vcache.copy_(bf16(vb))
+    lens = np.array([4000, 1, 2500, 3333, 64, Cmax - w.B], np.int32)
+    ids = di.block_ids(w, di.anchors(w))
+    out = torch.empty(w.nb, w.B, w.D, dtype=torch.bfloat16, device="cuda")
+    dr.draft_block(w.nb, i32(ids), i32(lens), out, max_ctx_hint=Cmax)
+    assert dr.status() == 0
+    want = orc.draft_block(w, W, ids, lens, oracle_cache(w, kb, vb, Cmax))
+    assert_close(f64(out), want, "hidden, long ragged contexts")
+
+
+@pytest.mark.parametrize("w", [MEDIUM, MEDIUM_B8, MEDIUM_G8, di.TINY], ids=lambda w: w.name)
+def test_attention_stage_spikes_ragged_nan_tail(w):
+    """The attention stage on given bf16 q, K, V. Key rows carry spikes of growing size
+    along the context (a common direction per kv head), so the running row maxima keep
+    rising past the rescale threshold; lengths are ragged (0, 1, 63..65 context rows,
+    the maximum); every cache row past ctx_len + B holds NaN, which must not reach the
+    output (masked scores, zeroed V rows)."""
+    nb, Cmax, layer = 6, 2200, 1
+    dr, _, _ = make(w, Cmax, w.B, max_batch=nb)
+    lens = np.array([Cmax - w.B, 0, 1, 63, 64, 1500][:nb], np.int32)
+    shp = (w.N, nb, w.Hkv, Cmax, w.hd)
+    K = 0.1 * orc.widen(di.normal_bf16("kspike", shp, 1.0, seed=5))
+    V = orc.widen(di.normal_bf16("vspike", shp, 1.0, seed=5))
+    r = orc.widen(di.normal_bf16("spike_dir", (w.N, w.Hkv, w.hd), 1.0, seed=5))
+    for m, pos in enumerate(range(40, Cmax, 150)):
+        K[:, :, :, pos, :] = (8.0 * (m + 1)) * r[:, None, :, :]
+    for i, L in enumerate(lens + w.B):
+        K[:, i, :, L:, :] = np.nan
+        V[:, i, :, L:, :] = np.nan
+    kb = di.f32_to_bf16_bits(K.astype(np.float32))
+    vb = di.f32_to_bf16_bits(V.astype(np.float32))
+    qb = di.normal_bf16("qspike", (nb, w.B, w.Hq, w.hd), 1.0, seed=5)
+    dr.kcache.copy_(bf16(kb))
+    dr.vcache.copy_(bf16(vb))
+    out = torch.empty(nb, w.B, w.Hq, w.hd, dtype=torch.bfloat16, device="cuda")
+    dr.attention(nb, layer, bf16(qb), i32(lens), out, max_ctx_hint=Cmax)
+    assert dr.status() == 0
+    q, Kw, Vw = orc.widen(qb), orc.widen(kb), orc.widen(vb)
+    grp = w.Hq // w.Hkv
+    want = np.zeros((nb, w.B, w.Hq, w.hd))
+    for i in range(nb):
+        L = int(lens[i]) + w.B
+        for h in range(w.Hq):
+            g = h // grp
+            want[i, :, h] = orc.softmax_attention(q[i, :, h], Kw[layer, i, g, :L], Vw[layer, i, g, :L])
+    assert_close(f64(out), want, f"attention {w.name}")
 
 
 # ----------------------------------------------------------------------------- conv / select
