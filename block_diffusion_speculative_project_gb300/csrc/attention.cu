@@ -18,8 +18,8 @@
 //
 // One CTA, 320 threads:
 //   warp 0       TMA producer: Q tile of the segment's pair ({64 of hd, Hq/Hkv heads, B
-//                rows} boxes from the qkv buffer) and per unit a K tile and a V tile
-//                (64 cache rows x hd, 128-byte swizzle) into a 4-stage ring.
+//                rows} boxes from the qkv buffer) and K and V tiles of two units (128
+//                cache rows x hd, 128-byte swizzle, one copy each) into a 3-stage ring.
 //   warp 1       MMA issuer: S = Q K^T (M = 128 query rows, the G*B real ones zero-padded,
 //                N = 64 keys, K = hd) into TMEM S buffer j % 2, then O_{j%2} += P V
 //                (N = hd, K = 64 keys; V read MN-major straight from its TMA tile).
@@ -42,16 +42,19 @@ namespace df {
 
 // Warp roles for NQ TMEM lane quarters of real query rows (NQ = 2 when G*B <= 64, else
 // 4): half 0 = warps [0, NQ), half 1 = warps [4, 4 + NQ) (warp w reads TMEM lanes of
-// quarter w % 4), then the producer and the MMA warp.
+// quarter w % 4), then the producer and the two MMA-issuing warps (S and PV: one
+// thread issuing both streams was the bottleneck, each tcgen05.mma taking tens of cycles
+// to issue).
 template <int NQ>
 struct AttnRoles {
   static constexpr int PRODUCER = NQ == 4 ? 8 : 2;
-  static constexpr int MMA = PRODUCER + 1;
-  static constexpr int THREADS = (NQ == 4 ? 10 : 6) * 32;
+  static constexpr int MMA = PRODUCER + 1;              // S = Q K^T issuer (and TMEM owner)
+  static constexpr int PV = NQ == 4 ? 10 : 6;           // O += P V issuer
+  static constexpr int THREADS = (PV + 1) * 32;
   static constexpr int HALF_THREADS = NQ * 32;
 };
 constexpr int kKeys = 64;           // keys per unit
-constexpr int kAttnStages = 4;
+constexpr int kAttnStages = 3;    // ring stages of two units each
 constexpr int kQRows = 128;         // MMA M: query rows, zero-padded beyond G*B
 constexpr int kAttnDrainSpin = 1 << 22;
 constexpr float kRescaleLog2 = 8.0f;
@@ -60,19 +63,19 @@ template <int HD>
 struct AttnCfg {
   static constexpr int ATOMS = HD / 64;               // 128-byte swizzle atoms across hd
   static constexpr int ATOM_Q = kQRows * 128;         // one atom of the Q tile
-  static constexpr int ATOM_KV = kKeys * 128;         // one atom of a K or V tile
+  static constexpr int ATOM_KV = 2 * kKeys * 128;     // one atom of a two-unit K or V tile
+  static constexpr int UNIT_KV = kKeys * 128;         // one unit's rows inside an atom
   static constexpr int Q_BYTES = ATOMS * ATOM_Q;
   static constexpr int KV_TILE = ATOMS * ATOM_KV;
-  static constexpr int STAGE = 2 * KV_TILE;           // K tile then V tile
-  static constexpr int P_BYTES = kQRows * kKeys * 2;  // P of one unit, bf16, K-major
+  static constexpr int STAGE = 2 * KV_TILE;           // K tile then V tile: [atom][2 units x 64 rows][128 B]
   static constexpr int OFF_KV = Q_BYTES;
-  static constexpr int OFF_P = OFF_KV + kAttnStages * STAGE;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int OFF_ML = OFF_BAR + 256;        // half 1's (max, sum) per row
+  static constexpr int OFF_BAR = OFF_KV + kAttnStages * STAGE;
+  static constexpr int OFF_ML = OFF_BAR + 512;        // half 1's (max, sum) per row
   static constexpr size_t SMEM = 1024 + OFF_ML + kQRows * 8;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL = 0;                // two S buffers of 64 columns
   static constexpr uint32_t O_COL = 128;              // O_0, O_1: hd columns each
+  static constexpr uint32_t P_COL = 128 + 2 * HD;     // 4 P buffers (unit j in j % 4): 64 bf16 keys = 32 columns each
 };
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -117,6 +120,8 @@ struct AttnWalk {
   int seg;    // segment index inside this CTA
   int seg_unit0;  // first unit of the current segment inside the pair
   int left;   // units left in this CTA's range, including the current one
+  int slot;   // 0: first unit of its ring stage, 1: second (same segment, next 64 keys)
+  int stage;  // ring stages used before this unit's stage
 };
 
 __device__ __forceinline__ void walk_set_pair(AttnWalk &w, const AttnParams &p) {
@@ -127,6 +132,11 @@ __device__ __forceinline__ void walk_set_pair(AttnWalk &w, const AttnParams &p) 
 __device__ __forceinline__ bool walk_first(const AttnWalk &w) { return w.unit == w.seg_unit0; }
 __device__ __forceinline__ bool walk_last(const AttnWalk &w) { return w.left == 1 || w.unit == w.U - 1; }
 __device__ __forceinline__ void walk_next(AttnWalk &w, const AttnParams &p) {
+  // the next unit shares this unit's stage when this is its first slot and the
+  // segment continues (then its keys follow directly)
+  const bool share = w.slot == 0 && !walk_last(w);
+  w.slot = share ? 1 : 0;
+  w.stage += share ? 0 : 1;
   --w.left;
   if (++w.unit == w.U) {
     ++w.pair;
@@ -148,21 +158,22 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *sQ = smem;
   uint8_t *sKV = smem + C::OFF_KV;
-  uint8_t *sP = smem + C::OFF_P;
   uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *kv_empty = kv_full + kAttnStages;
   uint64_t *s_full = kv_empty + kAttnStages;   // [2]
   uint64_t *s_empty = s_full + 2;              // [2]
-  uint64_t *p_full = s_empty + 2;              // [2]
-  uint64_t *p_empty = p_full + 2;              // [2]
-  uint64_t *q_full = p_empty + 2;
+  uint64_t *p_full = s_empty + 2;              // [4]: P of unit j in buffer j % 4
+  uint64_t *p_empty = p_full + 4;              // [4]
+  uint64_t *q_full = p_empty + 4;
   uint64_t *q_empty = q_full + 1;
   uint64_t *o_done = q_empty + 1;             // [2]: PV into O_h completed
   uint64_t *o_free = o_done + 2;              // both O read at a segment end
   uint64_t *ml_ready = o_free + 1;            // half 1's (max, sum) written
-  uint64_t *mma_done = ml_ready + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+  uint64_t *mma_done = ml_ready + 1;          // [2]: drain of the S and the PV issuer
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 2);
   int *sched = reinterpret_cast<int *>(tmem_slot + 1);  // [pair, unit, count]
+  static_assert((2 * kAttnStages + 2 + 2 + 4 + 4 + 2 + 2 + 4) * 8 + 4 + 12 <= C::OFF_ML - C::OFF_BAR,
+                "barrier region overflows");
   float2 *ml1 = reinterpret_cast<float2 *>(smem + C::OFF_ML);
 
   const int warp = threadIdx.x >> 5;
@@ -179,7 +190,9 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], HT);
       mbar_init(&p_full[b], HT);
+      mbar_init(&p_full[b + 2], HT);
       mbar_init(&p_empty[b], 1);
+      mbar_init(&p_empty[b + 2], 1);
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
@@ -187,7 +200,8 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
     mbar_init(&o_done[1], 1);
     mbar_init(o_free, HT);
     mbar_init(ml_ready, HT);
-    mbar_init(mma_done, 1);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
     fence_mbar_init();
   }
   if (warp == Ro::PRODUCER && lane == 0) {
@@ -200,16 +214,12 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
     tmem_relinquish();
   }
   if (warp < NQ) {
-    // Zero the padding rows of Q (rows >= R are never loaded) and of both P buffers,
-    // so the padded MMA rows compute on zeros.
+    // Zero the padding rows of Q (rows >= R are never loaded), so the padded MMA rows
+    // compute on zeros.
     const int t = threadIdx.x;
     for (int a = 0; a < C::ATOMS; ++a)
       for (int e = R * 8 + t; e < kQRows * 8; e += HT)
         *reinterpret_cast<uint4 *>(sQ + a * C::ATOM_Q + e * 16) = make_uint4(0, 0, 0, 0);
-    for (int e = R * 8 + t; e < kQRows * 8; e += HT) {
-      *reinterpret_cast<uint4 *>(sP + e * 16) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4 *>(sP + C::P_BYTES + e * 16) = make_uint4(0, 0, 0, 0);
-    }
     fence_proxy_async_smem();
   }
 
@@ -276,6 +286,8 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
   w0.seg = 0;
   w0.seg_unit0 = w0.unit;
   w0.left = nunits;
+  w0.slot = 0;
+  w0.stage = 0;
   if (nunits > 0) walk_set_pair(w0, p);
 
   if (warp == Ro::PRODUCER) {
@@ -286,7 +298,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
       const uint32_t q_bytes = static_cast<uint32_t>(C::ATOMS * R * 128);
       AttnWalk w = w0;
       bool ok = true;
-      int j = 0, q_loads = 0;
+      int j = 0, q_loads = 0, stages = 0;
       for (; j < nunits; ++j) {
         const int i = w.pair / p.Hkv, g = w.pair % p.Hkv;
         if (walk_first(w)) {
@@ -300,89 +312,99 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
             tma_load_3d(sQ + a * C::ATOM_Q, &p.tmQ, q_full, a * 64, g * G, i * p.B, pol_q);
           ++q_loads;
         }
-        const int st = j % kAttnStages;
-        if (j >= kAttnStages && !mbar_wait(&kv_empty[st], ((j / kAttnStages) & 1) ^ 1, p.max_spin)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
-        const int row = p.layer_row0 + (i * p.Hkv + g) * p.Cmax + w.unit * kKeys;
-        uint8_t *kt = sKV + st * C::STAGE;
-#pragma unroll
-        for (int a = 0; a < C::ATOMS; ++a) {
-          tma_load_2d(kt + a * C::ATOM_KV, &p.tmK, &kv_full[st], a * 64, row, pol_kv);
-          tma_load_2d(kt + C::KV_TILE + a * C::ATOM_KV, &p.tmV, &kv_full[st], a * 64, row, pol_kv);
+        if (w.slot == 0) {
+          // one copy each for K and V: 128 rows (this unit and the next 64 keys) of
+          // every 64-wide half of hd. A tensor copy from one SM costs about one DRAM
+          // round trip whatever its size, so the copies are made as large as smem allows.
+          const int st = w.stage % kAttnStages;
+          if (w.stage >= kAttnStages &&
+              !mbar_wait(&kv_empty[st], ((w.stage / kAttnStages) & 1) ^ 1, p.max_spin)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
+          const int row = p.layer_row0 + (i * p.Hkv + g) * p.Cmax + w.unit * kKeys;
+          uint8_t *kt = sKV + st * C::STAGE;
+          tma_load_3d(kt, &p.tmK, &kv_full[st], 0, row, 0, pol_kv);
+          tma_load_3d(kt + C::KV_TILE, &p.tmV, &kv_full[st], 0, row, 0, pol_kv);
+          stages = w.stage + 1;
         }
         walk_next(w, p);
       }
       if (!ok) flag_status(p.status, kStatusTimeout);
       // Every issued load must land before the CTA may exit (bounded).
-      for (int k = max(0, j - kAttnStages); k < j; ++k)
+      for (int k = max(0, stages - kAttnStages); k < stages; ++k)
         mbar_wait(&kv_full[k % kAttnStages], (k / kAttnStages) & 1, kAttnDrainSpin);
       if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, kAttnDrainSpin);
     }
   } else if (warp == Ro::MMA) {
     if (lane == 0 && nunits > 0) {
-      // ---------------- MMA issuer
+      // ---------------- S issuer: S(j) once its K tile has landed and S buffer j % 2 has
+      // been read by the softmax
       constexpr uint32_t id_s = idesc_bf16_f32(kQRows, kKeys);
-      constexpr uint32_t id_pv = idesc_bf16_f32(kQRows, HD) | kIdescBMajorMN;
-      const uint32_t q_addr = smem_u32(sQ);
-      AttnWalk w = w0;
+      const uint64_t q_desc0 = sw128_kmajor_desc(smem_u32(sQ));
+      const uint64_t kv_desc0 = sw128_kmajor_desc(smem_u32(sKV));
+      AttnWalk ws = w0;
       bool ok = true;
-      int jf = 0;                 // first unit of the current segment
-      int prev_jf = 0, prev_seg = 0;
-      for (int j = 0; j <= nunits && ok; ++j) {
-        if (j < nunits) {
-          const int st = j % kAttnStages, sb = j & 1;
-          if (walk_first(w)) {
-            jf = j;
-            if (!mbar_wait(q_full, w.seg & 1, p.max_spin)) ok = false;
-          }
-          if (ok && !mbar_wait(&kv_full[st], (j / kAttnStages) & 1, p.max_spin)) ok = false;
-          if (ok && j >= 2 && !mbar_wait(&s_empty[sb], ((j >> 1) - 1) & 1, p.max_spin)) ok = false;
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(sKV + st * C::STAGE);
+      for (int js = 0; js < nunits; ++js) {
+        const int st = ws.stage % kAttnStages, sb = js & 1;
+        if (walk_first(ws) && !mbar_wait(q_full, ws.seg & 1, p.max_spin)) ok = false;
+        // (the second unit of a stage landed with the first)
+        if (ok && ws.slot == 0 && !mbar_wait(&kv_full[st], (ws.stage / kAttnStages) & 1, p.max_spin)) ok = false;
+        if (ok && js >= 2 && !mbar_wait(&s_empty[sb], ((js >> 1) - 1) & 1, p.max_spin)) ok = false;
+        if (!ok) break;
+        tc_fence_after();
+        // descriptors differ only in their start-address field: add the k-step offset
+        const uint64_t kd = kv_desc0 + static_cast<uint64_t>((st * C::STAGE + ws.slot * C::UNIT_KV) >> 4);
+        const uint32_t d_s = tmem_base + C::S_COL + sb * kKeys;
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t qa = q_addr + (kk >> 2) * C::ATOM_Q + (kk & 3) * 32;
-            const uint32_t ka = k_addr + (kk >> 2) * C::ATOM_KV + (kk & 3) * 32;
-            tc_mma_bf16(tmem_base + C::S_COL + sb * kKeys, sw128_kmajor_desc(qa), sw128_kmajor_desc(ka),
-                        id_s, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(&s_full[sb]);
-          if (walk_last(w)) tc_commit(q_empty);
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t qo = static_cast<uint64_t>(((kk >> 2) * C::ATOM_Q + (kk & 3) * 32) >> 4);
+          const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * C::ATOM_KV + (kk & 3) * 32) >> 4);
+          tc_mma_bf16(d_s, q_desc0 + qo, kd + ko, id_s, kk > 0 ? 1u : 0u);
         }
-        if (j > 0) {
-          // PV of the previous unit into O of its half; the first unit of each half in
-          // a segment starts the accumulator (after both O of the last segment were read)
-          const int jp = j - 1, st = jp % kAttnStages, pb = jp & 1;
-          const bool start = jp < prev_jf + 2;
-          if (!mbar_wait(&p_full[pb], (jp >> 1) & 1, p.max_spin)) ok = false;
-          if (ok && start && prev_seg > 0 && !mbar_wait(o_free, (prev_seg - 1) & 1, p.max_spin)) ok = false;
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t p_addr = smem_u32(sP + pb * C::P_BYTES);
-          const uint32_t v_addr = smem_u32(sKV + st * C::STAGE + C::KV_TILE);
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk)
-            tc_mma_bf16(tmem_base + C::O_COL + pb * HD, sw128_kmajor_desc(p_addr + kk * 32),
-                        sw128_mnmajor_desc(v_addr + kk * 16 * 128, C::ATOM_KV), id_pv,
-                        (!start || kk > 0) ? 1u : 0u);
-          tc_commit(&o_done[pb]);
-          tc_commit(&p_empty[pb]);
-          tc_commit(&kv_empty[st]);
-        }
-        if (j < nunits) {
-          prev_jf = jf;
-          prev_seg = w.seg;
-          walk_next(w, p);
-        }
+        tc_commit(&s_full[sb]);
+        if (walk_last(ws)) tc_commit(q_empty);
+        walk_next(ws, p);
       }
       if (!ok) flag_status(p.status, kStatusTimeout);
       // Every issued MMA must complete before TMEM is freed (bounded).
-      tc_commit(mma_done);
-      mbar_wait(mma_done, 0, kAttnDrainSpin);
+      tc_commit(&mma_done[0]);
+      mbar_wait(&mma_done[0], 0, kAttnDrainSpin);
+    }
+  } else if (warp == Ro::PV) {
+    if (lane == 0 && nunits > 0) {
+      // ---------------- PV issuer: O_{j%2} += P(j) V(j) once P(j) is in tensor memory; the
+      // first unit of each half in a segment starts the accumulator (after both O of the
+      // previous segment were read); the last unit of a stage releases it
+      constexpr uint32_t id_pv = idesc_bf16_f32(kQRows, HD) | kIdescBMajorMN;
+      const uint64_t v_desc0 = sw128_mnmajor_desc(smem_u32(sKV + C::KV_TILE), C::ATOM_KV);
+      AttnWalk wp = w0;
+      int jf = 0;
+      bool ok = true;
+      for (int jp = 0; jp < nunits; ++jp) {
+        const int st = wp.stage % kAttnStages, pb = jp & 1, pq = jp & 3;
+        if (walk_first(wp)) jf = jp;
+        const bool start = jp < jf + 2;
+        if (!mbar_wait(&p_full[pq], (jp >> 2) & 1, p.max_spin)) ok = false;
+        if (ok && start && wp.seg > 0 && !mbar_wait(o_free, (wp.seg - 1) & 1, p.max_spin)) ok = false;
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t vd = v_desc0 + static_cast<uint64_t>((st * C::STAGE + wp.slot * C::UNIT_KV) >> 4);
+        const uint32_t d_o = tmem_base + C::O_COL + pb * HD;
+        const uint32_t a_p = tmem_base + C::P_COL + pq * 32;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          tc_mma_bf16_tmem_a(d_o, a_p + kk * 8, vd + static_cast<uint64_t>((kk * 16 * 128) >> 4), id_pv,
+                             (!start || kk > 0) ? 1u : 0u);
+        tc_commit(&o_done[pb]);
+        tc_commit(&p_empty[pq]);
+        if (wp.slot == 1 || walk_last(wp)) tc_commit(&kv_empty[st]);  // last unit of its stage
+        walk_next(wp, p);
+      }
+      if (!ok) flag_status(p.status, kStatusTimeout);
+      tc_commit(&mma_done[1]);
+      mbar_wait(&mma_done[1], 0, kAttnDrainSpin);
     }
   } else if ((warp & 3) < NQ) {
     // ---------------- softmax warps: half h = warp / 4 takes units j % 2 == h; thread r
@@ -402,7 +424,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
     bool ok = true;
     int jf = 0;
     for (int j = 0; j < nunits && ok; ++j) {
-      const int st = j % kAttnStages;
+      const int st = w.stage % kAttnStages;
       if (walk_first(w)) {
         jf = j;
         m_run = -FLT_MAX;
@@ -469,14 +491,15 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
             tmem_st32(o_mine + cc * 32, ov);
           }
         }
-        // P buffer `half` is free once PV of this half's previous unit has completed
-        ok = j < 2 || mbar_wait(&p_empty[half], ((j >> 1) - 1) & 1, p.max_spin);
+        // P buffer j % 4 is free once PV of unit j - 4 has completed
+        ok = j < 4 || mbar_wait(&p_empty[j & 3], ((j >> 2) - 1) & 1, p.max_spin);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        if (real) {
-          uint32_t pk[kKeys / 2];
+        if (warp_real) {
+          // P (bf16 pairs) into this half's P columns of the row's TMEM lane
+          float pk[kKeys / 2];
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
           const float mb = m_run * sl2;
 #pragma unroll
@@ -484,32 +507,28 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
             const float p0 = ex2_approx(fmaf(sv[c], sl2, -mb));
             const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, -mb));
             ls[(c >> 1) & 3] += p0 + p1;
-            pk[c >> 1] = pack_bf16x2(p0, p1);
+            pk[c >> 1] = real ? __uint_as_float(pack_bf16x2(p0, p1)) : 0.f;
           }
-          l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-          uint8_t *prow = sP + half * C::P_BYTES + r * 128;
-#pragma unroll
-          for (int c16 = 0; c16 < 8; ++c16)
-            *reinterpret_cast<uint4 *>(prow + ((c16 ^ (r & 7)) << 4)) =
-                make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+          if (real) l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          tmem_st32(trow + C::P_COL + (j & 3) * 32, pk);
         }
         if (nv < kKeys) {
           // V rows beyond the last key may hold anything (even NaN): zero them, P is 0 there.
-          ok = mbar_wait(&kv_full[st], (j / kAttnStages) & 1, p.max_spin);
+          ok = mbar_wait(&kv_full[st], (w.stage / kAttnStages) & 1, p.max_spin);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
           }
-          uint8_t *vt = sKV + st * C::STAGE + C::KV_TILE;
+          uint8_t *vt = sKV + st * C::STAGE + C::KV_TILE + w.slot * C::UNIT_KV;
           const int nz = (kKeys - nv) * 8;  // 16-byte chunks per atom
           for (int e = r; e < C::ATOMS * nz; e += HT) {
             const int a = e / nz, x = e % nz;
             *reinterpret_cast<uint4 *>(vt + a * C::ATOM_KV + nv * 128 + x * 16) = make_uint4(0, 0, 0, 0);
           }
         }
-        fence_proxy_async_smem();
+        if (nv < kKeys) fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&p_full[half]);
+        mbar_arrive(&p_full[j & 3]);
       }
 
       if (walk_last(w)) {

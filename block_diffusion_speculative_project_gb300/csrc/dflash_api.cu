@@ -235,8 +235,10 @@ int attention_params(const dflash_handle_s *h, const Ws &w, int nb, const void *
   AttnParams &ap = *out;
   DF_TRY(encode_3d(&ap.tmQ, q, c.hd, c.Hq, (uint64_t)nb * c.B, c.hd, ldq, c.Hq / c.Hkv, c.B));
   const uint64_t cache_rows = (uint64_t)c.N * c.max_batch * c.Hkv * c.Cmax;
-  DF_TRY(encode_2d(&ap.tmK, kcache, cache_rows, c.hd, c.hd, 64));
-  DF_TRY(encode_2d(&ap.tmV, vcache, cache_rows, c.hd, c.hd, 64));
+  // {64 of hd, cache rows, hd/64 halves}: one box = 128 rows of every half, stacked
+  // half after half as the MMA reads them
+  DF_TRY(encode_3d(&ap.tmK, kcache, 64, cache_rows, c.hd / 64, c.hd, 64, 128, c.hd / 64));
+  DF_TRY(encode_3d(&ap.tmV, vcache, 64, cache_rows, c.hd / 64, c.hd, 64, 128, c.hd / 64));
   ap.ctx_len = ctx_len;
   ap.o = static_cast<uint16_t *>(o);
   ap.part_o = w.at<float>(h->ws.apart);

@@ -511,6 +511,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     if (lane == 0 && nitems > 0) {
       // ---------------- MMA issuer
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(sA));
+      const uint64_t b_desc0 = sw128_kmajor_desc(smem_u32(sB));
       int it = 0;
       bool ok = true;
       for (int j = 0; j < nitems && ok; ++j) {
@@ -533,12 +535,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + st * C::A_BYTES);
-          const uint32_t b_addr = smem_u32(sB + st * C::B_BYTES);
+          // descriptors differ only in their start-address field (16-byte units)
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>((st * C::A_BYTES) >> 4);
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>((st * C::B_BYTES) >> 4);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma_bf16(d, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32),
-                        idesc, (kt > kt0 || k > 0) ? 1u : 0u);
+            tc_mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kt > kt0 || k > 0) ? 1u : 0u);
           tc_commit(&empty[st]);
         }
         if (!ok) break;

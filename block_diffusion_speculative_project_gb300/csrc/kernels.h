@@ -166,7 +166,7 @@ cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, cons
 // every sequence attends to the ctx_len + B contiguous cache rows of its heads.
 struct AttnParams {
   CUtensorMap tmQ;      // qkv buffer as {hd, Hq heads, nb*B rows}, box {64, Hq/Hkv, B}
-  CUtensorMap tmK;      // key cache of every layer as rows of hd: {hd, N*max_batch*Hkv*Cmax}, box {64, 64}
+  CUtensorMap tmK;      // key cache of every layer: {64, N*max_batch*Hkv*Cmax rows, hd/64}, box {64, 128, hd/64}
   CUtensorMap tmV;      // value cache, same shape
   const int *ctx_len;   // [nb]
   uint16_t *o;          // [nb*B, Hq*hd] bf16
