@@ -100,6 +100,15 @@ int encode_act(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols) {
   return encode_3d(m, ptr, cols, rows, 1, cols, rows * cols, 128, 1);
 }
 
+// Slab maps of the two-slab GEMM stages: a bf16 [rows, K] matrix (row stride K, K a
+// multiple of 64) as {64, rows, K/64} with the slab stride 128 bytes; one box = two
+// 64-column slabs of box_rows rows, stacked slab after slab.
+int encode_slabs(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
+  if (K % 64) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "slab map needs K %% 64 == 0 (K=%llu)",
+                          (unsigned long long)K);
+  return encode_3d(m, ptr, 64, rows, K / 64, K, 64, box_rows, 2);
+}
+
 constexpr int kBN = 128;       // tile width of the generic GEMMs
 constexpr int kBNTopk = 256;   // tile width of the LM head
 constexpr int kBNGateUp = 192; // gate|up GEMM: 96 gate + 96 up rows per tile (F/96 tiles)
@@ -389,7 +398,7 @@ int dflash_set_weights(dflash_handle_t h, const dflash_weights *w) {
   h->layers.assign(w->layers, w->layers + c.N);
   h->w.layers = h->layers.data();
   const int qkv_n = (c.Hq + 2 * c.Hkv) * c.hd;
-  DF_TRY(encode_2d(&h->tm_Wc, w->W_c, c.D, (uint64_t)c.L * c.Dt, (uint64_t)c.L * c.Dt, kBN));
+  DF_TRY(encode_slabs(&h->tm_Wc, w->W_c, c.D, (uint64_t)c.L * c.Dt, kBN));
   DF_TRY(encode_2d(&h->tm_lm, w->W_lm, c.V, c.D, c.D, kBNTopk));
   h->tm_qkv.resize(c.N);
   h->tm_kc.resize(c.N);
@@ -405,13 +414,16 @@ int dflash_set_weights(dflash_handle_t h, const dflash_weights *w) {
     if (!L.W_qkv || !L.Wk_c || !L.Wv_c || !L.W_o || !L.W_gate || !L.W_up || !L.W_down || !L.g_attn ||
         !L.g_ffn)
       return fail(DFLASH_ERR_INVALID_ARG, "layer %d: a weight pointer is NULL", n);
-    DF_TRY(encode_2d(&h->tm_qkv[n], L.W_qkv, qkv_n, c.D, c.D, kBN));
-    DF_TRY(encode_2d(&h->tm_kc[n], L.Wk_c, (uint64_t)c.Hkv * c.hd, c.D, c.D, kBN));
-    DF_TRY(encode_2d(&h->tm_vc[n], L.Wv_c, (uint64_t)c.Hkv * c.hd, c.D, c.D, kBN));
-    DF_TRY(encode_2d(&h->tm_o[n], L.W_o, c.D, (uint64_t)c.Hq * c.hd, (uint64_t)c.Hq * c.hd, kBN));
+    DF_TRY(encode_slabs(&h->tm_qkv[n], L.W_qkv, qkv_n, c.D, kBN));
+    DF_TRY(encode_slabs(&h->tm_kc[n], L.Wk_c, (uint64_t)c.Hkv * c.hd, c.D, kBN));
+    DF_TRY(encode_slabs(&h->tm_vc[n], L.Wv_c, (uint64_t)c.Hkv * c.hd, c.D, kBN));
+    DF_TRY(encode_slabs(&h->tm_o[n], L.W_o, c.D, (uint64_t)c.Hq * c.hd, kBN));
     DF_TRY(encode_2d(&h->tm_gate[n], L.W_gate, c.F, c.D, c.D, kBNGateUp / 2));
     DF_TRY(encode_2d(&h->tm_up[n], L.W_up, c.F, c.D, c.D, kBNGateUp / 2));
-    DF_TRY(encode_2d(&h->tm_down[n], L.W_down, c.D, c.F, c.F, kBN));
+    if (c.F % 64 == 0)
+      DF_TRY(encode_slabs(&h->tm_down[n], L.W_down, c.D, c.F, kBN));
+    else
+      DF_TRY(encode_2d(&h->tm_down[n], L.W_down, c.D, c.F, c.F, kBN));
     if (c.flags & DFLASH_FLAG_CONV) {
       for (int q = 0; q < 4; ++q) {
         if (!L.conv_W0[q] || !L.conv_W1[q] || !L.conv_base[q])
@@ -461,7 +473,8 @@ int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *hv, const i
   uint16_t *hh = w.at<uint16_t>(h->ws.h);
   {  // pre = hv * W_c^T
     GemmParams p = base_params(h, w);
-    DF_TRY(encode_act(&p.tmA, hv, rows, (uint64_t)c.L * c.Dt));
+    DF_TRY(encode_slabs(&p.tmA, hv, rows, (uint64_t)c.L * c.Dt, 128));
+    p.slabs = 2;
     p.tmB[0] = h->tm_Wc;
     p.M = rows;
     p.N = c.D;
@@ -474,7 +487,8 @@ int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *hv, const i
   DF_CUDA(launch_rmsnorm(pre, rows, c.D, bf(h->w.g_ctx), c.eps, hh, s));
   {  // K_c / V_c of every layer, scattered into the caches (committed rows only)
     GemmParams p = base_params(h, w);
-    DF_TRY(encode_act(&p.tmA, hh, rows, c.D));
+    DF_TRY(encode_slabs(&p.tmA, hh, rows, c.D, 128));
+    p.slabs = 2;
     for (int n = 0; n < c.N; ++n) {
       p.tmB[2 * n] = h->tm_kc[n];
       p.tmB[2 * n + 1] = h->tm_vc[n];
@@ -526,10 +540,15 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
   uint16_t *o = w.at<uint16_t>(h->ws.o);
   uint16_t *act = w.at<uint16_t>(h->ws.act);
 
-  CUtensorMap tm_u, tm_o, tm_act;
-  DF_TRY(encode_act(&tm_u, u, M, c.D));
-  DF_TRY(encode_act(&tm_o, o, M, (uint64_t)c.Hq * c.hd));
-  DF_TRY(encode_act(&tm_act, act, M, c.F));
+  CUtensorMap tm_u, tm_u2, tm_o, tm_act;
+  const bool down_slabs = c.F % 64 == 0;
+  DF_TRY(encode_act(&tm_u, u, M, c.D));          // gate|up (one slab per stage)
+  DF_TRY(encode_slabs(&tm_u2, u, M, c.D, 128));  // QKV
+  DF_TRY(encode_slabs(&tm_o, o, M, (uint64_t)c.Hq * c.hd, 128));
+  if (down_slabs)
+    DF_TRY(encode_slabs(&tm_act, act, M, c.F, 128));
+  else
+    DF_TRY(encode_act(&tm_act, act, M, c.F));
 
   DF_CUDA(launch_embed_rmsnorm(block_ids, bf(h->w.E), static_cast<const uint16_t *>(x0_relay), M, c.D,
                                c.V, x, conv ? nullptr : bf(h->layers[0].g_attn), c.eps, u, w.status(), s));
@@ -548,7 +567,8 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
     uint16_t *vc_n = static_cast<uint16_t *>(vcache) + n * cache_layer_elems(c);
     {  // q -> qkv buffer; k_b, v_b -> cache rows ctx_len + j; RoPE on q and k_b
       GemmParams p = base_params(h, w);
-      p.tmA = tm_u;
+      p.tmA = tm_u2;
+      p.slabs = 2;
       p.tmB[0] = h->tm_qkv[n];
       p.M = M;
       p.N = qkv_n;
@@ -571,6 +591,7 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
     {  // x += o W_O^T
       GemmParams p = base_params(h, w);
       p.tmA = tm_o;
+      p.slabs = 2;
       p.tmB[0] = h->tm_o[n];
       p.M = M;
       p.N = c.D;
@@ -602,6 +623,7 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
     {  // x += act W_down^T
       GemmParams p = base_params(h, w);
       p.tmA = tm_act;
+      p.slabs = down_slabs ? 2 : 1;
       p.tmB[0] = h->tm_down[n];
       p.M = M;
       p.N = c.D;

@@ -32,10 +32,21 @@ constexpr int kGemmThreads = 192;
 // Bound of the teardown waits for this CTA's own TMA copies and MMAs, which finish
 // without help from any other thread; independent of the caller's max_spin.
 constexpr int kDrainSpin = 1 << 22;
-template <int BN>
+// K slabs (64 columns each) one stage holds: two for the plain 128-wide GEMMs, whose
+// A and B tiles are then each one 32 KB copy (a tensor copy from one SM costs about
+// one DRAM round trip whatever its size, so the small-M GEMMs were bound by the copy
+// count), one for the dual and top-k tiles.
+template <int BN, int EPI>
+__host__ __device__ constexpr int gemm_slabs() {
+  return (BN == 128 && EPI != EPI_SWIGLU && EPI != EPI_DUAL_F32 && EPI != EPI_TOPK) ? 2 : 1;
+}
+
+template <int BN, int SL>
 struct TileCfg {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int A_SLAB = BM * BK * 2;
+  static constexpr int B_SLAB = BN * BK * 2;
+  static constexpr int A_BYTES = SL * A_SLAB;
+  static constexpr int B_BYTES = SL * B_SLAB;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = (200 * 1024 / STAGE) > 8 ? 8 : (200 * 1024 / STAGE);
   static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;  // power of two >= 2*BN
@@ -52,7 +63,7 @@ constexpr size_t kTopkStashBytes = 128 * 33 * sizeof(float);
 
 template <int BN, int EPI>
 constexpr size_t gemm_smem_bytes() {
-  return TileCfg<BN>::SMEM + (EPI == EPI_TOPK ? kTopkStashBytes : 0);
+  return TileCfg<BN, gemm_slabs<BN, EPI>()>::SMEM + (EPI == EPI_TOPK ? kTopkStashBytes : 0);
 }
 
 struct Item {
@@ -383,7 +394,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
-  using C = TileCfg<BN>;
+  using C = TileCfg<BN, gemm_slabs<BN, EPI>()>;
   static_assert(EPI == EPI_TOPK || C::RED_FITS, "cluster reduction buffers exceed the pipeline smem");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -452,14 +463,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       };
       auto load_a = [&](const Cursor &c, int st) {
         uint8_t *a = sA + st * C::A_BYTES;
-        if (p.a_grouped)
+        if (p.slabs == 2)  // A map {64, rows, K/64}: both slabs of the stage in one copy
+          tma_load_3d(a, &p.tmA, &full[st], 0, c.t.m * BM, c.kt * 2, pol_a);
+        else if (p.a_grouped)
           tma_load_3d(a, &p.tmA, &full[st], c.kt * BK, 0, c.t.m * p.a_S, pol_a);
         else
           tma_load_3d(a, &p.tmA, &full[st], c.kt * BK, c.t.m * BM, 0, pol_a);
       };
       auto load_b = [&](const Cursor &c, int st) {
         uint8_t *b = sB + st * C::B_BYTES;
-        if (p.dual) {
+        if (p.slabs == 2) {  // weight maps {64, N, K/64}
+          tma_load_3d(b, &p.tmB[c.t.g], &full[st], 0, c.t.n * BN, c.kt * 2, pol_w);
+        } else if (p.dual) {
           tma_load_2d(b, &p.tmB[0], &full[st], c.kt * BK, c.t.n * (BN / 2), pol_w);
           tma_load_2d(b + (BN / 2) * 128, &p.tmB[1], &full[st], c.kt * BK, c.t.n * (BN / 2), pol_w);
         } else {
@@ -539,8 +554,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
           const uint64_t ad = a_desc0 + static_cast<uint64_t>((st * C::A_BYTES) >> 4);
           const uint64_t bd = b_desc0 + static_cast<uint64_t>((st * C::B_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            tc_mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kt > kt0 || k > 0) ? 1u : 0u);
+          for (int sl = 0; sl < gemm_slabs<BN, EPI>(); ++sl) {
+            if (sl >= p.slabs) break;
+            const uint64_t as = ad + static_cast<uint64_t>((sl * C::A_SLAB) >> 4);
+            const uint64_t bs = bd + static_cast<uint64_t>((sl * C::B_SLAB) >> 4);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              tc_mma_bf16(d, as + 2 * k, bs + 2 * k, idesc, (kt > kt0 || sl > 0 || k > 0) ? 1u : 0u);
+          }
           tc_commit(&empty[st]);
         }
         if (!ok) break;
@@ -709,11 +730,12 @@ int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN) {
 // holds concurrently; 0 = unknown, then tiles * S <= num_sms) and every split keeps
 // >= 8 k-tiles. Multi-wave cluster launches measured slower than one persistent
 // unsplit wave, so larger tile counts stay unsplit.
-void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN, int num_sms,
+void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN, int slabs, int num_sms,
                int epi, const int *cluster_cap, int *splits_out, int *kps_out, int *items_out,
                int *grid_out, int *csplit_out) {
   const int tiles = gemm_tiles(M, tile_rows, N, groups, dual, BN);
-  const int kt = (K + BK - 1) / BK;
+  const int kt = (K + BK - 1) / BK;                            // 64-column k-tiles
+  const int kst = (K + BK * slabs - 1) / (BK * slabs);         // pipeline stages along K
   int best_s = 1;
   if (epi != EPI_TOPK)
     for (int S = 2; S <= 8; ++S) {
@@ -723,7 +745,7 @@ void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN,
     }
   *splits_out = 1;
   *csplit_out = best_s;
-  *kps_out = (kt + best_s - 1) / best_s;
+  *kps_out = (kst + best_s - 1) / best_s;
   *items_out = best_s > 1 ? tiles * best_s : tiles;
   *grid_out = best_s > 1 ? tiles * best_s : std::max(1, std::min(tiles, num_sms));
 }
@@ -773,6 +795,8 @@ template <int BN, int EPI>
 static cudaError_t plan_and_launch(GemmParams &p, int num_sms, cudaStream_t s) {
   const KernelSetup &ks = kernel_setup<BN, EPI>();
   if (ks.err != cudaSuccess) return ks.err;
+  if (p.slabs > gemm_slabs<BN, EPI>() || (p.slabs == 2 && (p.a_grouped || p.dual)))
+    return cudaErrorInvalidValue;
   int grid;
   p.csplit = 1;
   if (EPI == EPI_TOPK) {
@@ -784,7 +808,7 @@ static cudaError_t plan_and_launch(GemmParams &p, int num_sms, cudaStream_t s) {
     grid = ranges * p.m_tiles;
     p.items = grid;
   } else {
-    gemm_plan(p.M, p.tile_rows, p.N, p.K, p.groups, p.dual, BN, num_sms, p.epi, ks.cluster_cap,
+    gemm_plan(p.M, p.tile_rows, p.N, p.K, p.groups, p.dual, BN, p.slabs, num_sms, p.epi, ks.cluster_cap,
               &p.splits, &p.kt_per_split, &p.items, &grid, &p.csplit);
   }
   constexpr size_t smem = gemm_smem_bytes<BN, EPI>();
@@ -799,10 +823,12 @@ cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s) {
   p.m_tiles = (p.M + p.tile_rows - 1) / p.tile_rows;
   const int ncols = p.dual ? BN / 2 : BN;
   p.n_tiles = (p.N + ncols - 1) / ncols;
-  p.kt_total = (p.K + BK - 1) / BK;
-  // expect-tx bytes of one stage: the A box plus the B box(es)
+  if (p.slabs != 2) p.slabs = 1;
+  p.kt_total = (p.K + BK * p.slabs - 1) / (BK * p.slabs);  // stages along K
+  // expect-tx bytes of one stage: the A box plus the B box(es), per slab (a slab past
+  // K is zero-filled by the copy and still counted)
   const uint32_t a_rows = p.a_grouped ? (uint32_t)p.tile_rows : (uint32_t)BM;
-  p.stage_tx_bytes = a_rows * BK * 2 + (uint32_t)BN * BK * 2;
+  p.stage_tx_bytes = (uint32_t)p.slabs * (a_rows * BK * 2 + (uint32_t)BN * BK * 2);
   switch (BN * 16 + p.epi) {
     case 128 * 16 + EPI_BF16: return plan_and_launch<128, EPI_BF16>(p, num_sms, s);
     case 128 * 16 + EPI_F32: return plan_and_launch<128, EPI_F32>(p, num_sms, s);

@@ -114,6 +114,8 @@ struct GemmParams {
   int max_spin;
   int stall;         // test hook: issue no loads so the waits run out
   int csplit;        // >1: split K across the CTAs of a cluster, reduce through DSMEM
+  int slabs;         // 2: A and B maps carry a 64-column slab dimension and each stage
+                     // loads two slabs per copy (plain 128-wide GEMMs with K % 64 == 0)
 };
 
 struct GemmLaunch {
@@ -127,7 +129,7 @@ struct GemmLaunch {
 cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s);
 // cluster_cap[S] (S = 2..8): clusters of S CTAs the device keeps resident at once,
 // 0 = unknown; may be null.
-void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN, int num_sms,
+void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN, int slabs, int num_sms,
                int epi, const int *cluster_cap, int *splits, int *kt_per_split, int *items, int *grid,
                int *csplit);
 int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN);
