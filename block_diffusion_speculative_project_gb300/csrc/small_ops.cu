@@ -292,12 +292,93 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float *vals, cons
   }
 }
 
+// Merge of sorted per-part lists (the LM head's per-range top-k lists, parts <= 1024,
+// k <= 16): one CTA of 1024 threads per row. A candidate below the k-th best list head
+// cannot be in the top k (the k best heads already beat it), so (1) the k-th best head is
+// found by rank counting among the heads, (2) every candidate at or above it survives -
+// at most k lists x k entries - and (3) the survivors are placed by rank counting. All
+// comparisons use the strict order (value descending, then id ascending).
+constexpr int kHeadsThreads = 1024;
+constexpr int kHeadsMaxSurv = kTopkMax * kTopkMax;
+
+__global__ void __launch_bounds__(kHeadsThreads) topk_merge_heads_kernel(
+    const float *vals, const int *ids, int ncand, long long row_stride, long long part_stride, int parts,
+    int k, int *out_ids, float *out_vals) {
+  griddep_wait();
+  griddep_launch();
+  __shared__ float hv[kHeadsThreads];
+  __shared__ int hi[kHeadsThreads];
+  __shared__ float sv[kHeadsMaxSurv];
+  __shared__ int si[kHeadsMaxSurv];
+  __shared__ float thr_v;
+  __shared__ int thr_i, nsurv;
+  const int r = blockIdx.x, t = threadIdx.x;
+  const long long rowbase = (long long)r * row_stride;
+  if (t == 0) {
+    thr_v = -FLT_MAX;
+    thr_i = INT_MAX;
+    nsurv = 0;
+  }
+  if (t < parts) {
+    hv[t] = vals[(long long)t * part_stride + rowbase];
+    hi[t] = ids[(long long)t * part_stride + rowbase];
+  }
+  __syncthreads();
+  // (1) the k-th best head (when there are fewer than k lists every candidate survives)
+  if (t < parts && parts >= k) {
+    const float v = hv[t];
+    const int id = hi[t];
+    int rank = 0;
+    for (int q = 0; q < parts; ++q) rank += topk_before(hv[q], hi[q], v, id) ? 1 : 0;
+    if (rank == k - 1) {
+      thr_v = v;
+      thr_i = id;
+    }
+  }
+  __syncthreads();
+  // (2) survivors: candidates not after the threshold
+  const float tv = thr_v;
+  const int ti = thr_i;
+  const int total = parts * ncand;
+  for (int e = t; e < total; e += kHeadsThreads) {
+    const int part = e / ncand, c = e % ncand;
+    const long long idx = (long long)part * part_stride + rowbase + c;
+    const float v = vals[idx];
+    const int id = ids[idx];
+    if (!topk_before(tv, ti, v, id)) {
+      const int slot = atomicAdd(&nsurv, 1);
+      if (slot < kHeadsMaxSurv) {
+        sv[slot] = v;
+        si[slot] = id;
+      }
+    }
+  }
+  __syncthreads();
+  // (3) place the survivors by rank
+  const int ns = min(nsurv, kHeadsMaxSurv);
+  if (t < ns) {
+    const float v = sv[t];
+    const int id = si[t];
+    int rank = 0;
+    for (int q = 0; q < ns; ++q) rank += topk_before(sv[q], si[q], v, id) ? 1 : 0;
+    if (rank < k) {
+      out_vals[(size_t)r * k + rank] = v;
+      out_ids[(size_t)r * k + rank] = id;
+    }
+  }
+}
+
 cudaError_t launch_topk_merge(const float *vals, const int *ids, int rows, int ncand_per_row,
                               long long row_stride, long long part_stride, int parts, int k,
                               int *out_ids, float *out_vals, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  cudaError_t e = launch_pdl(topk_merge_kernel, dim3(rows), dim3(256), 0, s, vals, ids, ncand_per_row,
-                             row_stride, part_stride, parts, k, out_ids, out_vals);
+  cudaError_t e;
+  if (ids && parts > 1 && parts <= kHeadsThreads && ncand_per_row == k && k <= kTopkMax)
+    e = launch_pdl(topk_merge_heads_kernel, dim3(rows), dim3(kHeadsThreads), 0, s, vals, ids, ncand_per_row,
+                   row_stride, part_stride, parts, k, out_ids, out_vals);
+  else
+    e = launch_pdl(topk_merge_kernel, dim3(rows), dim3(256), 0, s, vals, ids, ncand_per_row, row_stride,
+                   part_stride, parts, k, out_ids, out_vals);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

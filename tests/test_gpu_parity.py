@@ -129,6 +129,23 @@ def test_lm_head_topk_stage(w):
                 assert 5 in row and row.index(5) < row.index(dup)
 
 
+@pytest.mark.parametrize("V,k", [(1000, 16), (1000, 5), (4096, 1)])
+def test_lm_head_topk_few_ranges(V, k):
+    """Fewer vocabulary ranges than k (every candidate reaches the final placement) and
+    small k, on the exact logits the kernel also returns."""
+    w = di.TINY.with_(name=f"tiny_v{V}", V=V)
+    dr, W, _ = make(w, 64, w.B)
+    hid_bits = di.normal_bf16("hidden_fr", (w.nb, w.B, w.D), 1.0)
+    ids = torch.empty(w.nb, w.B - 1, k, dtype=torch.int32, device="cuda")
+    vals = torch.empty(w.nb, w.B - 1, k, dtype=torch.float32, device="cuda")
+    logits = torch.empty(w.nb, w.B - 1, w.V, dtype=torch.float32, device="cuda")
+    dr.lm_head_topk(w.nb, bf16(hid_bits), k, ids, vals, logits)
+    gl = logits.cpu().numpy().reshape(-1, V).astype(np.float64)
+    oi, ov = orc.topk(gl, k)  # the selection rule on the GPU's own logits: exact
+    assert np.array_equal(ids.cpu().numpy().reshape(-1, k), oi)
+    assert np.array_equal(vals.cpu().numpy().reshape(-1, k), ov.astype(np.float32))
+
+
 # ----------------------------------------------------------------------------- ctx_project
 
 @pytest.mark.parametrize("w", [di.TINY, MEDIUM, MEDIUM_ALL], ids=lambda w: w.name)
