@@ -632,36 +632,54 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   const int R = G * p.B;
   const int r = blockIdx.y * kMergeWarps + warp;
   if (r >= R) return;
-  const long long T = attn_units_before(p, p.nb, lane);
+  // total units and the units before this pair, in one pass over the sequences
+  long long T = 0, before = 0;
+  for (int q = lane; q < p.nb; q += 32) {
+    const int u = attn_units(p, q);
+    T += u;
+    before += q < i ? u : 0;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    T += __shfl_xor_sync(0xffffffffu, T, o);
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+  }
+  T *= p.Hkv;
   const int Ge = T < p.grid ? static_cast<int>(T) : p.grid;
   const int U = attn_units(p, i);
-  const long long A = attn_units_before(p, i, lane) + (long long)g * U;
+  const long long A = before * p.Hkv + (long long)g * U;
   const int c0 = attn_cta_of(T, Ge, A), c1 = attn_cta_of(T, Ge, A + U - 1);
   if (c0 == c1) return;  // written whole by the attention kernel
   const float sl2 = rsqrtf(static_cast<float>(HD)) * 1.4426950408889634f;
   {
-    float M = -FLT_MAX;
-    for (int c = c0; c <= c1; ++c) M = fmaxf(M, p.part_ml[((size_t)(pair + c) * R + r) * 2]);
-    float L = 0.f, acc[E];
+    // one pass, rescaling to the running maximum (the partials' loads do not depend on
+    // each other, so they are in flight together)
+    float M = -FLT_MAX, L = 0.f, acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll 4
     for (int c = c0; c <= c1; ++c) {
       const size_t row = (size_t)(pair + c) * R + r;
       const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + row * 2);
-      const float wgt = exp2f((ml.x - M) * sl2);
-      L += ml.y * wgt;
+      float v[E];
       const float *src = p.part_o + row * HD + lane * E;
       if constexpr (E == 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(src);
-        acc[0] += v.x * wgt;
-        acc[1] += v.y * wgt;
-        acc[2] += v.z * wgt;
-        acc[3] += v.w * wgt;
+        const float4 x = *reinterpret_cast<const float4 *>(src);
+        v[0] = x.x;
+        v[1] = x.y;
+        v[2] = x.z;
+        v[3] = x.w;
       } else {
-        const float2 v = *reinterpret_cast<const float2 *>(src);
-        acc[0] += v.x * wgt;
-        acc[1] += v.y * wgt;
+        const float2 x = *reinterpret_cast<const float2 *>(src);
+        v[0] = x.x;
+        v[1] = x.y;
       }
+      const float Mn = fmaxf(M, ml.x);
+      const float a_old = exp2f((M - Mn) * sl2), a_new = exp2f((ml.x - Mn) * sl2);
+      L = L * a_old + ml.y * a_new;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = acc[e] * a_old + v[e] * a_new;
+      M = Mn;
     }
     const float inv = 1.0f / L;
     const int jq = r / G, hq = r % G;
