@@ -119,7 +119,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct WsLayout {
   size_t status = 0;
   size_t pre = 0, h = 0;                       // ctx_project
-  size_t x = 0, u = 0, qkv = 0, o = 0, act = 0, xb = 0, corr = 0;  // draft_block
+  size_t x = 0, u = 0, qkv = 0, o = 0, act = 0, xb = 0, corr = 0, ss = 0;  // draft_block
   size_t apart = 0, aml = 0;                   // attention partials
   size_t tk_vals = 0, tk_ids = 0;              // LM head top-k partial lists
   size_t sel_e = 0, sel_ab = 0, sel_g = 0;     // selector
@@ -170,6 +170,7 @@ void plan_workspace(dflash_handle_s *h) {
   L.o = take((size_t)Mb * c.Hq * c.hd * 2);
   L.act = take((size_t)Mb * c.F * 2);
   L.xb = take((size_t)Mb * c.D * 2);
+  L.ss = take((size_t)Mb * ((c.D + 127) / 128) * 4);  // deferred RMSNorm partial sums
   L.corr = take((c.flags & DFLASH_FLAG_CONV) ? (size_t)Mb * 2 * (c.D / c.conv_group) * 4 : 0);
   L.apart_ctas = apart_max;
   L.apart_bytes = apart_max * rows_attn * c.hd * 4;
@@ -555,12 +556,30 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
   AttnParams ap{};
   DF_TRY(attention_params(h, w, nb, qkv, qkv_n, kcache, vcache, ctx_len, max_ctx, o, &ap));
 
+  // Without the DFlash 2 convs the pre-norms after layer 0's attention norm are deferred:
+  // the residual GEMMs write u = bf16(x * g) and partial sums of x^2 (ss), and the next
+  // GEMM (gate|up, or the next layer's QKV) scales its rows by rsqrt(mean x^2 + eps).
+  // With the convs, x changes after those epilogues, so the norms stay separate kernels.
+  const bool deferred = !conv;
+  float *ss = w.at<float>(h->ws.ss);
+  const int ss_n = (c.D + kBN - 1) / kBN;
+  auto defer_out = [&](GemmParams &p, const void *g_next) {
+    if (!deferred || !g_next) return;
+    p.xg_out = u;
+    p.g_next = static_cast<const uint16_t *>(g_next);
+    p.ss_out = ss;
+  };
+  auto defer_in = [&](GemmParams &p) {
+    if (!deferred) return;
+    p.ss_in = ss;
+    p.ss_n = ss_n;
+    p.inv_d = 1.0f / static_cast<float>(c.D);
+    p.eps = c.eps;
+  };
   for (int n = 0; n < c.N; ++n) {
     const dflash_layer_weights &Lw = h->layers[n];
     if (conv) {
       DF_TRY(run_conv(h, w, n, 0, M, x, s));
-      DF_CUDA(launch_rmsnorm(x, M, c.D, bf(Lw.g_attn), c.eps, u, s));
-    } else if (n > 0) {
       DF_CUDA(launch_rmsnorm(x, M, c.D, bf(Lw.g_attn), c.eps, u, s));
     }
     uint16_t *kc_n = static_cast<uint16_t *>(kcache) + n * cache_layer_elems(c);
@@ -584,6 +603,7 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
       p.vc = vc_n;
       p.Hkv = c.Hkv;
       p.Cmax = c.Cmax;
+      if (n > 0) defer_in(p);
       DF_TRY(run_gemm(h, p, kBN, s));
     }
     ap.layer_row0 = n * c.max_batch * c.Hkv * c.Cmax;
@@ -599,13 +619,14 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
       p.epi = EPI_RESID;
       p.xres = x;
       p.ldo = c.D;
+      defer_out(p, Lw.g_ffn);
       DF_TRY(run_gemm(h, p, kBN, s));
     }
     if (conv) {
       DF_TRY(run_conv(h, w, n, 1, M, x, s));
       DF_TRY(run_conv(h, w, n, 2, M, x, s));
+      DF_CUDA(launch_rmsnorm(x, M, c.D, bf(Lw.g_ffn), c.eps, u, s));
     }
-    DF_CUDA(launch_rmsnorm(x, M, c.D, bf(Lw.g_ffn), c.eps, u, s));
     {  // act = silu(u W_gate^T) * (u W_up^T)
       GemmParams p = base_params(h, w);
       p.tmA = tm_u;
@@ -618,6 +639,7 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
       p.epi = EPI_SWIGLU;
       p.out = act;
       p.ldo = c.F;
+      defer_in(p);
       DF_TRY(run_gemm(h, p, kBNGateUp, s));
     }
     {  // x += act W_down^T
@@ -631,6 +653,7 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
       p.epi = EPI_RESID;
       p.xres = x;
       p.ldo = c.D;
+      if (n + 1 < c.N) defer_out(p, h->layers[n + 1].g_attn);
       DF_TRY(run_gemm(h, p, kBN, s));
     }
     if (conv) DF_TRY(run_conv(h, w, n, 3, M, x, s));

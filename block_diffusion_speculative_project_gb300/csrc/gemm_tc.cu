@@ -154,7 +154,8 @@ __device__ __forceinline__ void store_f32_32(float *dst, const float (&v)[32], i
   }
 }
 
-__device__ __forceinline__ void add_f32_32(float *dst, const float (&v)[32], int nvalid) {
+// dst += v; the new values are also returned in out (which may alias v).
+__device__ __forceinline__ void add_f32_32(float *dst, const float (&v)[32], int nvalid, float (&out)[32]) {
   if (nvalid >= 32 && aligned16(dst)) {
     float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
@@ -165,12 +166,42 @@ __device__ __forceinline__ void add_f32_32(float *dst, const float (&v)[32], int
       x.z += v[4 * q + 2];
       x.w += v[4 * q + 3];
       d4[q] = x;
+      out[4 * q] = x.x;
+      out[4 * q + 1] = x.y;
+      out[4 * q + 2] = x.z;
+      out[4 * q + 3] = x.w;
     }
   } else {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (i < nvalid) dst[i] += v[i];
+      if (i < nvalid) {
+        const float x = dst[i] + v[i];
+        dst[i] = x;
+        out[i] = x;
+      }
   }
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Deferred RMSNorm factor of a row: rsqrt(mean of squares + eps) from its partial sums.
+__device__ __forceinline__ float deferred_rms(const GemmParams &p, int row) {
+  const float *s = p.ss_in + (size_t)row * p.ss_n;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  int i = 0;
+  if ((p.ss_n & 3) == 0 && aligned16(s)) {
+    for (; i < p.ss_n; i += 4) {
+      const float4 x = *reinterpret_cast<const float4 *>(s + i);
+      a[0] += x.x;
+      a[1] += x.y;
+      a[2] += x.z;
+      a[3] += x.w;
+    }
+  }
+  for (; i < p.ss_n; ++i) a[i & 3] += s[i];
+  return rsqrtf(((a[0] + a[1]) + (a[2] + a[3])) * p.inv_d + p.eps);
 }
 
 // Rotation angle pos * inv_freq reduced to [-pi, pi] with a two-constant split of
@@ -246,7 +277,7 @@ template <int BN, int EPI, class Fetch>
 __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t, int row,
                                               bool row_ok, Fetch &&fetch, TopkState &tk,
                                               float *stash) {
-  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_RESID) {
+  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32) {
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       float v[32];
@@ -256,16 +287,58 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
       if (row_ok && nval > 0) {
         if constexpr (EPI == EPI_BF16)
           store_bf16_32(static_cast<uint16_t *>(p.out) + row * p.ldo + col0, v, nval);
-        else if constexpr (EPI == EPI_F32)
-          store_f32_32(static_cast<float *>(p.out) + row * p.ldo + col0, v, nval);
         else
-          add_f32_32(p.xres + row * p.ldo + col0, v, nval);
+          store_f32_32(static_cast<float *>(p.out) + row * p.ldo + col0, v, nval);
       }
     }
+  } else if constexpr (EPI == EPI_RESID) {
+    float ss = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      fetch(c, v);
+      const int col0 = t.n * BN + c * 32;
+      const int nval = min(32, p.N - col0);
+      if (row_ok && nval > 0) {
+        add_f32_32(p.xres + row * p.ldo + col0, v, nval, v);  // v <- x_new
+        if (p.xg_out) {
+          float gv[32];
+          if (nval >= 32 && aligned16(p.g_next + col0)) {
+            const uint4 *g4 = reinterpret_cast<const uint4 *>(p.g_next + col0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 w = g4[q];
+              const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                gv[8 * q + 2 * h] = __uint_as_float(wd[h] << 16);
+                gv[8 * q + 2 * h + 1] = __uint_as_float(wd[h] & 0xFFFF0000u);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) gv[i] = i < nval ? bf16_bits_to_f32(p.g_next[col0 + i]) : 0.f;
+          }
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float x0 = i < nval ? v[i] : 0.f, x1 = i + 1 < nval ? v[i + 1] : 0.f;
+            s0 = fmaf(x0, x0, s0);
+            s1 = fmaf(x1, x1, s1);
+            v[i] = x0 * gv[i];
+            v[i + 1] = x1 * gv[i + 1];
+          }
+          ss += s0 + s1;
+          store_bf16_32(p.xg_out + row * p.ldo + col0, v, nval);
+        }
+      }
+    }
+    if (p.xg_out && row_ok) p.ss_out[(size_t)row * p.n_tiles + t.n] = ss;
   } else if constexpr (EPI == EPI_ROPE) {
     const int half = p.hd >> 1;
     int seq = 0, pos = 0;
     bool pos_ok = false;
+    const float rs = (p.ss_in && row_ok) ? deferred_rms(p, row) : 1.f;
     if (row_ok) {
       seq = row / p.rows_per_seq;
       pos = p.ctx_len[seq] + row % p.rows_per_seq;
@@ -297,6 +370,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
         fetch((h0 + cc) >> 5, a);
         fetch((h0 + half + cc) >> 5, b);
         if (o) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            a[i] *= rs;
+            b[i] *= rs;
+          }
           if (rot) rope_pair(p, pos, cc, a, b);
           store_bf16_32(o + cc, a, 32);
           store_bf16_32(o + half + cc, b, 32);
@@ -304,6 +382,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
       }
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
+    const float rs = (p.ss_in && row_ok) ? deferred_rms(p, row) : 1.f;
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c) {
       float g[32], u[32];
@@ -313,7 +392,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
       const int nval = min(32, p.N - col0);
       if (row_ok && nval > 0) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + expf(-g[i])) * u[i];
+        for (int i = 0; i < 32; ++i) {
+          const float gi = g[i] * rs;
+          g[i] = gi / (1.0f + expf(-gi)) * (u[i] * rs);
+        }
         store_bf16_32(static_cast<uint16_t *>(p.out) + row * p.ldo + col0, g, nval);
       }
     }

@@ -113,6 +113,17 @@ struct GemmParams {
   int *status;
   int max_spin;
   int stall;         // test hook: issue no loads so the waits run out
+  // Deferred RMSNorm (pre-norm residual stream): the EPI_RESID epilogue also writes
+  // xg = bf16(x_new * g_next) and per-(row, column tile) partial sums of x_new^2
+  // (ss_out [M][n_tiles]); a consumer GEMM reading xg as A scales its accumulator row i
+  // by rsqrt(sum(ss_in[i][0..ss_n)) * inv_d + eps) before its epilogue (ROPE, SWIGLU),
+  // which equals the GEMM of RMSNorm(x) * g.
+  uint16_t *xg_out;
+  const uint16_t *g_next;
+  float *ss_out;
+  const float *ss_in;
+  int ss_n;
+  float inv_d, eps;
   int csplit;        // >1: split K across the CTAs of a cluster, reduce through DSMEM
   int slabs;         // 2: A and B maps carry a 64-column slab dimension and each stage
                      // loads two slabs per copy (plain 128-wide GEMMs with K % 64 == 0)

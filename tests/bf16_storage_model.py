@@ -4,8 +4,10 @@ full-size end-to-end hidden comparison (tests/test_gpu_fullsize.py).
 It builds the same inputs as that test for one sampled sequence and computes the drafter
 hidden twice with oracle functions: exactly (the fp64 oracle) and with every value that
 the kernel path stores in bf16 rounded to bf16 at that point (h and the appended K_c, V_c
-rows of the context projection; per layer the conv inputs of the correction GEMMs,
-u = RMSNorm(x), q, k_b, v_b, P, o and act; the final hidden). Everything else stays fp64.
+rows of the context projection; per layer the conv inputs of the correction GEMMs, the
+normalised GEMM input (u = RMSNorm(x) * g, or without the convs after layer 0's attention
+norm bf16(x * g) with the rsqrt(mean x^2 + eps) row factor applied after the GEMM), q,
+k_b, v_b, P, o and act; the final hidden). Everything else stays fp64.
 It prints the model's deviation from the exact oracle.
 
     python tests/bf16_storage_model.py WORKLOAD SEQUENCE
@@ -76,14 +78,19 @@ def model(w, si):
         prev[1:] = x[:-1]
         return k0 * x + k1 * prev
 
+    def rms(x):
+        return 1.0 / np.sqrt((x * x).mean(axis=1, keepdims=True) + w.eps)
+
     pos = C + np.arange(B)
     grp = Hq // Hkv
     for n in range(w.N):
         p = f"layer{n}."
         if conv:
             x = dconv(x, p + "conv0.")
-        u = rb(orc.rmsnorm(x, W[p + "g_attn"], w.eps))
-        qkv = u @ W[p + "W_qkv"].T
+        if conv or n == 0:
+            qkv = rb(orc.rmsnorm(x, W[p + "g_attn"], w.eps)) @ W[p + "W_qkv"].T
+        else:  # deferred norm: bf16(x * g) times the row factor after the GEMM
+            qkv = (rb(x * W[p + "g_attn"]) @ W[p + "W_qkv"].T) * rms(x)
         q = rb(orc.rope(qkv[:, :Hq * hd].reshape(B, Hq, hd), pos, w.rope_base))
         kb = rb(orc.rope(qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(B, Hkv, hd), pos, w.rope_base))
         vb = rb(qkv[:, (Hq + Hkv) * hd:].reshape(B, Hkv, hd))
@@ -98,8 +105,13 @@ def model(w, si):
         x = x + rb(o.reshape(B, -1)) @ W[p + "W_o"].T
         if conv:
             x = dconv(dconv(x, p + "conv1."), p + "conv2.")
-        u = rb(orc.rmsnorm(x, W[p + "g_ffn"], w.eps))
-        x = x + rb(orc.silu(u @ W[p + "W_gate"].T) * (u @ W[p + "W_up"].T)) @ W[p + "W_down"].T
+        if conv:
+            u = rb(orc.rmsnorm(x, W[p + "g_ffn"], w.eps))
+            gate, up = u @ W[p + "W_gate"].T, u @ W[p + "W_up"].T
+        else:
+            ug, r = rb(x * W[p + "g_ffn"]), rms(x)
+            gate, up = (ug @ W[p + "W_gate"].T) * r, (ug @ W[p + "W_up"].T) * r
+        x = x + rb(orc.silu(gate) * up) @ W[p + "W_down"].T
         if conv:
             x = dconv(x, p + "conv3.")
     return exact, rb(orc.rmsnorm(x, W["g_final"], w.eps))
