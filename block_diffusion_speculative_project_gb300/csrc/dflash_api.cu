@@ -122,7 +122,7 @@ struct WsLayout {
   size_t x = 0, u = 0, qkv = 0, o = 0, act = 0, xb = 0, corr = 0, ss = 0;  // draft_block
   size_t apart = 0, aml = 0;                   // attention partials
   size_t tk_vals = 0, tk_ids = 0;              // LM head top-k partial lists
-  size_t sel_e = 0, sel_ab = 0, sel_g = 0;     // selector
+  size_t sel_e = 0, sel_ab = 0, sel_g = 0, sel_t = 0;  // selector
   size_t total = 0;
   size_t apart_bytes = 0, apart_ctas = 0;
 };
@@ -184,6 +184,7 @@ void plan_workspace(dflash_handle_s *h) {
     L.sel_e = take((size_t)sel_rows * c.D * 2);
     L.sel_ab = take((size_t)sel_rows * 2 * c.sel_dim * 4);
     L.sel_g = take((size_t)Ml * c.sel_dim * 4);
+    L.sel_t = take((size_t)Ml * c.k_top * c.k_top * 4);  // step score tables
   }
   L.total = off;
 }
@@ -271,13 +272,16 @@ int attention_params(const dflash_handle_s *h, const Ws &w, int nb, const void *
 }
 
 // One DFlash 2 conv on the fp32 residual rows x [M, D].
+// xb_ready: the bf16 copy of x (workspace xb) was written by the producer of x (a
+// residual epilogue or the previous conv); write_next: also leave bf16(x') in xb for a
+// conv that follows directly.
 int run_conv(const dflash_handle_s *h, const Ws &w, int layer, int which, int M, float *x,
-             cudaStream_t s) {
+             cudaStream_t s, bool xb_ready = false, bool write_next = false) {
   const auto &c = h->cfg;
   const int ng = c.D / c.conv_group;
   uint16_t *xb = w.at<uint16_t>(w.L.xb);
   float *corr = w.at<float>(w.L.corr);
-  DF_CUDA(launch_f32_to_bf16(x, xb, (long long)M * c.D, s));
+  if (!xb_ready) DF_CUDA(launch_f32_to_bf16(x, xb, (long long)M * c.D, s));
   GemmParams p = base_params(h, w);
   DF_TRY(encode_act(&p.tmA, xb, M, c.D));
   p.tmB[0] = h->tm_c0[layer * 4 + which];
@@ -290,8 +294,8 @@ int run_conv(const dflash_handle_s *h, const Ws &w, int layer, int which, int M,
   p.out = corr;
   p.ldo = 2 * ng;
   DF_TRY(run_gemm(h, p, kBN, s));
-  DF_CUDA(launch_conv_apply(x, corr, bf(h->layers[layer].conv_base[which]), M, c.D, c.B,
-                            c.conv_group, s));
+  DF_CUDA(launch_conv_apply(x, write_next ? xb : nullptr, corr, bf(h->layers[layer].conv_base[which]), M, c.D,
+                            c.B, c.conv_group, s));
   return DFLASH_OK;
 }
 
@@ -579,7 +583,7 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
   for (int n = 0; n < c.N; ++n) {
     const dflash_layer_weights &Lw = h->layers[n];
     if (conv) {
-      DF_TRY(run_conv(h, w, n, 0, M, x, s));
+      DF_TRY(run_conv(h, w, n, 0, M, x, s, /*xb_ready=*/n > 0));
       DF_CUDA(launch_rmsnorm(x, M, c.D, bf(Lw.g_attn), c.eps, u, s));
     }
     uint16_t *kc_n = static_cast<uint16_t *>(kcache) + n * cache_layer_elems(c);
@@ -620,11 +624,12 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
       p.xres = x;
       p.ldo = c.D;
       defer_out(p, Lw.g_ffn);
+      if (conv) p.xg_out = w.at<uint16_t>(w.L.xb);  // bf16(x) for conv1
       DF_TRY(run_gemm(h, p, kBN, s));
     }
     if (conv) {
-      DF_TRY(run_conv(h, w, n, 1, M, x, s));
-      DF_TRY(run_conv(h, w, n, 2, M, x, s));
+      DF_TRY(run_conv(h, w, n, 1, M, x, s, true, /*write_next=*/true));
+      DF_TRY(run_conv(h, w, n, 2, M, x, s, true));
       DF_CUDA(launch_rmsnorm(x, M, c.D, bf(Lw.g_ffn), c.eps, u, s));
     }
     {  // act = silu(u W_gate^T) * (u W_up^T)
@@ -654,9 +659,10 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
       p.xres = x;
       p.ldo = c.D;
       if (n + 1 < c.N) defer_out(p, h->layers[n + 1].g_attn);
+      if (conv) p.xg_out = w.at<uint16_t>(w.L.xb);  // bf16(x) for conv3
       DF_TRY(run_gemm(h, p, kBN, s));
     }
-    if (conv) DF_TRY(run_conv(h, w, n, 3, M, x, s));
+    if (conv) DF_TRY(run_conv(h, w, n, 3, M, x, s, true, /*write_next=*/n + 1 < c.N));
   }
   DF_CUDA(launch_rmsnorm(x, M, c.D, bf(h->w.g_final), c.eps, static_cast<uint16_t *>(out_hidden), s));
   return DFLASH_OK;
@@ -874,7 +880,8 @@ int dflash2_select(dflash_handle_t h, int nb, int k, const int32_t *topk_ids, co
     p.ldo = c.sel_dim;
     DF_TRY(run_gemm(h, p, kBN, s));
   }
-  DF_CUDA(launch_select_walk(topk_ids, topk_vals, ab, gp, block_ids, nb, c.B, k, c.sel_dim, out_path, s));
+  DF_CUDA(launch_select_walk(topk_ids, topk_vals, ab, gp, w.at<float>(h->ws.sel_t), nb, c.B, k, c.sel_dim,
+                             out_path, s));
   return DFLASH_OK;
 }
 

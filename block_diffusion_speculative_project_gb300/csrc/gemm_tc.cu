@@ -303,7 +303,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
         add_f32_32(p.xres + row * p.ldo + col0, v, nval, v);  // v <- x_new
         if (p.xg_out) {
           float gv[32];
-          if (nval >= 32 && aligned16(p.g_next + col0)) {
+          if (!p.g_next) {  // plain bf16 copy of x (input of a DFlash 2 conv)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) gv[i] = 1.f;
+          } else if (nval >= 32 && aligned16(p.g_next + col0)) {
             const uint4 *g4 = reinterpret_cast<const uint4 *>(p.g_next + col0);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -333,7 +336,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
         }
       }
     }
-    if (p.xg_out && row_ok) p.ss_out[(size_t)row * p.n_tiles + t.n] = ss;
+    if (p.ss_out && row_ok) p.ss_out[(size_t)row * p.n_tiles + t.n] = ss;
   } else if constexpr (EPI == EPI_ROPE) {
     const int half = p.hd >> 1;
     int seq = 0, pos = 0;

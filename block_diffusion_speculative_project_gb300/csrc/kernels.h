@@ -114,8 +114,8 @@ struct GemmParams {
   int max_spin;
   int stall;         // test hook: issue no loads so the waits run out
   // Deferred RMSNorm (pre-norm residual stream): the EPI_RESID epilogue also writes
-  // xg = bf16(x_new * g_next) and per-(row, column tile) partial sums of x_new^2
-  // (ss_out [M][n_tiles]); a consumer GEMM reading xg as A scales its accumulator row i
+  // xg = bf16(x_new * g_next) (bf16(x_new) when g_next is null) and, when ss_out is set,
+  // per-(row, column tile) partial sums of x_new^2 (ss_out [M][n_tiles]); a consumer GEMM reading xg as A scales its accumulator row i
   // by rsqrt(sum(ss_in[i][0..ss_n)) * inv_d + eps) before its epilogue (ROPE, SWIGLU),
   // which equals the GEMM of RMSNorm(x) * g.
   uint16_t *xg_out;
@@ -163,14 +163,14 @@ cudaError_t launch_topk_merge(const float *vals, const int *ids, int rows, int n
                               long long row_stride, long long part_stride, int parts, int k,
                               int *out_ids, float *out_vals, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float *x, uint16_t *y, long long n, cudaStream_t s);
-cudaError_t launch_conv_apply(float *x, const float *corr, const uint16_t *base, int M, int D,
+cudaError_t launch_conv_apply(float *x, uint16_t *xb_out, const float *corr, const uint16_t *base, int M, int D,
                               int B, int group, cudaStream_t s);
 cudaError_t launch_gather_select(const int *block_ids, const int *cand_ids, int nb, int B, int k,
                                  const uint16_t *E, int D, int V, uint16_t *out, int *status,
                                  cudaStream_t s);
 cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, const float *AB,
-                               const float *G, const int *block_ids, int nb, int B, int k,
-                               int sel_dim, int *path, cudaStream_t s);
+                               const float *G, float *table, int nb, int B, int k, int sel_dim, int *path,
+                               cudaStream_t s);
 
 // ---------------------------------------------------------------- attention
 

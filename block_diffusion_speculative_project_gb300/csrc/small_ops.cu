@@ -404,8 +404,9 @@ cudaError_t launch_f32_to_bf16(const float *x, uint16_t *y, long long n, cudaStr
 // x'[t] = (b0 + c0[t][ch/group]) * x[t] + (b1 + c1[t][ch/group]) * x[t-1], x[-1] = 0.
 // corr [M, 2*D/group] holds c0 in columns [0, D/group) and c1 after them.
 // Rows are visited from last to first so x[t-1] is read before it is overwritten.
-__global__ void conv_apply_kernel(float *x, const float *corr, const uint16_t *base, int D, int B,
-                                  int group) {
+// Also writes bf16(x') into xb_out (when set): the input of the next conv's GEMM.
+__global__ void conv_apply_kernel(float *x, uint16_t *xb_out, const float *corr, const uint16_t *base, int D,
+                                  int B, int group) {
   griddep_wait();
   griddep_launch();
   const int i = blockIdx.x;
@@ -414,6 +415,7 @@ __global__ void conv_apply_kernel(float *x, const float *corr, const uint16_t *b
   const int ng = D / group;
   const float b0 = bits_to_f32(base[ch]), b1 = bits_to_f32(base[D + ch]);
   float *xb = x + (size_t)i * B * D;
+  uint16_t *ob = xb_out ? xb_out + (size_t)i * B * D : nullptr;
   const float *cb = corr + (size_t)i * B * 2 * ng;
   float prev = xb[(size_t)(B - 1) * D + ch];
   for (int t = B - 1; t >= 0; --t) {
@@ -421,15 +423,17 @@ __global__ void conv_apply_kernel(float *x, const float *corr, const uint16_t *b
     prev = t > 0 ? xb[(size_t)(t - 1) * D + ch] : 0.f;
     const float k0 = b0 + cb[(size_t)t * 2 * ng + ch / group];
     const float k1 = b1 + cb[(size_t)t * 2 * ng + ng + ch / group];
-    xb[(size_t)t * D + ch] = k0 * cur + k1 * prev;
+    const float y = k0 * cur + k1 * prev;
+    xb[(size_t)t * D + ch] = y;
+    if (ob) ob[(size_t)t * D + ch] = f32_to_bits(y);
   }
 }
 
-cudaError_t launch_conv_apply(float *x, const float *corr, const uint16_t *base, int M, int D,
+cudaError_t launch_conv_apply(float *x, uint16_t *xb_out, const float *corr, const uint16_t *base, int M, int D,
                               int B, int group, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   dim3 grid(M / B, (D + 255) / 256);
-  cudaError_t e = launch_pdl(conv_apply_kernel, grid, dim3(256), 0, s, x, corr, base, D, B, group);
+  cudaError_t e = launch_pdl(conv_apply_kernel, grid, dim3(256), 0, s, x, xb_out, corr, base, D, B, group);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -465,53 +469,79 @@ cudaError_t launch_gather_select(const int *block_ids, const int *cand_ids, int 
 // Selector walk, one CTA per sequence. AB [rows, 2*sel]: A | B projections of the
 // gathered tokens; per sequence the rows are [anchor, then candidate (t, c) for
 // t = 1..B-1, c = 0..k-1]. G [nb*(B-1), sel]: W_G z_t before the sigmoid.
-__global__ void __launch_bounds__(256) select_walk_kernel(const int *cand_ids,
-                                                          const float *cand_vals, const float *AB,
-                                                          const float *G, const int *block_ids,
-                                                          int B, int k, int sel, int *path) {
+// The scores of every step do not depend on the walk: for each offset t and each
+// possible previous choice a (the anchor at t = 1, one of the k candidates of t - 1
+// after that), S_t(a, b) = U_t(b) + sum_d A(a)_d G_t,d B(b)_d for the k candidates b of t.
+// select_table_kernel computes all of them at once (one CTA per (t, sequence), one thread
+// per (a, b)); select_walk_kernel then walks each sequence's table in shared memory:
+// a_t = argmax_b S_t(a_{t-1}, b), ties to the lower id.
+__global__ void __launch_bounds__(256) select_table_kernel(const float *cand_vals, const float *AB,
+                                                           const float *G, int B, int k, int sel,
+                                                           float *table) {
   griddep_wait();
   griddep_launch();
-  __shared__ float score[kTopkMax];
-  __shared__ int s_arow;
-  const int i = blockIdx.x;
+  extern __shared__ float gate[];  // [sel]
+  const int t = blockIdx.x + 1, i = blockIdx.y;
+  const float *Gt = G + ((size_t)i * (B - 1) + (t - 1)) * sel;
+  for (int d = threadIdx.x; d < sel; d += blockDim.x) gate[d] = 1.0f / (1.0f + expf(-Gt[d]));
+  __syncthreads();
+  const int ai = threadIdx.x >> 4, b = threadIdx.x & 15;
+  if (b >= k || ai >= k || (t == 1 && ai > 0)) return;
   const int per = 1 + (B - 1) * k;
   const float *ABi = AB + (size_t)i * per * 2 * sel;
-  if (threadIdx.x == 0) s_arow = 0;
+  const int arow = t == 1 ? 0 : 1 + (t - 2) * k + ai;
+  const float4 *ar = reinterpret_cast<const float4 *>(ABi + (size_t)arow * 2 * sel);
+  const float4 *br = reinterpret_cast<const float4 *>(ABi + (size_t)(1 + (t - 1) * k + b) * 2 * sel + sel);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int q = 0; q < sel / 4; ++q) {
+    const float4 x = ar[q], y = br[q];
+    const float *g = gate + 4 * q;
+    acc[0] = fmaf(x.x * g[0], y.x, acc[0]);
+    acc[1] = fmaf(x.y * g[1], y.y, acc[1]);
+    acc[2] = fmaf(x.z * g[2], y.z, acc[2]);
+    acc[3] = fmaf(x.w * g[3], y.w, acc[3]);
+  }
+  const size_t tr = (size_t)i * (B - 1) + (t - 1);
+  table[(tr * k + ai) * k + b] = cand_vals[tr * k + b] + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+}
+
+__global__ void __launch_bounds__(256) select_walk_kernel(const int *cand_ids, const float *table, int B,
+                                                          int k, int *path) {
+  griddep_wait();
+  griddep_launch();
+  extern __shared__ float tab[];  // [B-1][k][k] scores, then [B-1][k] candidate ids
+  const int i = blockIdx.x;
+  const int n = (B - 1) * k * k;
+  int *sid = reinterpret_cast<int *>(tab + n);
+  const float *ti = table + (size_t)i * n;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) tab[e] = ti[e];
+  for (int e = threadIdx.x; e < (B - 1) * k; e += blockDim.x) sid[e] = cand_ids[(size_t)i * (B - 1) * k + e];
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int t = 1; t < B; ++t) {
-    const int arow = s_arow;
-    const float *Ga = G + ((size_t)i * (B - 1) + (t - 1)) * sel;
-    for (int c = warp; c < k; c += 8) {
-      const int brow = 1 + (t - 1) * k + c;
-      float acc = 0.f;
-      for (int d = lane; d < sel; d += 32) {
-        const float gate = 1.0f / (1.0f + expf(-Ga[d]));
-        acc += ABi[(size_t)arow * 2 * sel + d] * gate * ABi[(size_t)brow * 2 * sel + sel + d];
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) score[c] = cand_vals[((size_t)i * (B - 1) + (t - 1)) * k + c] + acc;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const int *ids = cand_ids + ((size_t)i * (B - 1) + (t - 1)) * k;
+  if (threadIdx.x == 0) {
+    int ai = 0;
+    for (int t = 1; t < B; ++t) {
+      const float *row = tab + ((t - 1) * k + ai) * k;
+      const int *ids = sid + (t - 1) * k;
       int best = 0;
       for (int c = 1; c < k; ++c)
-        if (topk_before(score[c], ids[c], score[best], ids[best])) best = c;
+        if (topk_before(row[c], ids[c], row[best], ids[best])) best = c;
       path[(size_t)i * (B - 1) + (t - 1)] = ids[best];
-      s_arow = 1 + (t - 1) * k + best;
+      ai = best;
     }
-    __syncthreads();
   }
 }
 
 cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, const float *AB,
-                               const float *G, const int *block_ids, int nb, int B, int k,
-                               int sel_dim, int *path, cudaStream_t s) {
+                               const float *G, float *table, int nb, int B, int k, int sel_dim, int *path,
+                               cudaStream_t s) {
   if (nb <= 0) return cudaSuccess;
-  cudaError_t e = launch_pdl(select_walk_kernel, dim3(nb), dim3(256), 0, s, cand_ids, cand_vals, AB, G,
-                             block_ids, B, k, sel_dim, path);
+  if (k > 16 || sel_dim % 4 || B < 2) return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(select_table_kernel, dim3(B - 1, nb), dim3(256), (size_t)sel_dim * sizeof(float), s,
+                             cand_vals, AB, G, B, k, sel_dim, table);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(select_walk_kernel, dim3(nb), dim3(256), (size_t)(B - 1) * k * (k + 1) * sizeof(float), s, cand_ids,
+                 static_cast<const float *>(table), B, k, path);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
