@@ -20,6 +20,7 @@ Value recipe (the pages give no trained weights; these stand in for them):
                                residual stream diverges within two layers
   * verifier hidden states   ~ N(0, 1)
   * anchors                  ~ U{0 .. V-2};  mask id = V-1
+  * FiLM relay MLP W1, W2    ~ N(0, 0.02) (weights); its conditioning tokens ~ U{0 .. V-2}
 """
 from __future__ import annotations
 
@@ -35,6 +36,7 @@ CHUNK = 1 << 24  # elements per independent stream chunk
 FLAG_RELAY = 1
 FLAG_CONV = 2
 FLAG_SELECT = 4
+FLAG_FILM = 8
 
 
 @dataclass(frozen=True)
@@ -62,6 +64,11 @@ class Workload:
     eps: float = 1.0e-6
     sel_dim: int = 256
     conv_group: int = 16
+    film_dim: int = 0  # hidden width of the FiLM relay MLP; 0 = D/4
+
+    @property
+    def film_width(self) -> int:
+        return self.film_dim if self.film_dim > 0 else self.D // 4
 
     @property
     def mask_id(self) -> int:
@@ -83,9 +90,11 @@ SWEEP_NB32 = SWEEP_NB16.with_(name="qwen3_8b_shaped_b8_ragged1024_8192_nb32", nb
 SWEEP_NB64 = SWEEP_NB16.with_(name="qwen3_8b_shaped_b8_ragged1024_8192_nb64", nb=64)
 RELAY_DFLASH2 = QWEN3_8B.with_(name="qwen3_8b_shaped_relay_dflash2_b16_c4096_nb32", nb=32,
                                flags=FLAG_RELAY | FLAG_CONV | FLAG_SELECT)
+FILM_RELAY = QWEN3_8B.with_(name="qwen3_8b_shaped_film_relay_b16_c4096_nb32", nb=32,
+                            flags=FLAG_RELAY | FLAG_FILM)
 
 WORKLOADS = {w.name: w for w in (TINY, QWEN3_4B, QWEN3_8B, SWEEP_NB16, SWEEP_NB32,
-                                  SWEEP_NB64, RELAY_DFLASH2)}
+                                  SWEEP_NB64, RELAY_DFLASH2, FILM_RELAY)}
 
 
 # --------------------------------------------------------------------------- streams
@@ -185,6 +194,9 @@ def weight_shapes(w: Workload) -> dict:
                 s[p + f"conv{c}.W0"] = (w.D // w.conv_group, w.D)
                 s[p + f"conv{c}.W1"] = (w.D // w.conv_group, w.D)
                 s[p + f"conv{c}.base"] = (2, w.D)
+    if w.flags & FLAG_FILM:
+        s["film.W1"] = (w.film_width, 3 * w.D)
+        s["film.W2"] = (2 * w.D, w.film_width)
     if w.flags & FLAG_SELECT:
         s["W_A"] = (w.sel_dim, w.D)
         s["W_B"] = (w.sel_dim, w.D)
@@ -229,6 +241,13 @@ def tau_prev(w: Workload, seed: int = 0) -> np.ndarray:
 def accepted_prev(w: Workload, seed: int = 0) -> np.ndarray:
     """Previous round's accepted draft count a per sequence, U{0..B-1} (relay workload)."""
     return uniform_int("a_prev", (w.nb,), 0, w.B - 1, seed)
+
+
+def relay_tokens(w: Workload, seed: int = 0):
+    """FiLM relay conditioning tokens per sequence (relay workload): the verifier's
+    correction b and the draft's first rejected guess, each U{0..V-2}."""
+    return (uniform_int("relay_b", (w.nb,), 0, w.V - 2, seed),
+            uniform_int("relay_y", (w.nb,), 0, w.V - 2, seed))
 
 
 def verifier_rows(w: Workload, rows: int, seed: int = 0, name: str = "hv") -> np.ndarray:

@@ -15,8 +15,10 @@ Sources (page title, section):
             符号约定 table; 二、块扩散草稿 -- attention equations; 三、KV 注入 -- the H_c
             equation and the W_c size; 四、推理流程 -- draft_forward and dflash_cycle.
   [DFlow]   "DFlow 完全拆解" (pinghaoyang.com.cn/aigc/posts/dflow): 第一步 -- the h_i
-            projection; 第二步 -- the one-position shift; 推理循环可以怎么实现 -- relay
-            placement by absolute position; 问题不在拒绝 -- the accept / bonus split.
+            projection; 第二步 -- the one-position shift; 第三步 -- the FiLM relay
+            ([beta; gamma] = MLP_phi([E(b); E(y); h_i]), x = E_mask + beta * LN(h_i) + gamma);
+            推理循环可以怎么实现 -- relay placement by absolute position; 问题不在拒绝 --
+            the accept / bonus split.
   [DFlash2] "DFlash 2：正确 token 已在候选里" (bowenzhou.top/papers/2026/DFlash2):
             洞察一 -- the S_t(a,b) selector score and the greedy walk; 洞察二 -- the
             two-tap dynamic convolution.
@@ -30,6 +32,10 @@ Readings where the pages are silent or disagree (each is listed in the design doc):
   * tau counts the bonus token (1 <= tau <= B); T[j] verifies candidate c_{j+1};
   * relay rows k in [a+2, B-1] of the previous verify go to new offset j = k - a
     (plain add onto the mask embedding); top-k ties and selector ties go to the lower id;
+  * FiLM relay: MLP_phi = W2 silu(W1 c) (two bias-free linear layers, hidden width
+    film_dim), output split [beta; gamma] in that order; LN without its own gain or bias
+    (beta and gamma are the affine), eps as RMSNorm's; conditioning row h_i is the same
+    projected row h_k the plain form adds;
   * four convs per layer acting on the residual stream (before/after each sublayer),
     correction linear in the conv input, x_{-1} = 0 at offset 0;
   * selector A = W_A E[a], B = W_B E[b], G = sigmoid(W_G z_t), U_t = raw logit.
@@ -48,6 +54,7 @@ from dflash_inputs import bf16_bits_to_f32
 FLAG_RELAY = 1
 FLAG_CONV = 2
 FLAG_SELECT = 4
+FLAG_FILM = 8
 
 
 def widen(bits, dtype=np.float64) -> np.ndarray:
@@ -111,6 +118,40 @@ def sigmoid(x):
     return 1.0 / (1.0 + np.exp(-x))
 
 
+def layer_norm(x: np.ndarray, eps: float) -> np.ndarray:
+    """LayerNorm over the last axis, (x - mean) / sqrt(var + eps), population variance.
+
+    [DFlow] 第三步, the LN(h_i) of the relay input. The page gives no LN gain or bias;
+    beta and gamma already scale and shift every channel, so none is applied here.
+    """
+    mu = np.mean(x, axis=-1, keepdims=True)
+    var = np.mean((x - mu) ** 2, axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps)
+
+
+def film_mlp(W: dict, cond: np.ndarray):
+    """[beta; gamma] = MLP_phi(cond) = W2 silu(W1 cond), split in that order.
+
+    [DFlow] 第三步: a light MLP of the concatenation [E(b); E(y_{a+1}); h_i]; its depth
+    and width are not given on the page: two bias-free linear layers with SiLU between.
+    cond: [..., 3D] -> (beta [..., D], gamma [..., D]).
+    """
+    z = silu(cond @ W["film.W1"].T) @ W["film.W2"].T
+    D = z.shape[-1] // 2
+    return z[..., :D], z[..., D:]
+
+
+def film_relay_row(cfg, W: dict, h_i: np.ndarray, b: int, y: int) -> np.ndarray:
+    """Relayed row beta * LN(h_i) + gamma ([DFlow] 第三步, the x^{(r+1)}_i equation without
+    its E_mask term, which the block input adds).
+
+    b: the verifier's correction token, y: the draft's first rejected guess.
+    """
+    cond = np.concatenate([W["E"][b], W["E"][y], h_i])
+    beta, gamma = film_mlp(W, cond)
+    return beta * layer_norm(h_i, cfg.eps) + gamma
+
+
 def dyn_conv(x: np.ndarray, W0: np.ndarray, W1: np.ndarray, base: np.ndarray,
              group: int = 16) -> np.ndarray:
     """Two-tap dynamic depthwise convolution over one block's rows.
@@ -155,7 +196,7 @@ def fuse_context(cfg, W: dict, hv_rows: np.ndarray) -> np.ndarray:
 
 
 def ctx_project(cfg, W: dict, hv: np.ndarray, n_commit, ctx_len, cache: KVCache,
-                relay_a=None):
+                relay_a=None, relay_b=None, relay_y=None):
     """Append committed verifier rows to the context cache; build the relay input.
 
     hv: [nb, R, L*Dt]. Rows 0..n_commit[i]-1 of sequence i become context rows at
@@ -163,7 +204,9 @@ def ctx_project(cfg, W: dict, hv: np.ndarray, n_commit, ctx_len, cache: KVCache,
     With ``relay_a`` (the previous round's accepted count a per sequence), rows
     k in [a+2, B-1] move to new block offset j = k - a ([DFlow] 第二步: the verifier
     row at position p serves draft position p+1; 推理循环: rejected suffix after the
-    first rejection), giving x0_relay[i, j] = h_k (plain add form).
+    first rejection), giving x0_relay[i, j] = h_k (plain add form), or with ``relay_b``
+    and ``relay_y`` (per sequence: the verifier's correction b, the draft's rejected
+    guess y) the FiLM form film_relay_row(h_k, b, y) ([DFlow] 第三步).
 
     Returns (new_ctx_len [nb], x0_relay [nb, B, D] or None). ``cache`` is updated.
     """
@@ -188,7 +231,11 @@ def ctx_project(cfg, W: dict, hv: np.ndarray, n_commit, ctx_len, cache: KVCache,
             for j in range(2, B - a):
                 k = j + a
                 if k < R:
-                    x0r[i, j] = h[k]
+                    if relay_b is None:
+                        x0r[i, j] = h[k]
+                    else:
+                        x0r[i, j] = film_relay_row(cfg, W, h[k], int(relay_b[i]),
+                                                   int(relay_y[i]))
     return new_len, x0r
 
 
@@ -330,10 +377,11 @@ def select_path(cfg, W: dict, cand_ids: np.ndarray, cand_vals: np.ndarray,
 
 
 def draft_step(cfg, W: dict, hv, n_commit, ctx_len, cache: KVCache, block_ids, target,
-               relay_a=None, seqs=None):
+               relay_a=None, seqs=None, relay_b=None, relay_y=None):
     """One whole draft step: ctx_project -> draft_block -> LM head + top-k ->
     (selector) -> accept. Returns a dict of every stage's output."""
-    new_len, x0r = ctx_project(cfg, W, hv, n_commit, ctx_len, cache, relay_a)
+    new_len, x0r = ctx_project(cfg, W, hv, n_commit, ctx_len, cache, relay_a, relay_b,
+                               relay_y)
     hidden = draft_block(cfg, W, block_ids, new_len, cache, x0r, seqs)
     logits = lm_logits(W, hidden)
     ids, vals = topk(logits, cfg.k_top)

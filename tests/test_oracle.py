@@ -339,6 +339,143 @@ def test_ctx_project_cache_rows():
         assert not cache.K[n][0][:, 8:].any() and not cache.K[n][0][:, :5].any()
 
 
+# ----------------------------------------------------------------------------- FiLM relay
+
+def test_layer_norm_closed_forms():
+    eps = 1e-6
+    # a constant row has zero deviation from its mean
+    assert not orc.layer_norm(np.full((1, 8), 3.7), eps).any()
+    # +-c alternating: mean 0, population variance c^2
+    x = np.array([3.0, -3.0] * 4)
+    np.testing.assert_allclose(orc.layer_norm(x, eps), x / math.sqrt(9.0 + eps), rtol=1e-15)
+    # 1, 2, 3, 4: mean 5/2, population variance 5/4 (not the sample variance 5/3)
+    got = orc.layer_norm(np.array([1.0, 2.0, 3.0, 4.0]), eps)
+    np.testing.assert_allclose(got, np.array([-1.5, -0.5, 0.5, 1.5]) / math.sqrt(1.25 + eps),
+                               rtol=1e-15)
+
+
+def test_layer_norm_moments_and_invariance():
+    rng = np.random.default_rng(30)
+    x = rng.standard_normal((5, 64)) * 3 + 2
+    y = orc.layer_norm(x, 0.0)
+    np.testing.assert_allclose(y.mean(-1), 0.0, atol=1e-14)
+    np.testing.assert_allclose((y * y).mean(-1), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(orc.layer_norm(4.0 * x - 7.0, 0.0), y, rtol=1e-12, atol=1e-13)
+
+
+def film_cfg(**kw):
+    return small_cfg(flags=di.FLAG_RELAY | di.FLAG_FILM, film_dim=32, **kw)
+
+
+def film_case(cfg, seed):
+    W = rand_weights(cfg, seed)
+    rng = np.random.default_rng(seed + 1)
+    hv = rng.standard_normal((cfg.nb, cfg.B, cfg.L * cfg.Dt))
+    b = rng.integers(0, cfg.V - 1, cfg.nb)
+    y = rng.integers(0, cfg.V - 1, cfg.nb)
+    return W, hv, b, y
+
+
+def project(cfg, W, hv, a, b=None, y=None):
+    cache = orc.KVCache(cfg.N, cfg.nb, cfg.Hkv, 32, cfg.hd)
+    return orc.ctx_project(cfg, W, hv, [a[i] + 1 for i in range(cfg.nb)], [3] * cfg.nb, cache,
+                           relay_a=a, relay_b=b, relay_y=y)[1]
+
+
+def selection(D, blocks):
+    """[D, len(blocks) * D] with an identity in each block marked 1."""
+    return np.concatenate([np.eye(D) if on else np.zeros((D, D)) for on in blocks], axis=1)
+
+
+def test_film_selection_weights_pick_each_input():
+    """Selection-matrix weights turn the FiLM row into closed forms, one input at a time:
+    gamma = silu(h) alone; beta = silu(E[b]) or silu(E[y]) times LN(h). A swapped
+    concatenation order, a swapped beta/gamma split, a missing LN or a wrong relay row
+    fails one of them."""
+    from scipy.special import expit
+    cfg = film_cfg(nb=3)
+    D = cfg.D
+    a = [0, 2, 1]
+    W, hv, b, y = film_case(cfg, 31)
+    plain = project(cfg, W, hv, a)
+    zero = np.zeros((D, D))
+    eye = np.eye(D)
+    relayed = np.abs(plain).sum(-1) > 0
+
+    W["film.W1"] = selection(D, (0, 0, 1))
+    W["film.W2"] = np.concatenate([zero, eye])
+    got = project(cfg, W, hv, a, b, y)
+    np.testing.assert_allclose(got, plain * expit(plain), rtol=1e-13, atol=1e-15)
+
+    def ln(v):
+        return (v - v.mean(-1, keepdims=True)) / np.sqrt(v.var(-1, keepdims=True) + cfg.eps)
+
+    W["film.W2"] = np.concatenate([eye, zero])
+    for blocks, tok in (((1, 0, 0), b), ((0, 1, 0), y)):
+        W["film.W1"] = selection(D, blocks)
+        got = project(cfg, W, hv, a, b, y)
+        e = W["E"][tok]
+        want = (e * expit(e))[:, None, :] * ln(plain)
+        np.testing.assert_allclose(got[relayed], want[relayed], rtol=1e-12, atol=1e-14)
+        assert not got[~relayed].any()
+
+
+def test_film_zero_output_layer_turns_relay_off():
+    """W2 = 0 gives beta = gamma = 0: the relayed input is the mask embedding alone, so the
+    whole draft equals the draft with no relay."""
+    cfg = film_cfg(nb=2)
+    a = [1, 0]
+    W, hv, b, y = film_case(cfg, 32)
+    W["film.W2"] = np.zeros_like(W["film.W2"])
+    assert not project(cfg, W, hv, a, b, y).any()
+    ids = np.full((cfg.nb, cfg.B), cfg.mask_id, np.int32)
+    ids[:, 0] = [5, 9]
+    outs = []
+    for relay in (False, True):
+        cache = orc.KVCache(cfg.N, cfg.nb, cfg.Hkv, 32, cfg.hd)
+        fill_cache(cfg, cache, 3, np.random.default_rng(34))
+        kw = dict(relay_a=a, relay_b=b, relay_y=y) if relay else {}
+        outs.append(orc.draft_step(cfg, W, hv, [2, 1], [3, 3], cache, ids,
+                                   np.zeros((cfg.nb, cfg.B), np.int32), **kw)["hidden"])
+    np.testing.assert_array_equal(outs[0], outs[1])
+
+
+def test_film_brute_force_tiny():
+    """Scalar loops over a D = 2, film width 3 case with random (non-symmetric) weights:
+    catches a transposed W1 or W2 block that identity selections cannot."""
+    cfg = small_cfg(D=2, Dt=2, L=1, Hq=1, Hkv=1, hd=2, F=2, V=5, B=4, nb=1,
+                    flags=di.FLAG_RELAY | di.FLAG_FILM, film_dim=3)
+    rng = np.random.default_rng(35)
+    W = rand_weights(cfg, 36, std=0.7)
+    h = rng.standard_normal(2)
+    b, y = 3, 1
+    c = [W["E"][b][0], W["E"][b][1], W["E"][y][0], W["E"][y][1], h[0], h[1]]
+    hid = []
+    for r in range(3):
+        t = 0.0
+        for q in range(6):
+            t += W["film.W1"][r][q] * c[q]
+        hid.append(t / (1.0 + math.exp(-t)))
+    out = []
+    for r in range(4):
+        t = 0.0
+        for q in range(3):
+            t += W["film.W2"][r][q] * hid[q]
+        out.append(t)
+    mean = (h[0] + h[1]) / 2
+    var = ((h[0] - mean) ** 2 + (h[1] - mean) ** 2) / 2
+    want = [out[d] * (h[d] - mean) / math.sqrt(var + cfg.eps) + out[2 + d] for d in range(2)]
+    np.testing.assert_allclose(orc.film_relay_row(cfg, W, h, b, y), want, rtol=1e-12)
+
+
+def test_film_weight_shapes():
+    w = di.FILM_RELAY
+    s = di.weight_shapes(w)
+    assert s["film.W1"] == (w.D // 4, 3 * w.D)
+    assert s["film.W2"] == (2 * w.D, w.D // 4)
+    assert "film.W1" not in di.weight_shapes(di.QWEN3_8B)
+
+
 # ----------------------------------------------------------------------------- selector
 
 def test_selector_without_pair_term_is_per_position_argmax():
