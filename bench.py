@@ -54,6 +54,8 @@ def step_bytes_flops(w: di.Workload, ctx: np.ndarray, tp: np.ndarray):
     wbytes = 2 * (w.N * per_layer_w + w.D * w.L * w.Dt + w.V * w.D + 2 * w.D * w.N + 2 * w.D)
     if w.flags & di.FLAG_SELECT:
         wbytes += 2 * 3 * w.sel_dim * w.D
+    if w.flags & di.FLAG_FILM:
+        wbytes += 2 * 5 * w.D * w.film_width
     kv_bytes = int(ctx.sum()) * w.N * 2 * w.Hkv * w.hd * 2
     M = w.nb * w.B
     rows_proj = w.nb * w.B
@@ -62,23 +64,26 @@ def step_bytes_flops(w: di.Workload, ctx: np.ndarray, tp: np.ndarray):
     flops += 2 * M * w.N * (qkv_n * w.D + w.D * w.Hq * w.hd + 3 * w.F * w.D)
     flops += 2 * 2 * w.N * (w.Hq * w.B) * w.hd * int((ctx + w.B).sum())
     flops += 2 * w.nb * (w.B - 1) * w.V * w.D
+    if w.flags & di.FLAG_FILM:
+        flops += 2 * M * 5 * w.D * w.film_width
     return wbytes + kv_bytes + io, flops, wbytes, kv_bytes
 
 
 def kernels_per_step(w: di.Workload) -> int:
     """Launches of libdflash kernels in one step (see dflash_api.cu)."""
     n = 4                                 # ctx_project: W_c GEMM, RMSNorm, K/V GEMM, relay/len
-    conv = bool(w.flags & di.FLAG_CONV)
+    if w.flags & di.FLAG_FILM:
+        n += 4                            # FiLM: conditioning rows, W1 GEMM, W2 GEMM, apply
     n += 1                                # embedding (+ first RMSNorm)
-    per_layer = 7 + (1 if False else 0)   # QKV, attn split, attn merge, O, RMSNorm, gate|up, down
-    n += w.N * per_layer + (w.N - 1)      # RMSNorm before attention for layers 1..N-1
-    if conv:
-        n += 1                            # layer 0 attention RMSNorm is separate when CONV
-        n += w.N * 4 * 3                  # each conv: cast, GEMM, apply
+    per_layer = 6                         # QKV, attention, merge, O, gate|up, down (norms deferred)
+    if w.flags & di.FLAG_CONV:
+        per_layer += 4 * 2 + 2            # each conv: GEMM + apply; RMSNorm after conv0, conv2
+        n += 1                            # bf16 copy of the embedding for layer 0's conv0
+    n += w.N * per_layer
     n += 1                                # final RMSNorm
     n += 2                                # LM head GEMM + merge
     if w.flags & di.FLAG_SELECT:
-        n += 4                            # gather, A|B GEMM, G GEMM, walk
+        n += 5                            # gather, A|B GEMM, G GEMM, score table, walk
     n += 1                                # accept
     return n
 
@@ -197,16 +202,32 @@ def run_gpu(args, rank, world):
 
     # step inputs, resident in HBM
     hv_step = to_device_bf16(di.verifier_rows(w, w.B, seed, name="hv_step"), dev)
-    n_commit = i32(tp)
-    relay_a = i32(a) if relay else None
+    # every int32 input of the step lives in one device buffer, so that the end-to-end
+    # leg's single host-to-device copy is exactly what the step consumes
+    parts = {"n_commit": tp, "block": di.block_ids(w, di.anchors(w, seed)),
+             "target": np.zeros((w.nb, w.B), np.int32)}
+    if relay:
+        parts["relay_a"] = a
+    if w.flags & di.FLAG_FILM:
+        parts["relay_b"], parts["relay_y"] = di.relay_tokens(w, seed)
+    host_in_np = np.concatenate([np.asarray(v, np.int32).ravel() for v in parts.values()])
+    step_in = i32(host_in_np)
+    views, off = {}, 0
+    for name, v in parts.items():
+        n = int(np.asarray(v).size)
+        views[name] = step_in[off:off + n].view(np.asarray(v).shape)
+        off += n
+    n_commit = views["n_commit"]
+    relay_a = views.get("relay_a")
+    film = {k: views[k] for k in ("relay_b", "relay_y") if k in views}
     x0 = torch.empty(w.nb, w.B, w.D, dtype=torch.bfloat16, device=dev) if relay else None
-    block = i32(di.block_ids(w, di.anchors(w, seed)))
+    block = views["block"]
     hidden = torch.empty(w.nb, w.B, w.D, dtype=torch.bfloat16, device=dev)
     k = w.k_top
     tid = torch.empty(w.nb, w.B - 1, k, dtype=torch.int32, device=dev)
     tv = torch.empty(w.nb, w.B - 1, k, dtype=torch.float32, device=dev)
     path = torch.empty(w.nb, w.B - 1, dtype=torch.int32, device=dev)
-    target = i32(np.zeros((w.nb, w.B)))
+    target = views["target"]
     tau = i32(np.zeros(w.nb))
     bonus = i32(np.zeros(w.nb))
     select = bool(w.flags & di.FLAG_SELECT)
@@ -223,7 +244,8 @@ def run_gpu(args, rank, world):
 
     def step(s, lm_events=None):
         ctx_len.copy_(ctx_base)
-        dr.ctx_project(w.nb, w.B, hv_step, n_commit, ctx_len, relay_a=relay_a, x0_relay=x0, stream=s)
+        dr.ctx_project(w.nb, w.B, hv_step, n_commit, ctx_len, relay_a=relay_a, x0_relay=x0, stream=s,
+                       **film)
         dr.draft_block(w.nb, block, ctx_len, hidden, x0_relay=x0, max_ctx_hint=max_ctx, stream=s)
         if lm_events:
             lm_events[0].record(s)
@@ -303,8 +325,7 @@ def run_gpu(args, rank, world):
     # e2e through the public API with host buffers: H2D of the step's inputs from pinned
     # memory and D2H of its results, every step, inside the timed region
     host_hv = hv_step.cpu().pin_memory()
-    host_in = torch.cat([n_commit, block.flatten(), target.flatten()]).cpu().pin_memory()
-    dev_in = torch.empty_like(host_in, device=dev)
+    host_in = torch.from_numpy(host_in_np).pin_memory()
     host_out = torch.empty(w.nb * (2 + (w.B - 1) * k), dtype=torch.int32).pin_memory()
     e2e_steps = max(10, min(args.steps, 200))
     barrier()
@@ -313,7 +334,7 @@ def run_gpu(args, rank, world):
     with torch.cuda.stream(stream):
         for _ in range(e2e_steps):
             hv_step.copy_(host_hv, non_blocking=True)
-            dev_in.copy_(host_in, non_blocking=True)
+            step_in.copy_(host_in, non_blocking=True)
             graph.replay()
             out = torch.cat([tau, bonus, tid.flatten()])
             host_out.copy_(out, non_blocking=True)
@@ -392,6 +413,9 @@ def cpu_baseline(w: di.Workload, bits=None, budget_s: float = 15.0):
     if w.flags & di.FLAG_RELAY:
         a = di.accepted_prev(w).astype(np.int64)
         tp = a + 1
+    fb = fy = None
+    if w.flags & di.FLAG_FILM:
+        fb, fy = di.relay_tokens(w)
     ids = di.block_ids(w, di.anchors(w))
     rng = np.random.default_rng(7)
     done, t_used = 0, 0.0
@@ -406,7 +430,9 @@ def cpu_baseline(w: di.Workload, bits=None, budget_s: float = 15.0):
         hv = orc.widen(di.verifier_rows(w.with_(nb=1), w.B, name=f"hv_cpu{i}"), np.float32)
         t0 = time.perf_counter()
         orc.draft_step(w, W, hv, tp[i:i + 1], [base], cache, ids[i:i + 1],
-                       np.zeros((1, w.B), np.int32), relay_a=None if a is None else a[i:i + 1])
+                       np.zeros((1, w.B), np.int32), relay_a=None if a is None else a[i:i + 1],
+                       relay_b=None if fb is None else fb[i:i + 1],
+                       relay_y=None if fy is None else fy[i:i + 1])
         t_used += time.perf_counter() - t0
         done += 1
     per_seq = t_used / done

@@ -123,6 +123,7 @@ struct WsLayout {
   size_t apart = 0, aml = 0;                   // attention partials
   size_t tk_vals = 0, tk_ids = 0;              // LM head top-k partial lists
   size_t sel_e = 0, sel_ab = 0, sel_g = 0, sel_t = 0;  // selector
+  size_t film_cond = 0, film_hid = 0, film_bg = 0;     // FiLM relay
   size_t total = 0;
   size_t apart_bytes = 0, apart_ctas = 0;
 };
@@ -136,7 +137,7 @@ struct dflash_handle_s {
   bool have_weights = false;
   dflash_weights w{};
   std::vector<dflash_layer_weights> layers;
-  CUtensorMap tm_Wc, tm_lm, tm_A, tm_B, tm_G;
+  CUtensorMap tm_Wc, tm_lm, tm_A, tm_B, tm_G, tm_f1, tm_f2;
   std::vector<CUtensorMap> tm_qkv, tm_kc, tm_vc, tm_o, tm_gate, tm_up, tm_down;
   std::vector<CUtensorMap> tm_c0, tm_c1;  // [layer*4 + which]
   float inv_freq[64];
@@ -185,6 +186,11 @@ void plan_workspace(dflash_handle_s *h) {
     L.sel_ab = take((size_t)sel_rows * 2 * c.sel_dim * 4);
     L.sel_g = take((size_t)Ml * c.sel_dim * 4);
     L.sel_t = take((size_t)Ml * c.k_top * c.k_top * 4);  // step score tables
+  }
+  if (c.flags & DFLASH_FLAG_FILM) {
+    L.film_cond = take((size_t)Mb * 3 * c.D * 2);
+    L.film_hid = take((size_t)Mb * c.film_dim * 2);
+    L.film_bg = take((size_t)Mb * 2 * c.D * 4);
   }
   L.total = off;
 }
@@ -366,6 +372,10 @@ int dflash_create(const dflash_config *cfg, dflash_handle_t *out) {
   if (c.flags & DFLASH_FLAG_SELECT) {
     if (c.sel_dim <= 0 || c.sel_dim % 32) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "sel_dim must be a multiple of 32");
   }
+  if (c.flags & DFLASH_FLAG_FILM) {
+    if (!(c.flags & DFLASH_FLAG_RELAY)) return fail(DFLASH_ERR_INVALID_ARG, "DFLASH_FLAG_FILM requires DFLASH_FLAG_RELAY");
+    if (c.film_dim <= 0 || c.film_dim % 64) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "film_dim must be a positive multiple of 64");
+  }
   if (2LL * c.N > kMaxBMaps) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "2*N must be <= 12 (grouped K/V projection)");
   auto *h = new (std::nothrow) dflash_handle_s();
   if (!h) return fail(DFLASH_ERR_INVALID_ARG, "out of host memory");
@@ -444,6 +454,11 @@ int dflash_set_weights(dflash_handle_t h, const dflash_weights *w) {
     DF_TRY(encode_2d(&h->tm_B, w->W_B, c.sel_dim, c.D, c.D, kBN / 2));
     DF_TRY(encode_2d(&h->tm_G, w->W_G, c.sel_dim, c.D, c.D, kBN));
   }
+  if (c.flags & DFLASH_FLAG_FILM) {
+    if (!w->film_W1 || !w->film_W2) return fail(DFLASH_ERR_INVALID_ARG, "FiLM relay weights are NULL");
+    DF_TRY(encode_slabs(&h->tm_f1, w->film_W1, c.film_dim, 3ULL * c.D, kBN));
+    DF_TRY(encode_slabs(&h->tm_f2, w->film_W2, 2ULL * c.D, c.film_dim, kBN));
+  }
   h->have_weights = true;
   return DFLASH_OK;
 }
@@ -458,10 +473,13 @@ int dflash_status(dflash_handle_t h, void *ws, dflash_stream_t stream, int *code
   return DFLASH_OK;
 }
 
-int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *hv, const int32_t *n_commit,
-                       const int32_t *relay_a, int32_t *ctx_len, void *kcache, void *vcache,
-                       void *x0_relay, void *ws, size_t ws_bytes, dflash_stream_t stream) {
-  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+namespace {
+
+// relay_b / relay_y non-null selects the FiLM form of the relay rows.
+int ctx_project_impl(dflash_handle_t h, int nb, int R, const void *hv, const int32_t *n_commit,
+                     const int32_t *relay_a, const int32_t *relay_b, const int32_t *relay_y,
+                     int32_t *ctx_len, void *kcache, void *vcache, void *x0_relay, void *ws,
+                     size_t ws_bytes, dflash_stream_t stream) {
   const auto &c = h->cfg;
   if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
   if (R < 0 || R > c.max_proj_rows) return fail(DFLASH_ERR_INVALID_ARG, "R=%d outside [0, max_proj_rows]", R);
@@ -513,9 +531,72 @@ int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *hv, const i
     p.max_batch = c.max_batch;
     DF_TRY(run_gemm(h, p, kBN, s));
   }
+  const bool film = relay_b != nullptr;
   DF_CUDA(launch_relay_and_len(hh, nb, R, c.B, c.D, relay_a, n_commit, ctx_len,
-                               static_cast<uint16_t *>(x0_relay), c.Cmax, w.status(), s));
+                               film ? nullptr : static_cast<uint16_t *>(x0_relay), c.Cmax,
+                               w.status(), s));
+  if (film) {
+    const int M = nb * c.B;
+    uint16_t *cond = w.at<uint16_t>(h->ws.film_cond);
+    uint16_t *hid = w.at<uint16_t>(h->ws.film_hid);
+    float *bg = w.at<float>(h->ws.film_bg);
+    DF_CUDA(launch_film_cond(hh, bf(h->w.E), nb, R, c.B, c.D, c.V, relay_a, relay_b, relay_y, cond,
+                             w.status(), s));
+    {  // hidden = silu(W1 cond)
+      GemmParams p = base_params(h, w);
+      DF_TRY(encode_slabs(&p.tmA, cond, M, 3ULL * c.D, 128));
+      p.slabs = 2;
+      p.tmB[0] = h->tm_f1;
+      p.M = M;
+      p.N = c.film_dim;
+      p.K = 3 * c.D;
+      p.epi = EPI_BF16;
+      p.act = 1;
+      p.out = hid;
+      p.ldo = c.film_dim;
+      DF_TRY(run_gemm(h, p, kBN, s));
+    }
+    {  // [beta | gamma] = W2 hidden
+      GemmParams p = base_params(h, w);
+      DF_TRY(encode_slabs(&p.tmA, hid, M, c.film_dim, 128));
+      p.slabs = 2;
+      p.tmB[0] = h->tm_f2;
+      p.M = M;
+      p.N = 2 * c.D;
+      p.K = c.film_dim;
+      p.epi = EPI_F32;
+      p.out = bg;
+      p.ldo = 2 * c.D;
+      DF_TRY(run_gemm(h, p, kBN, s));
+    }
+    DF_CUDA(launch_film_apply(hh, bg, nb, R, c.B, c.D, relay_a, c.eps,
+                              static_cast<uint16_t *>(x0_relay), s));
+  }
   return DFLASH_OK;
+}
+
+}  // namespace
+
+int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *hv, const int32_t *n_commit,
+                       const int32_t *relay_a, int32_t *ctx_len, void *kcache, void *vcache,
+                       void *x0_relay, void *ws, size_t ws_bytes, dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  return ctx_project_impl(h, nb, R, hv, n_commit, relay_a, nullptr, nullptr, ctx_len, kcache,
+                          vcache, x0_relay, ws, ws_bytes, stream);
+}
+
+int dflash_ctx_project_film(dflash_handle_t h, int nb, int R, const void *hv,
+                            const int32_t *n_commit, const int32_t *relay_a, const int32_t *relay_b,
+                            const int32_t *relay_y, int32_t *ctx_len, void *kcache, void *vcache,
+                            void *x0_relay, void *ws, size_t ws_bytes, dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  const unsigned need = DFLASH_FLAG_RELAY | DFLASH_FLAG_FILM;
+  if ((h->cfg.flags & need) != need)
+    return fail(DFLASH_ERR_INVALID_ARG, "the FiLM relay needs DFLASH_FLAG_RELAY | DFLASH_FLAG_FILM");
+  if (!relay_a || !relay_b || !relay_y || !x0_relay)
+    return fail(DFLASH_ERR_INVALID_ARG, "relay_a, relay_b, relay_y and x0_relay must be non-NULL");
+  return ctx_project_impl(h, nb, R, hv, n_commit, relay_a, relay_b, relay_y, ctx_len, kcache,
+                          vcache, x0_relay, ws, ws_bytes, stream);
 }
 
 int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, const void *x0_relay,

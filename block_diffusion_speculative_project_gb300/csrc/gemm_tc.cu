@@ -285,8 +285,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
       const int col0 = t.n * BN + c * 32;
       const int nval = min(32, p.N - col0);
       if (row_ok && nval > 0) {
-        if constexpr (EPI == EPI_BF16)
+        if constexpr (EPI == EPI_BF16) {
+          if (p.act) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = v[i] / (1.0f + expf(-v[i]));
+          }
           store_bf16_32(static_cast<uint16_t *>(p.out) + row * p.ldo + col0, v, nval);
+        }
         else
           store_f32_32(static_cast<float *>(p.out) + row * p.ldo + col0, v, nval);
       }

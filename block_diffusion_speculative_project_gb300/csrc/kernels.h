@@ -127,6 +127,7 @@ struct GemmParams {
   int csplit;        // >1: split K across the CTAs of a cluster, reduce through DSMEM
   int slabs;         // 2: A and B maps carry a 64-column slab dimension and each stage
                      // loads two slabs per copy (plain 128-wide GEMMs with K % 64 == 0)
+  int act;           // EPI_BF16: 1 = silu(acc) before rounding
 };
 
 struct GemmLaunch {
@@ -157,6 +158,13 @@ cudaError_t launch_rmsnorm_rows(const float *x, int M, int D, const uint16_t *g,
 cudaError_t launch_relay_and_len(const uint16_t *h, int nb, int R, int B, int D,
                                  const int *relay_a, const int *n_commit, int *ctx_len,
                                  uint16_t *x0_relay, int Cmax, int *status, cudaStream_t s);
+// FiLM relay ([DFlow] 第三步): conditioning rows and the modulated relay rows, one row
+// per block offset (i, j); rows that are not relayed get zeros.
+cudaError_t launch_film_cond(const uint16_t *h, const uint16_t *E, int nb, int R, int B, int D,
+                             int V, const int *relay_a, const int *relay_b, const int *relay_y,
+                             uint16_t *cond, int *status, cudaStream_t s);
+cudaError_t launch_film_apply(const uint16_t *h, const float *bg, int nb, int R, int B, int D,
+                              const int *relay_a, float eps, uint16_t *x0, cudaStream_t s);
 cudaError_t launch_accept(const int *draft, const int *target, int nb, int B, int *tau, int *bonus,
                           cudaStream_t s);
 cudaError_t launch_topk_merge(const float *vals, const int *ids, int rows, int ncand_per_row,

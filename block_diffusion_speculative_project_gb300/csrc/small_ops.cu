@@ -1,5 +1,5 @@
 // CUDA-core kernels of the draft step: embedding gather, RMSNorm, relay placement,
-// greedy accept, top-k merge, DFlash 2 conv application and selector walk.
+// FiLM relay rows, greedy accept, top-k merge, DFlash 2 conv application and selector walk.
 // All are memory- or latency-bound row operations; each reads its inputs once with
 // 16-byte vector accesses where the row layout allows.
 #include <algorithm>
@@ -159,6 +159,131 @@ cudaError_t launch_relay_and_len(const uint16_t *h, int nb, int R, int B, int D,
   if (nb <= 0) return cudaSuccess;
   cudaError_t e = launch_pdl(relay_len_kernel, dim3(nb), dim3(256), 0, s, h, R, B, D, relay_a, n_commit,
                              ctx_len, x0_relay, Cmax, status);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- FiLM relay
+// [DFlow] 第三步. One CTA per block offset r = i*B + j of the next block. Offset j of
+// sequence i is relayed from previous row k = j + a_i when 2 <= j <= B-1-a_i and k < R
+// (the same placement as the plain relay).
+__device__ __forceinline__ bool film_relayed(const int *relay_a, int r, int B, int R, int &i,
+                                             int &k) {
+  i = r / B;
+  const int j = r - i * B;
+  const int a = relay_a[i];
+  k = j + a;
+  return a >= 0 && j >= 2 && j <= B - 1 - a && k < R;
+}
+
+// cond[r] = [E[b_i]; E[y_i]; h[i*R + k]] (bf16, 3D wide), zeros for offsets not relayed.
+__global__ void __launch_bounds__(256) film_cond_kernel(const uint16_t *h, const uint16_t *E, int R,
+                                                        int B, int D, int V, const int *relay_a,
+                                                        const int *relay_b, const int *relay_y,
+                                                        uint16_t *cond, int *status) {
+  griddep_wait();
+  griddep_launch();
+  const int r = blockIdx.x;
+  int i, k;
+  const bool take = film_relayed(relay_a, r, B, R, i, k);
+  const int n8 = D / 8;
+  uint4 *dst = reinterpret_cast<uint4 *>(cond + (size_t)r * 3 * D);
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  if (!take) {
+    for (int c = threadIdx.x; c < 3 * n8; c += 256) dst[c] = zero;
+    return;
+  }
+  const int b = relay_b[i];
+  const int y = relay_y[i];
+  const bool bok = b >= 0 && b < V;
+  const bool yok = y >= 0 && y < V;
+  if (threadIdx.x == 0 && !(bok && yok)) flag_status(status, kStatusCheck);
+  const uint4 *eb = reinterpret_cast<const uint4 *>(E + (size_t)(bok ? b : 0) * D);
+  const uint4 *ey = reinterpret_cast<const uint4 *>(E + (size_t)(yok ? y : 0) * D);
+  const uint4 *hk = reinterpret_cast<const uint4 *>(h + ((size_t)i * R + k) * D);
+  for (int c = threadIdx.x; c < n8; c += 256) {
+    dst[c] = bok ? eb[c] : zero;
+    dst[n8 + c] = yok ? ey[c] : zero;
+    dst[2 * n8 + c] = hk[c];
+  }
+}
+
+// x0[r] = bf16(beta * (h_k - mean) / sqrt(var + eps) + gamma), beta = bg[r][0..D),
+// gamma = bg[r][D..2D); zeros for offsets not relayed. Two-pass fp32 statistics.
+__global__ void __launch_bounds__(256) film_apply_kernel(const uint16_t *h, const float *bg, int R,
+                                                         int B, int D, const int *relay_a, float eps,
+                                                         uint16_t *x0) {
+  griddep_wait();
+  griddep_launch();
+  __shared__ float red[8];
+  const int r = blockIdx.x;
+  int i, k;
+  const bool take = film_relayed(relay_a, r, B, R, i, k);
+  uint4 *dst = reinterpret_cast<uint4 *>(x0 + (size_t)r * D);
+  const int n8 = D / 8;
+  if (!take) {
+    for (int c = threadIdx.x; c < n8; c += 256) dst[c] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4 *hk = reinterpret_cast<const uint4 *>(h + ((size_t)i * R + k) * D);
+  float s = 0.f;
+  for (int c = threadIdx.x; c < n8; c += 256) {
+    const uint4 v = hk[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      s += bits_to_f32(uint16_t(w[q] & 0xFFFFu)) + bits_to_f32(uint16_t(w[q] >> 16));
+  }
+  const float mean = block_sum_256(s, red) / D;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < n8; c += 256) {
+    const uint4 v = hk[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float d0 = bits_to_f32(uint16_t(w[q] & 0xFFFFu)) - mean;
+      const float d1 = bits_to_f32(uint16_t(w[q] >> 16)) - mean;
+      ss += d0 * d0 + d1 * d1;
+    }
+  }
+  const float rstd = rsqrtf(block_sum_256(ss, red) / D + eps);
+  const float *beta = bg + (size_t)r * 2 * D;
+  const float *gamma = beta + D;
+  for (int c = threadIdx.x; c < n8; c += 256) {
+    const uint4 v = hk[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const float4 b0 = reinterpret_cast<const float4 *>(beta)[2 * c];
+    const float4 b1 = reinterpret_cast<const float4 *>(beta)[2 * c + 1];
+    const float4 g0 = reinterpret_cast<const float4 *>(gamma)[2 * c];
+    const float4 g1 = reinterpret_cast<const float4 *>(gamma)[2 * c + 1];
+    const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float n0 = (bits_to_f32(uint16_t(w[q] & 0xFFFFu)) - mean) * rstd;
+      const float n1 = (bits_to_f32(uint16_t(w[q] >> 16)) - mean) * rstd;
+      o[q] = pack_bf16x2(bb[2 * q] * n0 + gg[2 * q], bb[2 * q + 1] * n1 + gg[2 * q + 1]);
+    }
+    dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_film_cond(const uint16_t *h, const uint16_t *E, int nb, int R, int B, int D,
+                             int V, const int *relay_a, const int *relay_b, const int *relay_y,
+                             uint16_t *cond, int *status, cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(film_cond_kernel, dim3(nb * B), dim3(256), 0, s, h, E, R, B, D, V,
+                             relay_a, relay_b, relay_y, cond, status);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_film_apply(const uint16_t *h, const float *bg, int nb, int R, int B, int D,
+                              const int *relay_a, float eps, uint16_t *x0, cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(film_apply_kernel, dim3(nb * B), dim3(256), 0, s, h, bg, R, B, D,
+                             relay_a, eps, x0);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

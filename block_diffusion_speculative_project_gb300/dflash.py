@@ -23,6 +23,7 @@ DFLASH_ERR_DEVICE_CHECK = -5
 FLAG_RELAY = 1
 FLAG_CONV = 2
 FLAG_SELECT = 4
+FLAG_FILM = 8
 FLAG_TEST_STALL = 1 << 30
 
 
@@ -38,7 +39,7 @@ class dflash_config(ctypes.Structure):
         ("rope_base", ctypes.c_float), ("eps", ctypes.c_float)] + [
         (n, ctypes.c_int) for n in ("mask_id", "Cmax", "max_batch", "max_proj_rows", "conv_group",
                                     "sel_dim")] + [
-        ("flags", ctypes.c_uint), ("max_spin", ctypes.c_int)]
+        ("flags", ctypes.c_uint), ("max_spin", ctypes.c_int), ("film_dim", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -52,7 +53,7 @@ class dflash_layer_weights(ctypes.Structure):
 
 class dflash_weights(ctypes.Structure):
     _fields_ = [(n, _P) for n in ("W_c", "g_ctx", "E", "W_lm", "g_final", "W_A", "W_B", "W_G")] + [
-        ("layers", ctypes.POINTER(dflash_layer_weights))]
+        ("layers", ctypes.POINTER(dflash_layer_weights)), ("film_W1", _P), ("film_W2", _P)]
 
 
 def _load():
@@ -69,6 +70,7 @@ def _load():
         "dflash_status": (i, [p, p, p, ctypes.POINTER(i)]),
         "dflash_last_error": (ctypes.c_char_p, []),
         "dflash_ctx_project": (i, [p, i, i, p, p, p, p, p, p, p, p, sz, p]),
+        "dflash_ctx_project_film": (i, [p, i, i, p, p, p, p, p, p, p, p, p, p, sz, p]),
         "dflash_draft_block": (i, [p, i, p, p, p, p, p, i, p, p, sz, p]),
         "dflash_lm_head_topk": (i, [p, i, p, i, p, p, p, p, sz, p]),
         "dflash_lm_head_topk_noalloc": (i, [p, i, p, i, p, p, p, p]),
@@ -87,7 +89,8 @@ def _load():
 
 LIB = _load()
 EXPORTED = ("dflash_create", "dflash_destroy", "dflash_set_weights", "dflash_workspace_size",
-            "dflash_status", "dflash_last_error", "dflash_ctx_project", "dflash_draft_block",
+            "dflash_status", "dflash_last_error", "dflash_ctx_project", "dflash_ctx_project_film",
+            "dflash_draft_block",
             "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_attention", "dflash_topk", "dflash_accept", "dflash2_conv", "dflash2_select")
 
 
@@ -141,6 +144,14 @@ def dflash_ctx_project(h, nb, R, hv, n_commit, relay_a, ctx_len, kcache, vcache,
     _check(LIB.dflash_ctx_project(h, nb, R, _ptr(hv), _ptr(n_commit), _ptr(relay_a), _ptr(ctx_len),
                                   _ptr(kcache), _ptr(vcache), _ptr(x0_relay), _ptr(ws),
                                   ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dflash_ctx_project_film(h, nb, R, hv, n_commit, relay_a, relay_b, relay_y, ctx_len, kcache,
+                            vcache, x0_relay, ws, stream=None) -> None:
+    _check(LIB.dflash_ctx_project_film(h, nb, R, _ptr(hv), _ptr(n_commit), _ptr(relay_a),
+                                       _ptr(relay_b), _ptr(relay_y), _ptr(ctx_len), _ptr(kcache),
+                                       _ptr(vcache), _ptr(x0_relay), _ptr(ws),
+                                       ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def dflash_draft_block(h, nb, block_ids, x0_relay, kcache, vcache, ctx_len, max_ctx_hint,

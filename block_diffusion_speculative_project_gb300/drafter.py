@@ -23,7 +23,7 @@ class Drafter:
     """One handle with its caches [N, max_batch, Hkv, Cmax, hd] and workspace.
 
     ``shape`` is any object with the workload fields D, Dt, L, N, Hq, Hkv, hd, F, V,
-    B, k_top, rope_base, eps, mask_id, flags, conv_group and sel_dim.
+    B, k_top, rope_base, eps, mask_id, flags, conv_group, sel_dim and film_width.
     ``weights`` maps the weight names of dflash_inputs.weight_shapes to bf16 device
     tensors.
     """
@@ -36,7 +36,7 @@ class Drafter:
             D=s.D, Dt=s.Dt, L=s.L, N=s.N, Hq=s.Hq, Hkv=s.Hkv, hd=s.hd, F=s.F, V=s.V, B=s.B,
             k_top=s.k_top, rope_base=s.rope_base, eps=s.eps, mask_id=s.mask_id, Cmax=Cmax,
             max_batch=max_batch, max_proj_rows=max_proj_rows, conv_group=s.conv_group,
-            sel_dim=s.sel_dim, flags=s.flags, max_spin=max_spin)
+            sel_dim=s.sel_dim, flags=s.flags, max_spin=max_spin, film_dim=s.film_width)
         self.h = _d.dflash_create(self.cfg)
         self.weights = weights
         P = lambda name: ctypes.c_void_p(weights[name].data_ptr()) if name in weights else None
@@ -53,7 +53,8 @@ class Drafter:
         self._layers = layers
         self.wstruct = _d.dflash_weights(W_c=P("W_c"), g_ctx=P("g_ctx"), E=P("E"), W_lm=P("W_lm"),
                                          g_final=P("g_final"), W_A=P("W_A"), W_B=P("W_B"),
-                                         W_G=P("W_G"), layers=layers)
+                                         W_G=P("W_G"), layers=layers, film_W1=P("film.W1"),
+                                         film_W2=P("film.W2"))
         _d.dflash_set_weights(self.h, self.wstruct)
         nbytes = _d.dflash_workspace_size(self.h)
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
@@ -71,9 +72,14 @@ class Drafter:
             pass
 
     # thin forwards -------------------------------------------------------------
-    def ctx_project(self, nb, R, hv, n_commit, ctx_len, relay_a=None, x0_relay=None, stream=None):
-        _d.dflash_ctx_project(self.h, nb, R, hv, n_commit, relay_a, ctx_len, self.kcache, self.vcache,
-                              x0_relay, self.ws, stream)
+    def ctx_project(self, nb, R, hv, n_commit, ctx_len, relay_a=None, x0_relay=None, stream=None,
+                    relay_b=None, relay_y=None):
+        if relay_b is not None or relay_y is not None:
+            _d.dflash_ctx_project_film(self.h, nb, R, hv, n_commit, relay_a, relay_b, relay_y, ctx_len,
+                                       self.kcache, self.vcache, x0_relay, self.ws, stream)
+        else:
+            _d.dflash_ctx_project(self.h, nb, R, hv, n_commit, relay_a, ctx_len, self.kcache,
+                                  self.vcache, x0_relay, self.ws, stream)
 
     def draft_block(self, nb, block_ids, ctx_len, out_hidden, x0_relay=None, max_ctx_hint=0,
                     stream=None):

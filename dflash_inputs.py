@@ -20,7 +20,10 @@ Value recipe (the pages give no trained weights; these stand in for them):
                                residual stream diverges within two layers
   * verifier hidden states   ~ N(0, 1)
   * anchors                  ~ U{0 .. V-2};  mask id = V-1
-  * FiLM relay MLP W1, W2    ~ N(0, 0.02) (weights); its conditioning tokens ~ U{0 .. V-2}
+  * FiLM relay MLP           W1 ~ N(0, 1/(3D)), W2 ~ N(0, 4/film_dim): fan-in scaled so
+                               that beta and gamma come out O(1), the size of the plain
+                               relay's h (at N(0, 0.02) they would be ~0.03, below what a
+                               bf16 comparison resolves); conditioning tokens ~ U{0 .. V-2}
 """
 from __future__ import annotations
 
@@ -211,6 +214,10 @@ def make_weight(name: str, shape, seed: int = 0) -> np.ndarray:
         return normal_bf16(name, shape, 0.02, mean=1.0, seed=seed)
     if ".conv" in name and base in ("W0", "W1"):
         return normal_bf16(name, shape, 0.02 / float(np.sqrt(shape[1])), seed=seed)
+    if name == "film.W1":
+        return normal_bf16(name, shape, 1.0 / float(np.sqrt(shape[1])), seed=seed)
+    if name == "film.W2":
+        return normal_bf16(name, shape, 2.0 / float(np.sqrt(shape[1])), seed=seed)
     if base == "base":
         x = _fill_normal(name, int(np.prod(shape)), seed).reshape(shape) * np.float32(0.02)
         x[0] += np.float32(1.0)

@@ -63,6 +63,7 @@ enum dflash_flags {
   DFLASH_FLAG_RELAY = 1,  /* DFlow relay rows are accepted by ctx_project / draft_block */
   DFLASH_FLAG_CONV = 2,   /* DFlash 2 two-tap dynamic conv, 4 per layer */
   DFLASH_FLAG_SELECT = 4, /* DFlash 2 path selector weights are registered */
+  DFLASH_FLAG_FILM = 8,   /* DFlow FiLM relay weights are registered (requires RELAY) */
   /* Test hook for the failure path: the GEMM producers issue no loads, so every
    * wait on them runs out after max_spin polls, DFLASH_ERR_TIMEOUT is recorded and
    * the kernels return with the context intact. Never set in production. */
@@ -91,6 +92,7 @@ typedef struct dflash_config {
   int sel_dim;        /* selector embedding width (256); used with SELECT */
   unsigned flags;     /* DFLASH_FLAG_* */
   int max_spin;       /* iteration bound of every device-side wait; 0 = default */
+  int film_dim;       /* FILM: hidden width of the relay MLP, multiple of 64 */
 } dflash_config;
 
 typedef struct dflash_layer_weights {
@@ -118,6 +120,8 @@ typedef struct dflash_weights {
   const void *W_B;     /* SELECT: bf16 [sel_dim, D] */
   const void *W_G;     /* SELECT: bf16 [sel_dim, D] */
   const dflash_layer_weights *layers; /* N entries; copied by dflash_set_weights */
+  const void *film_W1; /* FILM: bf16 [film_dim, 3*D], first layer of the relay MLP */
+  const void *film_W2; /* FILM: bf16 [2*D, film_dim], second layer; rows [0,D) beta, [D,2D) gamma */
 } dflash_weights;
 
 typedef struct dflash_handle_s *dflash_handle_t;
@@ -133,8 +137,8 @@ DFLASH_API int dflash_create(const dflash_config *cfg, dflash_handle_t *out);
 DFLASH_API int dflash_destroy(dflash_handle_t h);
 
 /* Register weight pointers (borrowed). Builds the TMA descriptors of every weight
- * matrix. All pointers must be 16-byte aligned; optional groups (conv, selector)
- * must be non-NULL when their flag is set. */
+ * matrix. All pointers must be 16-byte aligned; optional groups (conv, selector,
+ * FiLM relay) must be non-NULL when their flag is set. */
 DFLASH_API int dflash_set_weights(dflash_handle_t h, const dflash_weights *w);
 
 /* Bytes of workspace every step call of this handle needs (sized for max_batch,
@@ -167,6 +171,23 @@ DFLASH_API const char *dflash_last_error(void);
  * Prefill is the same call with R = the prompt length (R <= max_proj_rows). */
 DFLASH_API int dflash_ctx_project(dflash_handle_t h, int nb, int R, const void *hv,
                        const int32_t *n_commit, const int32_t *relay_a, int32_t *ctx_len,
+                       void *kcache, void *vcache, void *x0_relay, void *ws, size_t ws_bytes,
+                       dflash_stream_t stream);
+
+/* dflash_ctx_project with the FiLM form of the DFlow relay ([DFlow] 第三步, the
+ * [beta; gamma] = MLP_phi([E(b); E(y_{a+1}); h_i]) and x = E_mask + beta * LN(h_i) + gamma
+ * equations). Requires DFLASH_FLAG_RELAY | DFLASH_FLAG_FILM and registered film weights.
+ * Every argument of dflash_ctx_project keeps its meaning (relay_a is required), plus
+ *   relay_b   int32 [nb], device: the verifier's correction token b at the first rejection
+ *   relay_y   int32 [nb], device: the draft's rejected guess y_{a+1} there
+ * and x0_relay (required) receives, at each relayed offset j (row k = j + a),
+ *   beta * LN(h_k) + gamma with [beta; gamma] = W2 silu(W1 [E(b); E(y); h_k]),
+ * LN(v) = (v - mean v) / sqrt(var v + eps) (population variance, no gain or bias),
+ * rounded to bf16; 0 at every other offset. A token id outside [0, V) is reported as
+ * DFLASH_ERR_DEVICE_CHECK by dflash_status and its embedding read as zeros. */
+DFLASH_API int dflash_ctx_project_film(dflash_handle_t h, int nb, int R, const void *hv,
+                       const int32_t *n_commit, const int32_t *relay_a,
+                       const int32_t *relay_b, const int32_t *relay_y, int32_t *ctx_len,
                        void *kcache, void *vcache, void *x0_relay, void *ws, size_t ws_bytes,
                        dflash_stream_t stream);
 

@@ -4,7 +4,7 @@ full-size end-to-end hidden comparison (tests/test_gpu_fullsize.py).
 It builds the same inputs as that test for one sampled sequence and computes the drafter
 hidden twice with oracle functions: exactly (the fp64 oracle) and with every value that
 the kernel path stores in bf16 rounded to bf16 at that point (h and the appended K_c, V_c
-rows of the context projection; per layer the conv inputs of the correction GEMMs, the
+rows of the context projection; with the FiLM relay its MLP hidden and the relay row; per layer the conv inputs of the correction GEMMs, the
 normalised GEMM input (u = RMSNorm(x) * g, or without the convs after layer 0's attention
 norm bf16(x * g) with the rsqrt(mean x^2 + eps) row factor applied after the GEMM), q,
 k_b, v_b, P, o and act; the final hidden). Everything else stays fp64.
@@ -39,6 +39,10 @@ def model(w, si):
     if relay:
         a = di.accepted_prev(w).astype(np.int64)
         tp = a + 1
+    fb = fy = None
+    film = bool(w.flags & di.FLAG_FILM)
+    if film:
+        fb, fy = di.relay_tokens(w)
     base = ctx - tp
     Cmax = int(ctx.max()) + B
     hv = orc.widen(di.verifier_rows(w, B, name="hv_full")[si:si + 1])
@@ -50,7 +54,9 @@ def model(w, si):
     Ke = [cache.K[n][0].copy() for n in range(w.N)]
     Ve = [cache.V[n][0].copy() for n in range(w.N)]
     new_len, x0r = orc.ctx_project(w, W, hv, tp[si:si + 1], base[si:si + 1], cache,
-                                   relay_a=None if a is None else a[si:si + 1])
+                                   relay_a=None if a is None else a[si:si + 1],
+                                   relay_b=None if fb is None else fb[si:si + 1],
+                                   relay_y=None if fy is None else fy[si:si + 1])
     exact = orc.draft_block(w, W, ids, new_len, cache, x0r)[0]
 
     # the same step with the kernel path's bf16 storage points
@@ -68,7 +74,13 @@ def model(w, si):
         aa = int(a[si])
         for j in range(2, B - aa):
             if j + aa < B:
-                x[j] = x[j] + h[j + aa]
+                hk = h[j + aa]
+                if film:  # bf16 MLP hidden and relay row; beta, gamma in fp32 (here exact)
+                    cond = np.concatenate([W["E"][fb[si]], W["E"][fy[si]], hk])
+                    z = rb(orc.silu(cond @ W["film.W1"].T)) @ W["film.W2"].T
+                    x[j] = x[j] + rb(z[:w.D] * orc.layer_norm(hk, w.eps) + z[w.D:])
+                else:
+                    x[j] = x[j] + hk
 
     def dconv(x, p):
         xb = rb(x)

@@ -38,3 +38,21 @@ def test_binding_wraps_every_symbol_and_validates_without_gpu():
         raise AssertionError("hd=96 must be rejected")
     except dflash.DflashError as e:
         assert e.code == dflash.DFLASH_ERR_UNSUPPORTED_SHAPE
+
+
+def test_film_relay_config_is_validated_without_gpu():
+    from block_diffusion_speculative_project_gb300 import dflash
+    base = dict(D=256, Dt=256, L=5, N=2, Hq=4, Hkv=4, hd=64, F=688, V=4096, B=8, k_top=16,
+                rope_base=1e4, eps=1e-6, mask_id=4095, Cmax=80, max_batch=1, max_proj_rows=64,
+                conv_group=16, sel_dim=256)
+    for flags, film_dim, code in ((dflash.FLAG_FILM, 64, dflash.DFLASH_ERR_INVALID_ARG),
+                                  (dflash.FLAG_FILM | dflash.FLAG_RELAY, 96,
+                                   dflash.DFLASH_ERR_UNSUPPORTED_SHAPE),
+                                  (dflash.FLAG_FILM | dflash.FLAG_RELAY, 0,
+                                   dflash.DFLASH_ERR_UNSUPPORTED_SHAPE)):
+        cfg = dflash.dflash_config(flags=flags, film_dim=film_dim, **base)
+        try:
+            dflash.dflash_create(cfg)
+            raise AssertionError(f"flags={flags} film_dim={film_dim} must be rejected")
+        except dflash.DflashError as e:
+            assert e.code == code, (flags, film_dim, e)

@@ -41,7 +41,7 @@ _W = {}
 
 
 def weights_for(w):
-    key = (w.D, w.N, w.V, w.F, w.flags & (di.FLAG_CONV | di.FLAG_SELECT))
+    key = (w.D, w.N, w.V, w.F, w.flags & (di.FLAG_CONV | di.FLAG_SELECT | di.FLAG_FILM))
     if key not in _W:
         _W.clear()
         bits = di.make_weights(w)
@@ -61,6 +61,9 @@ def run_case(w, sample):
     if relay:
         a = di.accepted_prev(w).astype(np.int32)
         tp = a + 1
+    fb = fy = None
+    if w.flags & di.FLAG_FILM:
+        fb, fy = di.relay_tokens(w)
     base = ctx - tp
     Cmax = int(ctx.max()) + B
     dev = {n: drafter.to_device_bf16(v) for n, v in bits.items()}
@@ -82,8 +85,9 @@ def run_case(w, sample):
     hv = di.verifier_rows(w, B, name="hv_full")
     ctx_len = i32(base)
     x0 = torch.empty(nb, B, w.D, dtype=torch.bfloat16, device="cuda") if relay else None
+    film = {} if fb is None else dict(relay_b=i32(fb), relay_y=i32(fy))
     dr.ctx_project(nb, B, drafter.to_device_bf16(hv), i32(tp), ctx_len,
-                   relay_a=i32(a) if relay else None, x0_relay=x0)
+                   relay_a=i32(a) if relay else None, x0_relay=x0, **film)
     ids = di.block_ids(w, di.anchors(w))
     hid = torch.empty(nb, B, w.D, dtype=torch.bfloat16, device="cuda")
     dr.draft_block(nb, i32(ids), ctx_len, hid, x0_relay=x0, max_ctx_hint=int(ctx.max()))
@@ -106,7 +110,9 @@ def run_case(w, sample):
     # oracle on the sample
     s = np.array(sample)
     new_len, x0r = orc.ctx_project(w, W, orc.widen(hv[s]), tp[s], base[s], cache,
-                                   relay_a=None if a is None else a[s])
+                                   relay_a=None if a is None else a[s],
+                                   relay_b=None if fb is None else fb[s],
+                                   relay_y=None if fy is None else fy[s])
     assert np.array_equal(new_len, ctx[s])
     ohid = orc.draft_block(w, W, ids[s], new_len, cache, x0r)
     K, V = dr.kcache, dr.vcache
@@ -163,3 +169,8 @@ def test_fullsize_qwen3_8b_b8_ragged_nb64():
 
 def test_fullsize_relay_dflash2_nb32():
     run_case(di.RELAY_DFLASH2, [3])
+
+
+def test_fullsize_film_relay_nb32():
+    a = di.accepted_prev(di.FILM_RELAY)
+    run_case(di.FILM_RELAY, [int(np.argmin(a)), 3])  # the most relayed rows, and sequence 3

@@ -20,6 +20,8 @@ MEDIUM_B8 = MEDIUM.with_(name="medium_b8", B=8, nb=5)
 MEDIUM_ALL = MEDIUM.with_(name="medium_relay_conv_select",
                           flags=di.FLAG_RELAY | di.FLAG_CONV | di.FLAG_SELECT)
 MEDIUM_G8 = MEDIUM.with_(name="medium_gqa8_128_query_rows", Hq=16)  # (Hq/Hkv)*B = 128
+MEDIUM_FILM = MEDIUM.with_(name="medium_film_relay", flags=di.FLAG_RELAY | di.FLAG_FILM)
+TINY_FILM = di.TINY.with_(name="tiny_film_relay_nb4", nb=4, flags=di.FLAG_RELAY | di.FLAG_FILM)
 
 
 def lib():
@@ -148,7 +150,8 @@ def test_lm_head_topk_few_ranges(V, k):
 
 # ----------------------------------------------------------------------------- ctx_project
 
-@pytest.mark.parametrize("w", [di.TINY, MEDIUM, MEDIUM_ALL], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [di.TINY, MEDIUM, MEDIUM_ALL, TINY_FILM, MEDIUM_FILM],
+                         ids=lambda w: w.name)
 def test_ctx_project_stage(w):
     Cmax, R = 96, w.B
     dr, W, _ = make(w, Cmax, R)
@@ -162,13 +165,19 @@ def test_ctx_project_stage(w):
     c0 = rng.integers(0, Cmax - R, nb).astype(np.int32)
     relay = (w.flags & di.FLAG_RELAY) != 0
     a = rng.integers(0, w.B, nb).astype(np.int32) if relay else None
+    film = {}
+    if w.flags & di.FLAG_FILM:
+        b, y = rng.integers(0, w.V, (2, nb)).astype(np.int32)
+        film = dict(relay_b=b, relay_y=y)
+        a[0] = 0  # the most relayed rows
     ctx = i32(c0)
     x0 = torch.full((nb, w.B, w.D), float("nan"), dtype=torch.bfloat16, device="cuda") if relay else None
     dr.ctx_project(nb, R, bf16(hv_bits), i32(n_commit), ctx, relay_a=None if a is None else i32(a),
-                   x0_relay=x0)
+                   x0_relay=x0, **{k: i32(v) for k, v in film.items()})
     assert dr.status() == 0
     cache = orc.KVCache(w.N, nb, w.Hkv, Cmax, w.hd)
-    new_len, x0r = orc.ctx_project(w, W, orc.widen(hv_bits), n_commit, c0, cache, relay_a=a)
+    new_len, x0r = orc.ctx_project(w, W, orc.widen(hv_bits), n_commit, c0, cache, relay_a=a,
+                                   **film)
     assert np.array_equal(ctx.cpu().numpy(), new_len)
     K, V = f64(dr.kcache), f64(dr.vcache)
     for n in range(w.N):
@@ -181,6 +190,41 @@ def test_ctx_project_stage(w):
         g = f64(x0)
         assert_close(g, x0r, "x0_relay")
         assert np.array_equal(g == 0, x0r == 0), "relay placement"
+
+
+def test_film_relay_short_rows_and_bad_tokens():
+    """FiLM relay with fewer projected rows than the block (the k < R cut), every a from 0
+    to B-1 (B-1 and B-2 relay nothing), then an out-of-range token: reported, read as zeros."""
+    dflash, _ = lib()
+    w = TINY_FILM.with_(nb=8)
+    R = 5
+    dr, W, _ = make(w, 64, R)
+    hv_bits = di.verifier_rows(w, R, name="hv_film")
+    a = np.array([0, 1, 2, 3, 4, 5, 6, 7], np.int32)
+    b, y = di.relay_tokens(w)
+    n_commit = np.full(w.nb, R, np.int32)
+    x0 = torch.full((w.nb, w.B, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dr.ctx_project(w.nb, R, bf16(hv_bits), i32(n_commit), i32(np.zeros(w.nb)), relay_a=i32(a),
+                   x0_relay=x0, relay_b=i32(b), relay_y=i32(y))
+    assert dr.status() == 0
+    cache = orc.KVCache(w.N, w.nb, w.Hkv, 64, w.hd)
+    _, x0r = orc.ctx_project(w, W, orc.widen(hv_bits), n_commit, np.zeros(w.nb), cache,
+                             relay_a=a, relay_b=b, relay_y=y)
+    g = f64(x0)
+    assert_close(g, x0r, "x0_relay (FiLM)")
+    assert np.array_equal(np.abs(g).sum(-1) > 0, np.abs(x0r).sum(-1) > 0), "relay placement"
+    assert (np.abs(x0r).sum(-1) > 0).sum() == 3 + 2 + 1  # a = 0, 1, 2 with k < R = 5
+    bad_b = b.copy()
+    bad_b[0] = w.V
+    dr.ctx_project(w.nb, R, bf16(hv_bits), i32(np.zeros(w.nb)), i32(np.zeros(w.nb)), relay_a=i32(a),
+                   x0_relay=x0, relay_b=i32(bad_b), relay_y=i32(y))
+    assert dr.status() == dflash.DFLASH_ERR_DEVICE_CHECK
+    W0 = dict(W)  # the kernel reads the out-of-range row as zeros: an appended zero row E[V]
+    W0["E"] = np.concatenate([W["E"], np.zeros((1, w.D))])
+    _, x0z = orc.ctx_project(w, W0, orc.widen(hv_bits), np.zeros(w.nb), np.zeros(w.nb),
+                             orc.KVCache(w.N, w.nb, w.Hkv, 64, w.hd), relay_a=a, relay_b=bad_b,
+                             relay_y=y)
+    assert_close(f64(x0)[0], x0z[0], "x0_relay with an out-of-range b")
 
 
 # ----------------------------------------------------------------------------- draft_block
@@ -337,7 +381,7 @@ def test_select_stage():
 
 # ----------------------------------------------------------------------------- whole step
 
-@pytest.mark.parametrize("w", [di.TINY, MEDIUM_ALL], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [di.TINY, MEDIUM_ALL, MEDIUM_FILM], ids=lambda w: w.name)
 def test_full_step(w):
     """Prefill through ctx_project, then one draft step (append, draft, LM head, accept)."""
     Cmax, C = 96, 70
@@ -353,7 +397,12 @@ def test_full_step(w):
     hv = di.verifier_rows(w, w.B, name="hv_step")
     a = (tp - 1).astype(np.int32)
     x0 = torch.empty(nb, w.B, w.D, dtype=torch.bfloat16, device="cuda") if relay else None
-    dr.ctx_project(nb, w.B, bf16(hv), i32(tp), ctx, relay_a=i32(a) if relay else None, x0_relay=x0)
+    film = {}
+    if w.flags & di.FLAG_FILM:
+        b, y = di.relay_tokens(w)
+        film = dict(relay_b=b, relay_y=y)
+    dr.ctx_project(nb, w.B, bf16(hv), i32(tp), ctx, relay_a=i32(a) if relay else None, x0_relay=x0,
+                   **{k: i32(v) for k, v in film.items()})
     ids = di.block_ids(w, di.anchors(w))
     out = torch.empty(nb, w.B, w.D, dtype=torch.bfloat16, device="cuda")
     dr.draft_block(nb, i32(ids), ctx, out, x0_relay=x0, max_ctx_hint=C)
@@ -364,7 +413,7 @@ def test_full_step(w):
     dr.lm_head_topk(nb, out, k, tid, tv, tl)
     assert dr.status() == 0
     o = orc.draft_step(w, W, orc.widen(hv), tp, lens, cache, ids, np.zeros((nb, w.B), np.int32),
-                       relay_a=a if relay else None)
+                       relay_a=a if relay else None, **film)
     assert np.array_equal(ctx.cpu().numpy(), o["ctx_len"])
     assert int(o["ctx_len"].max()) <= C
     if relay:

@@ -476,6 +476,120 @@ def test_film_weight_shapes():
     assert "film.W1" not in di.weight_shapes(di.QWEN3_8B)
 
 
+# ----------------------------------------------------------------------------- sampling
+
+def test_philox_known_answer_vectors():
+    g = json.load(open(os.path.join(GOLDEN, "philox_kat.json")))
+    for case in g["cases"]:
+        ctr = [int(x, 16) for x in case["ctr"]]
+        key = [int(x, 16) for x in case["key"]]
+        got = [int(x) for x in orc.philox4x32(ctr, key)]
+        assert got == [int(x, 16) for x in case["out"]], case
+
+
+def test_uniforms_are_uniform_and_streams_independent():
+    from scipy import stats
+    u = orc.uniforms(12345, orc.STREAM_DRAFT, 7, 200000)
+    assert u.min() > 0.0 and u.max() < 1.0
+    assert stats.kstest(u, "uniform").pvalue > 1e-3
+    # one Philox call covers four consecutive indices: the words must not repeat
+    assert len(np.unique(u[:4])) == 4
+    v = orc.uniforms(12345, orc.STREAM_ACCEPT, 7, 200000)
+    w = orc.uniforms(12345, orc.STREAM_DRAFT, 8, 200000)
+    x = orc.uniforms(12346, orc.STREAM_DRAFT, 7, 200000)
+    for o in (v, w, x):
+        assert abs(np.corrcoef(u, o)[0, 1]) < 0.01
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5, 2.0])
+def test_gumbel_draws_follow_softmax(T):
+    from scipy import stats
+    logits = np.array([1.0, 0.2, -0.5, 2.0, 0.0])
+    n = 20000
+    draws = np.array([orc.gumbel_argmax(logits / T + orc.gumbel(orc.uniforms(99, 0, r, 5)))[0]
+                      for r in range(n)])
+    p = np.exp(logits / T) / np.exp(logits / T).sum()
+    obs = np.bincount(draws, minlength=5)
+    assert stats.chisquare(obs, p * n).pvalue > 1e-4
+
+
+def test_sample_candidates_rows_and_log_probs():
+    rng = np.random.default_rng(40)
+    U = rng.standard_normal((2, 3, 50)) * 2
+    ids, lse, logq, _ = orc.sample_candidates(U, 1.0, 7)
+    for i in range(2):
+        for t in range(3):
+            q = np.exp(U[i, t]) / np.exp(U[i, t]).sum()
+            assert math.isclose(logq[i, t], math.log(q[ids[i, t]]), rel_tol=1e-12)
+    # rows are distinct streams: the same logits in two rows draw independently
+    same = np.repeat(U[:1, :1], 400, axis=1)
+    ids2, _, _, _ = orc.sample_candidates(same, 1.0, 7)
+    assert len(np.unique(ids2)) > 10
+
+
+def verify_inputs(nb, B, V, seed, scale=1.5):
+    rng = np.random.default_rng(seed)
+    U = rng.standard_normal((nb, B - 1, V)) * scale
+    Z = rng.standard_normal((nb, B, V)) * scale
+    return U, Z
+
+
+def test_verify_equal_distributions_accept_every_candidate():
+    """p_j = q_{j+1} gives ratio 1 > u: every candidate is accepted, tau = B."""
+    U, Z = verify_inputs(3, 6, 40, 41)
+    Z[:, :5] = U
+    cand, _, _, _ = orc.sample_candidates(U, 1.0, 3)
+    tau, token = orc.verify_sample(U, cand, Z, 1.0, 3)
+    assert (tau == 6).all()
+    assert ((token >= 0) & (token < 40)).all()
+
+
+def test_verify_zero_target_probability_rejects_there():
+    """A candidate the target gives probability 0 is rejected, and the re-drawn token is
+    never that candidate (its residual max(0, 0 - q) is 0)."""
+    U, Z = verify_inputs(4, 6, 40, 42)
+    Z[:, :5] = U
+    cand, _, _, _ = orc.sample_candidates(U, 1.0, 5)
+    for i in range(4):
+        Z[i, 2, cand[i, 2]] = -np.inf
+    tau, token = orc.verify_sample(U, cand, Z, 1.0, 5)
+    assert (tau == 3).all()
+    assert (token != cand[:, 2]).all()
+
+
+def test_verify_is_lossless_monte_carlo():
+    """The first emitted token (accepted candidate, or the re-drawn one) follows the target
+    distribution p_0 whatever q is, and the acceptance rate is sum_v min(p_0, q_1)."""
+    from scipy import stats
+    zp = np.log(np.array([0.5, 0.3, 0.15, 0.05]))
+    zq = np.log(np.array([0.1, 0.2, 0.3, 0.4]))
+    U = zq[None, None, :]
+    Z = np.stack([zp, zp])[None]
+    n = 6000
+    first = np.zeros(n, np.int64)
+    acc = 0
+    for s in range(n):
+        cand, _, _, _ = orc.sample_candidates(U, 1.0, s)
+        tau, token = orc.verify_sample(U, cand, Z, 1.0, s)
+        first[s] = cand[0, 0] if tau[0] > 1 else token[0]
+        acc += int(tau[0] > 1)
+    p = np.exp(zp)
+    assert stats.chisquare(np.bincount(first, minlength=4), p * n).pvalue > 1e-4
+    a = np.minimum(p, np.exp(zq)).sum()
+    assert abs(acc / n - a) < 4 * math.sqrt(a * (1 - a) / n)
+
+
+def test_verify_temperature_scales_logits():
+    """Logits times T at temperature T are the same distributions as at T = 1."""
+    U, Z = verify_inputs(3, 5, 30, 43)
+    cand, _, _, _ = orc.sample_candidates(U, 1.0, 9)
+    c2, _, _, _ = orc.sample_candidates(U * 0.7, 0.7, 9)
+    assert np.array_equal(cand, c2)
+    t1 = orc.verify_sample(U, cand, Z, 1.0, 9)
+    t2 = orc.verify_sample(U * 0.7, cand, Z * 0.7, 0.7, 9)
+    assert np.array_equal(t1[0], t2[0]) and np.array_equal(t1[1], t2[1])
+
+
 # ----------------------------------------------------------------------------- selector
 
 def test_selector_without_pair_term_is_per_position_argmax():
