@@ -21,7 +21,11 @@ Sources (page title, section):
             the accept / bonus split.
   [DFlash2] "DFlash 2：正确 token 已在候选里" (bowenzhou.top/papers/2026/DFlash2):
             洞察一 -- the S_t(a,b) selector score and the greedy walk; 洞察二 -- the
-            two-tap dynamic convolution.
+            two-tap dynamic convolution; 洞察一 and Results -- sampling at temperature 1
+            with lossless rejection sampling.
+  [Philox]  Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3"
+            (SC 2011): the Philox4x32-10 counter-based generator, used for every random
+            number the sampling path draws.
 
 Readings where the pages are silent or disagree (each is listed in the design doc):
   * block layout [anchor, mask x (B-1)] at absolute positions C..C+B-1, C = context
@@ -38,7 +42,14 @@ Readings where the pages are silent or disagree (each is listed in the design doc):
     projected row h_k the plain form adds;
   * four convs per layer acting on the residual stream (before/after each sublayer),
     correction linear in the conv input, x_{-1} = 0 at offset 0;
-  * selector A = W_A E[a], B = W_B E[b], G = sigmoid(W_G z_t), U_t = raw logit.
+  * selector A = W_A E[a], B = W_B E[b], G = sigmoid(W_G z_t), U_t = raw logit;
+  * sampling at temperature T: q_t = softmax(U_t / T) over the whole vocabulary,
+    candidates drawn independently per offset (Gumbel-max); verify accepts c_{j+1} when
+    u_j < p_j(c_{j+1}) / q_{j+1}(c_{j+1}), p_j = softmax(Z_j / T) of the target row j;
+    the first rejection n emits a draw from max(0, p_n - q_{n+1}) (renormalised), or
+    from p_n when that is zero everywhere; all accepted emits a draw from p_{B-1};
+  * random numbers: Philox4x32-10 keyed by the 64-bit seed, counter (v // 4, row,
+    stream, 0), output word v % 4; u = (x >> 8 + 1/2) / 2^24; Gumbel g = -log(-log u).
 
 Parity status: every function here is pinned by tests/test_oracle.py (closed forms,
 invariants, brute force on tiny inputs, the pages' worked examples under tests/golden/).
@@ -374,6 +385,140 @@ def select_path(cfg, W: dict, cand_ids: np.ndarray, cand_vals: np.ndarray,
                 margins[i, t - 1] = best_s - sorted(scores)[-2]
             a = best_b
     return (path, margins) if return_margins else path
+
+
+# ----------------------------------------------------------------------------- sampling
+
+PHILOX_M = (0xD2511F53, 0xCD9E8D57)   # [Philox] round multipliers of Philox4x32
+PHILOX_W = (0x9E3779B9, 0xBB67AE85)   # [Philox] Weyl key increments
+_M32 = np.uint64(0xFFFFFFFF)
+
+STREAM_DRAFT = 0     # candidate draws, row = sequence * (B-1) + offset - 1
+STREAM_ACCEPT = 1    # acceptance uniforms, row = sequence, index = step n
+STREAM_EMIT = 2      # residual / bonus draw, row = sequence
+
+
+def philox4x32(ctr, key, rounds: int = 10):
+    """Philox4x32-R of [Philox], vectorised: ctr is four uint arrays (broadcastable),
+    key two ints. Each round: (hi, lo) of M0 * c0 and M1 * c2 give
+    (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0); the key gains (W0, W1) before every round
+    after the first. Returns four uint64 arrays holding 32-bit words."""
+    c0, c1, c2, c3 = (np.asarray(c, dtype=np.uint64) & _M32 for c in ctr)
+    k0, k1 = np.uint64(key[0] & 0xFFFFFFFF), np.uint64(key[1] & 0xFFFFFFFF)
+    m0, m1 = np.uint64(PHILOX_M[0]), np.uint64(PHILOX_M[1])
+    for r in range(rounds):
+        if r:
+            k0 = (k0 + np.uint64(PHILOX_W[0])) & _M32
+            k1 = (k1 + np.uint64(PHILOX_W[1])) & _M32
+        p0 = m0 * c0            # < 2^64: exact in uint64
+        p1 = m1 * c2
+        c0, c1, c2, c3 = ((p1 >> np.uint64(32)) ^ c1 ^ k0, p1 & _M32,
+                          (p0 >> np.uint64(32)) ^ c3 ^ k1, p0 & _M32)
+    return c0, c1, c2, c3
+
+
+def uniforms(seed: int, stream: int, row: int, n: int) -> np.ndarray:
+    """u_v in (0, 1) for v = 0..n-1 of (seed, stream, row): word v % 4 of Philox4x32-10
+    at counter (v // 4, row, stream, 0), key (seed low, seed high); u = (w >> 8 + 0.5) / 2^24
+    (24 bits, never 0 or 1)."""
+    v = np.arange(n, dtype=np.uint64)
+    words = philox4x32((v >> np.uint64(2), np.uint64(row), np.uint64(stream), np.uint64(0)),
+                       (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))
+    w = np.choose((v & np.uint64(3)).astype(np.int64), words)
+    return ((w >> np.uint64(8)).astype(np.float64) + 0.5) / float(1 << 24)
+
+
+def gumbel(u: np.ndarray) -> np.ndarray:
+    return -np.log(-np.log(u))
+
+
+def logsumexp(x: np.ndarray) -> float:
+    m = np.max(x)
+    return float(m + np.log(np.sum(np.exp(x - m))))
+
+
+def gumbel_argmax(score: np.ndarray):
+    """argmax with ties to the lower id, and the margin to the runner-up."""
+    best = int(np.argmax(score))   # first index of the maximum = lowest id
+    if score.size < 2:
+        return best, np.inf
+    top2 = np.partition(score, -2)[-2:]
+    return best, float(top2[1] - top2[0])
+
+
+def sample_candidates(logits: np.ndarray, T: float, seed: int):
+    """Draft sampling at temperature T ([DFlash2] 洞察一 / Results: sampling at T = 1).
+
+    logits [nb, B-1, V] = U_t for offsets t = 1..B-1. Each offset draws independently
+    from q_t = softmax(U_t / T) by Gumbel-max: c_t = argmax_v U_t(v)/T + g_v with g from
+    stream STREAM_DRAFT, row i*(B-1) + t-1. Returns ids [nb, B-1], lse [nb, B-1]
+    (logsumexp of U_t / T), logq [nb, B-1] (log q_t(c_t)) and the Gumbel margins."""
+    nb, bm1, V = logits.shape
+    ids = np.zeros((nb, bm1), np.int32)
+    lse = np.zeros((nb, bm1))
+    logq = np.zeros((nb, bm1))
+    margin = np.zeros((nb, bm1))
+    for i in range(nb):
+        for t in range(bm1):
+            x = logits[i, t] / T
+            row = i * bm1 + t
+            c, m = gumbel_argmax(x + gumbel(uniforms(seed, STREAM_DRAFT, row, V)))
+            ids[i, t], margin[i, t] = c, m
+            lse[i, t] = logsumexp(x)
+            logq[i, t] = x[c] - lse[i, t]
+    return ids, lse, logq, margin
+
+
+def verify_sample(draft_logits: np.ndarray, cand: np.ndarray, target_logits: np.ndarray,
+                  T: float, seed: int, return_detail: bool = False):
+    """Lossless rejection sampling of a drafted block ([DFlash2] Results: lossless
+    rejection sampling at T = 1; [DFlash] 四、推理流程 dflash_cycle step ④, the rejected
+    position is re-drawn from the target and the last step yields the bonus token).
+
+    draft_logits [nb, B-1, V] (offsets 1..B-1), cand [nb, B-1], target_logits [nb, B, V]
+    (row j = the target's distribution after block offset j). With p_j = softmax(Z_j/T),
+    q_t = softmax(U_t/T): step n accepts c_{n+1} when u_n < p_n(c) / q_{n+1}(c), u_n the
+    uniform of stream STREAM_ACCEPT, row i, index n. At the first rejection n the emitted
+    token is argmax_v log r(v) + g_v over r = max(0, p_n - q_{n+1}) > 0 (or over log p_n
+    when r is zero everywhere); with every candidate accepted it is a draw from p_{B-1};
+    g from stream STREAM_EMIT, row i. Returns (tau = n + 1, token) and, with
+    ``return_detail``, the per-step acceptance margins |log u - log(p/q)| and the
+    emitted draw's Gumbel margin."""
+    nb, bm1, V = draft_logits.shape
+    tau = np.zeros(nb, np.int32)
+    token = np.zeros(nb, np.int32)
+    acc_margin = np.full((nb, bm1), np.inf)
+    emit_margin = np.zeros(nb)
+    for i in range(nb):
+        u = uniforms(seed, STREAM_ACCEPT, i, bm1)
+        n = 0
+        while n < bm1:
+            c = int(cand[i, n])
+            zp = target_logits[i, n] / T
+            zq = draft_logits[i, n] / T
+            log_ratio = (zp[c] - logsumexp(zp)) - (zq[c] - logsumexp(zq))
+            acc_margin[i, n] = abs(math.log(u[n]) - log_ratio)
+            if math.log(u[n]) < log_ratio:
+                n += 1
+            else:
+                break
+        g = gumbel(uniforms(seed, STREAM_EMIT, i, V))
+        if n < bm1:
+            zp = target_logits[i, n] / T
+            zq = draft_logits[i, n] / T
+            r = np.exp(zp - logsumexp(zp)) - np.exp(zq - logsumexp(zq))
+            if (r > 0).any():
+                with np.errstate(divide="ignore"):
+                    score = np.where(r > 0, np.log(np.where(r > 0, r, 1.0)), -np.inf) + g
+            else:
+                score = zp + g
+        else:
+            score = target_logits[i, bm1] / T + g
+        token[i], emit_margin[i] = gumbel_argmax(score)
+        tau[i] = n + 1
+    if return_detail:
+        return tau, token, acc_margin, emit_margin
+    return tau, token
 
 
 def draft_step(cfg, W: dict, hv, n_commit, ctx_len, cache: KVCache, block_ids, target,
