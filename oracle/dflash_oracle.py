@@ -49,7 +49,8 @@ Readings where the pages are silent or disagree (each is listed in the design doc):
     the first rejection n emits a draw from max(0, p_n - q_{n+1}) (renormalised), or
     from p_n when that is zero everywhere; all accepted emits a draw from p_{B-1};
   * random numbers: Philox4x32-10 keyed by the 64-bit seed, counter (v // 4, row,
-    stream, 0), output word v % 4; u = (x >> 8 + 1/2) / 2^24; Gumbel g = -log(-log u).
+    stream, 0), output word v % 4; u = ((x >> 9) + 1/2) / 2^23 (exact in fp32, so both
+    sides start from the same u); Gumbel g = -log(-log u).
 
 Parity status: every function here is pinned by tests/test_oracle.py (closed forms,
 invariants, brute force on tiny inputs, the pages' worked examples under tests/golden/).
@@ -419,13 +420,13 @@ def philox4x32(ctr, key, rounds: int = 10):
 
 def uniforms(seed: int, stream: int, row: int, n: int) -> np.ndarray:
     """u_v in (0, 1) for v = 0..n-1 of (seed, stream, row): word v % 4 of Philox4x32-10
-    at counter (v // 4, row, stream, 0), key (seed low, seed high); u = (w >> 8 + 0.5) / 2^24
-    (24 bits, never 0 or 1)."""
+    at counter (v // 4, row, stream, 0), key (seed low, seed high); u = ((w >> 9) + 0.5) / 2^23
+    (23 random bits, never 0 or 1, exactly representable in fp32)."""
     v = np.arange(n, dtype=np.uint64)
     words = philox4x32((v >> np.uint64(2), np.uint64(row), np.uint64(stream), np.uint64(0)),
                        (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))
     w = np.choose((v & np.uint64(3)).astype(np.int64), words)
-    return ((w >> np.uint64(8)).astype(np.float64) + 0.5) / float(1 << 24)
+    return ((w >> np.uint64(9)).astype(np.float64) + 0.5) / float(1 << 23)
 
 
 def gumbel(u: np.ndarray) -> np.ndarray:
