@@ -66,6 +66,10 @@ def step_bytes_flops(w: di.Workload, ctx: np.ndarray, tp: np.ndarray):
     flops += 2 * w.nb * (w.B - 1) * w.V * w.D
     if w.flags & di.FLAG_FILM:
         flops += 2 * M * 5 * w.D * w.film_width
+    if w.temperature > 0:
+        # draft logits written by the LM head and read by the draw; target logits read for
+        # their normaliser; two rows per sequence read again by the residual draw
+        io += 2 * w.nb * (w.B - 1) * w.V * 4 + w.nb * w.B * w.V * 4 + w.nb * 2 * w.V * 4
     return wbytes + kv_bytes + io, flops, wbytes, kv_bytes
 
 
@@ -84,7 +88,10 @@ def kernels_per_step(w: di.Workload) -> int:
     n += 2                                # LM head GEMM + merge
     if w.flags & di.FLAG_SELECT:
         n += 5                            # gather, A|B GEMM, G GEMM, score table, walk
-    n += 1                                # accept
+    if w.temperature > 0:
+        n += 2 + 4                        # draw (partial, merge); verify (target lse x2, walk x2)
+    else:
+        n += 1                            # accept
     return n
 
 
@@ -233,6 +240,12 @@ def run_gpu(args, rank, world):
     select = bool(w.flags & di.FLAG_SELECT)
     draft = path if select else tid[..., 0]
     draft_c = torch.empty(w.nb, w.B - 1, dtype=torch.int32, device=dev)
+    sampling = w.temperature > 0
+    if sampling:  # the target model's verify logits stand resident in HBM (it runs on this GPU)
+        draft_logits = torch.empty(w.nb, w.B - 1, w.V, dtype=torch.float32, device=dev)
+        draft_lse = torch.empty(w.nb, w.B - 1, dtype=torch.float32, device=dev)
+        tgt_logits = torch.from_numpy(di.target_logits(w, seed)).to(dev)
+        sample_seed = 0x5EED_0000 + seed
     max_ctx = int(ctx.max())
     stream = torch.cuda.Stream(device=dev)
     try:  # event-record nodes inside the captured step (torch >= 2.7)
@@ -249,9 +262,15 @@ def run_gpu(args, rank, world):
         dr.draft_block(w.nb, block, ctx_len, hidden, x0_relay=x0, max_ctx_hint=max_ctx, stream=s)
         if lm_events:
             lm_events[0].record(s)
-        dr.lm_head_topk(w.nb, hidden, k, tid, tv, stream=s)
+        dr.lm_head_topk(w.nb, hidden, k, tid, tv, draft_logits if sampling else None, stream=s)
         if lm_events:
             lm_events[1].record(s)
+        if sampling:
+            dr.sample(w.nb * (w.B - 1), draft_logits, w.temperature, sample_seed, draft_c, draft_lse,
+                      stream=s)
+            dr.verify_sample(w.nb, draft_logits, draft_lse, draft_c, tgt_logits, w.temperature,
+                             sample_seed, tau, bonus, stream=s)
+            return
         if select:
             dr.select(w.nb, k, tid, tv, hidden, block, path, stream=s)
         draft_c.copy_(draft)
@@ -262,7 +281,8 @@ def run_gpu(args, rank, world):
     stream.synchronize()
     if dr.status(stream) != 0:
         raise RuntimeError("device status reports an error after the first step")
-    target.copy_(i32(di.target_row_from_draft(draft_c.cpu().numpy(), w.V, seed)))
+    if not sampling:
+        target.copy_(i32(di.target_row_from_draft(draft_c.cpu().numpy(), w.V, seed)))
 
     # capture one step in a CUDA graph (warm-up launches above configured every kernel)
     graph = torch.cuda.CUDAGraph()
@@ -352,6 +372,8 @@ def run_gpu(args, rank, world):
     hbm, tf_burst, tf_sus, src = load_peaks()
     total_bytes, flops, wbytes, kvbytes = step_bytes_flops(w, ctx, tp)
     lm_bytes = 2 * w.V * w.D + 2 * w.nb * (w.B - 1) * w.D + 8 * w.nb * (w.B - 1) * k
+    if w.temperature > 0:
+        lm_bytes += 4 * w.nb * (w.B - 1) * w.V  # the fp32 logits the draw reads
     lm_avg = float(np.mean(lm_ms))
     achieved = lm_bytes / (lm_avg * 1e-3) / 1e9
     traffic = traffic_from_profile(os.path.join(ROOT, "block_diffusion_speculative_project_gb300",
@@ -417,6 +439,7 @@ def cpu_baseline(w: di.Workload, bits=None, budget_s: float = 15.0):
     if w.flags & di.FLAG_FILM:
         fb, fy = di.relay_tokens(w)
     ids = di.block_ids(w, di.anchors(w))
+    Z = di.target_logits(w).astype(np.float32) if w.temperature > 0 else None
     rng = np.random.default_rng(7)
     done, t_used = 0, 0.0
     while t_used < budget_s and done < w.nb:
@@ -429,10 +452,13 @@ def cpu_baseline(w: di.Workload, bits=None, budget_s: float = 15.0):
             cache.V[n][0][:, :base] = rng.standard_normal((w.Hkv, base, w.hd), dtype=np.float32)
         hv = orc.widen(di.verifier_rows(w.with_(nb=1), w.B, name=f"hv_cpu{i}"), np.float32)
         t0 = time.perf_counter()
-        orc.draft_step(w, W, hv, tp[i:i + 1], [base], cache, ids[i:i + 1],
-                       np.zeros((1, w.B), np.int32), relay_a=None if a is None else a[i:i + 1],
-                       relay_b=None if fb is None else fb[i:i + 1],
-                       relay_y=None if fy is None else fy[i:i + 1])
+        o = orc.draft_step(w, W, hv, tp[i:i + 1], [base], cache, ids[i:i + 1],
+                           np.zeros((1, w.B), np.int32), relay_a=None if a is None else a[i:i + 1],
+                           relay_b=None if fb is None else fb[i:i + 1],
+                           relay_y=None if fy is None else fy[i:i + 1])
+        if w.temperature > 0:
+            cand, _, _, _ = orc.sample_candidates(o["logits"], w.temperature, i)
+            orc.verify_sample(o["logits"], cand, Z[i:i + 1], w.temperature, i)
         t_used += time.perf_counter() - t0
         done += 1
     per_seq = t_used / done

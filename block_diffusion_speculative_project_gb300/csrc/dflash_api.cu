@@ -124,6 +124,7 @@ struct WsLayout {
   size_t tk_vals = 0, tk_ids = 0;              // LM head top-k partial lists
   size_t sel_e = 0, sel_ab = 0, sel_g = 0, sel_t = 0;  // selector
   size_t film_cond = 0, film_hid = 0, film_bg = 0;     // FiLM relay
+  size_t smp_part = 0, smp_lse = 0, ver_part = 0, ver_nrej = 0;  // sampling
   size_t total = 0;
   size_t apart_bytes = 0, apart_ctas = 0;
 };
@@ -187,6 +188,10 @@ void plan_workspace(dflash_handle_s *h) {
     L.sel_g = take((size_t)Ml * c.sel_dim * 4);
     L.sel_t = take((size_t)Ml * c.k_top * c.k_top * 4);  // step score tables
   }
+  L.smp_part = take((size_t)Mb * kSampleMaxSlices * 16);
+  L.smp_lse = take((size_t)Mb * 4);
+  L.ver_part = take((size_t)c.max_batch * kSampleMaxSlices * 16);
+  L.ver_nrej = take((size_t)c.max_batch * 4);
   if (c.flags & DFLASH_FLAG_FILM) {
     L.film_cond = take((size_t)Mb * 3 * c.D * 2);
     L.film_hid = take((size_t)Mb * c.film_dim * 2);
@@ -891,6 +896,53 @@ int dflash_accept(dflash_handle_t h, int nb, const int32_t *draft, const int32_t
   if (nb == 0) return DFLASH_OK;
   if (!draft || !target || !out_tau || !out_bonus) return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor");
   DF_CUDA(launch_accept(draft, target, nb, h->cfg.B, out_tau, out_bonus, stream));
+  return DFLASH_OK;
+}
+
+int dflash_sample(dflash_handle_t h, int rows, const float *logits, float temperature,
+                  uint64_t seed, int row0, int32_t *out_ids, float *out_lse, float *out_logq,
+                  void *ws, size_t ws_bytes, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+  const auto &c = h->cfg;
+  if (rows < 0 || rows > c.max_batch * c.B)
+    return fail(DFLASH_ERR_INVALID_ARG, "rows=%d outside [0, max_batch*B]", rows);
+  if (!(temperature > 0.f) || !std::isfinite(temperature))
+    return fail(DFLASH_ERR_INVALID_ARG, "temperature must be positive and finite");
+  if (row0 < 0) return fail(DFLASH_ERR_INVALID_ARG, "row0 must be >= 0");
+  if (rows == 0) return DFLASH_OK;
+  if (!logits || !out_ids || !out_lse) return fail(DFLASH_ERR_INVALID_ARG, "logits, out_ids and out_lse must be non-NULL");
+  DF_TRY(check_ws(h, ws, ws_bytes));
+  Ws w{static_cast<uint8_t *>(ws), h->ws};
+  const int S = sample_slices(rows, c.V, h->num_sms);
+  DF_CUDA(launch_sample(logits, c.V, rows, c.V, 1.f / temperature, seed, 0, row0, S,
+                        w.at<float4>(h->ws.smp_part), out_ids, out_lse,
+                        out_logq ? out_logq : w.at<float>(h->ws.smp_lse), stream));
+  return DFLASH_OK;
+}
+
+int dflash_verify_sample(dflash_handle_t h, int nb, const float *draft_logits, const float *draft_lse,
+                         const int32_t *cand, const float *target_logits, float temperature,
+                         uint64_t seed, int32_t *out_tau, int32_t *out_token, void *ws,
+                         size_t ws_bytes, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+  const auto &c = h->cfg;
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (!(temperature > 0.f) || !std::isfinite(temperature))
+    return fail(DFLASH_ERR_INVALID_ARG, "temperature must be positive and finite");
+  if (nb == 0) return DFLASH_OK;
+  if (!draft_logits || !draft_lse || !cand || !target_logits || !out_tau || !out_token)
+    return fail(DFLASH_ERR_INVALID_ARG, "every verify argument must be non-NULL");
+  DF_TRY(check_ws(h, ws, ws_bytes));
+  Ws w{static_cast<uint8_t *>(ws), h->ws};
+  const float inv_T = 1.f / temperature;
+  const int rows = nb * c.B;
+  float *tlse = w.at<float>(h->ws.smp_lse);
+  DF_CUDA(launch_sample(target_logits, c.V, rows, c.V, inv_T, seed, -1, 0,
+                        sample_slices(rows, c.V, h->num_sms), w.at<float4>(h->ws.smp_part), nullptr,
+                        tlse, nullptr, stream));
+  DF_CUDA(launch_verify(draft_logits, draft_lse, cand, target_logits, tlse, nb, c.B, c.V, inv_T, seed,
+                        sample_slices(nb, c.V, h->num_sms), w.at<float4>(h->ws.ver_part),
+                        w.at<int>(h->ws.ver_nrej), out_tau, out_token, stream));
   return DFLASH_OK;
 }
 

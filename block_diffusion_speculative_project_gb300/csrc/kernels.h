@@ -180,6 +180,23 @@ cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, cons
                                const float *G, float *table, int nb, int B, int k, int sel_dim, int *path,
                                cudaStream_t s);
 
+// ---------------------------------------------------------------- sampling (sampling.cu)
+
+constexpr int kSampleMaxSlices = 64;
+// Slices per logit row of the sampling passes (rows * S CTAs, at least 1024 elements each).
+int sample_slices(int rows, int V, int num_sms);
+// Draws ids[r] ~ softmax(logits[r] * inv_T) (Philox stream `stream`, row row0 + r) and
+// writes lse[r] (and logq[r] = log q(ids[r])); stream < 0: lse only (ids, logq unused).
+// part: rows * S float4 of scratch.
+cudaError_t launch_sample(const float *logits, long long ld, int rows, int V, float inv_T,
+                          unsigned long long seed, int stream, int row0, int S, float4 *part,
+                          int *ids, float *lse, float *logq, cudaStream_t s);
+// Rejection-sampling verify of nb blocks; part: nb * S float4, nrej: nb ints of scratch.
+cudaError_t launch_verify(const float *draft_logits, const float *draft_lse, const int *cand,
+                          const float *target_logits, const float *target_lse, int nb, int B, int V,
+                          float inv_T, unsigned long long seed, int S, float4 *part, int *nrej,
+                          int *tau, int *token, cudaStream_t s);
+
 // ---------------------------------------------------------------- attention
 
 // Context attention of one drafter layer (see attention.cu). The block's own K/V rows

@@ -77,6 +77,9 @@ def _load():
         "dflash_attention": (i, [p, i, i, p, p, p, p, i, p, p, sz, p]),
         "dflash_topk": (i, [p, i, i, p, i, p, p, p, sz, p]),
         "dflash_accept": (i, [p, i, p, p, p, p, p]),
+        "dflash_sample": (i, [p, i, p, ctypes.c_float, ctypes.c_uint64, i, p, p, p, p, sz, p]),
+        "dflash_verify_sample": (i, [p, i, p, p, p, p, ctypes.c_float, ctypes.c_uint64, p, p, p, sz,
+                                     p]),
         "dflash2_conv": (i, [p, i, i, i, p, p, sz, p]),
         "dflash2_select": (i, [p, i, i, p, p, p, p, p, p, sz, p]),
     }
@@ -91,7 +94,8 @@ LIB = _load()
 EXPORTED = ("dflash_create", "dflash_destroy", "dflash_set_weights", "dflash_workspace_size",
             "dflash_status", "dflash_last_error", "dflash_ctx_project", "dflash_ctx_project_film",
             "dflash_draft_block",
-            "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_attention", "dflash_topk", "dflash_accept", "dflash2_conv", "dflash2_select")
+            "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_attention", "dflash_topk", "dflash_accept", "dflash_sample", "dflash_verify_sample", "dflash2_conv",
+            "dflash2_select")
 
 
 def _check(rc: int):
@@ -188,6 +192,21 @@ def dflash_topk(h, rows, cols, logits, k, out_ids, out_vals, ws=None, stream=Non
 def dflash_accept(h, nb, draft, target, out_tau, out_bonus, stream=None) -> None:
     _check(LIB.dflash_accept(h, nb, _ptr(draft), _ptr(target), _ptr(out_tau), _ptr(out_bonus),
                              _stream(stream)))
+
+
+def dflash_sample(h, rows, logits, temperature, seed, row0, out_ids, out_lse, out_logq, ws,
+                  stream=None) -> None:
+    _check(LIB.dflash_sample(h, rows, _ptr(logits), float(temperature), int(seed), int(row0),
+                             _ptr(out_ids), _ptr(out_lse), _ptr(out_logq), _ptr(ws),
+                             ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dflash_verify_sample(h, nb, draft_logits, draft_lse, cand, target_logits, temperature, seed,
+                         out_tau, out_token, ws, stream=None) -> None:
+    _check(LIB.dflash_verify_sample(h, nb, _ptr(draft_logits), _ptr(draft_lse), _ptr(cand),
+                                    _ptr(target_logits), float(temperature), int(seed),
+                                    _ptr(out_tau), _ptr(out_token), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def dflash2_conv(h, layer, which, nb, x, ws, stream=None) -> None:

@@ -92,6 +92,16 @@ class Drafter:
     def accept(self, nb, draft, target, out_tau, out_bonus, stream=None):
         _d.dflash_accept(self.h, nb, draft, target, out_tau, out_bonus, stream)
 
+    def sample(self, rows, logits, temperature, seed, out_ids, out_lse, out_logq=None, row0=0,
+               stream=None):
+        _d.dflash_sample(self.h, rows, logits, temperature, seed, row0, out_ids, out_lse, out_logq,
+                         self.ws, stream)
+
+    def verify_sample(self, nb, draft_logits, draft_lse, cand, target_logits, temperature, seed,
+                      out_tau, out_token, stream=None):
+        _d.dflash_verify_sample(self.h, nb, draft_logits, draft_lse, cand, target_logits, temperature,
+                                seed, out_tau, out_token, self.ws, stream)
+
     def conv(self, layer, which, nb, x, stream=None):
         _d.dflash2_conv(self.h, layer, which, nb, x, self.ws, stream)
 

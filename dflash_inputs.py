@@ -19,6 +19,7 @@ Value recipe (the pages give no trained weights; these stand in for them):
                                N(0, 0.02) the two-tap conv is quadratic in x and the
                                residual stream diverges within two layers
   * verifier hidden states   ~ N(0, 1)
+  * target logits (sampling verify) ~ 2 N(0, 1), fp32
   * anchors                  ~ U{0 .. V-2};  mask id = V-1
   * FiLM relay MLP           W1 ~ N(0, 1/(3D)), W2 ~ N(0, 4/film_dim): fan-in scaled so
                                that beta and gamma come out O(1), the size of the plain
@@ -68,6 +69,7 @@ class Workload:
     sel_dim: int = 256
     conv_group: int = 16
     film_dim: int = 0  # hidden width of the FiLM relay MLP; 0 = D/4
+    temperature: float = 0.0  # 0: greedy draft and exact-match accept; > 0: sampling
 
     @property
     def film_width(self) -> int:
@@ -95,9 +97,10 @@ RELAY_DFLASH2 = QWEN3_8B.with_(name="qwen3_8b_shaped_relay_dflash2_b16_c4096_nb3
                                flags=FLAG_RELAY | FLAG_CONV | FLAG_SELECT)
 FILM_RELAY = QWEN3_8B.with_(name="qwen3_8b_shaped_film_relay_b16_c4096_nb32", nb=32,
                             flags=FLAG_RELAY | FLAG_FILM)
+SAMPLING_T1 = QWEN3_8B.with_(name="qwen3_8b_shaped_sampling_t1_b16_c4096_nb8", temperature=1.0)
 
 WORKLOADS = {w.name: w for w in (TINY, QWEN3_4B, QWEN3_8B, SWEEP_NB16, SWEEP_NB32,
-                                  SWEEP_NB64, RELAY_DFLASH2, FILM_RELAY)}
+                                  SWEEP_NB64, RELAY_DFLASH2, FILM_RELAY, SAMPLING_T1)}
 
 
 # --------------------------------------------------------------------------- streams
@@ -156,6 +159,16 @@ def normal_bf16(name: str, shape, std: float, mean: float = 0.0, seed: int = 0) 
     if mean != 0.0:
         x += np.float32(mean)
     return f32_to_bf16_bits(x).reshape(shape)
+
+
+def normal_f32(name: str, shape, std: float = 1.0, seed: int = 0) -> np.ndarray:
+    """float32 std * N(0, 1) from the stream `name`, for inputs the path takes in fp32
+    (logit rows of the sampling calls)."""
+    shape = tuple(int(s) for s in shape)
+    x = _fill_normal(name, int(np.prod(shape)) if shape else 1, seed)
+    if std != 1.0:
+        x *= np.float32(std)
+    return x.reshape(shape)
 
 
 def uniform_int(name: str, shape, lo: int, hi: int, seed: int = 0) -> np.ndarray:
@@ -255,6 +268,13 @@ def relay_tokens(w: Workload, seed: int = 0):
     correction b and the draft's first rejected guess, each U{0..V-2}."""
     return (uniform_int("relay_b", (w.nb,), 0, w.V - 2, seed),
             uniform_int("relay_y", (w.nb,), 0, w.V - 2, seed))
+
+
+def target_logits(w: Workload, seed: int = 0) -> np.ndarray:
+    """Target-model logits of the verify pass [nb, B, V] (fp32), 2 * N(0, 1): the target
+    model itself is not part of the draft step, its output row j (the distribution after
+    block offset j) is an input of the sampling verify."""
+    return normal_f32("target_logits", (w.nb, w.B, w.V), 2.0, seed)
 
 
 def verifier_rows(w: Workload, rows: int, seed: int = 0, name: str = "hv") -> np.ndarray:

@@ -278,6 +278,41 @@ DFLASH_API int dflash_topk(dflash_handle_t h, int rows, int cols, const float *l
 DFLASH_API int dflash_accept(dflash_handle_t h, int nb, const int32_t *draft, const int32_t *target,
                   int32_t *out_tau, int32_t *out_bonus, dflash_stream_t stream);
 
+/* Draft sampling at temperature T > 0 ([DFlash2] 洞察一 and Results: sampling at T = 1;
+ * each block offset draws independently from its own distribution, as the one-pass draft
+ * predicts every position independently). Row r of `logits` draws
+ *   out_ids[r] ~ softmax(logits[r] / T)
+ * by Gumbel-max, argmax_v logits[r][v]/T - log(-log u_v) (ties to the lower id), with u_v
+ * from Philox4x32-10 (Salmon et al., SC 2011) keyed by `seed`: word v % 4 of the block at
+ * counter (v / 4, row0 + r, 0, 0), u = ((w >> 9) + 1/2) / 2^23.
+ *   rows      number of rows, <= max_batch * B (for a draft: nb * (B-1), row0 = 0, so that
+ *             offset t of sequence i is row i*(B-1) + t-1)
+ *   logits    f32 [rows, V] (e.g. the out_logits of dflash_lm_head_topk)
+ *   out_ids   int32 [rows]; -1 only for a row whose every logit is NaN
+ *   out_lse   f32 [rows]: log sum_v exp(logits[r][v] / T)
+ *   out_logq  f32 [rows] or NULL: log q(out_ids[r]) = logits[r][id] / T - out_lse[r] */
+DFLASH_API int dflash_sample(dflash_handle_t h, int rows, const float *logits, float temperature,
+                  uint64_t seed, int row0, int32_t *out_ids, float *out_lse, float *out_logq,
+                  void *ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* Lossless rejection-sampling verify of nb drafted blocks at temperature T > 0 ([DFlash2]
+ * Results: lossless rejection sampling; [DFlash] 四、推理流程 dflash_cycle step ④: the
+ * rejected position is re-drawn from the target, the last step yields the bonus token).
+ * With p_j = softmax(target_logits[i][j] / T) and q_t = softmax(draft_logits[i][t-1] / T):
+ * step j = 0..B-2 accepts c = cand[i][j] when log u_j < log p_j(c) - log q_{j+1}(c),
+ * u_j = Philox uniform of counter (j / 4, i, 1, 0); n = the first rejected step (B-1 when
+ * none). out_token[i] is a draw (Gumbel-max, Philox counter (v / 4, i, 2, 0)) from
+ * max(0, p_n - q_{n+1}) renormalised, from p_n when that residual is zero everywhere,
+ * or from p_{B-1} when every candidate was accepted. out_tau[i] = n + 1.
+ *   draft_logits   f32 [nb, B-1, V]: U_t for offsets 1..B-1
+ *   draft_lse      f32 [nb, B-1]: log sum exp(U_t / T) (out_lse of dflash_sample)
+ *   cand           int32 [nb, B-1]: the drafted candidates (an id outside [0, V) is rejected)
+ *   target_logits  f32 [nb, B, V]: row j = the target's logits after block offset j */
+DFLASH_API int dflash_verify_sample(dflash_handle_t h, int nb, const float *draft_logits,
+                  const float *draft_lse, const int32_t *cand, const float *target_logits,
+                  float temperature, uint64_t seed, int32_t *out_tau, int32_t *out_token,
+                  void *ws, size_t ws_bytes, dflash_stream_t stream);
+
 /* DFlash 2 two-tap dynamic depthwise conv ([DFlash2] 洞察二), in place:
  * x'_t = k_{t,0} * x_t + k_{t,1} * x_{t-1}, k_{t,j} = base_j + expand(W_j x_t),
  * one correction per conv_group channels, x_{-1} = 0 at block offset 0.
