@@ -265,7 +265,7 @@ def run_gpu(args, rank, world):
         dr.lm_head_topk(w.nb, hidden, k, tid, tv, draft_logits if sampling else None, stream=s)
         if lm_events:
             lm_events[1].record(s)
-        if sampling:
+        if sampling:  # draw over the written logits, then the verify
             dr.sample(w.nb * (w.B - 1), draft_logits, w.temperature, sample_seed, draft_c, draft_lse,
                       stream=s)
             dr.verify_sample(w.nb, draft_logits, draft_lse, draft_c, tgt_logits, w.temperature,
@@ -373,7 +373,7 @@ def run_gpu(args, rank, world):
     total_bytes, flops, wbytes, kvbytes = step_bytes_flops(w, ctx, tp)
     lm_bytes = 2 * w.V * w.D + 2 * w.nb * (w.B - 1) * w.D + 8 * w.nb * (w.B - 1) * k
     if w.temperature > 0:
-        lm_bytes += 4 * w.nb * (w.B - 1) * w.V  # the fp32 logits the draw reads
+        lm_bytes += 4 * w.nb * (w.B - 1) * w.V  # the fp32 logits the verify reads
     lm_avg = float(np.mean(lm_ms))
     achieved = lm_bytes / (lm_avg * 1e-3) / 1e9
     traffic = traffic_from_profile(os.path.join(ROOT, "block_diffusion_speculative_project_gb300",

@@ -188,7 +188,7 @@ void plan_workspace(dflash_handle_s *h) {
     L.sel_g = take((size_t)Ml * c.sel_dim * 4);
     L.sel_t = take((size_t)Ml * c.k_top * c.k_top * 4);  // step score tables
   }
-  L.smp_part = take((size_t)Mb * kSampleMaxSlices * 16);
+  L.smp_part = take((size_t)std::max(Mb * kSampleMaxSlices, h->num_sms * Ml) * 32);
   L.smp_lse = take((size_t)Mb * 4);
   L.ver_part = take((size_t)c.max_batch * kSampleMaxSlices * 16);
   L.ver_nrej = take((size_t)c.max_batch * 4);
@@ -754,18 +754,17 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
   return DFLASH_OK;
 }
 
-int dflash_lm_head_topk(dflash_handle_t h, int nb, const void *hidden, int k, int32_t *out_ids,
-                        float *out_vals, float *out_logits, void *ws, size_t ws_bytes,
-                        dflash_stream_t stream) {
-  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+namespace {
+
+// LM head on block offsets 1..B-1 with the fused top-k; with temperature > 0 also the fused
+// draw (out_cand, out_lse, out_logq). out_ids == NULL skips the top-k merge.
+int lm_head_impl(dflash_handle_t h, int nb, const void *hidden, int k, int32_t *out_ids,
+                 float *out_vals, float *out_logits, float temperature, uint64_t seed,
+                 int32_t *out_cand, float *out_lse, float *out_logq, void *ws, size_t ws_bytes,
+                 cudaStream_t s) {
   const auto &c = h->cfg;
-  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
-  if (k < 1 || k > c.k_top) return fail(DFLASH_ERR_INVALID_ARG, "k=%d outside [1, k_top]", k);
-  if (nb == 0) return DFLASH_OK;
-  if (!hidden || !out_ids || !out_vals) return fail(DFLASH_ERR_INVALID_ARG, "hidden and outputs must be non-NULL");
   DF_TRY(check_ws(h, ws, ws_bytes));
   Ws w{static_cast<uint8_t *>(ws), h->ws};
-  cudaStream_t s = stream;
   const int R = c.B - 1;
   const int S = 128 / R;
   const int Ml = nb * R;
@@ -785,11 +784,62 @@ int dflash_lm_head_topk(dflash_handle_t h, int nb, const void *hidden, int k, in
   p.part_vals = w.at<float>(h->ws.tk_vals);
   p.part_ids = w.at<int>(h->ws.tk_ids);
   p.logits_out = out_logits;
+  if (temperature > 0.f) {
+    p.smp_part = w.at<float4>(h->ws.smp_part);
+    p.smp_inv_T = 1.f / temperature;
+    p.smp_stream = 0;
+    p.smp_seed = seed;
+  }
   DF_TRY(run_gemm(h, p, kBNTopk, s));
   const int ranges = p.items / p.m_tiles;
   if (ranges > h->num_sms) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "top-k ranges exceed the plan");
-  DF_CUDA(launch_topk_merge(p.part_vals, p.part_ids, Ml, k, k, (long long)Ml * k, ranges, k, out_ids,
-                            out_vals, s));
+  if (out_ids)
+    DF_CUDA(launch_topk_merge(p.part_vals, p.part_ids, Ml, k, k, (long long)Ml * k, ranges, k, out_ids,
+                              out_vals, s));
+  if (temperature > 0.f)
+    DF_CUDA(launch_draw_merge(p.smp_part, Ml, ranges, 1, Ml, out_cand, out_lse,
+                              out_logq ? out_logq : w.at<float>(h->ws.smp_lse), s));
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+int dflash_lm_head_topk(dflash_handle_t h, int nb, const void *hidden, int k, int32_t *out_ids,
+                        float *out_vals, float *out_logits, void *ws, size_t ws_bytes,
+                        dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  const auto &c = h->cfg;
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (k < 1 || k > c.k_top) return fail(DFLASH_ERR_INVALID_ARG, "k=%d outside [1, k_top]", k);
+  if (nb == 0) return DFLASH_OK;
+  if (!hidden || !out_ids || !out_vals) return fail(DFLASH_ERR_INVALID_ARG, "hidden and outputs must be non-NULL");
+  return lm_head_impl(h, nb, hidden, k, out_ids, out_vals, out_logits, 0.f, 0, nullptr, nullptr, nullptr,
+                      ws, ws_bytes, stream);
+}
+
+int dflash_lm_head_sample(dflash_handle_t h, int nb, const void *hidden, float temperature,
+                          uint64_t seed, int32_t *out_cand, float *out_lse, float *out_logq,
+                          float *out_logits, int k, int32_t *out_ids, float *out_vals, void *ws,
+                          size_t ws_bytes, dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  const auto &c = h->cfg;
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (!(temperature > 0.f) || !std::isfinite(temperature))
+    return fail(DFLASH_ERR_INVALID_ARG, "temperature must be positive and finite");
+  if (out_ids && (k < 1 || k > c.k_top)) return fail(DFLASH_ERR_INVALID_ARG, "k=%d outside [1, k_top]", k);
+  if (out_ids && !out_vals) return fail(DFLASH_ERR_INVALID_ARG, "out_vals must accompany out_ids");
+  if (nb == 0) return DFLASH_OK;
+  if (!hidden || !out_cand || !out_lse) return fail(DFLASH_ERR_INVALID_ARG, "hidden, out_cand and out_lse must be non-NULL");
+  return lm_head_impl(h, nb, hidden, out_ids ? k : c.k_top, out_ids, out_vals, out_logits, temperature,
+                      seed, out_cand, out_lse, out_logq, ws, ws_bytes, stream);
+}
+
+int dflash_draw_gumbel(int n, uint64_t seed, int stream_id, int row, float *out_u, float *out_g,
+                       dflash_stream_t stream) {
+  if (n < 0 || stream_id < 0 || row < 0) return fail(DFLASH_ERR_INVALID_ARG, "n, stream_id and row must be >= 0");
+  if (n == 0) return DFLASH_OK;
+  if (!out_u || !out_g) return fail(DFLASH_ERR_INVALID_ARG, "out_u and out_g must be non-NULL");
+  DF_CUDA(launch_draw_gumbel(n, seed, stream_id, row, out_u, out_g, stream));
   return DFLASH_OK;
 }
 

@@ -23,6 +23,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sampling.cuh"
 
 namespace df {
 
@@ -238,6 +239,7 @@ struct TopkState {
   float worst_v;
   int worst_id;
   int worst_slot;
+  DrawState dr;  // the draw at temperature T when sampling (smp_part set)
 };
 
 __device__ __forceinline__ void topk_init(TopkState &tk) {
@@ -249,6 +251,7 @@ __device__ __forceinline__ void topk_init(TopkState &tk) {
   tk.worst_v = -FLT_MAX;
   tk.worst_id = INT_MAX;
   tk.worst_slot = 0;
+  draw_init(tk.dr);
 }
 
 __device__ __forceinline__ void topk_replace_worst(TopkState &tk, float v, int id) {
@@ -476,6 +479,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
           if (topk_before(x, col0 + i, tk.worst_v, tk.worst_id)) topk_replace_worst(tk, x, col0 + i);
         }
       }
+      // the draw at temperature T (scales v in place, so it runs after the top-k)
+      if (p.smp_part && nval > 0)
+        draw_chunk32(tk.dr, v, p.smp_inv_T, col0, nval, (uint32_t)row, (uint32_t)p.smp_stream, p.smp_seed);
     }
   }
 }
@@ -709,6 +715,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
         const int range = blockIdx.x / p.m_tiles;
         const int row = m * p.tile_rows + r;
         if (r < p.tile_rows && row < p.M) {
+          if (p.smp_part) draw_store(p.smp_part + 2 * ((size_t)range * p.M + row), tk.dr);
           // order the members (value descending, ties to the lower id) by rank
           float *pv = p.part_vals + ((size_t)range * p.M + row) * p.topk_k;
           int *pi = p.part_ids + ((size_t)range * p.M + row) * p.topk_k;

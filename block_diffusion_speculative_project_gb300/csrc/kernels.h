@@ -128,6 +128,13 @@ struct GemmParams {
   int slabs;         // 2: A and B maps carry a 64-column slab dimension and each stage
                      // loads two slabs per copy (plain 128-wide GEMMs with K % 64 == 0)
   int act;           // EPI_BF16: 1 = silu(acc) before rounding
+  // EPI_TOPK draw at temperature 1 / smp_inv_T (smp_part set): per (vocabulary range, row)
+  // the partial draw of Philox stream smp_stream, row = the LM-head row, two float4 per
+  // entry at smp_part[2 * (range * M + row)]
+  float4 *smp_part;
+  float smp_inv_T;
+  int smp_stream;
+  unsigned long long smp_seed;
 };
 
 struct GemmLaunch {
@@ -187,10 +194,17 @@ constexpr int kSampleMaxSlices = 64;
 int sample_slices(int rows, int V, int num_sms);
 // Draws ids[r] ~ softmax(logits[r] * inv_T) (Philox stream `stream`, row row0 + r) and
 // writes lse[r] (and logq[r] = log q(ids[r])); stream < 0: lse only (ids, logq unused).
-// part: rows * S float4 of scratch.
+// part: rows * S * 2 float4 of scratch.
 cudaError_t launch_sample(const float *logits, long long ld, int rows, int V, float inv_T,
                           unsigned long long seed, int stream, int row0, int S, float4 *part,
                           int *ids, float *lse, float *logq, cudaStream_t s);
+// Merge of partial draws (two float4 each) at entries r * row_stride + k * slice_stride.
+cudaError_t launch_draw_merge(const float4 *part, int rows, int S, long long row_stride,
+                              long long slice_stride, int *ids, float *lse, float *logq, cudaStream_t s);
+// Philox uniforms and Gumbel values of (seed, stream, row) for v < n (a check of the random
+// numbers every draw uses).
+cudaError_t launch_draw_gumbel(int n, unsigned long long seed, int stream, int row, float *u, float *g,
+                               cudaStream_t s);
 // Rejection-sampling verify of nb blocks; part: nb * S float4, nrej: nb ints of scratch.
 cudaError_t launch_verify(const float *draft_logits, const float *draft_lse, const int *cand,
                           const float *target_logits, const float *target_lse, int nb, int B, int V,

@@ -17,180 +17,139 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sampling.cuh"
 
 namespace df {
 
 namespace {
 
-constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
-constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
-constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
-constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
-
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    if (r) {
-      k0 += kPhiloxW0;
-      k1 += kPhiloxW1;
-    }
-    const uint32_t hi0 = __umulhi(kPhiloxM0, c.x), lo0 = kPhiloxM0 * c.x;
-    const uint32_t hi1 = __umulhi(kPhiloxM1, c.z), lo1 = kPhiloxM1 * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-  }
-  return c;
-}
-
-__device__ __forceinline__ float philox_u(uint32_t w) {
-  return (static_cast<float>(w >> 9) + 0.5f) * 1.1920928955078125e-07f;  // 2^-23
-}
-
-// Gumbel value of one uniform; logf (not the fast approximation): the largest scores come
-// from u close to 1, where log u is tiny and needs full relative precision.
-__device__ __forceinline__ float gumbel_of(float u) { return -logf(-logf(u)); }
-
-// Uniform of element v of (stream, row).
-__device__ __forceinline__ float philox_uniform(unsigned long long seed, int stream, int row, int v) {
-  const uint4 w = philox4x32_10(make_uint4((uint32_t)(v >> 2), (uint32_t)row, (uint32_t)stream, 0u),
-                                (uint32_t)seed, (uint32_t)(seed >> 32));
-  const int q = v & 3;
-  return philox_u(q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w);
-}
-
-struct Best {
-  float v;
-  int id;
-};
-
-__device__ __forceinline__ void best_take(Best &b, float v, int id) {
-  if (v > b.v || (v == b.v && id < b.id)) {
-    b.v = v;
-    b.id = id;
-  }
-}
-
-// Online log-sum-exp state: sum of exp(x - m).
-__device__ __forceinline__ void lse_add(float &m, float &s, float x) {
-  if (x == -INFINITY) return;  // probability 0
-  if (x > m) {
-    s = s * __expf(m - x) + 1.f;
-    m = x;
-  } else {
-    s += __expf(x - m);
-  }
-}
-
-__device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2) {
-  if (m2 == -INFINITY) return;
-  if (m2 > m) {
-    s = s * __expf(m - m2) + s2;
-    m = m2;
-  } else {
-    s += s2 * __expf(m2 - m);
-  }
-}
-
-// CTA-wide reduction (256 threads) of (m, s, best); result valid in thread 0.
-__device__ __forceinline__ void cta_reduce(float &m, float &s, Best &b) {
-  __shared__ float rm[8], rs[8], rb[8];
+// CTA-wide merge (256 threads) of a draw state; the result is valid in thread 0.
+__device__ __forceinline__ void cta_reduce(DrawState &d) {
+  __shared__ float rm[8], rs[8], rb[8], rx[8];
   __shared__ int ri[8];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    const float b2 = __shfl_xor_sync(0xffffffffu, b.v, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, b.id, o);
-    lse_merge(m, s, m2, s2);
-    best_take(b, b2, i2);
+    DrawState e;
+    e.m = __shfl_xor_sync(0xffffffffu, d.m, o);
+    e.s = __shfl_xor_sync(0xffffffffu, d.s, o);
+    e.best = __shfl_xor_sync(0xffffffffu, d.best, o);
+    e.x = __shfl_xor_sync(0xffffffffu, d.x, o);
+    e.id = __shfl_xor_sync(0xffffffffu, d.id, o);
+    draw_merge(d, e);
   }
   const int w = threadIdx.x >> 5;
   if ((threadIdx.x & 31) == 0) {
-    rm[w] = m;
-    rs[w] = s;
-    rb[w] = b.v;
-    ri[w] = b.id;
+    rm[w] = d.m;
+    rs[w] = d.s;
+    rb[w] = d.best;
+    rx[w] = d.x;
+    ri[w] = d.id;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int k = 1; k < 8; ++k) {
-      lse_merge(m, s, rm[k], rs[k]);
-      best_take(b, rb[k], ri[k]);
+      DrawState e;
+      e.m = rm[k];
+      e.s = rs[k];
+      e.best = rb[k];
+      e.x = rx[k];
+      e.id = ri[k];
+      draw_merge(d, e);
     }
   }
 }
 
 }  // namespace
 
-// Partial statistics of row r, slice s: part[r * S + s] = {max, sum exp(x - max), best
-// Gumbel score, best id} over x = logits[r * ld + v] * inv_T, v in the slice. With
-// stream < 0 no Gumbel score is formed (best = -inf, id = INT_MAX).
+// Partial draw of row r, slice s (entry (r * S + s) of two float4, see draw_store) over
+// x = logits[r * ld + v] * inv_T, v in the slice; Philox row row0 + r of `stream`. With
+// stream < 0 only the log-sum-exp is formed (no Gumbel values). Each thread takes groups
+// of four consecutive elements (one Philox block), four groups per iteration so that four
+// 16-byte loads are in flight; vec: rows start 16-byte aligned and ld % 4 == 0.
 __global__ void __launch_bounds__(256) sample_partial_kernel(const float *logits, long long ld, int V,
                                                              int chunk, float inv_T,
                                                              unsigned long long seed, int stream,
-                                                             int row0, float4 *part) {
+                                                             int row0, int vec, float4 *part) {
   griddep_wait();
   griddep_launch();
   const int s = blockIdx.x, r = blockIdx.y, S = gridDim.x;
   const int lo = s * chunk;
   const int hi = min(V, lo + chunk);
   const float *x = logits + (long long)r * ld;
-  float m = -INFINITY, sum = 0.f;
-  Best b{-INFINITY, INT_MAX};
-  // groups of four consecutive elements share one Philox block (chunk is a multiple of 4)
-  for (int g = lo + 4 * threadIdx.x; g < hi; g += 4 * 256) {
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (stream >= 0)
-      w = philox4x32_10(make_uint4((uint32_t)(g >> 2), (uint32_t)(row0 + r), (uint32_t)stream, 0u),
-                        (uint32_t)seed, (uint32_t)(seed >> 32));
+  DrawState d;
+  draw_init(d);
+  auto load4 = [&](int g, float (&o)[4]) {
+    if (vec && g + 4 <= hi) {
+      const float4 f = *reinterpret_cast<const float4 *>(x + g);
+      o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) o[q] = (g + q < hi) ? x[g + q] : -INFINITY;
+    }
+  };
+  auto take4 = [&](int g, const float (&o)[4]) {
+    if (stream < 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (g + q < hi) lse_add(d.m, d.s, o[q] * inv_T);
+      return;
+    }
+    const uint4 w = philox4x32_10(make_uint4((uint32_t)(g >> 2), (uint32_t)(row0 + r), (uint32_t)stream, 0u),
+                                  (uint32_t)seed, (uint32_t)(seed >> 32));
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int v = g + q;
-      if (v < hi) {
-        const float xv = x[v] * inv_T;
-        lse_add(m, sum, xv);
-        if (stream >= 0) best_take(b, xv + gumbel_of(philox_u(ww[q])), v);
-      }
-    }
+    for (int q = 0; q < 4; ++q)
+      if (g + q < hi) draw_add(d, o[q] * inv_T, gumbel_fast(ww[q]), g + q);
+  };
+  constexpr int kStep = 4 * 256;
+  int g = lo + 4 * threadIdx.x;
+  for (; g + 3 * kStep < hi; g += 4 * kStep) {  // four 16-byte loads in flight
+    float a[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) load4(g + u * kStep, a[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) take4(g + u * kStep, a[u]);
   }
-  cta_reduce(m, sum, b);
-  if (threadIdx.x == 0) part[(long long)r * S + s] = make_float4(m, sum, b.v, __int_as_float(b.id));
+  for (; g < hi; g += kStep) {
+    float a0[4];
+    load4(g, a0);
+    take4(g, a0);
+  }
+  cta_reduce(d);
+  if (threadIdx.x == 0) draw_store(part + 2 * ((long long)r * S + s), d);
 }
 
-// One warp per row: combine the S slices. Writes lse[r] = max + log(sum) and, when ids is
-// set, ids[r] = the Gumbel argmax and logq[r] = logits[r][id] * inv_T - lse[r].
+// One warp per row r: merge the partial draws at entries r * row_stride + k * slice_stride,
+// k < S. Writes lse[r] and, when ids is set, ids[r] (-1 when every score is NaN) and
+// logq[r] = x[id] - lse[r].
 __global__ void __launch_bounds__(128) sample_merge_kernel(const float4 *part, int rows, int S,
-                                                           const float *logits, long long ld,
-                                                           float inv_T, int *ids, float *lse,
-                                                           float *logq) {
+                                                           long long row_stride, long long slice_stride,
+                                                           int *ids, float *lse, float *logq) {
   griddep_wait();
   griddep_launch();
   const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
-  float m = -INFINITY, s = 0.f;
-  Best b{-INFINITY, INT_MAX};
-  for (int k = lane; k < S; k += 32) {
-    const float4 p = part[(long long)r * S + k];
-    lse_merge(m, s, p.x, p.y);
-    best_take(b, p.z, __float_as_int(p.w));
-  }
+  DrawState d;
+  draw_init(d);
+  for (int k = lane; k < S; k += 32) draw_merge(d, draw_load(part + 2 * (r * row_stride + k * slice_stride)));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    const float b2 = __shfl_xor_sync(0xffffffffu, b.v, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, b.id, o);
-    lse_merge(m, s, m2, s2);
-    best_take(b, b2, i2);
+    DrawState e;
+    e.m = __shfl_xor_sync(0xffffffffu, d.m, o);
+    e.s = __shfl_xor_sync(0xffffffffu, d.s, o);
+    e.best = __shfl_xor_sync(0xffffffffu, d.best, o);
+    e.x = __shfl_xor_sync(0xffffffffu, d.x, o);
+    e.id = __shfl_xor_sync(0xffffffffu, d.id, o);
+    draw_merge(d, e);
   }
   if (lane == 0) {
-    const float l = m + logf(s);
+    const float l = d.m + logf(d.s);
     lse[r] = l;
-    if (ids) {  // no winner only when every score is NaN: id -1
-      const bool ok = b.id != INT_MAX;
-      ids[r] = ok ? b.id : -1;
-      logq[r] = ok ? logits[(long long)r * ld + b.id] * inv_T - l : -INFINITY;
+    if (ids) {
+      const bool ok = d.id != INT_MAX;
+      ids[r] = ok ? d.id : -1;
+      logq[r] = ok ? d.x - l : -INFINITY;
     }
   }
 }
@@ -249,7 +208,7 @@ __global__ void __launch_bounds__(256) verify_partial_kernel(
     for (int q = 0; q < 4; ++q) {
       const int v = g + q;
       if (v < hi) {
-        const float gv = gumbel_of(philox_u(ww[q]));
+        const float gv = gumbel_fast(ww[q]);
         const float lp = zp[v] * inv_T - lzp;
         best_take(f, lp + gv, v);
         if (!all) {
@@ -288,28 +247,60 @@ __global__ void __launch_bounds__(256) verify_partial_kernel(
   }
 }
 
-// One thread per sequence: tau = n + 1; token = the residual draw when some r(v) > 0 (and
+// One warp per sequence: tau = n + 1; token = the residual draw when some r(v) > 0 (and
 // n < B-1), else the fallback draw.
-__global__ void verify_merge_kernel(const float4 *part, const int *nrej, int nb, int B, int S,
-                                    int *tau, int *token) {
+__global__ void __launch_bounds__(128) verify_merge_kernel(const float4 *part, const int *nrej, int nb,
+                                                           int B, int S, int *tau, int *token) {
   griddep_wait();
   griddep_launch();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (i >= nb) return;
   Best b{-INFINITY, INT_MAX}, f{-INFINITY, INT_MAX};
-  for (int k = 0; k < S; ++k) {
+  for (int k = lane; k < S; k += 32) {
     const float4 p = part[(long long)i * S + k];
     best_take(b, p.x, __float_as_int(p.y));
     best_take(f, p.z, __float_as_int(p.w));
   }
-  const int n = nrej[i];
-  tau[i] = n + 1;
-  const int t = (n < B - 1 && b.id != INT_MAX) ? b.id : f.id;
-  token[i] = t != INT_MAX ? t : -1;  // -1 only when every score is NaN
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float b2 = __shfl_xor_sync(0xffffffffu, b.v, o);
+    const int bi2 = __shfl_xor_sync(0xffffffffu, b.id, o);
+    const float f2 = __shfl_xor_sync(0xffffffffu, f.v, o);
+    const int fi2 = __shfl_xor_sync(0xffffffffu, f.id, o);
+    best_take(b, b2, bi2);
+    best_take(f, f2, fi2);
+  }
+  if (lane == 0) {
+    const int n = nrej[i];
+    tau[i] = n + 1;
+    const int t = (n < B - 1 && b.id != INT_MAX) ? b.id : f.id;
+    token[i] = t != INT_MAX ? t : -1;  // -1 only when every score is NaN
+  }
+}
+
+// u[v] and g[v] = Gumbel value of element v < n of (seed, stream, row).
+__global__ void __launch_bounds__(256) draw_gumbel_kernel(int n, unsigned long long seed, int stream,
+                                                          int row, float *u, float *g) {
+  const int v = blockIdx.x * 256 + threadIdx.x;
+  if (v >= n) return;
+  const uint4 w = philox4x32_10(make_uint4((uint32_t)(v >> 2), (uint32_t)row, (uint32_t)stream, 0u),
+                                (uint32_t)seed, (uint32_t)(seed >> 32));
+  const int q = v & 3;
+  const uint32_t word = q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w;
+  u[v] = philox_u(word);
+  g[v] = gumbel_fast(word);
+}
+
+cudaError_t launch_draw_gumbel(int n, unsigned long long seed, int stream, int row, float *u, float *g,
+                               cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  draw_gumbel_kernel<<<(n + 255) / 256, 256, 0, s>>>(n, seed, stream, row, u, g);
+  return cudaGetLastError();
 }
 
 int sample_slices(int rows, int V, int num_sms) {
-  int S = (4 * num_sms + rows - 1) / max(rows, 1);
+  int S = (8 * num_sms) / max(rows, 1);  // one resident wave of about 8 CTAs per SM
   const int max_s = (V + 1023) / 1024;  // at least 1024 elements per slice
   S = max(1, min(S, min(max_s, kSampleMaxSlices)));
   return S;
@@ -321,11 +312,18 @@ cudaError_t launch_sample(const float *logits, long long ld, int rows, int V, fl
                           unsigned long long seed, int stream, int row0, int S, float4 *part,
                           int *ids, float *lse, float *logq, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
+  const int vec = (ld % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
   cudaError_t e = launch_pdl(sample_partial_kernel, dim3(S, rows), dim3(256), 0, s, logits, ld, V,
-                             slice_chunk(V, S), inv_T, seed, stream, row0, part);
+                             slice_chunk(V, S), inv_T, seed, stream, row0, vec, part);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(sample_merge_kernel, dim3((rows + 3) / 4), dim3(128), 0, s, (const float4 *)part, rows,
-                 S, logits, ld, inv_T, ids, lse, logq);
+  return launch_draw_merge(part, rows, S, S, 1, ids, lse, logq, s);
+}
+
+cudaError_t launch_draw_merge(const float4 *part, int rows, int S, long long row_stride,
+                              long long slice_stride, int *ids, float *lse, float *logq, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(sample_merge_kernel, dim3((rows + 3) / 4), dim3(128), 0, s, part, rows, S,
+                             row_stride, slice_stride, ids, lse, logq);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -339,7 +337,7 @@ cudaError_t launch_verify(const float *draft_logits, const float *draft_lse, con
                              draft_lse, cand, target_logits, target_lse, B, V, slice_chunk(V, S),
                              inv_T, seed, part, nrej);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(verify_merge_kernel, dim3((nb + 127) / 128), dim3(128), 0, s, (const float4 *)part,
+  e = launch_pdl(verify_merge_kernel, dim3((nb + 3) / 4), dim3(128), 0, s, (const float4 *)part,
                  (const int *)nrej, nb, B, S, tau, token);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

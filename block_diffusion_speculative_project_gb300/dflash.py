@@ -78,6 +78,9 @@ def _load():
         "dflash_topk": (i, [p, i, i, p, i, p, p, p, sz, p]),
         "dflash_accept": (i, [p, i, p, p, p, p, p]),
         "dflash_sample": (i, [p, i, p, ctypes.c_float, ctypes.c_uint64, i, p, p, p, p, sz, p]),
+        "dflash_lm_head_sample": (i, [p, i, p, ctypes.c_float, ctypes.c_uint64, p, p, p, p, i, p, p, p,
+                                      sz, p]),
+        "dflash_draw_gumbel": (i, [i, ctypes.c_uint64, i, i, p, p, p]),
         "dflash_verify_sample": (i, [p, i, p, p, p, p, ctypes.c_float, ctypes.c_uint64, p, p, p, sz,
                                      p]),
         "dflash2_conv": (i, [p, i, i, i, p, p, sz, p]),
@@ -94,7 +97,8 @@ LIB = _load()
 EXPORTED = ("dflash_create", "dflash_destroy", "dflash_set_weights", "dflash_workspace_size",
             "dflash_status", "dflash_last_error", "dflash_ctx_project", "dflash_ctx_project_film",
             "dflash_draft_block",
-            "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_attention", "dflash_topk", "dflash_accept", "dflash_sample", "dflash_verify_sample", "dflash2_conv",
+            "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_attention", "dflash_topk", "dflash_accept", "dflash_sample", "dflash_verify_sample",
+            "dflash_lm_head_sample", "dflash_draw_gumbel", "dflash2_conv",
             "dflash2_select")
 
 
@@ -199,6 +203,19 @@ def dflash_sample(h, rows, logits, temperature, seed, row0, out_ids, out_lse, ou
     _check(LIB.dflash_sample(h, rows, _ptr(logits), float(temperature), int(seed), int(row0),
                              _ptr(out_ids), _ptr(out_lse), _ptr(out_logq), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dflash_lm_head_sample(h, nb, hidden, temperature, seed, out_cand, out_lse, out_logq, out_logits,
+                          k, out_ids, out_vals, ws, stream=None) -> None:
+    _check(LIB.dflash_lm_head_sample(h, nb, _ptr(hidden), float(temperature), int(seed),
+                                     _ptr(out_cand), _ptr(out_lse), _ptr(out_logq), _ptr(out_logits),
+                                     int(k), _ptr(out_ids), _ptr(out_vals), _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dflash_draw_gumbel(n, seed, stream_id, row, out_u, out_g, stream=None) -> None:
+    _check(LIB.dflash_draw_gumbel(int(n), int(seed), int(stream_id), int(row), _ptr(out_u), _ptr(out_g),
+                                  _stream(stream)))
 
 
 def dflash_verify_sample(h, nb, draft_logits, draft_lse, cand, target_logits, temperature, seed,

@@ -97,6 +97,11 @@ class Drafter:
         _d.dflash_sample(self.h, rows, logits, temperature, seed, row0, out_ids, out_lse, out_logq,
                          self.ws, stream)
 
+    def lm_head_sample(self, nb, hidden, temperature, seed, out_cand, out_lse, out_logq=None,
+                       out_logits=None, k=0, out_ids=None, out_vals=None, stream=None):
+        _d.dflash_lm_head_sample(self.h, nb, hidden, temperature, seed, out_cand, out_lse, out_logq,
+                                 out_logits, k, out_ids, out_vals, self.ws, stream)
+
     def verify_sample(self, nb, draft_logits, draft_lse, cand, target_logits, temperature, seed,
                       out_tau, out_token, stream=None):
         _d.dflash_verify_sample(self.h, nb, draft_logits, draft_lse, cand, target_logits, temperature,

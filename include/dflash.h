@@ -295,6 +295,27 @@ DFLASH_API int dflash_sample(dflash_handle_t h, int rows, const float *logits, f
                   uint64_t seed, int row0, int32_t *out_ids, float *out_lse, float *out_logq,
                   void *ws, size_t ws_bytes, dflash_stream_t stream);
 
+/* The LM head with the draft draw fused into its epilogue: the logits of offsets 1..B-1
+ * ([DFlash] dflash_cycle, [1:]) are drawn from as dflash_sample draws from them, while
+ * they are computed, so they need not be written or read again.
+ *   hidden     bf16 [nb, B, D] (out_hidden of dflash_draft_block)
+ *   out_cand   int32 [nb, B-1]: c_t ~ softmax(U_t / T), Philox row i*(B-1) + t-1, stream 0
+ *   out_lse    f32 [nb, B-1]: log sum_v exp(U_t(v) / T)
+ *   out_logq   f32 [nb, B-1] or NULL: log q_t(c_t)
+ *   out_logits f32 [nb, B-1, V] or NULL: U_t (dflash_verify_sample needs them)
+ *   k, out_ids, out_vals: the top-k of dflash_lm_head_topk, or out_ids = NULL for none. */
+DFLASH_API int dflash_lm_head_sample(dflash_handle_t h, int nb, const void *hidden, float temperature,
+                  uint64_t seed, int32_t *out_cand, float *out_lse, float *out_logq,
+                  float *out_logits, int k, int32_t *out_ids, float *out_vals, void *ws,
+                  size_t ws_bytes, dflash_stream_t stream);
+
+/* The random numbers every draw uses, for checking them: for v < n, out_u[v] = the Philox
+ * uniform of element v of (seed, stream_id, row) (word v % 4 of the block at counter
+ * (v / 4, row, stream_id, 0)) and out_g[v] = its Gumbel value -log(-log u) as the draws
+ * compute it (absolute error about 1e-6). Needs no handle. */
+DFLASH_API int dflash_draw_gumbel(int n, uint64_t seed, int stream_id, int row, float *out_u,
+                  float *out_g, dflash_stream_t stream);
+
 /* Lossless rejection-sampling verify of nb drafted blocks at temperature T > 0 ([DFlash2]
  * Results: lossless rejection sampling; [DFlash] 四、推理流程 dflash_cycle step ④: the
  * rejected position is re-drawn from the target, the last step yields the bonus token).

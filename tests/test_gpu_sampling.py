@@ -240,3 +240,63 @@ def test_sampling_full_step_medium():
     assert compared >= nb // 2
     print(f"end-to-end sampling: {decided.sum()}/{decided.size} draws and {compared}/{nb} "
           f"verifies compared exactly; tau {list(gt)}")
+
+
+def test_philox_uniforms_bit_exact_and_gumbel_error():
+    """The kernels' random numbers against the oracle's Philox4x32-10: uniforms bit-exact
+    (both are ((w >> 9) + 1/2) / 2^23, exact in fp32) over 4M elements of three streams,
+    Gumbel values within 5e-6 of the fp64 -log(-log u)."""
+    from block_diffusion_speculative_project_gb300 import dflash
+    n = 1 << 22
+    for seed, stream, row in ((0x0123_4567_89AB_CDEF, 0, 3), (7, 1, 0), (2 ** 63 + 5, 2, 65535)):
+        u = torch.empty(n, dtype=torch.float32, device="cuda")
+        g = torch.empty(n, dtype=torch.float32, device="cuda")
+        dflash.dflash_draw_gumbel(n, seed, stream, row, u, g)
+        torch.cuda.synchronize()
+        ou = orc.uniforms(seed, stream, row, n)
+        assert np.array_equal(u.cpu().numpy().astype(np.float64), ou), f"uniforms stream {stream}"
+        err = np.abs(g.cpu().numpy().astype(np.float64) - orc.gumbel(ou))
+        assert err.max() < 5e-6, f"Gumbel error {err.max():.2e} stream {stream}"
+        print(f"stream {stream}: Gumbel max abs error {err.max():.2e}")
+
+
+@pytest.mark.parametrize("V,nb,B,T", [(151936, 2, 16, 1.0), (5003, 9, 16, 0.6), (4097, 5, 8, 1.0)])
+def test_lm_head_fused_draw(V, nb, B, T):
+    """dflash_lm_head_sample on seeded bf16 hidden rows against the oracle's LM head and
+    draw: the fp32-accumulated logits are within 1e-3 of the fp64 ones, so the draws
+    compare exactly where the oracle's margin exceeds 2e-3; lse within 1e-3."""
+    from block_diffusion_speculative_project_gb300 import drafter
+    w = di.TINY.with_(V=V, B=B, nb=nb)
+    bits = di.make_weights(w)
+    dev = {k: drafter.to_device_bf16(v) for k, v in bits.items()}
+    dr = drafter.Drafter(w, dev, nb, 80, 8)
+    hid = di.normal_bf16(f"hid_draw_{V}", (nb, B, w.D), 1.0)
+    seed = 99 + V
+    cand = i32(np.zeros((nb, B - 1)))
+    lse = t32(np.zeros((nb, B - 1)))
+    logq = t32(np.zeros((nb, B - 1)))
+    logits = torch.empty(nb, B - 1, V, dtype=torch.float32, device="cuda")
+    ids = i32(np.zeros((nb, B - 1, w.k_top)))
+    vals = t32(np.zeros((nb, B - 1, w.k_top)))
+    dr.lm_head_sample(nb, drafter.to_device_bf16(hid), T, seed, cand, lse, logq, logits, w.k_top, ids, vals)
+    assert dr.status() == 0
+    W = orc.widen_all({"W_lm": bits["W_lm"]})
+    ol = orc.lm_logits(W, orc.widen(hid))
+    assert np.abs(logits.cpu().numpy() - ol).max() < 1e-3
+    oc, olse, ologq, om = orc.sample_candidates(ol, T, seed)
+    gc = cand.cpu().numpy()
+    dec = om > 2e-3
+    assert np.array_equal(gc[dec], oc[dec])
+    assert dec.mean() > 0.9
+    np.testing.assert_allclose(lse.cpu().numpy(), olse, atol=1e-3, rtol=1e-5)
+    same = gc == oc
+    np.testing.assert_allclose(logq.cpu().numpy()[same], ologq[same], atol=2e-3)
+    # the top-k of the same launch is unchanged by the draw
+    oi, _ = orc.topk(ol, w.k_top)
+    assert (ids.cpu().numpy()[..., 0] == oi[..., 0]).mean() > 0.95
+    # the draw from the written logits (dflash_sample) is the same draw
+    c2 = i32(np.zeros((nb, B - 1)))
+    l2 = t32(np.zeros((nb, B - 1)))
+    dr.sample(nb * (B - 1), logits, T, seed, c2, l2)
+    assert np.array_equal(c2.cpu().numpy(), gc)
+    np.testing.assert_allclose(l2.cpu().numpy(), lse.cpu().numpy(), rtol=1e-5, atol=1e-5)
