@@ -88,18 +88,37 @@ __global__ void __launch_bounds__(256) sample_partial_kernel(const float *logits
     }
   };
   auto take4 = [&](int g, const float (&o)[4]) {
-    if (stream < 0) {
+    float x[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (g + q < hi) lse_add(d.m, d.s, o[q] * inv_T);
-      return;
+    for (int q = 0; q < 4; ++q) x[q] = (g + q < hi) ? o[q] * inv_T : -INFINITY;
+    const float m4 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    if (m4 == -INFINITY) return;
+    // log-sum-exp: one rescale per group when its max is a new maximum
+    if (m4 > d.m) {
+      d.s = (d.m == -INFINITY) ? 0.f : d.s * __expf(d.m - m4);
+      d.m = m4;
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d.s += __expf(x[q] - d.m);
+    if (stream < 0) return;
+    // the draw: nothing in the group can reach the best score -> no random numbers needed
+    const float d_min = d.best - m4;
+    if (d_min > kGumbelMax) return;
     const uint4 w = philox4x32_10(make_uint4((uint32_t)(g >> 2), (uint32_t)(row0 + r), (uint32_t)stream, 0u),
                                   (uint32_t)seed, (uint32_t)(seed >> 32));
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    const float tthr = draw_t_threshold(d_min);
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (g + q < hi) draw_add(d, o[q] * inv_T, gumbel_fast(ww[q]), g + q);
+    for (int q = 0; q < 4; ++q) {
+      if (x[q] != -INFINITY && philox_t(ww[q]) <= tthr) {
+        const float sc = x[q] + gumbel_fast(ww[q]);
+        if (sc > d.best || (sc == d.best && g + q < d.id)) {
+          d.best = sc;
+          d.id = g + q;
+          d.x = x[q];
+        }
+      }
+    }
   };
   constexpr int kStep = 4 * 256;
   int g = lo + 4 * threadIdx.x;
@@ -300,7 +319,14 @@ cudaError_t launch_draw_gumbel(int n, unsigned long long seed, int stream, int r
 }
 
 int sample_slices(int rows, int V, int num_sms) {
-  int S = (8 * num_sms) / max(rows, 1);  // one resident wave of about 8 CTAs per SM
+  // one resident wave of the slice kernel: SMs x CTAs per SM (from its register use)
+  static int per_sm = [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sample_partial_kernel, 256, 0) != cudaSuccess || n < 1)
+      n = 4;
+    return n;
+  }();
+  int S = (per_sm * num_sms) / max(rows, 1);
   const int max_s = (V + 1023) / 1024;  // at least 1024 elements per slice
   S = max(1, min(S, min(max_s, kSampleMaxSlices)));
   return S;

@@ -71,6 +71,21 @@ __device__ __forceinline__ float gumbel_fast(uint32_t w) {
   return -__logf(E);
 }
 
+// Largest Gumbel value gumbel_fast returns (u = 1 - 2^-24 gives 16.636), rounded up.
+constexpr float kGumbelMax = 16.7f;
+
+// Draw pruning. An element of logit x can beat the running best score `best` only if its
+// Gumbel value reaches d = best - x, i.e. E = -log u <= exp(-d). Since -log u >= t = 1 - u,
+// t > exp(-d) (1 + 1e-5) rules it out; the factor covers the fast exponential (relative
+// error ~5e-7) and gumbel_fast's own error (~2e-6), so a pruned element's computed score is
+// strictly below best. t = (2^23 - k - 1/2) 2^-23 is exact for k = w >> 9.
+__device__ __forceinline__ float draw_t_threshold(float d_min) {
+  return d_min <= 0.f ? 2.f : __expf(-d_min) * 1.00001f;
+}
+__device__ __forceinline__ float philox_t(uint32_t w) {
+  return (static_cast<float>((1u << 23) - (w >> 9)) - 0.5f) * 1.1920928955078125e-07f;
+}
+
 // Uniform of element v of (stream, row).
 __device__ __forceinline__ float philox_uniform(unsigned long long seed, int stream, int row, int v) {
   const uint4 w = philox4x32_10(make_uint4((uint32_t)(v >> 2), (uint32_t)row, (uint32_t)stream, 0u),
@@ -191,16 +206,21 @@ __device__ __forceinline__ void draw_chunk32(DrawState &d, float (&v)[32], float
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int c = 16 * h + i;
-      const bool ok = c < nval;
-      v[c] = ok ? v[c] * inv_T : -INFINITY;
-      sc[i] = ok ? v[c] + gumbel_fast(w[i]) : -INFINITY;
-      sx[i] = v[c];
-      ix[i] = i;
+      v[c] = c < nval ? v[c] * inv_T : -INFINITY;
     }
     float mx = v[16 * h];
 #pragma unroll
     for (int i = 1; i < 16; ++i) mx = fmaxf(mx, v[16 * h + i]);
     if (mx == -INFINITY) continue;  // nothing valid in this half
+    const float tthr = draw_t_threshold(d.best - mx);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = 16 * h + i;
+      sc[i] = -INFINITY;
+      if (v[c] != -INFINITY && philox_t(w[i]) <= tthr) sc[i] = v[c] + gumbel_fast(w[i]);
+      sx[i] = v[c];
+      ix[i] = i;
+    }
     float e[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) e[i] = __expf(v[16 * h + i] - mx);
