@@ -51,11 +51,14 @@ struct TileCfg {
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = (200 * 1024 / STAGE) > 8 ? 8 : (200 * 1024 / STAGE);
   static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;  // power of two >= 2*BN
-  static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE + 256;
   // Cluster split-K reuses the pipeline smem: the staged partial tile (BM rows of
-  // RED_STRIDE floats) followed by the reduced row slice (at most BM / 2 rows).
+  // RED_STRIDE floats) followed by the reduced row slice (at most BM / 2 rows). The
+  // pipeline region is the larger of the stage ring and that; barriers follow it.
   static constexpr int RED_STRIDE = BN + 4;
-  static constexpr bool RED_FITS = size_t(BM + BM / 2) * RED_STRIDE * 4 <= size_t(STAGES) * STAGE;
+  static constexpr size_t RED_BYTES = size_t(BM + BM / 2) * RED_STRIDE * 4;
+  static constexpr size_t PIPE = size_t(STAGES) * STAGE > RED_BYTES ? size_t(STAGES) * STAGE : RED_BYTES;
+  static constexpr size_t SMEM = 1024 + PIPE + 256;
+  static constexpr bool RED_FITS = RED_BYTES <= PIPE;
 };
 
 // Top-k epilogue: a per-thread stash of one 32-value chunk (stride 33 floats, so the
@@ -497,13 +500,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + C::STAGES * C::A_BYTES;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::PIPE);
   uint64_t *empty = full + C::STAGES;
   uint64_t *acc_full = empty + C::STAGES;
   uint64_t *acc_empty = acc_full + 2;
   uint64_t *mma_done = acc_empty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
-  float *stash_base = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE + 256);
+  float *stash_base = reinterpret_cast<float *>(smem + C::PIPE + 256);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
