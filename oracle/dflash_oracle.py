@@ -48,6 +48,11 @@ Readings where the pages are silent or disagree (each is listed in the design doc):
     u_j < p_j(c_{j+1}) / q_{j+1}(c_{j+1}), p_j = softmax(Z_j / T) of the target row j;
     the first rejection n emits a draw from max(0, p_n - q_{n+1}) (renormalised), or
     from p_n when that is zero everywhere; all accepted emits a draw from p_{B-1};
+  * sampling walk (DFlash 2): step t draws among the k candidates of offset t from
+    softmax_c(S_t(a_{t-1}, b_c) / T); the walk's draft distribution is that softmax on the
+    candidates and 0 elsewhere, and the verify uses it in place of softmax(U_t / T);
+  * Recall@k at offset t: the target token is among the k candidates, counted over the
+    blocks whose offsets before t all held their target token among theirs;
   * random numbers: Philox4x32-10 keyed by the 64-bit seed, counter (v // 4, row,
     stream, 0), output word v % 4; u = ((x >> 9) + 1/2) / 2^23 (exact in fp32, so both
     sides start from the same u); Gumbel g = -log(-log u).
@@ -397,6 +402,7 @@ _M32 = np.uint64(0xFFFFFFFF)
 STREAM_DRAFT = 0     # candidate draws, row = sequence * (B-1) + offset - 1
 STREAM_ACCEPT = 1    # acceptance uniforms, row = sequence, index = step n
 STREAM_EMIT = 2      # residual / bonus draw, row = sequence
+STREAM_WALK = 3      # selector walk draws, row = sequence * (B-1) + offset - 1, index = slot
 
 
 def philox4x32(ctr, key, rounds: int = 10):
@@ -520,6 +526,106 @@ def verify_sample(draft_logits: np.ndarray, cand: np.ndarray, target_logits: np.
     if return_detail:
         return tau, token, acc_margin, emit_margin
     return tau, token
+
+
+def selector_scores(cfg, W: dict, cand_ids, cand_vals, hidden, i: int, t: int, a: int):
+    """S_t(a, b_c) for the k candidates c of offset t of sequence i ([DFlash2] 洞察一):
+    U_t(b) + sum_d A(a)_d G_t,d B(b)_d, A = W_A E[a], B = W_B E[b], G = sigmoid(W_G z_t)."""
+    G = sigmoid(W["W_G"] @ hidden[i, t])
+    Aa = W["W_A"] @ W["E"][a]
+    k = cand_ids.shape[-1]
+    return np.array([cand_vals[i, t - 1, c] + np.sum(Aa * G * (W["W_B"] @ W["E"][int(cand_ids[i, t - 1, c])]))
+                     for c in range(k)])
+
+
+def select_walk_sample(cfg, W: dict, cand_ids, cand_vals, hidden, anchor, T: float, seed: int):
+    """DFlash 2 sampling walk ([DFlash2] 洞察一: sampling draws from the same score
+    distribution the greedy walk maximises). From a_0 = anchor, step t draws slot
+    c_t = argmax_c S_t(a_{t-1}, b_c)/T + g_c (Gumbel, stream STREAM_WALK, row
+    i*(B-1) + t-1, index c; ties to the lower token id) and a_t = b_{c_t}.
+    Returns path [nb, B-1], walk_logq [nb, B-1, k] = log softmax_c(S_t(a_{t-1}, b_c)/T) on
+    the walked prefix, and the Gumbel margins."""
+    nb, bm1, k = cand_ids.shape
+    path = np.zeros((nb, bm1), np.int32)
+    logq = np.zeros((nb, bm1, k))
+    margin = np.zeros((nb, bm1))
+    for i in range(nb):
+        a = int(anchor[i])
+        for t in range(1, bm1 + 1):
+            x = selector_scores(cfg, W, cand_ids, cand_vals, hidden, i, t, a) / T
+            sc = x + gumbel(uniforms(seed, STREAM_WALK, i * bm1 + t - 1, k))
+            ids = cand_ids[i, t - 1].astype(np.int64)
+            order = np.lexsort((ids, -sc))          # best score first, ties to the lower id
+            c = int(order[0])
+            margin[i, t - 1] = sc[order[0]] - sc[order[1]] if k > 1 else np.inf
+            logq[i, t - 1] = x - logsumexp(x)
+            path[i, t - 1] = ids[c]
+            a = int(ids[c])
+    return path, logq, margin
+
+
+def verify_sample_walk(cand_ids, walk_logq, path, target_logits, T: float, seed: int,
+                       return_detail: bool = False):
+    """verify_sample with the sampling walk's draft distribution: q_{t}(v) =
+    exp(walk_logq[t-1, c]) for v = cand_ids[t-1, c], 0 for every other token. The
+    acceptance test, the residual max(0, p - q), the fallback and the bonus draw, their
+    streams and ties are those of verify_sample."""
+    nb, bm1, k = cand_ids.shape
+    V = target_logits.shape[-1]
+    tau = np.zeros(nb, np.int32)
+    token = np.zeros(nb, np.int32)
+    acc_margin = np.full((nb, bm1), np.inf)
+    emit_margin = np.zeros(nb)
+    for i in range(nb):
+        u = uniforms(seed, STREAM_ACCEPT, i, bm1)
+        n = 0
+        while n < bm1:
+            c = int(path[i, n])
+            zp = target_logits[i, n] / T
+            slot = int(np.nonzero(cand_ids[i, n] == c)[0][0])
+            log_ratio = (zp[c] - logsumexp(zp)) - walk_logq[i, n, slot]
+            acc_margin[i, n] = abs(math.log(u[n]) - log_ratio)
+            if math.log(u[n]) < log_ratio:
+                n += 1
+            else:
+                break
+        g = gumbel(uniforms(seed, STREAM_EMIT, i, V))
+        if n < bm1:
+            zp = target_logits[i, n] / T
+            p = np.exp(zp - logsumexp(zp))
+            q = np.zeros(V)
+            q[cand_ids[i, n].astype(np.int64)] = np.exp(walk_logq[i, n])
+            r = p - q
+            if (r > 0).any():
+                with np.errstate(divide="ignore"):
+                    score = np.where(r > 0, np.log(np.where(r > 0, r, 1.0)), -np.inf) + g
+            else:
+                score = zp + g
+        else:
+            score = target_logits[i, bm1] / T + g
+        token[i], emit_margin[i] = gumbel_argmax(score)
+        tau[i] = n + 1
+    if return_detail:
+        return tau, token, acc_margin, emit_margin
+    return tau, token
+
+
+def recall_at_k(cand_ids, target):
+    """Recall@k instrumentation ([DFlash2] Why DFlash 2, the Recall@1 / Recall@16 table):
+    at offset t the target token T[t-1] is among the k candidates of offset t, counted over
+    the blocks whose offsets 1..t-1 all held their target token. Returns (hits [B-1],
+    eligible [B-1]) summed over the nb blocks."""
+    nb, bm1, k = cand_ids.shape
+    hits = np.zeros(bm1, np.int64)
+    eligible = np.zeros(bm1, np.int64)
+    for i in range(nb):
+        for t in range(bm1):
+            eligible[t] += 1
+            if int(target[i, t]) in set(int(x) for x in cand_ids[i, t]):
+                hits[t] += 1
+            else:
+                break
+    return hits, eligible
 
 
 def draft_step(cfg, W: dict, hv, n_commit, ctx_len, cache: KVCache, block_ids, target,

@@ -649,6 +649,114 @@ def test_shape_pins_from_pages():
     assert abs(n / 1e6 - s["quoted_M"]) < s["abs_tol_M"]
 
 
+# ----------------------------------------------------------------------------- sampling walk
+
+def walk_case(seed=50, nb=2, B=5, k=4, D=8, V=40):
+    cfg = small_cfg(D=D, V=V, B=B, nb=nb, flags=di.FLAG_SELECT, sel_dim=8)
+    W = rand_weights(cfg, seed, std=0.5)
+    rng = np.random.default_rng(seed + 1)
+    cand = np.stack([np.stack([rng.choice(V, k, replace=False) for _ in range(B - 1)])
+                     for _ in range(nb)]).astype(np.int32)
+    vals = rng.standard_normal((nb, B - 1, k)) * 1.5
+    hid = rng.standard_normal((nb, B, D))
+    anchor = rng.integers(0, V, nb)
+    return cfg, W, cand, vals, hid, anchor
+
+
+def test_walk_without_pair_term_draws_from_candidate_softmax():
+    """W_A = 0 removes the pair term: S_t(a, b_c) = U_t(b_c) whatever a, so the walk's
+    log q is log softmax(U_t / T) on the candidates and its draws follow it."""
+    from scipy import stats
+    cfg, W, cand, vals, hid, anchor = walk_case()
+    W["W_A"] = np.zeros_like(W["W_A"])
+    T = 0.8
+    _, logq, _ = orc.select_walk_sample(cfg, W, cand, vals, hid, anchor, T, 3)
+    x = vals / T
+    want = x - np.log(np.exp(x).sum(-1, keepdims=True))
+    np.testing.assert_allclose(logq, want, rtol=1e-12, atol=1e-12)
+    n = 3000
+    first = [orc.select_walk_sample(cfg, W, cand[:1], vals[:1], hid[:1], anchor[:1], T, s)[0][0, 0]
+             for s in range(n)]
+    slots = [int(np.nonzero(cand[0, 0] == c)[0][0]) for c in first]
+    p = np.exp(want[0, 0])
+    assert stats.chisquare(np.bincount(slots, minlength=4), p * n).pvalue > 1e-4
+
+
+def test_walk_draws_of_different_offsets_are_independent():
+    """Each step has its own Philox row: with the pair term off and the same candidate
+    scores at offsets 1 and 2, the two draws are independent (chi-square on the joint
+    counts), not copies of each other."""
+    from scipy import stats
+    cfg, W, cand, vals, hid, anchor = walk_case(seed=54, nb=1, B=3, k=3)
+    W["W_A"] = np.zeros_like(W["W_A"])
+    vals[0, 1] = vals[0, 0] = np.array([0.3, 0.0, -0.2])
+    cand[0, 1] = cand[0, 0]
+    n = 3000
+    joint = np.zeros((3, 3))
+    for sd in range(n):
+        path, _, _ = orc.select_walk_sample(cfg, W, cand, vals, hid, anchor, 1.0, sd)
+        s1 = int(np.nonzero(cand[0, 0] == path[0, 0])[0][0])
+        s2 = int(np.nonzero(cand[0, 1] == path[0, 1])[0][0])
+        joint[s1, s2] += 1
+    assert stats.chi2_contingency(joint).pvalue > 1e-4
+    assert np.trace(joint) < 0.6 * n
+
+
+def test_walk_at_low_temperature_is_the_greedy_walk():
+    cfg, W, cand, vals, hid, anchor = walk_case(seed=51, nb=3)
+    greedy, margins = orc.select_path(cfg, W, cand, vals, hid, anchor, return_margins=True)
+    path, logq, _ = orc.select_walk_sample(cfg, W, cand, vals, hid, anchor, 1e-5, 9)
+    assert (margins > 1e-2).all()
+    assert np.array_equal(path, greedy)
+    np.testing.assert_allclose(np.exp(logq).sum(-1), 1.0, rtol=1e-12)
+
+
+def test_verify_walk_equals_dense_verify_with_minus_inf_logits():
+    """The walk's sparse q, written as dense logits (log q on the candidates, -inf
+    elsewhere), gives the dense verify the same distribution: identical tau and token."""
+    cfg, W, cand, vals, hid, anchor = walk_case(seed=52, nb=6, B=6, k=4, V=30)
+    path, logq, _ = orc.select_walk_sample(cfg, W, cand, vals, hid, anchor, 1.0, 4)
+    rng = np.random.default_rng(53)
+    Z = rng.standard_normal((6, 6, 30)) * 1.5
+    for i in range(6):  # make acceptance likely: the target favours the walked tokens
+        for t in range(5):
+            Z[i, t, path[i, t]] += 2.0
+    dense = np.full((6, 5, 30), -np.inf)
+    for i in range(6):
+        for t in range(5):
+            dense[i, t, cand[i, t]] = logq[i, t]
+    a = orc.verify_sample_walk(cand, logq, path, Z, 1.0, 11)
+    b = orc.verify_sample(dense, path, Z, 1.0, 11)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert len(np.unique(a[0])) > 1
+
+
+def test_verify_walk_is_lossless_monte_carlo():
+    from scipy import stats
+    p = np.array([0.4, 0.25, 0.2, 0.1, 0.05])
+    cand = np.array([[[3, 0, 2]]], np.int32)
+    q = np.array([0.5, 0.2, 0.3])
+    logq = np.log(q)[None, None]
+    Z = np.log(np.stack([p, p]))[None]
+    n = 6000
+    first = np.zeros(n, np.int64)
+    for s in range(n):
+        c = cand[0, 0, orc.gumbel_argmax(logq[0, 0] + orc.gumbel(orc.uniforms(s, 3, 0, 3)))[0]]
+        tau, tok = orc.verify_sample_walk(cand, logq, np.array([[c]], np.int32), Z, 1.0, s)
+        first[s] = c if tau[0] > 1 else tok[0]
+    assert stats.chisquare(np.bincount(first, minlength=5), p * n).pvalue > 1e-4
+
+
+def test_recall_at_k_hand_case():
+    cand = np.array([[[1, 2], [3, 4], [5, 6]],     # targets 2, 4, 9: hits at 1, 2; miss at 3
+                     [[1, 2], [3, 4], [5, 6]],     # targets 7, ...: miss at 1, stops
+                     [[7, 8], [9, 1], [2, 3]]],    # targets 8, 1, 3: all three hit
+                    np.int32)
+    target = np.array([[2, 4, 9], [7, 4, 5], [8, 1, 3]])
+    hits, eligible = orc.recall_at_k(cand, target)
+    assert list(hits) == [2, 2, 1] and list(eligible) == [3, 2, 2]
+
+
 # ----------------------------------------------------------------------------- whole step
 
 def test_tiny_step_runs_and_is_deterministic():
