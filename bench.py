@@ -67,9 +67,12 @@ def step_bytes_flops(w: di.Workload, ctx: np.ndarray, tp: np.ndarray):
     if w.flags & di.FLAG_FILM:
         flops += 2 * M * 5 * w.D * w.film_width
     if w.temperature > 0:
-        # draft logits written by the LM head and read by the draw; target logits read for
-        # their normaliser; two rows per sequence read again by the residual draw
-        io += 2 * w.nb * (w.B - 1) * w.V * 4 + w.nb * w.B * w.V * 4 + w.nb * 2 * w.V * 4
+        # draft logits written by the LM head and read by the draw (not with the DFlash 2
+        # walk); target logits read for their normaliser; one target row (and one draft
+        # row) per sequence read again by the residual draw
+        if not w.flags & di.FLAG_SELECT:
+            io += 2 * w.nb * (w.B - 1) * w.V * 4 + w.nb * w.V * 4
+        io += w.nb * w.B * w.V * 4 + w.nb * w.V * 4
     return wbytes + kv_bytes + io, flops, wbytes, kv_bytes
 
 
@@ -88,7 +91,9 @@ def kernels_per_step(w: di.Workload) -> int:
     n += 2                                # LM head GEMM + merge
     if w.flags & di.FLAG_SELECT:
         n += 5                            # gather, A|B GEMM, G GEMM, score table, walk
-    if w.temperature > 0:
+    if w.temperature > 0 and w.flags & di.FLAG_SELECT:
+        n += 4                            # verify of the sampling walk (target lse x2, walk x2)
+    elif w.temperature > 0:
         n += 2 + 4                        # draw (partial, merge); verify (target lse x2, walk x2)
     else:
         n += 1                            # accept
@@ -242,8 +247,11 @@ def run_gpu(args, rank, world):
     draft_c = torch.empty(w.nb, w.B - 1, dtype=torch.int32, device=dev)
     sampling = w.temperature > 0
     if sampling:  # the target model's verify logits stand resident in HBM (it runs on this GPU)
-        draft_logits = torch.empty(w.nb, w.B - 1, w.V, dtype=torch.float32, device=dev)
+        # the plain draw needs the draft logits; the DFlash 2 walk's draft distribution lives
+        # on the k candidates, so it needs none
+        draft_logits = None if select else torch.empty(w.nb, w.B - 1, w.V, dtype=torch.float32, device=dev)
         draft_lse = torch.empty(w.nb, w.B - 1, dtype=torch.float32, device=dev)
+        walk_logq = torch.empty(w.nb, w.B - 1, k, dtype=torch.float32, device=dev)
         tgt_logits = torch.from_numpy(di.target_logits(w, seed)).to(dev)
         sample_seed = 0x5EED_0000 + seed
     max_ctx = int(ctx.max())
@@ -265,6 +273,12 @@ def run_gpu(args, rank, world):
         dr.lm_head_topk(w.nb, hidden, k, tid, tv, draft_logits if sampling else None, stream=s)
         if lm_events:
             lm_events[1].record(s)
+        if sampling and select:  # DFlash 2 sampling walk, verified against its distribution
+            dr.select_sample(w.nb, k, tid, tv, hidden, block, w.temperature, sample_seed, path, walk_logq,
+                             stream=s)
+            dr.verify_sample_walk(w.nb, k, tid, walk_logq, path, tgt_logits, w.temperature, sample_seed,
+                                  tau, bonus, stream=s)
+            return
         if sampling:  # draw over the written logits, then the verify
             dr.sample(w.nb * (w.B - 1), draft_logits, w.temperature, sample_seed, draft_c, draft_lse,
                       stream=s)
@@ -372,8 +386,8 @@ def run_gpu(args, rank, world):
     hbm, tf_burst, tf_sus, src = load_peaks()
     total_bytes, flops, wbytes, kvbytes = step_bytes_flops(w, ctx, tp)
     lm_bytes = 2 * w.V * w.D + 2 * w.nb * (w.B - 1) * w.D + 8 * w.nb * (w.B - 1) * k
-    if w.temperature > 0:
-        lm_bytes += 4 * w.nb * (w.B - 1) * w.V  # the fp32 logits the verify reads
+    if w.temperature > 0 and not w.flags & di.FLAG_SELECT:
+        lm_bytes += 4 * w.nb * (w.B - 1) * w.V  # the fp32 logits the draw reads
     lm_avg = float(np.mean(lm_ms))
     achieved = lm_bytes / (lm_avg * 1e-3) / 1e9
     traffic = traffic_from_profile(os.path.join(ROOT, "block_diffusion_speculative_project_gb300",
@@ -456,7 +470,11 @@ def cpu_baseline(w: di.Workload, bits=None, budget_s: float = 15.0):
                            np.zeros((1, w.B), np.int32), relay_a=None if a is None else a[i:i + 1],
                            relay_b=None if fb is None else fb[i:i + 1],
                            relay_y=None if fy is None else fy[i:i + 1])
-        if w.temperature > 0:
+        if w.temperature > 0 and w.flags & di.FLAG_SELECT:
+            path, logq, _ = orc.select_walk_sample(w, W, o["ids"], o["vals"], o["hidden"], ids[i:i + 1, 0],
+                                                   w.temperature, i)
+            orc.verify_sample_walk(o["ids"], logq, path, Z[i:i + 1], w.temperature, i)
+        elif w.temperature > 0:
             cand, _, _, _ = orc.sample_candidates(o["logits"], w.temperature, i)
             orc.verify_sample(o["logits"], cand, Z[i:i + 1], w.temperature, i)
         t_used += time.perf_counter() - t0

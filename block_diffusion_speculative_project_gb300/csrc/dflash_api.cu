@@ -1011,10 +1011,13 @@ int dflash2_conv(dflash_handle_t h, int layer, int which, int nb, float *x, void
   return run_conv(h, w, layer, which, nb * c.B, x, stream);
 }
 
-int dflash2_select(dflash_handle_t h, int nb, int k, const int32_t *topk_ids, const float *topk_vals,
-                   const void *hidden, const int32_t *block_ids, int32_t *out_path, void *ws,
-                   size_t ws_bytes, dflash_stream_t stream) {
-  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+namespace {
+
+// The selector's scores for every (offset, previous candidate, candidate), then the greedy
+// walk (walk_logq == NULL) or the sampling walk at temperature T.
+int select_impl(dflash_handle_t h, int nb, int k, const int32_t *topk_ids, const float *topk_vals,
+                const void *hidden, const int32_t *block_ids, float temperature, uint64_t seed,
+                int32_t *out_path, float *walk_logq, void *ws, size_t ws_bytes, cudaStream_t s) {
   const auto &c = h->cfg;
   if (!(c.flags & DFLASH_FLAG_SELECT)) return fail(DFLASH_ERR_INVALID_ARG, "DFLASH_FLAG_SELECT is not set");
   if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
@@ -1024,7 +1027,6 @@ int dflash2_select(dflash_handle_t h, int nb, int k, const int32_t *topk_ids, co
     return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor");
   DF_TRY(check_ws(h, ws, ws_bytes));
   Ws w{static_cast<uint8_t *>(ws), h->ws};
-  cudaStream_t s = stream;
   const int per = 1 + (c.B - 1) * k;
   const int rows = nb * per;
   uint16_t *eg = w.at<uint16_t>(h->ws.sel_e);
@@ -1063,8 +1065,75 @@ int dflash2_select(dflash_handle_t h, int nb, int k, const int32_t *topk_ids, co
     p.ldo = c.sel_dim;
     DF_TRY(run_gemm(h, p, kBN, s));
   }
-  DF_CUDA(launch_select_walk(topk_ids, topk_vals, ab, gp, w.at<float>(h->ws.sel_t), nb, c.B, k, c.sel_dim,
-                             out_path, s));
+  float *table = w.at<float>(h->ws.sel_t);
+  if (!walk_logq) {
+    DF_CUDA(launch_select_walk(topk_ids, topk_vals, ab, gp, table, nb, c.B, k, c.sel_dim, out_path, s));
+  } else {
+    DF_CUDA(launch_select_table(topk_vals, ab, gp, table, nb, c.B, k, c.sel_dim, s));
+    DF_CUDA(launch_select_walk_sample(topk_ids, table, nb, c.B, k, 1.f / temperature, seed, out_path,
+                                      walk_logq, s));
+  }
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+int dflash2_select(dflash_handle_t h, int nb, int k, const int32_t *topk_ids, const float *topk_vals,
+                   const void *hidden, const int32_t *block_ids, int32_t *out_path, void *ws,
+                   size_t ws_bytes, dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  return select_impl(h, nb, k, topk_ids, topk_vals, hidden, block_ids, 0.f, 0, out_path, nullptr, ws,
+                     ws_bytes, stream);
+}
+
+int dflash2_select_sample(dflash_handle_t h, int nb, int k, const int32_t *topk_ids,
+                          const float *topk_vals, const void *hidden, const int32_t *block_ids,
+                          float temperature, uint64_t seed, int32_t *out_path, float *out_walk_logq,
+                          void *ws, size_t ws_bytes, dflash_stream_t stream) {
+  if (!h || !h->have_weights) return fail(DFLASH_ERR_INVALID_ARG, "handle without weights");
+  if (!(temperature > 0.f) || !std::isfinite(temperature))
+    return fail(DFLASH_ERR_INVALID_ARG, "temperature must be positive and finite");
+  if (!out_walk_logq && nb > 0) return fail(DFLASH_ERR_INVALID_ARG, "out_walk_logq must be non-NULL");
+  return select_impl(h, nb, k, topk_ids, topk_vals, hidden, block_ids, temperature, seed, out_path,
+                     out_walk_logq, ws, ws_bytes, stream);
+}
+
+int dflash_verify_sample_walk(dflash_handle_t h, int nb, int k, const int32_t *cand_ids,
+                              const float *walk_logq, const int32_t *path, const float *target_logits,
+                              float temperature, uint64_t seed, int32_t *out_tau, int32_t *out_token,
+                              void *ws, size_t ws_bytes, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+  const auto &c = h->cfg;
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (k < 1 || k > kTopkMax) return fail(DFLASH_ERR_INVALID_ARG, "k=%d outside [1, 16]", k);
+  if (!(temperature > 0.f) || !std::isfinite(temperature))
+    return fail(DFLASH_ERR_INVALID_ARG, "temperature must be positive and finite");
+  if (nb == 0) return DFLASH_OK;
+  if (!cand_ids || !walk_logq || !path || !target_logits || !out_tau || !out_token)
+    return fail(DFLASH_ERR_INVALID_ARG, "every verify argument must be non-NULL");
+  DF_TRY(check_ws(h, ws, ws_bytes));
+  Ws w{static_cast<uint8_t *>(ws), h->ws};
+  const float inv_T = 1.f / temperature;
+  const int rows = nb * c.B;
+  float *tlse = w.at<float>(h->ws.smp_lse);
+  DF_CUDA(launch_sample(target_logits, c.V, rows, c.V, inv_T, seed, -1, 0,
+                        sample_slices(rows, c.V, h->num_sms), w.at<float4>(h->ws.smp_part), nullptr,
+                        tlse, nullptr, stream));
+  DF_CUDA(launch_verify_walk(cand_ids, walk_logq, k, path, target_logits, tlse, nb, c.B, c.V, inv_T, seed,
+                             sample_slices(nb, c.V, h->num_sms), w.at<float4>(h->ws.ver_part),
+                             w.at<int>(h->ws.ver_nrej), out_tau, out_token, stream));
+  return DFLASH_OK;
+}
+
+int dflash_recall_at_k(dflash_handle_t h, int nb, int k, const int32_t *cand_ids, const int32_t *target,
+                       int32_t *hits, int32_t *eligible, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+  const auto &c = h->cfg;
+  if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
+  if (k < 1 || k > kTopkMax) return fail(DFLASH_ERR_INVALID_ARG, "k=%d outside [1, 16]", k);
+  if (nb == 0) return DFLASH_OK;
+  if (!cand_ids || !target || !hits || !eligible) return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor");
+  DF_CUDA(launch_recall_at_k(cand_ids, target, nb, c.B, k, hits, eligible, stream));
   return DFLASH_OK;
 }
 

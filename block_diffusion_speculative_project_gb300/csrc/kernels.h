@@ -183,6 +183,16 @@ cudaError_t launch_conv_apply(float *x, uint16_t *xb_out, const float *corr, con
 cudaError_t launch_gather_select(const int *block_ids, const int *cand_ids, int nb, int B, int k,
                                  const uint16_t *E, int D, int V, uint16_t *out, int *status,
                                  cudaStream_t s);
+// The selector's score table [nb][B-1][k][k] alone (the sampling walk reads it).
+cudaError_t launch_select_table(const float *cand_vals, const float *AB, const float *G, float *table,
+                                int nb, int B, int k, int sel_dim, cudaStream_t s);
+// Sampling walk over the table (sampling.cu): path [nb][B-1] and walk_logq [nb][B-1][k].
+cudaError_t launch_select_walk_sample(const int *cand_ids, const float *table, int nb, int B, int k,
+                                      float inv_T, unsigned long long seed, int *path, float *walk_logq,
+                                      cudaStream_t s);
+// Recall@k counts (atomic adds into hits[B-1], eligible[B-1]).
+cudaError_t launch_recall_at_k(const int *cand_ids, const int *target, int nb, int B, int k, int *hits,
+                               int *eligible, cudaStream_t s);
 cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, const float *AB,
                                const float *G, float *table, int nb, int B, int k, int sel_dim, int *path,
                                cudaStream_t s);
@@ -205,6 +215,11 @@ cudaError_t launch_draw_merge(const float4 *part, int rows, int S, long long row
 // numbers every draw uses).
 cudaError_t launch_draw_gumbel(int n, unsigned long long seed, int stream, int row, float *u, float *g,
                                cudaStream_t s);
+// Rejection-sampling verify against the sampling walk's sparse draft distribution.
+cudaError_t launch_verify_walk(const int *cand_ids, const float *walk_logq, int k, const int *path,
+                               const float *target_logits, const float *target_lse, int nb, int B, int V,
+                               float inv_T, unsigned long long seed, int S, float4 *part, int *nrej,
+                               int *tau, int *token, cudaStream_t s);
 // Rejection-sampling verify of nb blocks; part: nb * S float4, nrej: nb ints of scratch.
 cudaError_t launch_verify(const float *draft_logits, const float *draft_lse, const int *cand,
                           const float *target_logits, const float *target_lse, int nb, int B, int V,

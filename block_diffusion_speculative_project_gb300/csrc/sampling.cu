@@ -180,15 +180,22 @@ __global__ void __launch_bounds__(128) sample_merge_kernel(const float4 *part, i
 // the score log r(v) + g_v, and the fallback score log p_n(v) + g_v for the case that r is
 // nowhere positive; after B-1 acceptances, log p_{B-1}(v) + g_v.
 // part[i * S + s] = {best, id, fallback best, fallback id}; nrej[i] = n (slice 0).
+//
+// With walk_ids set, the draft distribution of offset t is the sampling walk's: q_t(v) =
+// exp(walk_logq[t-1][c]) for v = walk_ids[t-1][c] (c < wk), 0 elsewhere (draft_logits and
+// draft_lse unused); a non-candidate's residual is then p itself.
 __global__ void __launch_bounds__(256) verify_partial_kernel(
     const float *draft_logits, const float *draft_lse, const int *cand, const float *target_logits,
     const float *target_lse, int B, int V, int chunk, float inv_T, unsigned long long seed,
-    float4 *part, int *nrej) {
+    float4 *part, int *nrej, const int *walk_ids, const float *walk_logq, int wk) {
   griddep_wait();
   griddep_launch();
   __shared__ int n_sh;
+  __shared__ int sid[kTopkMax];
+  __shared__ float sq[kTopkMax];
   const int s = blockIdx.x, i = blockIdx.y, S = gridDim.x;
   const int bm1 = B - 1;
+  const bool walk = walk_ids != nullptr;
   if (threadIdx.x < 32) {
     const int j = threadIdx.x;
     bool acc = true;
@@ -196,7 +203,14 @@ __global__ void __launch_bounds__(256) verify_partial_kernel(
       const int c = cand[i * bm1 + j];
       if (c >= 0 && c < V) {
         const float lp = target_logits[((long long)i * B + j) * V + c] * inv_T - target_lse[i * B + j];
-        const float lq = draft_logits[((long long)i * bm1 + j) * V + c] * inv_T - draft_lse[i * bm1 + j];
+        float lq = INFINITY;  // a token the walk could not have drawn is rejected
+        if (walk) {
+          const int *ids = walk_ids + ((long long)i * bm1 + j) * wk;
+          for (int q = 0; q < wk; ++q)
+            if (ids[q] == c) lq = walk_logq[((long long)i * bm1 + j) * wk + q];
+        } else {
+          lq = draft_logits[((long long)i * bm1 + j) * V + c] * inv_T - draft_lse[i * bm1 + j];
+        }
         acc = logf(philox_uniform(seed, 1, i, j)) < lp - lq;
       } else {
         acc = false;  // an id outside the vocabulary is never accepted
@@ -211,11 +225,16 @@ __global__ void __launch_bounds__(256) verify_partial_kernel(
   __syncthreads();
   const int n = n_sh;
   if (s == 0 && threadIdx.x == 0) nrej[i] = n;
+  if (walk && n < bm1 && threadIdx.x < wk) {
+    sid[threadIdx.x] = walk_ids[((long long)i * bm1 + n) * wk + threadIdx.x];
+    sq[threadIdx.x] = __expf(walk_logq[((long long)i * bm1 + n) * wk + threadIdx.x]);
+  }
+  __syncthreads();
   const float *zp = target_logits + ((long long)i * B + n) * V;
   const float lzp = target_lse[i * B + n];
   const bool all = n == bm1;
-  const float *zq = all ? zp : draft_logits + ((long long)i * bm1 + n) * V;
-  const float lzq = all ? 0.f : draft_lse[i * bm1 + n];
+  const float *zq = (all || walk) ? zp : draft_logits + ((long long)i * bm1 + n) * V;
+  const float lzq = (all || walk) ? 0.f : draft_lse[i * bm1 + n];
   const int lo = s * chunk;
   const int hi = min(V, lo + chunk);
   Best b{-INFINITY, INT_MAX}, f{-INFINITY, INT_MAX};
@@ -231,8 +250,24 @@ __global__ void __launch_bounds__(256) verify_partial_kernel(
         const float lp = zp[v] * inv_T - lzp;
         best_take(f, lp + gv, v);
         if (!all) {
-          const float r = __expf(lp) - __expf(zq[v] * inv_T - lzq);
-          if (r > 0.f) best_take(b, logf(r) + gv, v);
+          if (walk) {
+            bool is_cand = false;
+            float qv = 0.f;
+            for (int q = 0; q < wk; ++q)
+              if (sid[q] == v) {
+                is_cand = true;
+                qv = sq[q];
+              }
+            if (!is_cand) {
+              best_take(b, lp + gv, v);
+            } else {
+              const float r = __expf(lp) - qv;
+              if (r > 0.f) best_take(b, logf(r) + gv, v);
+            }
+          } else {
+            const float r = __expf(lp) - __expf(zq[v] * inv_T - lzq);
+            if (r > 0.f) best_take(b, logf(r) + gv, v);
+          }
         }
       }
     }
@@ -361,10 +396,96 @@ cudaError_t launch_verify(const float *draft_logits, const float *draft_lse, con
   if (nb <= 0) return cudaSuccess;
   cudaError_t e = launch_pdl(verify_partial_kernel, dim3(S, nb), dim3(256), 0, s, draft_logits,
                              draft_lse, cand, target_logits, target_lse, B, V, slice_chunk(V, S),
-                             inv_T, seed, part, nrej);
+                             inv_T, seed, part, nrej, (const int *)nullptr, (const float *)nullptr, 0);
   if (e != cudaSuccess) return e;
   e = launch_pdl(verify_merge_kernel, dim3((nb + 3) / 4), dim3(128), 0, s, (const float4 *)part,
                  (const int *)nrej, nb, B, S, tau, token);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify_walk(const int *cand_ids, const float *walk_logq, int k, const int *path,
+                               const float *target_logits, const float *target_lse, int nb, int B, int V,
+                               float inv_T, unsigned long long seed, int S, float4 *part, int *nrej,
+                               int *tau, int *token, cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  if (k < 1 || k > kTopkMax) return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(verify_partial_kernel, dim3(S, nb), dim3(256), 0, s, (const float *)nullptr,
+                             (const float *)nullptr, path, target_logits, target_lse, B, V, slice_chunk(V, S),
+                             inv_T, seed, part, nrej, cand_ids, walk_logq, k);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(verify_merge_kernel, dim3((nb + 3) / 4), dim3(128), 0, s, (const float4 *)part,
+                 (const int *)nrej, nb, B, S, tau, token);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Sampling walk of the DFlash 2 selector: one CTA per sequence; the sequence's score table
+// [B-1][k][k] and candidate ids are staged in shared memory, then warp 0 walks: lane c < k
+// scores x_c = S_t(a_{t-1}, b_c) / T plus its Gumbel value (Philox stream 3, row
+// i*(B-1) + t-1, element c), the warp takes the best (ties to the lower token id), and
+// every lane writes log q_c = x_c - logsumexp(x).
+__global__ void __launch_bounds__(128) select_walk_sample_kernel(const int *cand_ids, const float *table,
+                                                                 int B, int k, float inv_T,
+                                                                 unsigned long long seed, int *path,
+                                                                 float *walk_logq) {
+  griddep_wait();
+  griddep_launch();
+  extern __shared__ float tab[];  // [B-1][k][k] scores, then [B-1][k] candidate ids
+  const int i = blockIdx.x;
+  const int bm1 = B - 1;
+  const int n = bm1 * k * k;
+  int *sid = reinterpret_cast<int *>(tab + n);
+  const float *ti = table + (size_t)i * n;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) tab[e] = ti[e];
+  for (int e = threadIdx.x; e < bm1 * k; e += blockDim.x) sid[e] = cand_ids[(size_t)i * bm1 * k + e];
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int a = 0;  // slot of the previous choice (offset 1 reads the anchor's row 0)
+  for (int t = 1; t < B; ++t) {
+    const int row = i * bm1 + t - 1;
+    const bool on = lane < k;
+    const float x = on ? tab[((t - 1) * k + a) * k + lane] * inv_T : -INFINITY;
+    const int id = on ? sid[(t - 1) * k + lane] : INT_MAX;
+    float sc = -INFINITY;
+    if (on) {
+      const uint4 w = philox4x32_10(make_uint4((uint32_t)(lane >> 2), (uint32_t)row, 3u, 0u), (uint32_t)seed,
+                                    (uint32_t)(seed >> 32));
+      const int q = lane & 3;
+      sc = x + gumbel_fast(q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w);
+    }
+    float bsc = sc, m = x;
+    int bid = id, bslot = lane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float sc2 = __shfl_xor_sync(0xffffffffu, bsc, o);
+      const int id2 = __shfl_xor_sync(0xffffffffu, bid, o);
+      const int sl2 = __shfl_xor_sync(0xffffffffu, bslot, o);
+      if (sc2 > bsc || (sc2 == bsc && id2 < bid)) {
+        bsc = sc2;
+        bid = id2;
+        bslot = sl2;
+      }
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    }
+    float e = on ? __expf(x - m) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+    if (on) walk_logq[(size_t)row * k + lane] = x - (m + logf(e));
+    if (lane == 0) path[row] = bid;
+    a = bslot;
+  }
+}
+
+cudaError_t launch_select_walk_sample(const int *cand_ids, const float *table, int nb, int B, int k,
+                                      float inv_T, unsigned long long seed, int *path, float *walk_logq,
+                                      cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  if (k < 1 || k > 16 || B < 2) return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(select_walk_sample_kernel, dim3(nb), dim3(128),
+                             (size_t)(B - 1) * k * (k + 1) * sizeof(float), s, cand_ids, table, B, k, inv_T,
+                             seed, path, walk_logq);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

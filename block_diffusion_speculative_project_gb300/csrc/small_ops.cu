@@ -657,6 +657,46 @@ __global__ void __launch_bounds__(256) select_walk_kernel(const int *cand_ids, c
   }
 }
 
+cudaError_t launch_select_table(const float *cand_vals, const float *AB, const float *G, float *table,
+                                int nb, int B, int k, int sel_dim, cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  if (k > 16 || sel_dim % 4 || B < 2) return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(select_table_kernel, dim3(B - 1, nb), dim3(256), (size_t)sel_dim * sizeof(float), s,
+                             cand_vals, AB, G, B, k, sel_dim, table);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- Recall@k
+// One thread per block: offsets t = 1.. while the target token T[t-1] is among the k
+// candidates of offset t: eligible[t-1] and hits[t-1] count it; the first miss is counted
+// as eligible only and ends the block.
+__global__ void recall_at_k_kernel(const int *cand_ids, const int *target, int nb, int B, int k,
+                                   int *hits, int *eligible) {
+  griddep_wait();
+  griddep_launch();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= nb) return;
+  for (int t = 0; t < B - 1; ++t) {
+    atomicAdd(&eligible[t], 1);
+    const int want = target[(size_t)i * B + t];
+    const int *c = cand_ids + ((size_t)i * (B - 1) + t) * k;
+    bool hit = false;
+    for (int q = 0; q < k; ++q) hit |= c[q] == want;
+    if (!hit) break;
+    atomicAdd(&hits[t], 1);
+  }
+}
+
+cudaError_t launch_recall_at_k(const int *cand_ids, const int *target, int nb, int B, int k, int *hits,
+                               int *eligible, cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(recall_at_k_kernel, dim3((nb + 127) / 128), dim3(128), 0, s, cand_ids, target, nb,
+                             B, k, hits, eligible);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, const float *AB,
                                const float *G, float *table, int nb, int B, int k, int sel_dim, int *path,
                                cudaStream_t s) {

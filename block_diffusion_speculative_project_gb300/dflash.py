@@ -85,6 +85,11 @@ def _load():
                                      p]),
         "dflash2_conv": (i, [p, i, i, i, p, p, sz, p]),
         "dflash2_select": (i, [p, i, i, p, p, p, p, p, p, sz, p]),
+        "dflash2_select_sample": (i, [p, i, i, p, p, p, p, ctypes.c_float, ctypes.c_uint64, p, p, p, sz,
+                                      p]),
+        "dflash_verify_sample_walk": (i, [p, i, i, p, p, p, p, ctypes.c_float, ctypes.c_uint64, p, p, p,
+                                          sz, p]),
+        "dflash_recall_at_k": (i, [p, i, i, p, p, p, p, p]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -98,7 +103,8 @@ EXPORTED = ("dflash_create", "dflash_destroy", "dflash_set_weights", "dflash_wor
             "dflash_status", "dflash_last_error", "dflash_ctx_project", "dflash_ctx_project_film",
             "dflash_draft_block",
             "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_attention", "dflash_topk", "dflash_accept", "dflash_sample", "dflash_verify_sample",
-            "dflash_lm_head_sample", "dflash_draw_gumbel", "dflash2_conv",
+            "dflash_lm_head_sample", "dflash_draw_gumbel", "dflash2_select_sample",
+            "dflash_verify_sample_walk", "dflash_recall_at_k", "dflash2_conv",
             "dflash2_select")
 
 
@@ -224,6 +230,27 @@ def dflash_verify_sample(h, nb, draft_logits, draft_lse, cand, target_logits, te
                                     _ptr(target_logits), float(temperature), int(seed),
                                     _ptr(out_tau), _ptr(out_token), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dflash2_select_sample(h, nb, k, topk_ids, topk_vals, hidden, block_ids, temperature, seed,
+                          out_path, out_walk_logq, ws, stream=None) -> None:
+    _check(LIB.dflash2_select_sample(h, nb, k, _ptr(topk_ids), _ptr(topk_vals), _ptr(hidden),
+                                     _ptr(block_ids), float(temperature), int(seed), _ptr(out_path),
+                                     _ptr(out_walk_logq), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream)))
+
+
+def dflash_verify_sample_walk(h, nb, k, cand_ids, walk_logq, path, target_logits, temperature, seed,
+                              out_tau, out_token, ws, stream=None) -> None:
+    _check(LIB.dflash_verify_sample_walk(h, nb, k, _ptr(cand_ids), _ptr(walk_logq), _ptr(path),
+                                         _ptr(target_logits), float(temperature), int(seed),
+                                         _ptr(out_tau), _ptr(out_token), _ptr(ws),
+                                         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dflash_recall_at_k(h, nb, k, cand_ids, target, hits, eligible, stream=None) -> None:
+    _check(LIB.dflash_recall_at_k(h, nb, k, _ptr(cand_ids), _ptr(target), _ptr(hits), _ptr(eligible),
+                                  _stream(stream)))
 
 
 def dflash2_conv(h, layer, which, nb, x, ws, stream=None) -> None:

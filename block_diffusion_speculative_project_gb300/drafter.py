@@ -114,6 +114,19 @@ class Drafter:
         _d.dflash2_select(self.h, nb, k, topk_ids, topk_vals, hidden, block_ids, out_path, self.ws,
                           stream)
 
+    def select_sample(self, nb, k, topk_ids, topk_vals, hidden, block_ids, temperature, seed, out_path,
+                      out_walk_logq, stream=None):
+        _d.dflash2_select_sample(self.h, nb, k, topk_ids, topk_vals, hidden, block_ids, temperature, seed,
+                                 out_path, out_walk_logq, self.ws, stream)
+
+    def verify_sample_walk(self, nb, k, cand_ids, walk_logq, path, target_logits, temperature, seed,
+                           out_tau, out_token, stream=None):
+        _d.dflash_verify_sample_walk(self.h, nb, k, cand_ids, walk_logq, path, target_logits, temperature,
+                                     seed, out_tau, out_token, self.ws, stream)
+
+    def recall_at_k(self, nb, k, cand_ids, target, hits, eligible, stream=None):
+        _d.dflash_recall_at_k(self.h, nb, k, cand_ids, target, hits, eligible, stream)
+
     def attention(self, nb, layer, q, ctx_len, out_o, max_ctx_hint=0, stream=None):
         _d.dflash_attention(self.h, nb, layer, q, self.kcache, self.vcache, ctx_len, max_ctx_hint,
                             out_o, self.ws, stream)

@@ -98,9 +98,12 @@ RELAY_DFLASH2 = QWEN3_8B.with_(name="qwen3_8b_shaped_relay_dflash2_b16_c4096_nb3
 FILM_RELAY = QWEN3_8B.with_(name="qwen3_8b_shaped_film_relay_b16_c4096_nb32", nb=32,
                             flags=FLAG_RELAY | FLAG_FILM)
 SAMPLING_T1 = QWEN3_8B.with_(name="qwen3_8b_shaped_sampling_t1_b16_c4096_nb8", temperature=1.0)
+DFLASH2_SAMPLING_T1 = QWEN3_8B.with_(name="qwen3_8b_shaped_dflash2_sampling_t1_b16_c4096_nb8",
+                                     temperature=1.0, flags=FLAG_CONV | FLAG_SELECT)
 
 WORKLOADS = {w.name: w for w in (TINY, QWEN3_4B, QWEN3_8B, SWEEP_NB16, SWEEP_NB32,
-                                  SWEEP_NB64, RELAY_DFLASH2, FILM_RELAY, SAMPLING_T1)}
+                                  SWEEP_NB64, RELAY_DFLASH2, FILM_RELAY, SAMPLING_T1,
+                                  DFLASH2_SAMPLING_T1)}
 
 
 # --------------------------------------------------------------------------- streams

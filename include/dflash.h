@@ -334,6 +334,41 @@ DFLASH_API int dflash_verify_sample(dflash_handle_t h, int nb, const float *draf
                   float temperature, uint64_t seed, int32_t *out_tau, int32_t *out_token,
                   void *ws, size_t ws_bytes, dflash_stream_t stream);
 
+/* DFlash 2 sampling walk ([DFlash2] 洞察一: sampling draws from the same score
+ * distribution the greedy walk maximises): the scores S_t(a, b) of dflash2_select, then
+ * from a_0 = the anchor each offset t draws slot c among its k candidates from
+ * softmax_c(S_t(a_{t-1}, b_c) / T) by Gumbel-max (Philox counter (c / 4, i*(B-1) + t-1, 3, 0);
+ * ties to the lower token id) and a_t = b_c.
+ *   out_path       int32 [nb, B-1]: the drawn tokens
+ *   out_walk_logq  f32 [nb, B-1, k]: log softmax_c(S_t(a_{t-1}, b_c) / T) along the drawn
+ *                  path: the walk's draft distribution for dflash_verify_sample_walk.
+ * Other arguments as dflash2_select. */
+DFLASH_API int dflash2_select_sample(dflash_handle_t h, int nb, int k, const int32_t *topk_ids,
+                  const float *topk_vals, const void *hidden, const int32_t *block_ids,
+                  float temperature, uint64_t seed, int32_t *out_path, float *out_walk_logq,
+                  void *ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* dflash_verify_sample with the sampling walk's draft distribution: q_t(v) =
+ * exp(walk_logq[t-1][c]) for v = cand_ids[t-1][c], 0 for every other token (so the
+ * residual of a non-candidate is p itself, and a drawn token outside the candidates is
+ * rejected). Acceptance, residual, fallback and bonus draws as dflash_verify_sample.
+ *   cand_ids   int32 [nb, B-1, k] (the top-k ids the walk chose from)
+ *   walk_logq  f32 [nb, B-1, k] (out_walk_logq of dflash2_select_sample)
+ *   path       int32 [nb, B-1] (out_path of dflash2_select_sample) */
+DFLASH_API int dflash_verify_sample_walk(dflash_handle_t h, int nb, int k, const int32_t *cand_ids,
+                  const float *walk_logq, const int32_t *path, const float *target_logits,
+                  float temperature, uint64_t seed, int32_t *out_tau, int32_t *out_token,
+                  void *ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* Recall@k instrumentation ([DFlash2] Why DFlash 2, the Recall@1 / Recall@16 table,
+ * conditioned on every earlier position being right): for each block, offsets t = 1, 2, ...
+ * count eligible[t-1] += 1 and, while target[i][t-1] is among cand_ids[i][t-1][0..k),
+ * hits[t-1] += 1; the first miss ends the block. hits and eligible (int32 [B-1], device)
+ * are accumulated atomically: the caller zeroes them to start a tally.
+ *   cand_ids  int32 [nb, B-1, k]; target int32 [nb, B] (T[j] is the token after offset j) */
+DFLASH_API int dflash_recall_at_k(dflash_handle_t h, int nb, int k, const int32_t *cand_ids,
+                  const int32_t *target, int32_t *hits, int32_t *eligible, dflash_stream_t stream);
+
 /* DFlash 2 two-tap dynamic depthwise conv ([DFlash2] 洞察二), in place:
  * x'_t = k_{t,0} * x_t + k_{t,1} * x_{t-1}, k_{t,j} = base_j + expand(W_j x_t),
  * one correction per conv_group channels, x_{-1} = 0 at block offset 0.

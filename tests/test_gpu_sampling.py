@@ -300,3 +300,108 @@ def test_lm_head_fused_draw(V, nb, B, T):
     dr.sample(nb * (B - 1), logits, T, seed, c2, l2)
     assert np.array_equal(c2.cpu().numpy(), gc)
     np.testing.assert_allclose(l2.cpu().numpy(), lse.cpu().numpy(), rtol=1e-5, atol=1e-5)
+
+
+# ----------------------------------------------------------------------------- DFlash 2 sampling walk
+
+SEL = di.Workload("medium_select_walk", D=512, Dt=192, L=5, N=1, Hq=8, Hkv=2, hd=128, F=1000,
+                  V=5003, B=16, nb=6, C=300, flags=di.FLAG_SELECT)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5])
+def test_select_walk_sample_stage(T):
+    """dflash2_select_sample against the oracle's walk on the same candidates, values and
+    hidden rows. The scores come from bf16 GEMMs (within 1e-2 (1 + |U|) of fp64), so the
+    walks agree step by step while the oracle's Gumbel margin exceeds that; after the first
+    step under it the prefixes may part and the rest of that sequence is not compared."""
+    from block_diffusion_speculative_project_gb300 import drafter
+    w = SEL
+    bits = di.make_weights(w)
+    W = orc.widen_all(bits)
+    dev = {k: drafter.to_device_bf16(v) for k, v in bits.items()}
+    dr = drafter.Drafter(w, dev, w.nb, 64, w.B)
+    rng = np.random.default_rng(61)
+    k = w.k_top
+    cand = np.stack([rng.permutation(w.V)[:k] for _ in range(w.nb * (w.B - 1))]).reshape(w.nb, w.B - 1, k)
+    vals = (rng.standard_normal((w.nb, w.B - 1, k)) * 2).astype(np.float32)
+    hid_bits = di.normal_bf16("walk_hidden", (w.nb, w.B, w.D), 1.0)
+    ids = di.block_ids(w, di.anchors(w))
+    seed = 2024
+    path = i32(np.zeros((w.nb, w.B - 1)))
+    logq = t32(np.zeros((w.nb, w.B - 1, k)))
+    dr.select_sample(w.nb, k, i32(cand), torch.tensor(vals, device="cuda"), drafter.to_device_bf16(hid_bits),
+                     i32(ids), T, seed, path, logq)
+    assert dr.status() == 0
+    opath, ologq, margin = orc.select_walk_sample(w, W, cand, vals.astype(np.float64), orc.widen(hid_bits),
+                                                  ids[:, 0], T, seed)
+    gp, gl = path.cpu().numpy(), logq.cpu().numpy()
+    decided = 0
+    for i in range(w.nb):
+        for t in range(w.B - 1):
+            err = np.abs(gl[i, t] - ologq[i, t])
+            assert (err <= 2e-2 / T + 1e-2 * np.abs(ologq[i, t])).all(), (
+                f"log q seq {i} offset {t + 1}: max err {err.max():.3e}; gpu {gl[i, t][:4]} oracle {ologq[i, t][:4]}")
+            if margin[i, t] <= 1e-2 * max(1.0, abs(vals[i, t]).max()) / T:
+                assert gp[i, t] in cand[i, t]
+                break
+            assert gp[i, t] == opath[i, t], f"seq {i} offset {t + 1}"
+            decided += 1
+    assert decided >= w.nb * (w.B - 1) // 2
+    print(f"T={T}: {decided}/{w.nb * (w.B - 1)} walk steps compared exactly")
+
+
+def test_verify_sample_walk_stage():
+    """dflash_verify_sample_walk on the oracle's walk (candidates, log q, path) and seeded
+    target logits that favour the walked tokens, against the oracle's sparse verify."""
+    nb, B, V, k, seed = 48, 16, 5003, 16, 81
+    dr = handle(V, B)
+    rng = np.random.default_rng(82)
+    cand = np.stack([rng.permutation(V)[:k] for _ in range(nb * (B - 1))]).reshape(nb, B - 1, k).astype(np.int32)
+    x = rng.standard_normal((nb, B - 1, k)) * 1.5
+    logq = x - np.log(np.exp(x).sum(-1, keepdims=True))
+    slot = np.array([[orc.gumbel_argmax(logq[i, t] + orc.gumbel(orc.uniforms(seed, 3, i * (B - 1) + t, k)))[0]
+                      for t in range(B - 1)] for i in range(nb)])
+    path = np.take_along_axis(cand, slot[..., None], -1)[..., 0]
+    Z = logits_rows("walkZ", (nb, B, V), 1.0)
+    for i in range(nb):
+        for t in range(B - 1):
+            Z[i, t, cand[i, t]] += 4.0 + x[i, t]      # the target leans toward the candidates
+    lq32 = logq.astype(np.float32).astype(np.float64)
+    tau = i32(np.zeros(nb))
+    tok = i32(np.zeros(nb))
+    dr.verify_sample_walk(nb, k, i32(cand), t32(lq32), i32(path), t32(Z), 1.0, seed, tau, tok)
+    assert dr.status() == 0
+    otau, otok, am, em = orc.verify_sample_walk(cand, lq32, path, Z.astype(np.float32).astype(np.float64),
+                                                1.0, seed, return_detail=True)
+    gt, gk = tau.cpu().numpy(), tok.cpu().numpy()
+    exact = 0
+    for i in range(nb):
+        n = otau[i] - 1
+        if (am[i, :min(n + 1, B - 1)] > DELTA).all():
+            assert gt[i] == otau[i], f"seq {i}: tau {gt[i]} vs {otau[i]}"
+            if em[i] > DELTA:
+                assert gk[i] == otok[i], f"seq {i}: token {gk[i]} vs {otok[i]}"
+                exact += 1
+    assert exact >= 0.9 * nb
+    assert len(np.unique(otau)) >= 4
+    print(f"walk verify: tau histogram {np.bincount(otau, minlength=B + 1)}; {exact}/{nb} exact")
+
+
+def test_recall_at_k_counts():
+    nb, B, V, k = 40, 8, 999, 4
+    dr = handle(V, B)
+    rng = np.random.default_rng(83)
+    cand = np.stack([rng.permutation(V)[:k] for _ in range(nb * (B - 1))]).reshape(nb, B - 1, k).astype(np.int32)
+    target = rng.integers(0, V, (nb, B)).astype(np.int32)
+    hit = rng.random((nb, B - 1)) < 0.8                      # plant hits at 80% of the offsets
+    for i in range(nb):
+        for t in range(B - 1):
+            if hit[i, t]:
+                target[i, t] = cand[i, t, rng.integers(0, k)]
+    hits = i32(np.zeros(B - 1))
+    elig = i32(np.zeros(B - 1))
+    dr.recall_at_k(nb, k, i32(cand), i32(target), hits, elig)
+    dr.recall_at_k(nb, k, i32(cand), i32(target), hits, elig)  # counts accumulate
+    oh, oe = orc.recall_at_k(cand, target)
+    assert np.array_equal(hits.cpu().numpy(), 2 * oh) and np.array_equal(elig.cpu().numpy(), 2 * oe)
+    assert oe[0] == nb and oh[-1] > 0
