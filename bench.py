@@ -33,7 +33,8 @@ import dflash_inputs as di  # noqa: E402
 
 DEFAULT_WORKLOAD = di.QWEN3_8B.name
 METRIC = "draft blocks/sec (Qwen3-8B-shaped, B=16)"
-PROJ_CHUNK = 512
+PROJ_CHUNK = 2048   # rows per sequence of one ctx_project call when filling the context
+PREFILL_ROWS = 2048  # prompt rows per sequence of the measured prefill
 
 
 def load_peaks():
@@ -194,7 +195,7 @@ def run_gpu(args, rank, world):
     bits = di.make_weights(w, seed)
     weights = {k: to_device_bf16(v, dev) for k, v in bits.items()}
     t_gen = time.time() - t0
-    dr = Drafter(w, weights, w.nb, Cmax, max(PROJ_CHUNK, w.B))
+    dr = Drafter(w, weights, w.nb, Cmax, max(PROJ_CHUNK, PREFILL_ROWS, w.B))
     i32 = lambda x: torch.tensor(np.asarray(x, np.int32), device=dev)
 
     # prefill C_i - tau_prev_i context rows per sequence (outside every timed region)
@@ -378,6 +379,28 @@ def run_gpu(args, rank, world):
     h2d = host_hv.numel() * 2 + host_in.numel() * 4
     d2h = host_out.numel() * 4
 
+    # prompt prefill through dflash_ctx_project (the large-context path, compute-bound W_c
+    # GEMM over nb * PREFILL_ROWS rows): after the step timing, so rewriting the first
+    # context rows of the caches does not matter any more
+    hv_pre = torch.randn(w.nb, PREFILL_ROWS, w.L * w.Dt, device=dev, generator=g).to(torch.bfloat16)
+    pre_commit = i32(np.full(w.nb, PREFILL_ROWS))
+    pre_zero = i32(np.zeros(w.nb))
+    pre_len = pre_zero.clone()
+    pre_ms = []
+    with torch.cuda.stream(stream):
+        for rep in range(4):
+            pre_len.copy_(pre_zero)
+            p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            p0.record(stream)
+            dr.ctx_project(w.nb, PREFILL_ROWS, hv_pre, pre_commit, pre_len, stream=stream)
+            p1.record(stream)
+            stream.synchronize()
+            if rep:
+                pre_ms.append(p0.elapsed_time(p1))
+    if dr.status(stream) != 0:
+        raise RuntimeError("device status reports an error after the prefill")
+    del hv_pre
+
     # max over ranks
     ms_step, e2e_s = max_over_ranks([ms_total / args.steps, e2e_s], dev)
 
@@ -394,6 +417,9 @@ def run_gpu(args, rank, world):
                                                 "csrc", "gemm_tc.cu"))
     blocks = w.nb * world
     value = blocks / (ms_step * 1e-3)
+    pre_rows = w.nb * PREFILL_ROWS
+    pre_flops = 2 * pre_rows * w.D * (w.L * w.Dt + 2 * w.N * w.Hkv * w.hd)
+    pre_t = float(np.mean(pre_ms)) * 1e-3
     step_t_roof = max(total_bytes / (hbm * 1e9), flops / (tf_sus * 1e12 if tf_sus else tf_burst * 1e12))
     line = {
         "metric": METRIC if args.workload == DEFAULT_WORKLOAD else f"draft blocks/sec ({args.workload})",
@@ -420,6 +446,11 @@ def run_gpu(args, rank, world):
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
                      "avg_launch_ms": round(lm_avg, 4), "bytes_per_launch": lm_bytes},
+        "prefill": {"rows_per_seq": PREFILL_ROWS, "rows": pre_rows, "ms": round(pre_t * 1e3, 4),
+                    "prompt_rows_per_s": round(pre_rows / pre_t, 1), "bound": "tensor",
+                    "achieved": round(pre_flops / pre_t / 1e12, 1), "peak": tf_burst, "unit": "TFLOP/s",
+                    "frac": round(pre_flops / pre_t / 1e12 / tf_burst, 4),
+                    "what": "dflash_ctx_project: W_c GEMM, RMSNorm, K/V GEMMs of every layer into the caches"},
         "e2e": {"value": round(blocks * e2e_steps / e2e_s, 2), "unit": "blocks/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": kernels_per_step(w) * args.steps,

@@ -174,3 +174,42 @@ def test_fullsize_relay_dflash2_nb32():
 def test_fullsize_film_relay_nb32():
     a = di.accepted_prev(di.FILM_RELAY)
     run_case(di.FILM_RELAY, [int(np.argmin(a)), 3])  # the most relayed rows, and sequence 3
+
+
+def test_fullsize_prefill_qwen3_8b_2048_rows():
+    """The large-context path: dflash_ctx_project over 2048 prompt rows per sequence at the
+    Qwen3-8B shape (M = 4096 rows through the W_c and K/V GEMMs, 32 m-tiles), one sequence
+    from position 0 committing every row, one from position 100 committing 1500. The
+    oracle computes sampled rows one by one (rows are independent): h, then K_c / V_c of
+    every layer at those positions, compared at the stated tolerance; rows outside the
+    appended range stay untouched."""
+    from block_diffusion_speculative_project_gb300 import drafter
+    w = di.QWEN3_8B.with_(nb=2)
+    bits, W = weights_for(w)
+    R = 2048
+    start = np.array([0, 100], np.int32)
+    commit = np.array([R, 1500], np.int32)
+    Cmax = int((start + commit).max()) + w.B + 8
+    dev = {n: drafter.to_device_bf16(v) for n, v in bits.items()}
+    dr = drafter.Drafter(w, dev, w.nb, Cmax, R)
+    hv = di.verifier_rows(w, R, name="hv_prefill_2048")
+    ctx = torch.tensor(start, device="cuda")
+    dr.ctx_project(w.nb, R, drafter.to_device_bf16(hv), torch.tensor(commit, device="cuda"), ctx)
+    assert dr.status() == 0
+    assert np.array_equal(ctx.cpu().numpy(), start + commit)
+    rows = [0, 1, 63, 64, 127, 128, 129, 700, 1023, 1024, 1499, 1500, 2046, 2047]
+    K, V = dr.kcache, dr.vcache
+    for i in range(w.nb):
+        sel = [r for r in rows if r < commit[i]]
+        h = orc.fuse_context(w, W, orc.widen(hv[i, sel]))
+        for n in range(w.N):
+            for j, r in enumerate(sel):
+                pos = int(start[i]) + r
+                k = (W[f"layer{n}.Wk_c"] @ h[j]).reshape(w.Hkv, w.hd)
+                v = (W[f"layer{n}.Wv_c"] @ h[j]).reshape(w.Hkv, w.hd)
+                ok = orc.rope(k[None], pos, w.rope_base)[0]
+                assert_close(K[n, i, :, pos].float().cpu().numpy(), ok, f"K_c seq {i} row {r} layer {n}")
+                assert_close(V[n, i, :, pos].float().cpu().numpy(), v, f"V_c seq {i} row {r} layer {n}")
+        end = int(start[i] + commit[i])
+        assert not K[:, i, :, end:].float().abs().sum().item(), "rows past the append"
+        assert not K[:, i, :, :int(start[i])].float().abs().sum().item(), "rows before the append"
