@@ -764,24 +764,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       float *slice = reinterpret_cast<float *>(smem) + BM * C::RED_STRIDE;
       const uint32_t red0 = smem_u32(smem);
       const int units = per * (BN / 4);
-      for (int e = threadIdx.x - 64; e < units; e += 128) {
-        const int rr = e / (BN / 4), c4 = e % (BN / 4);
-        const uint32_t off = static_cast<uint32_t>(((row0 + rr) * C::RED_STRIDE + c4 * 4) * 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int src0 = 0; src0 < p.csplit; src0 += 2) {
-          float4 x0 = ld_cluster_f4(cluster_map(red0 + off, static_cast<uint32_t>(src0)));
-          float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (src0 + 1 < p.csplit) x1 = ld_cluster_f4(cluster_map(red0 + off, static_cast<uint32_t>(src0 + 1)));
-          acc.x += x0.x;
-          acc.y += x0.y;
-          acc.z += x0.z;
-          acc.w += x0.w;
-          acc.x += x1.x;
-          acc.y += x1.y;
-          acc.z += x1.z;
-          acc.w += x1.w;
+      // four units per thread at a time, two ranks' loads each (8 cluster loads in
+      // flight): the sum is latency-bound, and each unit's additions stay in rank order
+      constexpr int kU = 4;
+      for (int e0 = threadIdx.x - 64; e0 < units; e0 += 128 * kU) {
+        uint32_t off[kU];
+        float4 acc[kU];
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int e = min(e0 + k * 128, units - 1);  // a clamped duplicate is not stored
+          const int rr = e / (BN / 4), c4 = e % (BN / 4);
+          off[k] = static_cast<uint32_t>(((row0 + rr) * C::RED_STRIDE + c4 * 4) * 4);
+          acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        *reinterpret_cast<float4 *>(slice + rr * C::RED_STRIDE + c4 * 4) = acc;
+        for (int src0 = 0; src0 < p.csplit; src0 += 2) {
+          float4 x0[kU], x1[kU];
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            x0[k] = ld_cluster_f4(cluster_map(red0 + off[k], static_cast<uint32_t>(src0)));
+            x1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (src0 + 1 < p.csplit)
+              x1[k] = ld_cluster_f4(cluster_map(red0 + off[k], static_cast<uint32_t>(src0 + 1)));
+          }
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            acc[k].x += x0[k].x;
+            acc[k].y += x0[k].y;
+            acc[k].z += x0[k].z;
+            acc[k].w += x0[k].w;
+            acc[k].x += x1[k].x;
+            acc[k].y += x1[k].y;
+            acc[k].z += x1[k].z;
+            acc[k].w += x1[k].w;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int e = e0 + k * 128;
+          if (e < units) {
+            const int rr = e / (BN / 4), c4 = e % (BN / 4);
+            *reinterpret_cast<float4 *>(slice + rr * C::RED_STRIDE + c4 * 4) = acc[k];
+          }
+        }
       }
       named_bar_sync(1, 128);
       // Phase 2: the owner thread of each row of the slice runs the epilogue.
