@@ -279,13 +279,16 @@ __device__ __forceinline__ void topk_replace_worst(TopkState &tk, float v, int i
 // Runs the epilogue of one output tile. `fetch(c, v)` returns the 32 fp32 values of
 // accumulator columns [32c, 32c+32) of this thread's row; it is called by every lane
 // (tcgen05.ld is warp-collective); only the stores depend on row validity.
+// cpart / nparts: this thread runs the row's 32-column chunks c with c % nparts == cpart
+// (nparts adjacent lanes share the row; nparts = 1 when one thread owns the whole row).
+// Every lane of the warp must call it (the RMS partial sums are combined by shuffles).
 template <int BN, int EPI, class Fetch>
 __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t, int row,
                                               bool row_ok, Fetch &&fetch, TopkState &tk,
-                                              float *stash) {
+                                              float *stash, int cpart = 0, int nparts = 1) {
   if constexpr (EPI == EPI_BF16 || EPI == EPI_F32) {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = cpart; c < BN / 32; c += nparts) {
       float v[32];
       fetch(c, v);
       const int col0 = t.n * BN + c * 32;
@@ -305,7 +308,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
   } else if constexpr (EPI == EPI_RESID) {
     float ss = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = cpart; c < BN / 32; c += nparts) {
       float v[32];
       fetch(c, v);
       const int col0 = t.n * BN + c * 32;
@@ -347,7 +350,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
         }
       }
     }
-    if (p.ss_out && row_ok) p.ss_out[(size_t)row * p.n_tiles + t.n] = ss;
+    for (int o = 1; o < nparts; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (p.ss_out && row_ok && cpart == 0) p.ss_out[(size_t)row * p.n_tiles + t.n] = ss;
   } else if constexpr (EPI == EPI_ROPE) {
     const int half = p.hd >> 1;
     int seq = 0, pos = 0;
@@ -379,7 +383,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
         }
       }
 #pragma unroll 1
-      for (int cc = 0; cc < half; cc += 32) {
+      for (int cc = 32 * cpart; cc < half; cc += 32 * nparts) {
         float a[32], b[32];
         fetch((h0 + cc) >> 5, a);
         fetch((h0 + half + cc) >> 5, b);
@@ -398,7 +402,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
   } else if constexpr (EPI == EPI_SWIGLU) {
     const float rs = (p.ss_in && row_ok) ? deferred_rms(p, row) : 1.f;
 #pragma unroll 1
-    for (int c = 0; c < BN / 64; ++c) {
+    for (int c = cpart; c < BN / 64; c += nparts) {
       float g[32], u[32];
       fetch(c, g);
       fetch(c + BN / 64, u);
@@ -417,7 +421,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
     }
   } else if constexpr (EPI == EPI_DUAL_F32) {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = cpart; c < BN / 32; c += nparts) {
       float v[32];
       fetch(c, v);
       const int which = c >= BN / 64 ? 1 : 0;
@@ -447,7 +451,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
     for (int h0 = 0; h0 < BN; h0 += p.hd) {
       const int head = (t.n * BN + h0) / p.hd;
 #pragma unroll 1
-      for (int cc = 0; cc < half; cc += 32) {
+      for (int cc = 32 * cpart; cc < half; cc += 32 * nparts) {
         float a[32], b[32];
         fetch((h0 + cc) >> 5, a);
         fetch((h0 + half + cc) >> 5, b);
@@ -808,13 +812,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
         }
       }
       named_bar_sync(1, 128);
-      // Phase 2: the owner thread of each row of the slice runs the epilogue.
-      if (r >= row0 && r < row0 + per) {
+      // Phase 2: the slice's rows spread over the 128 epilogue threads, nparts adjacent
+      // lanes per row, each running the epilogue on its share of the row's chunks.
+      {
+        const int nparts = per * 4 <= 128 ? 4 : per * 2 <= 128 ? 2 : 1;
+        const int rl = r / nparts, cpart = r % nparts;
+        const bool active = rl < per;
+        const int rt = row0 + rl;  // row inside the tile
         const Item t = item_at(p, 0);
-        const int row = t.m * p.tile_rows + r;
-        const bool row_ok = (r < p.tile_rows) && (row < p.M);
-        const float *mine = slice + (r - row0) * C::RED_STRIDE;
+        const int row = t.m * p.tile_rows + rt;
+        const bool row_ok = active && (rt < p.tile_rows) && (row < p.M);
+        const float *mine = slice + (active ? rl : 0) * C::RED_STRIDE;
         auto fetch = [&](int c, float (&v)[32]) {
+          if (!active) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = 0.f;
+            return;
+          }
           const float4 *src = reinterpret_cast<const float4 *>(mine + c * 32);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -827,7 +841,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
         };
         TopkState tk;
         float *stash = nullptr;
-        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, tk, stash);
+        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, tk, stash, cpart, nparts);
       }
     }
     __syncwarp();
