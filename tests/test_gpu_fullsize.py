@@ -237,3 +237,63 @@ def test_fullsize_prefill_qwen3_8b_2048_rows():
         end = int(start[i] + commit[i])
         assert not K[:, i, :, end:].float().abs().sum().item(), "rows past the append"
         assert not K[:, i, :, :int(start[i])].float().abs().sum().item(), "rows before the append"
+
+
+def test_fullsize_sampling_launch_shapes_qwen3_8b():
+    """The sampling workload's launches at their bench shapes (8 sequences, B = 16,
+    V = 151936): the draw over 120 logit rows, the verify of 8 blocks and the DFlash 2
+    walk's verify at k = 16, on seeded logits both sides read. Decisions compare exactly
+    where the oracle's margin exceeds 1e-3 (fp32 against fp64 scores), otherwise the GPU's
+    choice must lie within that margin; the acceptance counts must vary."""
+    from block_diffusion_speculative_project_gb300 import drafter
+    w = di.SAMPLING_T1
+    nb, B, V, k, T, seed = w.nb, w.B, w.V, w.k_top, w.temperature, 0x5EED
+    small = di.TINY.with_(V=V, B=B)
+    dev = {n: drafter.to_device_bf16(v) for n, v in di.make_weights(small).items()}
+    dr = drafter.Drafter(small, dev, nb, 80, 8)
+    t32 = lambda x: torch.tensor(np.asarray(x, np.float32), device="cuda")
+    i32 = lambda x: torch.tensor(np.asarray(x, np.int32), device="cuda")
+    U = di.normal_f32("fs_draft_logits", (nb, B - 1, V), 2.0).astype(np.float64)
+    Z = di.target_logits(w).astype(np.float64)
+    Z[:, :B - 1] = U + 0.3 * Z[:, :B - 1]           # the target leans toward the draft
+    cand = i32(np.zeros((nb, B - 1)))
+    lse = t32(np.zeros((nb, B - 1)))
+    dr.sample(nb * (B - 1), t32(U), T, seed, cand, lse)
+    oc, olse, _, om = orc.sample_candidates(U, T, seed)
+    gc = cand.cpu().numpy()
+    dec = om > 1e-3
+    assert np.array_equal(gc[dec], oc[dec]) and dec.mean() > 0.95
+    np.testing.assert_allclose(lse.cpu().numpy(), olse, rtol=1e-5, atol=1e-4)
+    tau = i32(np.zeros(nb))
+    tok = i32(np.zeros(nb))
+    dr.verify_sample(nb, t32(U), t32(olse), i32(oc), t32(Z), T, seed, tau, tok)
+    otau, otok, am, em = orc.verify_sample(U, oc, Z, T, seed, return_detail=True)
+    gt, gk = tau.cpu().numpy(), tok.cpu().numpy()
+    for i in range(nb):
+        if (am[i, :min(int(otau[i]), B - 1)] > 1e-3).all():
+            assert gt[i] == otau[i], f"seq {i}: tau {gt[i]} vs {otau[i]}"
+            if em[i] > 1e-3:
+                assert gk[i] == otok[i], f"seq {i}: token {gk[i]} vs {otok[i]}"
+    assert len(np.unique(otau)) > 1
+    # the DFlash 2 walk's verify at the same shapes
+    rng = np.random.default_rng(23)
+    cids = np.stack([rng.permutation(V)[:k] for _ in range(nb * (B - 1))]).reshape(nb, B - 1, k).astype(np.int32)
+    x = rng.standard_normal((nb, B - 1, k)) * 1.5
+    logq = (x - np.log(np.exp(x).sum(-1, keepdims=True))).astype(np.float32).astype(np.float64)
+    path = cids[..., 0]
+    Zw = Z.copy()
+    for i in range(nb):
+        for t in range(B - 1):
+            Zw[i, t, path[i, t]] += 12.0 if (i + t) % 5 else 0.0  # mostly accepted walked tokens
+    dr.verify_sample_walk(nb, k, i32(cids), t32(logq), i32(path), t32(Zw), T, seed, tau, tok)
+    wt, wk_, wam, wem = orc.verify_sample_walk(cids, logq, path, Zw.astype(np.float32).astype(np.float64), T, seed,
+                                               return_detail=True)
+    gt, gk = tau.cpu().numpy(), tok.cpu().numpy()
+    for i in range(nb):
+        if (wam[i, :min(int(wt[i]), B - 1)] > 1e-3).all():
+            assert gt[i] == wt[i], f"walk seq {i}: tau {gt[i]} vs {wt[i]}"
+            if wem[i] > 1e-3:
+                assert gk[i] == wk_[i], f"walk seq {i}: token {gk[i]} vs {wk_[i]}"
+    assert len(np.unique(wt)) > 1
+    assert dr.status() == 0
+    print(f"sampling launch shapes: draws {dec.sum()}/{dec.size} exact; tau {list(otau)}; walk tau {list(wt)}")
