@@ -202,7 +202,7 @@ DFLASH_API int dflash_ctx_project_film(dflash_handle_t h, int nb, int R, const v
  *                rows [ctx_len[i], ctx_len[i] + B) of sequence i, which the attention
  *                then reads with the context rows; those rows are scratch (the next
  *                dflash_ctx_project overwrites the committed ones).
- *   ctx_len      int32 [nb]: context rows per sequence (after this round's append);
+ *   ctx_len      int32 [nb]: context rows per sequence (after this step's append);
  *                ctx_len[i] + B must be <= Cmax.
  *   max_ctx_hint host int: an upper bound on every ctx_len[i] (0 = Cmax - B). A
  *                ctx_len[i] above min(hint, Cmax - B), or negative, is reported as
