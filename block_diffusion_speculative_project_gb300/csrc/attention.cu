@@ -623,8 +623,10 @@ constexpr int kMergeWarps = 8;
 template <int HD>
 __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const AttnParams p) {
   constexpr int E = HD / 32;
-  griddep_wait();
-  griddep_launch();
+  // The schedule (which CTAs share this pair) reads only ctx_len, written long before by
+  // the context append: the attention triggers this launch after its own
+  // griddepcontrol.wait, so every kernel before the attention has completed. It is
+  // computed before waiting for the attention, and pairs written whole return at once.
   const int pair = blockIdx.x;
   const int i = pair / p.Hkv, g = pair % p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -650,6 +652,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   const long long A = before * p.Hkv + (long long)g * U;
   const int c0 = attn_cta_of(T, Ge, A), c1 = attn_cta_of(T, Ge, A + U - 1);
   if (c0 == c1) return;  // written whole by the attention kernel
+  griddep_wait();
+  griddep_launch();
   const float sl2 = rsqrtf(static_cast<float>(HD)) * 1.4426950408889634f;
   {
     // one pass, rescaling to the running maximum (the partials' loads do not depend on
