@@ -163,16 +163,18 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
   uint64_t *s_full = kv_empty + kAttnStages;   // [2]
   uint64_t *s_empty = s_full + 2;              // [2]
   uint64_t *p_full = s_empty + 2;              // [4]: P of unit j in buffer j % 4
-  uint64_t *p_empty = p_full + 4;              // [4]
+  // [4]: PV of unit j (and every MMA before it) completed. Each buffer's phases are waited
+  // in order by the half that owns it, so one parity wait is exact for any PV that half
+  // has issued P for: the PV four units earlier is already known complete.
+  uint64_t *p_empty = p_full + 4;
   uint64_t *q_full = p_empty + 4;
   uint64_t *q_empty = q_full + 1;
-  uint64_t *o_done = q_empty + 1;             // [2]: PV into O_h completed
-  uint64_t *o_free = o_done + 2;              // both O read at a segment end
+  uint64_t *o_free = q_empty + 1;             // both O read at a segment end
   uint64_t *ml_ready = o_free + 1;            // half 1's (max, sum) written
   uint64_t *mma_done = ml_ready + 1;          // [2]: drain of the S and the PV issuer
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 2);
   int *sched = reinterpret_cast<int *>(tmem_slot + 1);  // [pair, unit, count]
-  static_assert((2 * kAttnStages + 2 + 2 + 4 + 4 + 2 + 2 + 4) * 8 + 4 + 12 <= C::OFF_ML - C::OFF_BAR,
+  static_assert((2 * kAttnStages + 2 + 2 + 4 + 4 + 2 + 4) * 8 + 4 + 12 <= C::OFF_ML - C::OFF_BAR,
                 "barrier region overflows");
   float2 *ml1 = reinterpret_cast<float2 *>(smem + C::OFF_ML);
 
@@ -196,8 +198,6 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    mbar_init(&o_done[0], 1);
-    mbar_init(&o_done[1], 1);
     mbar_init(o_free, HT);
     mbar_init(ml_ready, HT);
     mbar_init(&mma_done[0], 1);
@@ -397,7 +397,6 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
         for (int kk = 0; kk < kKeys / 16; ++kk)
           tc_mma_bf16_tmem_a(d_o, a_p + kk * 8, vd + static_cast<uint64_t>((kk * 16 * 128) >> 4), id_pv,
                              (!start || kk > 0) ? 1u : 0u);
-        tc_commit(&o_done[pb]);
         tc_commit(&p_empty[pq]);
         if (wp.slot == 1 || walk_last(wp)) tc_commit(&kv_empty[st]);  // last unit of its stage
         walk_next(wp, p);
@@ -476,7 +475,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
         }
         if (!first && __any_sync(0xffffffffu, need)) {
           // O_h *= alpha once PV of this half's previous unit has completed
-          ok = mbar_wait(&o_done[half], ((j >> 1) - 1) & 1, p.max_spin);
+          ok = mbar_wait(&p_empty[(j - 2) & 3], ((j - 2) >> 2) & 1, p.max_spin);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -540,7 +539,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
           // hand (max, sum) to half 0 once O_1 is final; the slot is free once half 0
           // has read the previous segment's
           ok = seg == 0 || mbar_wait(o_free, (seg - 1) & 1, p.max_spin);
-          if (ok && last_h[1] >= 0) ok = mbar_wait(&o_done[1], (last_h[1] >> 1) & 1, p.max_spin);
+          if (ok && last_h[1] >= 0) ok = mbar_wait(&p_empty[last_h[1] & 3], (last_h[1] >> 2) & 1, p.max_spin);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -549,7 +548,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
           tc_fence_before();
           mbar_arrive(ml_ready);
         } else {
-          ok = last_h[0] < 0 || mbar_wait(&o_done[0], (last_h[0] >> 1) & 1, p.max_spin);
+          ok = last_h[0] < 0 || mbar_wait(&p_empty[last_h[0] & 3], (last_h[0] >> 2) & 1, p.max_spin);
           if (ok) ok = mbar_wait(ml_ready, seg & 1, p.max_spin);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;

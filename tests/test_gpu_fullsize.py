@@ -41,6 +41,10 @@ STATED_FRACTION = 0.93
 _W = {}
 
 
+def f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
 def weights_for(w):
     key = (w.D, w.N, w.V, w.F, w.flags & (di.FLAG_CONV | di.FLAG_SELECT | di.FLAG_FILM))
     if key not in _W:
@@ -297,3 +301,52 @@ def test_fullsize_sampling_launch_shapes_qwen3_8b():
     assert len(np.unique(wt)) > 1
     assert dr.status() == 0
     print(f"sampling launch shapes: draws {dec.sum()}/{dec.size} exact; tau {list(otau)}; walk tau {list(wt)}")
+
+
+def test_fullsize_attention_repeats_bitwise_qwen3_8b_nb32():
+    """The attention stage at the 32-sequence Qwen3-8B shape (C = 4096, B = 16): 65 key
+    units per (sequence, kv head) pair over 152 CTAs, 109.5 units each, so some CTAs run
+    three segments, the last only a few units long, right after a whole pair. Each half's
+    final PV into O must have completed before O is read at a segment's end; a read that
+    runs ahead of it gives outputs that change from run to run. Four runs on the same
+    inputs must agree bit for bit, and sequences 0 and 4 (which hold such short segments,
+    on kv head 5) match the oracle."""
+    from block_diffusion_speculative_project_gb300 import drafter
+    w = di.QWEN3_8B.with_(name="attn_nb32", N=1, V=4096, L=1, nb=32, B=16)
+    nb, B, C = w.nb, w.B, 4096
+    Cmax = C + B
+    dev = {n: drafter.to_device_bf16(v) for n, v in di.make_weights(w).items()}
+    dr = drafter.Drafter(w, dev, nb, Cmax, B)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    dr.kcache.normal_(generator=g)
+    dr.vcache.normal_(generator=g)
+    sample = [0, 4]
+    kv = {}
+    for i in sample:
+        kb = di.normal_bf16(f"attn_k{i}", (w.Hkv, Cmax, w.hd), 1.0)
+        vb = di.normal_bf16(f"attn_v{i}", (w.Hkv, Cmax, w.hd), 1.0)
+        dr.kcache[0, i].copy_(drafter.to_device_bf16(kb))
+        dr.vcache[0, i].copy_(drafter.to_device_bf16(vb))
+        kv[i] = (orc.widen(kb), orc.widen(vb))
+    qb = di.normal_bf16("attn_q_nb32", (nb, B, w.Hq, w.hd), 1.0)
+    q = drafter.to_device_bf16(qb)
+    ctx = torch.full((nb,), C, dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(4):
+        o = torch.zeros(nb, B, w.Hq, w.hd, dtype=torch.bfloat16, device="cuda")
+        dr.attention(nb, 0, q, ctx, o, max_ctx_hint=C)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert dr.status() == 0
+    ref = outs[0].view(torch.int16)
+    for r in range(1, len(outs)):
+        diff = (outs[r].view(torch.int16) != ref).any(dim=(1, 3)).nonzero().tolist()
+        assert not diff, f"run {r}: (sequence, query head) outputs differ from run 0: {diff[:8]}"
+    qw = orc.widen(qb)
+    grp = w.Hq // w.Hkv
+    for i in sample:
+        K, V = kv[i]
+        want = np.stack([orc.softmax_attention(qw[i, :, h], K[h // grp], V[h // grp]) for h in range(w.Hq)], 1)
+        assert_close(f64(outs[0][i]), want, f"attention nb32 seq {i}")
+
