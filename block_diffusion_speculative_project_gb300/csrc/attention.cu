@@ -223,9 +223,10 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
     fence_proxy_async_smem();
   }
 
-  griddep_wait();
-  if (threadIdx.x == 0) griddep_launch();
-
+  // The schedule reads only ctx_len, final before any kernel of the drafter starts (the
+  // first one waits for the context append before it lets the next launch): it is
+  // computed while the QKV GEMM still runs; the q / k_b / v_b inputs are read after the
+  // griddepcontrol.wait below.
   if (warp == Ro::PRODUCER) {
     // Schedule: total units, this CTA's range, and the pair/unit it starts at.
     const long long T = attn_units_before(p, p.nb, lane);
@@ -275,6 +276,8 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
         if (c < 0 || c > p.max_ctx || c > p.Cmax - p.B) flag_status(p.status, kStatusCheck);
       }
   }
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
