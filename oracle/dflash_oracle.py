@@ -56,6 +56,9 @@ Readings where the pages are silent or disagree (each is listed in the design doc):
   * random numbers: Philox4x32-10 keyed by the 64-bit seed, counter (v // 4, row,
     stream, 0), output word v % 4; u = ((x >> 9) + 1/2) / 2^23 (exact in fp32, so both
     sides start from the same u); Gumbel g = -log(-log u).
+  * paged cache: the projected K/V of a sequence sit in pages of PAGE_ROWS = 64 rows (one
+    attention key unit); a per-sequence block table names the page of each run of 64
+    rows, so sequences with a common prefix can point at the same pages.
 
 Parity status: every function here is pinned by tests/test_oracle.py (closed forms,
 invariants, brute force on tiny inputs, the pages' worked examples under tests/golden/).
@@ -199,6 +202,36 @@ class KVCache:
     def __init__(self, N: int, nb: int, Hkv: int, Cmax: int, hd: int, dtype=np.float64):
         self.K = [[np.zeros((Hkv, Cmax, hd), dtype) for _ in range(nb)] for _ in range(N)]
         self.V = [[np.zeros((Hkv, Cmax, hd), dtype) for _ in range(nb)] for _ in range(N)]
+
+
+PAGE_ROWS = 64
+
+
+def paged_rows(pool: np.ndarray, table, i: int, n_rows: int, page_rows: int = PAGE_ROWS) -> np.ndarray:
+    """Rows 0..n_rows-1 of sequence i, read from a paged pool of one layer.
+
+    [DFlash] 四、推理流程, the engineering note: the drafter's cache holds the projected
+    K/V, and requests that share a prefix reuse them through a radix cache. Reading: the
+    cache is cut into pages of page_rows rows, pool [P][Hkv][page_rows][hd], and table[i][q]
+    names the page that holds rows q*page_rows .. (q+1)*page_rows - 1 of sequence i.
+    Returns [Hkv][n_rows][hd].
+    """
+    out = np.empty((pool.shape[1], n_rows, pool.shape[3]), pool.dtype)
+    for r in range(n_rows):
+        out[:, r, :] = pool[table[i][r // page_rows], :, r % page_rows, :]
+    return out
+
+
+def cache_from_pages(poolK: np.ndarray, poolV: np.ndarray, table, nb: int, Cmax: int) -> KVCache:
+    """The per-sequence cache a paged pool and block table describe. poolK, poolV:
+    [N][P][Hkv][PAGE_ROWS][hd]; sequence i of the result is rows 0..Cmax-1 of table row i."""
+    N, _, Hkv, _, hd = poolK.shape
+    c = KVCache(N, nb, Hkv, Cmax, hd, poolK.dtype)
+    for n in range(N):
+        for i in range(nb):
+            c.K[n][i][:] = paged_rows(poolK[n], table, i, Cmax)
+            c.V[n][i][:] = paged_rows(poolV[n], table, i, Cmax)
+    return c
 
 
 # ----------------------------------------------------------------------------- step

@@ -339,6 +339,60 @@ def test_ctx_project_cache_rows():
         assert not cache.K[n][0][:, 8:].any() and not cache.K[n][0][:, :5].any()
 
 
+# ----------------------------------------------------------------------------- paged cache
+
+def test_paged_rows_hand_case():
+    """Pages of 4 rows, 2 heads, hd 1; pool[p, h, r] = 100 p + 10 h + r. Table row 0 is
+    [2, 0]: its rows 0..3 come from page 2, rows 4..7 from page 0."""
+    pool = np.array([[[[100.0 * p + 10 * h + r] for r in range(4)] for h in range(2)] for p in range(4)])
+    table = [[2, 0], [1, 3]]
+    got = orc.paged_rows(pool, table, 0, 7, page_rows=4)
+    assert got.shape == (2, 7, 1)
+    assert got[0, :, 0].tolist() == [200, 201, 202, 203, 0, 1, 2]
+    assert got[1, :, 0].tolist() == [210, 211, 212, 213, 10, 11, 12]
+    got = orc.paged_rows(pool, table, 1, 8, page_rows=4)
+    assert got[1, :, 0].tolist() == [110, 111, 112, 113, 310, 311, 312, 313]
+
+
+def test_paged_identity_table_is_the_contiguous_layout():
+    """With table[i][q] = i * pages_per_seq + q the pool is the contiguous cache
+    [nb][Hkv][Cmax][hd] cut into pages: a reshape, whatever the contents."""
+    rng = np.random.default_rng(31)
+    N, nb, Hkv, pps, hd = 2, 3, 2, 3, 4
+    Cmax = pps * orc.PAGE_ROWS
+    poolK = rng.standard_normal((N, nb * pps, Hkv, orc.PAGE_ROWS, hd))
+    poolV = rng.standard_normal((N, nb * pps, Hkv, orc.PAGE_ROWS, hd))
+    table = [[i * pps + q for q in range(pps)] for i in range(nb)]
+    c = orc.cache_from_pages(poolK, poolV, table, nb, Cmax)
+    contK = poolK.reshape(N, nb, pps, Hkv, orc.PAGE_ROWS, hd).transpose(0, 1, 3, 2, 4, 5)
+    contK = contK.reshape(N, nb, Hkv, Cmax, hd)
+    contV = poolV.reshape(N, nb, pps, Hkv, orc.PAGE_ROWS, hd).transpose(0, 1, 3, 2, 4, 5)
+    contV = contV.reshape(N, nb, Hkv, Cmax, hd)
+    for n in range(N):
+        for i in range(nb):
+            assert np.array_equal(c.K[n][i], contK[n, i])
+            assert np.array_equal(c.V[n][i], contV[n, i])
+
+
+def test_paged_relabelling_and_shared_prefix():
+    """Renaming the physical pages (pool and table permuted together) changes no logical
+    row; two sequences whose tables share their first pages read the same prefix rows."""
+    rng = np.random.default_rng(32)
+    P, Hkv, hd = 6, 2, 3
+    pool = rng.standard_normal((P, Hkv, orc.PAGE_ROWS, hd))
+    table = [[4, 1, 5], [4, 1, 0]]
+    perm = rng.permutation(P)                      # page q moves to slot perm[q]
+    pool2 = np.empty_like(pool)
+    pool2[perm] = pool
+    table2 = [[int(perm[q]) for q in row] for row in table]
+    n = 3 * orc.PAGE_ROWS
+    for i in range(2):
+        assert np.array_equal(orc.paged_rows(pool, table, i, n), orc.paged_rows(pool2, table2, i, n))
+    a, b = orc.paged_rows(pool, table, 0, n), orc.paged_rows(pool, table, 1, n)
+    assert np.array_equal(a[:, :2 * orc.PAGE_ROWS], b[:, :2 * orc.PAGE_ROWS])
+    assert not np.array_equal(a[:, 2 * orc.PAGE_ROWS:], b[:, 2 * orc.PAGE_ROWS:])
+
+
 # ----------------------------------------------------------------------------- FiLM relay
 
 def test_layer_norm_closed_forms():
