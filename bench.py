@@ -191,12 +191,17 @@ def run_gpu(args, rank, world):
         tp = (a + 1).astype(np.int32)
     base = (ctx - tp).astype(np.int32)
     Cmax = int(ctx.max()) + w.B
+    if w.paged:
+        Cmax = -(-Cmax // di.PAGE_ROWS) * di.PAGE_ROWS
     t0 = time.time()
     bits = di.make_weights(w, seed)
     weights = {k: to_device_bf16(v, dev) for k, v in bits.items()}
     t_gen = time.time() - t0
-    dr = Drafter(w, weights, w.nb, Cmax, max(PROJ_CHUNK, PREFILL_ROWS, w.B))
+    num_pages = w.nb * (Cmax // di.PAGE_ROWS) if w.paged else 0
+    dr = Drafter(w, weights, w.nb, Cmax, max(PROJ_CHUNK, PREFILL_ROWS, w.B), num_pages=num_pages)
     i32 = lambda x: torch.tensor(np.asarray(x, np.int32), device=dev)
+    if w.paged:  # every sequence's pages in a seeded shuffled order
+        dr.set_block_table(i32(di.block_table(w.nb, Cmax, seed)))
 
     # prefill C_i - tau_prev_i context rows per sequence (outside every timed region)
     g = torch.Generator(device=dev)

@@ -325,11 +325,32 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
-          const int row = p.layer_row0 + (i * p.Hkv + g) * p.Cmax + w.unit * kKeys;
           uint8_t *kt = sKV + st * C::STAGE;
-          tma_load_3d(kt, &p.tmK, &kv_full[st], 0, row, 0, pol_kv);
-          tma_load_3d(kt + C::KV_TILE, &p.tmV, &kv_full[st], 0, row, 0, pol_kv);
+          if (p.page_table == nullptr) {
+            mbar_arrive_expect_tx(&kv_full[st], C::STAGE);
+            const int row = p.layer_row0 + (i * p.Hkv + g) * p.Cmax + w.unit * kKeys;
+            tma_load_3d(kt, &p.tmK, &kv_full[st], 0, row, 0, pol_kv);
+            tma_load_3d(kt + C::KV_TILE, &p.tmV, &kv_full[st], 0, row, 0, pol_kv);
+          } else {
+            // paged: each unit is one page; its 64 rows of every atom land where the
+            // two-unit copy puts them (atom a, unit slot u)
+            const int nu = walk_last(w) ? 1 : 2;
+            mbar_arrive_expect_tx(&kv_full[st], static_cast<uint32_t>(nu * 2 * C::ATOMS * C::UNIT_KV));
+            for (int u = 0; u < nu; ++u) {
+              int pg = p.page_table[(long long)i * p.pages_per_seq + w.unit + u];
+              if (pg < 0 || pg >= p.num_pages) {
+                flag_status(p.status, kStatusCheck);
+                pg = 0;
+              }
+              const int row = p.layer_row0 + (pg * p.Hkv + g) * kPageRows;
+#pragma unroll
+              for (int a = 0; a < C::ATOMS; ++a) {
+                uint8_t *dst = kt + a * C::ATOM_KV + u * C::UNIT_KV;
+                tma_load_3d(dst, &p.tmK, &kv_full[st], 0, row, a, pol_kv);
+                tma_load_3d(dst + C::KV_TILE, &p.tmV, &kv_full[st], 0, row, a, pol_kv);
+              }
+            }
+          }
           stages = w.stage + 1;
         }
         walk_next(w, p);

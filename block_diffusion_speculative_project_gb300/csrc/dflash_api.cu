@@ -143,6 +143,7 @@ struct dflash_handle_s {
   std::vector<CUtensorMap> tm_c0, tm_c1;  // [layer*4 + which]
   float inv_freq[64];
   WsLayout ws;
+  const int32_t *block_table = nullptr;  // paged caches: [max_batch][Cmax / kPageRows]
 };
 
 namespace {
@@ -244,8 +245,27 @@ int run_gemm(const dflash_handle_s *h, GemmParams &p, int BN, cudaStream_t s) {
 
 const uint16_t *bf(const void *p) { return static_cast<const uint16_t *>(p); }
 
-size_t cache_layer_elems(const dflash_config &c) {
-  return (size_t)c.max_batch * c.Hkv * c.Cmax * c.hd;
+// Cache rows (of hd elements) of one layer: [max_batch][Hkv][Cmax], or the page pool
+// [num_pages][Hkv][kPageRows].
+size_t cache_layer_rows(const dflash_config &c) {
+  return c.num_pages > 0 ? (size_t)c.num_pages * c.Hkv * kPageRows : (size_t)c.max_batch * c.Hkv * c.Cmax;
+}
+size_t cache_layer_elems(const dflash_config &c) { return cache_layer_rows(c) * c.hd; }
+
+// A call that touches a paged cache needs the block table.
+int check_paging(const dflash_handle_s *h) {
+  if (h->cfg.num_pages > 0 && !h->block_table)
+    return fail(DFLASH_ERR_INVALID_ARG, "paged caches need dflash_set_block_table first");
+  return DFLASH_OK;
+}
+
+// Page-table fields of a GEMM that writes cache rows.
+void set_paging(const dflash_handle_s *h, GemmParams &p) {
+  const auto &c = h->cfg;
+  p.page_table = c.num_pages > 0 ? h->block_table : nullptr;
+  p.pages_per_seq = c.Cmax / kPageRows;
+  p.num_pages = c.num_pages;
+  p.layer_rows = (long long)cache_layer_rows(c);
 }
 
 // Attention launch parameters for nb sequences: q rows of stride ldq (elements) with
@@ -256,11 +276,17 @@ int attention_params(const dflash_handle_s *h, const Ws &w, int nb, const void *
   const auto &c = h->cfg;
   AttnParams &ap = *out;
   DF_TRY(encode_3d(&ap.tmQ, q, c.hd, c.Hq, (uint64_t)nb * c.B, c.hd, ldq, c.Hq / c.Hkv, c.B));
-  const uint64_t cache_rows = (uint64_t)c.N * c.max_batch * c.Hkv * c.Cmax;
+  const uint64_t cache_rows = (uint64_t)c.N * cache_layer_rows(c);
+  const bool paged = c.num_pages > 0;
   // {64 of hd, cache rows, hd/64 halves}: one box = 128 rows of every half, stacked
-  // half after half as the MMA reads them
-  DF_TRY(encode_3d(&ap.tmK, kcache, 64, cache_rows, c.hd / 64, c.hd, 64, 128, c.hd / 64));
-  DF_TRY(encode_3d(&ap.tmV, vcache, 64, cache_rows, c.hd / 64, c.hd, 64, 128, c.hd / 64));
+  // half after half as the MMA reads them; paged: one box = one page (64 rows) of one half
+  DF_TRY(encode_3d(&ap.tmK, kcache, 64, cache_rows, c.hd / 64, c.hd, 64, paged ? 64 : 128,
+                   paged ? 1 : c.hd / 64));
+  DF_TRY(encode_3d(&ap.tmV, vcache, 64, cache_rows, c.hd / 64, c.hd, 64, paged ? 64 : 128,
+                   paged ? 1 : c.hd / 64));
+  ap.page_table = paged ? h->block_table : nullptr;
+  ap.pages_per_seq = c.Cmax / kPageRows;
+  ap.num_pages = c.num_pages;
   ap.ctx_len = ctx_len;
   ap.o = static_cast<uint16_t *>(o);
   ap.part_o = w.at<float>(h->ws.apart);
@@ -365,6 +391,13 @@ int dflash_create(const dflash_config *cfg, dflash_handle_t *out) {
   if (c.Cmax <= c.B) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "Cmax must exceed B");
   if ((long long)c.N * c.max_batch * c.Hkv * c.Cmax >= (1LL << 31))
     return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "N*max_batch*Hkv*Cmax cache rows must be < 2^31");
+  if (c.num_pages < 0) return fail(DFLASH_ERR_INVALID_ARG, "num_pages must be >= 0");
+  if (c.num_pages > 0) {
+    if (c.Cmax % kPageRows)
+      return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "a paged cache needs Cmax %% %d == 0", kPageRows);
+    if ((long long)c.N * c.num_pages * c.Hkv * kPageRows >= (1LL << 31))
+      return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "N*num_pages*Hkv*%d cache rows must be < 2^31", kPageRows);
+  }
   if (c.k_top < 1 || c.k_top > kTopkMax) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "k_top must be in 1..16");
   if (c.D % 64 || (c.L * c.Dt) % 64 || (c.Hq * c.hd) % 64 || c.F % 8)
     return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "D, L*Dt, Hq*hd must be multiples of 64 and F of 8");
@@ -468,6 +501,15 @@ int dflash_set_weights(dflash_handle_t h, const dflash_weights *w) {
   return DFLASH_OK;
 }
 
+int dflash_set_block_table(dflash_handle_t h, const int32_t *table) {
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle must be non-NULL");
+  if (h->cfg.num_pages <= 0) return fail(DFLASH_ERR_INVALID_ARG, "the handle's caches are not paged");
+  if (!table || reinterpret_cast<uintptr_t>(table) % 4)
+    return fail(DFLASH_ERR_INVALID_ARG, "block table must be a non-NULL 4-byte aligned device pointer");
+  h->block_table = table;
+  return DFLASH_OK;
+}
+
 int dflash_status(dflash_handle_t h, void *ws, dflash_stream_t stream, int *code) {
   if (!h || !ws || !code) return fail(DFLASH_ERR_INVALID_ARG, "handle, ws and code must be non-NULL");
   int v = 0;
@@ -489,6 +531,7 @@ int ctx_project_impl(dflash_handle_t h, int nb, int R, const void *hv, const int
   if (nb < 0 || nb > c.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "nb=%d outside [0, max_batch]", nb);
   if (R < 0 || R > c.max_proj_rows) return fail(DFLASH_ERR_INVALID_ARG, "R=%d outside [0, max_proj_rows]", R);
   if (nb == 0 || R == 0) return DFLASH_OK;
+  DF_TRY(check_paging(h));
   if (!hv || !n_commit || !ctx_len || !kcache || !vcache)
     return fail(DFLASH_ERR_INVALID_ARG, "hv, n_commit, ctx_len and the caches must be non-NULL");
   if (relay_a && !(c.flags & DFLASH_FLAG_RELAY))
@@ -534,6 +577,7 @@ int ctx_project_impl(dflash_handle_t h, int nb, int R, const void *hv, const int
     p.Hkv = c.Hkv;
     p.Cmax = c.Cmax;
     p.max_batch = c.max_batch;
+    set_paging(h, p);
     DF_TRY(run_gemm(h, p, kBN, s));
   }
   const bool film = relay_b != nullptr;
@@ -614,6 +658,7 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
   if (nb == 0) return DFLASH_OK;
   if (!block_ids || !kcache || !vcache || !ctx_len || !out_hidden)
     return fail(DFLASH_ERR_INVALID_ARG, "block_ids, caches, ctx_len and out_hidden must be non-NULL");
+  DF_TRY(check_paging(h));
   if (x0_relay && !(c.flags & DFLASH_FLAG_RELAY))
     return fail(DFLASH_ERR_INVALID_ARG, "x0_relay given but DFLASH_FLAG_RELAY is not set");
   if (max_ctx_hint < 0 || max_ctx_hint > c.Cmax)
@@ -693,10 +738,11 @@ int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, cons
       p.vc = vc_n;
       p.Hkv = c.Hkv;
       p.Cmax = c.Cmax;
+      set_paging(h, p);
       if (n > 0) defer_in(p);
       DF_TRY(run_gemm(h, p, kBN, s));
     }
-    ap.layer_row0 = n * c.max_batch * c.Hkv * c.Cmax;
+    ap.layer_row0 = static_cast<int>(n * cache_layer_rows(c));
     DF_CUDA(launch_attention(ap, s));
     {  // x += o W_O^T
       GemmParams p = base_params(h, w);
@@ -916,12 +962,13 @@ int dflash_attention(dflash_handle_t h, int nb, int layer, const void *q, const 
     return fail(DFLASH_ERR_INVALID_ARG, "max_ctx_hint=%d outside [0, Cmax]", max_ctx_hint);
   if (nb == 0) return DFLASH_OK;
   if (!q || !kcache || !vcache || !ctx_len || !out_o) return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor");
+  DF_TRY(check_paging(h));
   DF_TRY(check_ws(h, ws, ws_bytes));
   Ws w{static_cast<uint8_t *>(ws), h->ws};
   const int max_ctx = max_ctx_hint > 0 ? std::min(max_ctx_hint, c.Cmax - c.B) : c.Cmax - c.B;
   AttnParams ap{};
   DF_TRY(attention_params(h, w, nb, q, c.Hq * c.hd, kcache, vcache, ctx_len, max_ctx, out_o, &ap));
-  ap.layer_row0 = layer * c.max_batch * c.Hkv * c.Cmax;
+  ap.layer_row0 = static_cast<int>(layer * cache_layer_rows(c));
   DF_CUDA(launch_attention(ap, stream));
   return DFLASH_OK;
 }

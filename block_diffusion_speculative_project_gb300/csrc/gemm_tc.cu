@@ -218,6 +218,16 @@ __device__ __forceinline__ void rope_sincos(float angle, float *sn, float *cs) {
   __sincosf(r, sn, cs);
 }
 
+// Row of (sequence, kv head, position) inside one layer's cache, in units of hd elements:
+// [max_batch][Hkv][Cmax] contiguous, or through the page table [num_pages][Hkv][kPageRows].
+// -1 when the page table names a page outside the pool (the caller skips the row).
+__device__ __forceinline__ long long cache_row(const GemmParams &p, int seq, int head, int pos) {
+  if (p.page_table == nullptr) return ((long long)seq * p.Hkv + head) * p.Cmax + pos;
+  const int pg = p.page_table[(long long)seq * p.pages_per_seq + pos / kPageRows];
+  if (pg < 0 || pg >= p.num_pages) return -1;
+  return ((long long)pg * p.Hkv + head) * kPageRows + pos % kPageRows;
+}
+
 __device__ __forceinline__ void rope_pair(const GemmParams &p, int pos, int d0, float (&a)[32],
                                           float (&b)[32]) {
   const float fpos = static_cast<float>(pos);
@@ -376,8 +386,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
           const int kvh = (gcol - p.q_cols) / p.hd;  // 0..2*Hkv-1
           const bool isv = kvh >= p.Hkv;
           const int head = isv ? kvh - p.Hkv : kvh;
-          o = static_cast<uint16_t *>(isv ? p.vc : p.kc) +
-              (((size_t)seq * p.Hkv + head) * p.Cmax + pos) * (size_t)p.hd;
+          const long long cr = cache_row(p, seq, head, pos);
+          if (cr >= 0)
+            o = static_cast<uint16_t *>(isv ? p.vc : p.kc) + cr * p.hd;
+          else
+            flag_status(p.status, kStatusCheck);
         } else {
           flag_status(p.status, kStatusCheck);
         }
@@ -456,9 +469,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
         fetch((h0 + cc) >> 5, a);
         fetch((h0 + half + cc) >> 5, b);
         if (live && head < p.Hkv) {
+          const long long cr = cache_row(p, seq, head, pos);
+          if (cr < 0) {
+            flag_status(p.status, kStatusCheck);
+            continue;
+          }
           if (isk) rope_pair(p, pos, cc, a, b);
-          uint16_t *o = cache + ((((size_t)layer * p.max_batch + seq) * p.Hkv + head) * p.Cmax + pos) *
-                                    (size_t)p.hd;
+          uint16_t *o = cache + (layer * p.layer_rows + cr) * p.hd;
           store_bf16_32(o + cc, a, 32);
           store_bf16_32(o + half + cc, b, 32);
         }

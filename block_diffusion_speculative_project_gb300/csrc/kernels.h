@@ -52,6 +52,7 @@ constexpr int kStatusTimeout = 1;  // a bounded wait ran out
 constexpr int kStatusCheck = 2;    // a bounds check failed (index skipped)
 
 constexpr int kNumSMsDefault = 152;
+constexpr int kPageRows = 64;      // rows per page of a paged cache (one attention key unit)
 
 // ---------------------------------------------------------------- GEMM engine
 
@@ -104,6 +105,13 @@ struct GemmParams {
   void *vc;
   const int *n_commit;
   int Hkv, Cmax, max_batch;
+  // Paged cache (page_table non-null): row pos of sequence seq lives in page
+  // page_table[seq * pages_per_seq + pos / kPageRows], row pos % kPageRows; a page holds
+  // the kPageRows rows of every kv head. Pages outside [0, num_pages) are reported and
+  // not written.
+  const int *page_table;
+  int pages_per_seq, num_pages;
+  long long layer_rows;  // EPI_KV: cache rows of one layer (the layer stride, in rows)
   // top-k (EPI_TOPK)
   int topk_k;
   int tiles_per_cta;
@@ -240,7 +248,11 @@ struct AttnParams {
   float *part_o;        // [slots][G*B rows][hd] unnormalised partial outputs
   float *part_ml;       // [slots][G*B rows][2] (running max, running sum)
   int nb, B, Hq, Hkv, hd, Cmax, max_batch;
-  int layer_row0;       // first cache row of this layer: layer * max_batch * Hkv * Cmax
+  int layer_row0;       // first cache row of this layer: layer * (rows of one layer)
+  // Paged cache (page_table non-null): tmK / tmV are {64, pool rows, hd/64} with box
+  // {64, 64, 1}, and unit u of sequence i is page page_table[i * pages_per_seq + u].
+  const int *page_table;
+  int pages_per_seq, num_pages;
   int max_ctx;          // caller's bound on ctx_len (larger values are reported and clamped)
   int grid;             // CTAs of the attention launch (work is split evenly over them)
   int *status;

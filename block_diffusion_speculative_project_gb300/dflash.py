@@ -39,7 +39,11 @@ class dflash_config(ctypes.Structure):
         ("rope_base", ctypes.c_float), ("eps", ctypes.c_float)] + [
         (n, ctypes.c_int) for n in ("mask_id", "Cmax", "max_batch", "max_proj_rows", "conv_group",
                                     "sel_dim")] + [
-        ("flags", ctypes.c_uint), ("max_spin", ctypes.c_int), ("film_dim", ctypes.c_int)]
+        ("flags", ctypes.c_uint), ("max_spin", ctypes.c_int), ("film_dim", ctypes.c_int),
+        ("num_pages", ctypes.c_int)]
+
+
+DFLASH_PAGE_ROWS = 64
 
 
 _P = ctypes.c_void_p
@@ -66,6 +70,7 @@ def _load():
         "dflash_create": (i, [ctypes.POINTER(dflash_config), ctypes.POINTER(p)]),
         "dflash_destroy": (i, [p]),
         "dflash_set_weights": (i, [p, ctypes.POINTER(dflash_weights)]),
+        "dflash_set_block_table": (i, [p, p]),
         "dflash_workspace_size": (i, [p, ctypes.POINTER(sz)]),
         "dflash_status": (i, [p, p, p, ctypes.POINTER(i)]),
         "dflash_last_error": (ctypes.c_char_p, []),
@@ -99,7 +104,8 @@ def _load():
 
 
 LIB = _load()
-EXPORTED = ("dflash_create", "dflash_destroy", "dflash_set_weights", "dflash_workspace_size",
+EXPORTED = ("dflash_create", "dflash_destroy", "dflash_set_weights", "dflash_set_block_table",
+            "dflash_workspace_size",
             "dflash_status", "dflash_last_error", "dflash_ctx_project", "dflash_ctx_project_film",
             "dflash_draft_block",
             "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_attention", "dflash_topk", "dflash_accept", "dflash_sample", "dflash_verify_sample",
@@ -137,6 +143,11 @@ def dflash_destroy(h) -> None:
 
 def dflash_set_weights(h, w: dflash_weights) -> None:
     _check(LIB.dflash_set_weights(h, ctypes.byref(w)))
+
+
+def dflash_set_block_table(h, table) -> None:
+    """table: int32 device tensor [max_batch, Cmax / DFLASH_PAGE_ROWS] (borrowed)."""
+    _check(LIB.dflash_set_block_table(h, _ptr(table)))
 
 
 def dflash_workspace_size(h) -> int:

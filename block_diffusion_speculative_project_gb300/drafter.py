@@ -20,7 +20,9 @@ def to_device_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
 
 
 class Drafter:
-    """One handle with its caches [N, max_batch, Hkv, Cmax, hd] and workspace.
+    """One handle with its caches [N, max_batch, Hkv, Cmax, hd] and workspace; with
+    ``num_pages`` > 0 the caches are page pools [N, num_pages, Hkv, 64, hd] read and
+    written through the block table given to ``set_block_table``.
 
     ``shape`` is any object with the workload fields D, Dt, L, N, Hq, Hkv, hd, F, V,
     B, k_top, rope_base, eps, mask_id, flags, conv_group, sel_dim and film_width.
@@ -29,14 +31,15 @@ class Drafter:
     """
 
     def __init__(self, shape, weights: dict, max_batch: int, Cmax: int, max_proj_rows: int,
-                 max_spin: int = 0, device="cuda"):
+                 max_spin: int = 0, device="cuda", num_pages: int = 0):
         self.shape = shape
         s = shape
         self.cfg = _d.dflash_config(
             D=s.D, Dt=s.Dt, L=s.L, N=s.N, Hq=s.Hq, Hkv=s.Hkv, hd=s.hd, F=s.F, V=s.V, B=s.B,
             k_top=s.k_top, rope_base=s.rope_base, eps=s.eps, mask_id=s.mask_id, Cmax=Cmax,
             max_batch=max_batch, max_proj_rows=max_proj_rows, conv_group=s.conv_group,
-            sel_dim=s.sel_dim, flags=s.flags, max_spin=max_spin, film_dim=s.film_width)
+            sel_dim=s.sel_dim, flags=s.flags, max_spin=max_spin, film_dim=s.film_width,
+            num_pages=num_pages)
         self.h = _d.dflash_create(self.cfg)
         self.weights = weights
         P = lambda name: ctypes.c_void_p(weights[name].data_ptr()) if name in weights else None
@@ -58,10 +61,20 @@ class Drafter:
         _d.dflash_set_weights(self.h, self.wstruct)
         nbytes = _d.dflash_workspace_size(self.h)
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
-        cshape = (s.N, max_batch, s.Hkv, Cmax, s.hd)
+        cshape = ((s.N, num_pages, s.Hkv, _d.DFLASH_PAGE_ROWS, s.hd) if num_pages > 0
+                  else (s.N, max_batch, s.Hkv, Cmax, s.hd))
         self.kcache = torch.zeros(cshape, dtype=torch.bfloat16, device=device)
         self.vcache = torch.zeros(cshape, dtype=torch.bfloat16, device=device)
         self.max_batch, self.Cmax, self.max_proj_rows = max_batch, Cmax, max_proj_rows
+        self.num_pages = num_pages
+        self.block_table = None
+
+    def set_block_table(self, table: torch.Tensor):
+        """Register the int32 device block table [max_batch, Cmax / 64] (kept alive here)."""
+        assert table.dtype == torch.int32 and table.is_cuda and table.is_contiguous()
+        assert tuple(table.shape) == (self.max_batch, self.Cmax // _d.DFLASH_PAGE_ROWS)
+        self.block_table = table
+        _d.dflash_set_block_table(self.h, table)
 
     def __del__(self):
         try:

@@ -70,6 +70,7 @@ class Workload:
     conv_group: int = 16
     film_dim: int = 0  # hidden width of the FiLM relay MLP; 0 = D/4
     temperature: float = 0.0  # 0: greedy draft and exact-match accept; > 0: sampling
+    paged: bool = False  # caches as pools of 64-row pages behind a block table
 
     @property
     def film_width(self) -> int:
@@ -100,10 +101,22 @@ FILM_RELAY = QWEN3_8B.with_(name="qwen3_8b_shaped_film_relay_b16_c4096_nb32", nb
 SAMPLING_T1 = QWEN3_8B.with_(name="qwen3_8b_shaped_sampling_t1_b16_c4096_nb8", temperature=1.0)
 DFLASH2_SAMPLING_T1 = QWEN3_8B.with_(name="qwen3_8b_shaped_dflash2_sampling_t1_b16_c4096_nb8",
                                      temperature=1.0, flags=FLAG_CONV | FLAG_SELECT)
+PAGED_KV = QWEN3_8B.with_(name="qwen3_8b_shaped_paged_kv_b16_c4096_nb8", paged=True)
+PAGED_KV_NB64 = SWEEP_NB64.with_(name="qwen3_8b_shaped_paged_kv_b8_ragged1024_8192_nb64", paged=True)
 
 WORKLOADS = {w.name: w for w in (TINY, QWEN3_4B, QWEN3_8B, SWEEP_NB16, SWEEP_NB32,
                                   SWEEP_NB64, RELAY_DFLASH2, FILM_RELAY, SAMPLING_T1,
-                                  DFLASH2_SAMPLING_T1)}
+                                  DFLASH2_SAMPLING_T1, PAGED_KV, PAGED_KV_NB64)}
+
+PAGE_ROWS = 64
+
+
+def block_table(nb: int, Cmax: int, seed: int = 0, name: str = "pages") -> np.ndarray:
+    """int32 [nb, Cmax / 64]: every sequence's pages, handed out in a seeded random order
+    (as a free list that has seen many requests come and go would), no page shared."""
+    pps = Cmax // PAGE_ROWS
+    g = np.random.Generator(np.random.PCG64(_seedseq(name, seed)))
+    return g.permutation(nb * pps).astype(np.int32).reshape(nb, pps)
 
 
 # --------------------------------------------------------------------------- streams

@@ -26,6 +26,16 @@
  * KV cache layout (both K and V): bf16 [N][max_batch][Hkv][Cmax][hd]; sequence i of
  * a call uses slot i. K rows hold RoPE-rotated keys.
  *
+ * Paged KV cache (cfg.num_pages > 0; reading of [DFlash] 四、推理流程, the engineering
+ * note: the projected K/V are what the drafter's cache keeps, and requests with a common
+ * prefix reuse them through a radix cache): both caches are pools of pages,
+ * bf16 [N][num_pages][Hkv][DFLASH_PAGE_ROWS][hd]. Row r of sequence i (every layer, every
+ * kv head) is row r % DFLASH_PAGE_ROWS of page table[i][r / DFLASH_PAGE_ROWS] of the
+ * block table registered by dflash_set_block_table. Sequences may share pages for rows
+ * that no call of the step writes (a common prefix); the rows a call appends (context
+ * rows ctx_len .. ctx_len + n_commit - 1, block rows ctx_len .. ctx_len + B - 1) must
+ * lie in pages no other sequence of the call reads or writes.
+ *
  * Block layout (reading of [DFlash] 符号约定 and 四、推理流程): block i is
  * [anchor, mask_id x (B-1)] at absolute positions ctx_len[i] .. ctx_len[i]+B-1,
  * where ctx_len counts the context rows in the cache; offsets 1..B-1 carry the
@@ -93,7 +103,12 @@ typedef struct dflash_config {
   unsigned flags;     /* DFLASH_FLAG_* */
   int max_spin;       /* iteration bound of every device-side wait; 0 = default */
   int film_dim;       /* FILM: hidden width of the relay MLP, multiple of 64 */
+  int num_pages;      /* 0: contiguous caches; > 0: paged caches of this many pages
+                         (Cmax a multiple of DFLASH_PAGE_ROWS; see the layout above) */
 } dflash_config;
+
+/* Rows per page of a paged cache (one 64-key unit of the attention). */
+#define DFLASH_PAGE_ROWS 64
 
 typedef struct dflash_layer_weights {
   const void *W_qkv;  /* bf16 [(Hq+2*Hkv)*hd, D]: rows q heads, then k_b heads, then v_b heads */
@@ -140,6 +155,15 @@ DFLASH_API int dflash_destroy(dflash_handle_t h);
  * matrix. All pointers must be 16-byte aligned; optional groups (conv, selector,
  * FiLM relay) must be non-NULL when their flag is set. */
 DFLASH_API int dflash_set_weights(dflash_handle_t h, const dflash_weights *w);
+
+/* Register the block table of a paged cache (borrowed device pointer, int32
+ * [max_batch][Cmax / DFLASH_PAGE_ROWS], 4-byte aligned). Kernels read it when they run,
+ * so the caller may change entries between calls in stream order. Every call that
+ * touches the caches needs it when cfg.num_pages > 0 (DFLASH_ERR_INVALID_ARG before
+ * any launch otherwise). An entry outside [0, num_pages) that a call reaches is
+ * reported as DFLASH_ERR_DEVICE_CHECK by dflash_status: its rows are not written and
+ * are read from page 0. DFLASH_ERR_INVALID_ARG for a contiguous handle. */
+DFLASH_API int dflash_set_block_table(dflash_handle_t h, const int32_t *table);
 
 /* Bytes of workspace every step call of this handle needs (sized for max_batch,
  * max_proj_rows and Cmax). The caller allocates it (256-byte aligned). */

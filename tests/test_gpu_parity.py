@@ -29,12 +29,14 @@ def lib():
     return dflash, drafter
 
 
-def make(w, Cmax, max_proj_rows, seed=0, max_batch=None, max_spin=0, flags_extra=0, bits=None):
+def make(w, Cmax, max_proj_rows, seed=0, max_batch=None, max_spin=0, flags_extra=0, bits=None,
+         num_pages=0):
     _, drafter = lib()
     bits = di.make_weights(w, seed) if bits is None else bits
     dev = {k: drafter.to_device_bf16(v) for k, v in bits.items()}
     shape = w.with_(flags=w.flags | flags_extra) if flags_extra else w
-    dr = drafter.Drafter(shape, dev, max_batch or w.nb, Cmax, max_proj_rows, max_spin=max_spin)
+    dr = drafter.Drafter(shape, dev, max_batch or w.nb, Cmax, max_proj_rows, max_spin=max_spin,
+                         num_pages=num_pages)
     return dr, orc.widen_all(bits), bits
 
 
