@@ -56,3 +56,34 @@ def test_film_relay_config_is_validated_without_gpu():
             raise AssertionError(f"flags={flags} film_dim={film_dim} must be rejected")
         except dflash.DflashError as e:
             assert e.code == code, (flags, film_dim, e)
+
+
+def test_paged_config_is_validated_without_gpu():
+    from block_diffusion_speculative_project_gb300 import dflash
+    base = dict(D=256, Dt=256, L=5, N=2, Hq=4, Hkv=4, hd=64, F=688, V=4096, B=8, k_top=16,
+                rope_base=1e4, eps=1e-6, mask_id=4095, max_batch=1, max_proj_rows=64,
+                conv_group=16, sel_dim=256)
+    for Cmax, num_pages, code in ((80, 4, dflash.DFLASH_ERR_UNSUPPORTED_SHAPE),   # Cmax % 64
+                                  (128, -1, dflash.DFLASH_ERR_INVALID_ARG),
+                                  (128, 1 << 30, dflash.DFLASH_ERR_UNSUPPORTED_SHAPE)):  # rows >= 2^31
+        cfg = dflash.dflash_config(Cmax=Cmax, num_pages=num_pages, **base)
+        try:
+            dflash.dflash_create(cfg)
+            raise AssertionError(f"Cmax={Cmax} num_pages={num_pages} must be rejected")
+        except dflash.DflashError as e:
+            assert e.code == code, (Cmax, num_pages, e)
+    try:
+        dflash.dflash_set_block_table(None, None)
+        raise AssertionError("a NULL handle must be rejected")
+    except dflash.DflashError as e:
+        assert e.code == dflash.DFLASH_ERR_INVALID_ARG
+
+
+def test_seeded_block_tables_are_permutations():
+    import numpy as np
+    import dflash_inputs as di
+    t = di.block_table(5, 4 * di.PAGE_ROWS, seed=3)
+    assert t.shape == (5, 4) and t.dtype == np.int32
+    assert sorted(t.ravel().tolist()) == list(range(20))
+    assert np.array_equal(t, di.block_table(5, 4 * di.PAGE_ROWS, seed=3))
+    assert not np.array_equal(t, di.block_table(5, 4 * di.PAGE_ROWS, seed=4))
