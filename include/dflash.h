@@ -231,7 +231,11 @@ DFLASH_API int dflash_ctx_project_film(dflash_handle_t h, int nb, int R, const v
  *   max_ctx_hint host int: an upper bound on every ctx_len[i] (0 = Cmax - B). A
  *                ctx_len[i] above min(hint, Cmax - B), or negative, is reported as
  *                DFLASH_ERR_DEVICE_CHECK by dflash_status (and clamped).
- *   out_hidden   bf16 [nb, B, D]: final RMSNorm output (input of the LM head). */
+ *   out_hidden   bf16 [nb, B, D]: final RMSNorm output (input of the LM head).
+ * Results are bitwise reproducible for the same inputs and the same ctx_len of every
+ * sequence of the call: the attention splits the keys over CTAs by the lengths alone.
+ * Other sequences' lengths move those split points, so a sequence's output may then
+ * differ in rounding (within the stated tolerance), never more. */
 DFLASH_API int dflash_draft_block(dflash_handle_t h, int nb, const int32_t *block_ids, const void *x0_relay,
                        void *kcache, void *vcache, const int32_t *ctx_len,
                        int max_ctx_hint, void *out_hidden, void *ws, size_t ws_bytes,
