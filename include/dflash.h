@@ -1,7 +1,8 @@
 /*
  * dflash.h -- C ABI of libdflash: the one-pass block-diffusion draft step
- * (DFlash drafter with KV injection, DFlow relay, DFlash 2 selector and conv)
- * on one NVIDIA GB300 GPU (sm_103a).
+ * (DFlash drafter with KV injection, DFlow relay in plain and FiLM form, DFlash 2
+ * selector and conv, greedy accept or sampling with rejection-sampling verify,
+ * contiguous or paged KV cache) on one NVIDIA GB300 GPU (sm_103a).
  *
  * Sources (page title, section):
  *   [DFlash]  "DFlash 投机解码：块扩散草稿与 KV 注入" (caijizhuo.github.io)
