@@ -5,7 +5,8 @@
 // Source: "DFlash 投机解码：块扩散草稿与 KV 注入", 二、块扩散草稿 (attention equations).
 //
 // K_b and V_b were written by the QKV GEMM into cache rows [ctx_len, ctx_len + B), so a
-// (sequence, kv head) pair attends to L = ctx_len + B contiguous cache rows.
+// (sequence, kv head) pair attends to cache rows [0, ctx_len + B): one contiguous range,
+// or 64-row pages named by the block table (one page per 64-key unit).
 //
 // Work decomposition (even split of the streamed bytes): the keys of every pair are cut
 // into 64-key units; the units of all pairs, in (sequence, kv head) order, are divided
@@ -16,23 +17,25 @@
 // partials of the pair in CTA order. The split points depend on the batch's context
 // lengths only, so results are deterministic for a given batch.
 //
-// One CTA, 320 threads:
-//   warp 0       TMA producer: Q tile of the segment's pair ({64 of hd, Hq/Hkv heads, B
-//                rows} boxes from the qkv buffer) and K and V tiles of two units (128
-//                cache rows x hd, 128-byte swizzle, one copy each) into a 3-stage ring.
-//   warp 1       MMA issuer: S = Q K^T (M = 128 query rows, the G*B real ones zero-padded,
-//                N = 64 keys, K = hd) into TMEM S buffer j % 2, then O_{j%2} += P V
-//                (N = hd, K = 64 keys; V read MN-major straight from its TMA tile).
-//   warps 2..9   softmax, two halves of four warps: half h takes the units j with
-//                j % 2 == h and keeps its own running max, running sum and O_h, so the
-//                two halves work on consecutive units at once. Thread r of a half owns
-//                query row r (its TMEM lane): it reads S, masks keys beyond L, updates
-//                its max and sum in fp32 (exp2 with the 1/sqrt(hd) * log2(e) scale
-//                folded in) and writes P (bf16) to shared memory for the PV MMA. O_h is
-//                rescaled in TMEM only when the row's max grows by more than 2^8 in
-//                probability scale, so P stays <= 256 and most units need no O round
-//                trip. At the end of a segment half 0 merges (m, l, O) of both halves
-//                and writes the output or the partial.
+// One CTA, 7 warps when G*B <= 64 query rows, else 11 (AttnRoles below):
+//   TMA producer  Q tile of the segment's pair ({64 of hd, Hq/Hkv heads, B rows} boxes
+//                 from the qkv buffer) and K and V tiles of two units (128 cache rows x hd,
+//                 128-byte swizzle; one copy each, or one per unit and 64-column half when
+//                 paged) into a 3-stage ring.
+//   S issuer      S = Q K^T (M = 128 query rows, the G*B real ones zero-padded, N = 64
+//                 keys, K = hd) into TMEM S buffer j % 2; owns the TMEM allocation.
+//   PV issuer     O_{j%2} += P V (N = hd, K = 64 keys; P read from TMEM buffer j % 4, V
+//                 MN-major straight from its TMA tile); its commit on P buffer j % 4 also
+//                 tells the softmax half that PV(j) is complete.
+//   softmax       two halves; half h takes the units j with j % 2 == h and keeps its own
+//                 running max, running sum and O_h, so the two halves work on consecutive
+//                 units at once. Thread r of a half owns query row r (its TMEM lane): it
+//                 reads S, masks keys beyond L, updates its max and sum in fp32 (exp2 with
+//                 the 1/sqrt(hd) * log2(e) scale folded in) and writes P (bf16) to TMEM.
+//                 O_h is rescaled in TMEM only when the row's max grows by more than 2^8
+//                 in probability scale, so P stays <= 256 and most units need no O round
+//                 trip. At the end of a segment half 0 merges (m, l, O) of both halves and
+//                 writes the output or the partial.
 #include <cfloat>
 
 #include "common.cuh"

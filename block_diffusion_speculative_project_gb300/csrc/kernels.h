@@ -238,10 +238,12 @@ cudaError_t launch_verify(const float *draft_logits, const float *draft_lse, con
 
 // Context attention of one drafter layer (see attention.cu). The block's own K/V rows
 // have already been written to cache rows [ctx_len, ctx_len + B) by the QKV GEMM, so
-// every sequence attends to the ctx_len + B contiguous cache rows of its heads.
+// every sequence attends to cache rows [0, ctx_len + B) of its heads (contiguous, or
+// through the page table).
 struct AttnParams {
   CUtensorMap tmQ;      // qkv buffer as {hd, Hq heads, nb*B rows}, box {64, Hq/Hkv, B}
   CUtensorMap tmK;      // key cache of every layer: {64, N*max_batch*Hkv*Cmax rows, hd/64}, box {64, 128, hd/64}
+                        // (paged: {64, N*num_pages*Hkv*64 rows, hd/64}, box {64, 64, 1})
   CUtensorMap tmV;      // value cache, same shape
   const int *ctx_len;   // [nb]
   uint16_t *o;          // [nb*B, Hq*hd] bf16
