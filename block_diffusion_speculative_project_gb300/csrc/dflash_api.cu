@@ -1,6 +1,7 @@
 // C ABI of libdflash (declared in include/dflash.h): argument validation, TMA
 // descriptor encoding, workspace layout and the launch sequence of each step call.
-// All compute runs in the kernels of gemm_tc.cu, attention.cu and small_ops.cu.
+// All compute runs in the kernels of gemm_tc.cu, attention.cu, sampling.cu and
+// small_ops.cu.
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
