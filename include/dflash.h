@@ -157,7 +157,9 @@ DFLASH_API int dflash_destroy(dflash_handle_t h);
  * FiLM relay) must be non-NULL when their flag is set. */
 DFLASH_API int dflash_set_weights(dflash_handle_t h, const dflash_weights *w);
 
-/* Register the block table of a paged cache (borrowed device pointer, int32
+/* Register the block table of a paged cache (the layout above: a reading of [DFlash]
+ * 四、推理流程, the note on reusing the projected cache across requests with a common
+ * prefix). The table is a borrowed device pointer, int32
  * [max_batch][Cmax / DFLASH_PAGE_ROWS], 4-byte aligned). Kernels read it when they run,
  * so the caller may change entries between calls in stream order. Every call that
  * touches the caches needs it when cfg.num_pages > 0 (DFLASH_ERR_INVALID_ARG before
@@ -292,7 +294,9 @@ DFLASH_API int dflash_attention(dflash_handle_t h, int nb, int layer, const void
                                 dflash_stream_t stream);
 
 /* Top-k of each row of an fp32 matrix with the same ordering rule as
- * dflash_lm_head_topk (value descending, ties to the lower column).
+ * dflash_lm_head_topk (value descending, ties to the lower column; [DFlash2] 洞察一 keeps
+ * the top-16 per position). No counterpart call on the pages: it checks the selection rule
+ * on exact inputs.
  *   logits f32 [rows, cols]; out_ids int32 [rows, k]; out_vals f32 [rows, k]; k 1..16. */
 DFLASH_API int dflash_topk(dflash_handle_t h, int rows, int cols, const float *logits, int k,
                 int32_t *out_ids, float *out_vals, void *ws, size_t ws_bytes,
@@ -338,7 +342,8 @@ DFLASH_API int dflash_lm_head_sample(dflash_handle_t h, int nb, const void *hidd
                   float *out_logits, int k, int32_t *out_ids, float *out_vals, void *ws,
                   size_t ws_bytes, dflash_stream_t stream);
 
-/* The random numbers every draw uses, for checking them: for v < n, out_u[v] = the Philox
+/* The random numbers every draw uses, for checking them (the pages fix no generator:
+ * Philox4x32-10, Salmon et al., SC 2011): for v < n, out_u[v] = the Philox
  * uniform of element v of (seed, stream_id, row) (word v % 4 of the block at counter
  * (v / 4, row, stream_id, 0)) and out_g[v] = its Gumbel value -log(-log u) as the draws
  * compute it (absolute error about 1e-6). Needs no handle. */
@@ -377,7 +382,9 @@ DFLASH_API int dflash2_select_sample(dflash_handle_t h, int nb, int k, const int
                   float temperature, uint64_t seed, int32_t *out_path, float *out_walk_logq,
                   void *ws, size_t ws_bytes, dflash_stream_t stream);
 
-/* dflash_verify_sample with the sampling walk's draft distribution: q_t(v) =
+/* dflash_verify_sample with the sampling walk's draft distribution ([DFlash2] 洞察一: the
+ * walk samples from the same score distribution, and Results: lossless rejection sampling
+ * restores the target's distribution): q_t(v) =
  * exp(walk_logq[t-1][c]) for v = cand_ids[t-1][c], 0 for every other token (so the
  * residual of a non-candidate is p itself, and a drawn token outside the candidates is
  * rejected). Acceptance, residual, fallback and bonus draws as dflash_verify_sample.
