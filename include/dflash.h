@@ -160,7 +160,7 @@ DFLASH_API int dflash_set_weights(dflash_handle_t h, const dflash_weights *w);
 /* Register the block table of a paged cache (the layout above: a reading of [DFlash]
  * 四、推理流程, the note on reusing the projected cache across requests with a common
  * prefix). The table is a borrowed device pointer, int32
- * [max_batch][Cmax / DFLASH_PAGE_ROWS], 4-byte aligned). Kernels read it when they run,
+ * [max_batch][Cmax / DFLASH_PAGE_ROWS], 4-byte aligned. Kernels read it when they run,
  * so the caller may change entries between calls in stream order. Every call that
  * touches the caches needs it when cfg.num_pages > 0 (DFLASH_ERR_INVALID_ARG before
  * any launch otherwise). An entry outside [0, num_pages) that a call reaches is
