@@ -27,7 +27,7 @@ Sources (page title, section):
             (SC 2011): the Philox4x32-10 counter-based generator, used for every random
             number the sampling path draws.
 
-Readings where the pages are silent or disagree (each is listed in the design doc):
+Readings where the pages are silent or disagree:
   * block layout [anchor, mask x (B-1)] at absolute positions C..C+B-1, C = context
     rows after the append; offset 0 yields no candidate ([DFlash] 符号约定, dflash_cycle);
   * pre-norm residual layer x += Attn(RMSNorm(x)); x += FFN(RMSNorm(x)); final RMSNorm;

@@ -811,7 +811,76 @@ def test_recall_at_k_hand_case():
     assert list(hits) == [2, 2, 1] and list(eligible) == [3, 2, 2]
 
 
+# ----------------------------------------------------------------------------- LM head rows
+
+def test_lm_logits_rows_are_mask_offsets_one_to_b_minus_one():
+    # [DFlash] 四、推理流程, dflash_cycle: the draft takes the LM head of the block's
+    # hidden rows from offset 1 on (the anchor at offset 0 is already known and yields no
+    # candidate). Offset j of sequence i carries a one-hot at column c(i, j); W_lm is a
+    # non-symmetric permutation (row perm[c] reads column c), so logits row (i, t-1) peaks
+    # at vocabulary id perm[c(i, t)]. Offsets 0..B-2 instead of 1..B-1, or W_lm applied
+    # transposed, move every peak.
+    D, B, nb = 16, 6, 2
+    rng = np.random.default_rng(31)
+    perm = rng.permutation(D)
+    while np.array_equal(perm[perm], np.arange(D)):  # not an involution: W_lm != W_lm^T
+        perm = rng.permutation(D)
+    W = {"W_lm": np.zeros((D, D))}
+    W["W_lm"][perm, np.arange(D)] = 1.0
+    col = np.array([[(5 * i + 3 * j + 1) % D for j in range(B)] for i in range(nb)])
+    hidden = np.zeros((nb, B, D))
+    for i in range(nb):
+        for j in range(B):
+            hidden[i, j, col[i, j]] = 2.0 + j + (50.0 if j == 0 else 0.0)  # the anchor row is loud
+    logits = orc.lm_logits(W, hidden)
+    assert logits.shape == (nb, B - 1, D)
+    for i in range(nb):
+        for t in range(1, B):
+            assert int(np.argmax(logits[i, t - 1])) == perm[col[i, t]]
+            assert logits[i, t - 1].max() == 2.0 + t
+    assert logits.max() < 50.0  # the anchor row never reaches the logits
+
+
 # ----------------------------------------------------------------------------- whole step
+
+def test_draft_step_accept_reads_the_selector_path():
+    # [DFlash2] 洞察一: with the selector on, the greedy walk's path replaces the per-offset
+    # top-1 as the draft that the verifier checks. Large W_A / W_B make the pair term
+    # dominate, so the path leaves the top-1 at offset 1 of some sequence; a target row that
+    # repeats the path then accepts every candidate (tau = B, bonus = T[B-1]), and one that
+    # repeats the top-1 stops at the first offset where they differ.
+    import copy
+    cfg = small_cfg(flags=di.FLAG_SELECT, sel_dim=8, k_top=6, nb=4)
+    W = rand_weights(cfg, seed=5)
+    W["W_A"] = 3.0 * np.random.default_rng(6).standard_normal(W["W_A"].shape)
+    W["W_B"] = 3.0 * np.random.default_rng(7).standard_normal(W["W_B"].shape)
+    rng = np.random.default_rng(8)
+    cache = orc.KVCache(cfg.N, cfg.nb, cfg.Hkv, 40, cfg.hd)
+    fill_cache(cfg, cache, 12, rng)
+    hv = rng.standard_normal((cfg.nb, 3, cfg.L * cfg.Dt))
+    ids = rng.integers(0, cfg.V - 1, (cfg.nb, cfg.B)).astype(np.int32)
+    ids[:, 1:] = cfg.V - 1
+    args = (hv, [3] * cfg.nb, [12] * cfg.nb)
+    first = orc.draft_step(cfg, W, *args, copy.deepcopy(cache), ids, np.zeros((cfg.nb, cfg.B), np.int32))
+    path, top1 = first["path"], first["ids"][..., 0]
+    differs = path[:, 0] != top1[:, 0]
+    assert differs.any()
+    assert np.array_equal(first["draft"], path)
+    bonus_tok = np.arange(cfg.nb, dtype=np.int32) + 7
+    t_path = np.concatenate([path, bonus_tok[:, None]], axis=1).astype(np.int32)
+    o = orc.draft_step(cfg, W, *args, copy.deepcopy(cache), ids, t_path)
+    assert np.array_equal(o["path"], path)
+    assert o["tau"].tolist() == [cfg.B] * cfg.nb
+    assert o["bonus"].tolist() == bonus_tok.tolist()
+    t_top1 = np.concatenate([top1, bonus_tok[:, None]], axis=1).astype(np.int32)
+    o = orc.draft_step(cfg, W, *args, copy.deepcopy(cache), ids, t_top1)
+    for i in range(cfg.nb):
+        m = int(np.argmax(path[i] != top1[i])) if (path[i] != top1[i]).any() else cfg.B - 1
+        assert int(o["tau"][i]) == m + 1
+        assert int(o["bonus"][i]) == int(t_top1[i, m])
+    assert (o["tau"][differs] == 1).all()
+
+
 
 def test_tiny_step_runs_and_is_deterministic():
     cfg = di.TINY
