@@ -8,6 +8,7 @@ captured in a CUDA graph and replayed; K timed replays are bracketed by a barrie
 a device synchronize, timed with CUDA events on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+  python bench.py --profile-case {lm_head,draft_block,ctx_project,sampling} [--layers N] ...
 
 N > 1 (torchrun, one process per GPU) runs N independent replicas (the step shards
 by sequence with no exchange); value = sequences of all ranks / the slowest rank's
@@ -175,13 +176,14 @@ def max_over_ranks(values, device=None):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_gpu(args, rank, world):
+def measure_workload(args, w, weights, dev, world, steps, warmup, full=True):
+    """Set up one workload on this GPU (caches, context prefill, step inputs), capture its
+    step in a CUDA graph and time `steps` replays; with `full`, also the LM head inside the
+    step, the end-to-end leg through host buffers and the prompt prefill. Returns the raw
+    measurements (times are maxima over ranks)."""
     import torch
     from block_diffusion_speculative_project_gb300.drafter import Drafter, to_device_bf16
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    w = di.WORKLOADS[args.workload]
     seed = 0  # every replica runs the same workload
     ctx = di.context_lengths(w, seed).astype(np.int32)
     tp = di.tau_prev(w, seed).astype(np.int32)
@@ -193,10 +195,6 @@ def run_gpu(args, rank, world):
     Cmax = int(ctx.max()) + w.B
     if w.paged:
         Cmax = -(-Cmax // di.PAGE_ROWS) * di.PAGE_ROWS
-    t0 = time.time()
-    bits = di.make_weights(w, seed)
-    weights = {k: to_device_bf16(v, dev) for k, v in bits.items()}
-    t_gen = time.time() - t0
     num_pages = w.nb * (Cmax // di.PAGE_ROWS) if w.paged else 0
     dr = Drafter(w, weights, w.nb, Cmax, max(PROJ_CHUNK, PREFILL_ROWS, w.B), num_pages=num_pages)
     i32 = lambda x: torch.tensor(np.asarray(x, np.int32), device=dev)
@@ -230,10 +228,11 @@ def run_gpu(args, rank, world):
         parts["relay_b"], parts["relay_y"] = di.relay_tokens(w, seed)
     host_in_np = np.concatenate([np.asarray(v, np.int32).ravel() for v in parts.values()])
     step_in = i32(host_in_np)
-    views, off = {}, 0
+    views, spans, off = {}, {}, 0
     for name, v in parts.items():
         n = int(np.asarray(v).size)
         views[name] = step_in[off:off + n].view(np.asarray(v).shape)
+        spans[name] = (off, off + n)
         off += n
     n_commit = views["n_commit"]
     relay_a = views.get("relay_a")
@@ -302,7 +301,12 @@ def run_gpu(args, rank, world):
     if dr.status(stream) != 0:
         raise RuntimeError("device status reports an error after the first step")
     if not sampling:
-        target.copy_(i32(di.target_row_from_draft(draft_c.cpu().numpy(), w.V, seed)))
+        trow = di.target_row_from_draft(draft_c.cpu().numpy(), w.V, seed)
+        target.copy_(i32(trow))
+        # the host copy of the step's inputs carries the same target row, so the end-to-end
+        # leg runs exactly the step the timed region runs
+        t0_, t1_ = spans["target"]
+        host_in_np[t0_:t1_] = np.asarray(trow, np.int32).ravel()
 
     # capture one step in a CUDA graph (warm-up launches above configured every kernel)
     graph = torch.cuda.CUDAGraph()
@@ -318,7 +322,7 @@ def run_gpu(args, rank, world):
             with torch.cuda.graph(lm_graph, stream=stream):
                 step(stream, ev_lm)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         with torch.cuda.stream(stream):
             graph.replay()
     stream.synchronize()
@@ -337,7 +341,7 @@ def run_gpu(args, rank, world):
     torch.cuda.nvtx.range_push("timed")
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             graph.replay()
         e1.record(stream)
     stream.synchronize()
@@ -350,7 +354,7 @@ def run_gpu(args, rank, world):
     # dominant kernel (LM head GEMM + top-k): events on its stream inside the replayed
     # graph, averaged over replays of the same step
     lm_ms = []
-    for _ in range(max(5, min(50, args.steps // 10))):
+    for _ in range(max(5, min(50, steps // 10))):
         with torch.cuda.stream(stream):
             if lm_graph is not None:
                 lm_graph.replay()
@@ -362,52 +366,122 @@ def run_gpu(args, rank, world):
         raise RuntimeError("device status reports an error after the timed steps")
     tau_h = tau.cpu().numpy()
 
-    # e2e through the public API with host buffers: H2D of the step's inputs from pinned
-    # memory and D2H of its results, every step, inside the timed region
-    host_hv = hv_step.cpu().pin_memory()
-    host_in = torch.from_numpy(host_in_np).pin_memory()
-    host_out = torch.empty(w.nb * (2 + (w.B - 1) * k), dtype=torch.int32).pin_memory()
-    e2e_steps = max(10, min(args.steps, 200))
-    barrier()
-    torch.cuda.synchronize(dev)
-    t_e2e = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(e2e_steps):
-            hv_step.copy_(host_hv, non_blocking=True)
-            step_in.copy_(host_in, non_blocking=True)
-            graph.replay()
-            out = torch.cat([tau, bonus, tid.flatten()])
-            host_out.copy_(out, non_blocking=True)
-            stream.synchronize()
-    e2e_s = time.perf_counter() - t_e2e
-    barrier()
-    h2d = host_hv.numel() * 2 + host_in.numel() * 4
-    d2h = host_out.numel() * 4
+    e2e = pre_ms = None
+    if full:
+        # e2e through the public API with host buffers: H2D of the step's inputs from pinned
+        # memory and D2H of its results, every step, inside the timed region. Each step waits
+        # for its results on the host before the next begins (the next step's inputs come from
+        # the verifier, which needs this step's draft). Events split each step into the copies
+        # in, the step, the copy out; the rest is host-side launch and wake-up time.
+        host_hv = hv_step.cpu().pin_memory()
+        host_in = torch.from_numpy(host_in_np).pin_memory()
+        host_out = torch.empty(w.nb * (2 + (w.B - 1) * k), dtype=torch.int32).pin_memory()
+        out_dev = torch.empty_like(host_out, device=dev)
+        nt = w.nb * (w.B - 1) * k
+        e2e_steps = 300
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(e2e_steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        t_e2e = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for it in range(e2e_steps):
+                ev = evs[it]
+                ev[0].record(stream)
+                hv_step.copy_(host_hv, non_blocking=True)
+                step_in.copy_(host_in, non_blocking=True)
+                ev[1].record(stream)
+                graph.replay()
+                ev[2].record(stream)
+                out_dev[:w.nb].copy_(tau)
+                out_dev[w.nb:2 * w.nb].copy_(bonus)
+                out_dev[2 * w.nb:].copy_(tid.view(nt))
+                host_out.copy_(out_dev, non_blocking=True)
+                ev[3].record(stream)
+                stream.synchronize()
+        e2e_s = time.perf_counter() - t_e2e
+        barrier()
+        e2e_parts = np.array([[ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[2].elapsed_time(ev[3])]
+                              for ev in evs]).mean(axis=0)
+        if not np.array_equal(host_out[:w.nb].numpy(), tau.cpu().numpy()):
+            raise RuntimeError("the end-to-end leg's result differs from the device result")
+        h2d = host_hv.numel() * 2 + host_in.numel() * 4
+        d2h = host_out.numel() * 4
 
-    # prompt prefill through dflash_ctx_project (the large-context path, compute-bound W_c
-    # GEMM over nb * PREFILL_ROWS rows): after the step timing, so rewriting the first
-    # context rows of the caches does not matter any more
-    hv_pre = torch.randn(w.nb, PREFILL_ROWS, w.L * w.Dt, device=dev, generator=g).to(torch.bfloat16)
-    pre_commit = i32(np.full(w.nb, PREFILL_ROWS))
-    pre_zero = i32(np.zeros(w.nb))
-    pre_len = pre_zero.clone()
-    pre_ms = []
-    with torch.cuda.stream(stream):
-        for rep in range(4):
-            pre_len.copy_(pre_zero)
-            p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            p0.record(stream)
-            dr.ctx_project(w.nb, PREFILL_ROWS, hv_pre, pre_commit, pre_len, stream=stream)
-            p1.record(stream)
-            stream.synchronize()
-            if rep:
-                pre_ms.append(p0.elapsed_time(p1))
-    if dr.status(stream) != 0:
-        raise RuntimeError("device status reports an error after the prefill")
-    del hv_pre
+        # prompt prefill through dflash_ctx_project (the large-context path, compute-bound W_c
+        # GEMM over nb * PREFILL_ROWS rows): after the step timing, so rewriting the first
+        # context rows of the caches does not matter any more
+        hv_pre = torch.randn(w.nb, PREFILL_ROWS, w.L * w.Dt, device=dev, generator=g).to(torch.bfloat16)
+        pre_commit = i32(np.full(w.nb, PREFILL_ROWS))
+        pre_zero = i32(np.zeros(w.nb))
+        pre_len = pre_zero.clone()
+        pre_ms = []
+        with torch.cuda.stream(stream):
+            for rep in range(4):
+                pre_len.copy_(pre_zero)
+                p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                p0.record(stream)
+                dr.ctx_project(w.nb, PREFILL_ROWS, hv_pre, pre_commit, pre_len, stream=stream)
+                p1.record(stream)
+                stream.synchronize()
+                if rep:
+                    pre_ms.append(p0.elapsed_time(p1))
+        if dr.status(stream) != 0:
+            raise RuntimeError("device status reports an error after the prefill")
+        del hv_pre
+        e2e = dict(steps=e2e_steps, s=e2e_s, parts=e2e_parts, h2d=h2d, d2h=d2h)
+    e2e_s = e2e["s"] if e2e else 0.0
+    ms_step, e2e_s = max_over_ranks([ms_total / steps, e2e_s], dev)
+    if e2e:
+        e2e["s"] = e2e_s
+    return dict(w=w, ctx=ctx, tp=tp, k=k, ms_step=ms_step, lm_ms=lm_ms, clk=clk, tau=tau_h, e2e=e2e,
+                pre_ms=pre_ms)
 
-    # max over ranks
-    ms_step, e2e_s = max_over_ranks([ms_total / args.steps, e2e_s], dev)
+
+def step_summary(m, world):
+    """Blocks/s and the step's roofline fraction of one measured workload."""
+    w = m["w"]
+    hbm, tf_burst, tf_sus, _ = load_peaks()
+    total_bytes, flops, _, _ = step_bytes_flops(w, m["ctx"], m["tp"])
+    step_t_roof = max(total_bytes / (hbm * 1e9), flops / (tf_sus * 1e12 if tf_sus else tf_burst * 1e12))
+    value = w.nb * world / (m["ms_step"] * 1e-3)
+    return {"value": round(value, 2), "unit": "blocks/s", "ms_per_step": round(m["ms_step"], 4),
+            "draft_tokens_per_s": round(value * (w.B - 1), 1),
+            "step_roofline": {"bytes": total_bytes, "flops": flops, "t_roofline_ms": round(step_t_roof * 1e3, 4),
+                              "frac": round(step_t_roof * 1e3 / m["ms_step"], 4)},
+            "config": {"nb_per_gpu": w.nb, "B": w.B, "context": int(m["ctx"].mean()),
+                       "context_range": [int(m["ctx"].min()), int(m["ctx"].max())]},
+            "clocks": m["clk"], "tau_mean": round(float(m["tau"].mean()), 3)}
+
+
+# The north star's batch-64 serving configuration, timed in the same process as the
+# default workload so that one benchmark run reports both.
+EXTRA_WORKLOADS = (di.SWEEP_NB64.name,)
+
+
+def run_gpu(args, rank, world):
+    import torch
+    from block_diffusion_speculative_project_gb300.drafter import to_device_bf16
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = di.WORKLOADS[args.workload]
+    t0 = time.time()
+    bits = di.make_weights(w, 0)
+    weights = {k: to_device_bf16(v, dev) for k, v in bits.items()}
+    t_gen = time.time() - t0
+    m = measure_workload(args, w, weights, dev, world, args.steps, args.warmup, full=True)
+    extra = {}
+    if args.workload == DEFAULT_WORKLOAD and not args.no_extra_workloads:
+        for name in EXTRA_WORKLOADS:
+            torch.cuda.empty_cache()
+            m2 = measure_workload(args, di.WORKLOADS[name], weights, dev, world, max(args.steps, 100),
+                                  args.warmup, full=False)
+            extra[name] = step_summary(m2, world)
+            extra[name]["steps"] = max(args.steps, 100)
+    ctx, tp, k, lm_ms, clk, tau_h, pre_ms = m["ctx"], m["tp"], m["k"], m["lm_ms"], m["clk"], m["tau"], m["pre_ms"]
+    ms_step = m["ms_step"]
+    e2e_steps, e2e_s, e2e_parts = m["e2e"]["steps"], m["e2e"]["s"], m["e2e"]["parts"]
+    h2d, d2h = m["e2e"]["h2d"], m["e2e"]["d2h"]
 
     if rank != 0:
         return None
@@ -457,15 +531,23 @@ def run_gpu(args, rank, world):
                     "frac": round(pre_flops / pre_t / 1e12 / tf_burst, 4),
                     "what": "dflash_ctx_project: W_c GEMM, RMSNorm, K/V GEMMs of every layer into the caches"},
         "e2e": {"value": round(blocks * e2e_steps / e2e_s, 2), "unit": "blocks/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+                "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 4),
+                "breakdown_ms": {"h2d": round(float(e2e_parts[0]), 4), "step": round(float(e2e_parts[1]), 4),
+                                 "d2h": round(float(e2e_parts[2]), 4),
+                                 "host": round(e2e_s * 1e3 / e2e_steps - float(e2e_parts.sum()), 4)}},
         "gpu_launches": kernels_per_step(w) * args.steps,
         "clocks": clk,
         "tau_mean": round(float(tau_h.mean()), 3),
         "setup_s": {"weights": round(t_gen, 1)},
     }
+    if extra:
+        line["workloads"] = extra
     if not args.no_cpu_baseline and rank == 0:
         line["cpu_baseline"] = cpu_baseline(w, bits, args.cpu_seconds)
     return line
+
+
 
 
 # ----------------------------------------------------------------------------- oracle (CPU)
@@ -548,6 +630,100 @@ def run_reference(args, rank, world):
             "setup_s": {"weights": round(gen, 1)}}
 
 
+# ----------------------------------------------------------------------------- profiling cases
+
+def run_profile_case(args):
+    """Small, self-contained cases of the step's kernels for ncu captures (no JSON line,
+    no timing contract): weights and caches come from a device-side generator, so a case
+    starts in seconds and holds little device memory.
+
+      lm_head      the LM head + top-k of the workload (the full vocabulary)
+      draft_block  dflash_draft_block with --layers layers (default 1) and a 4096-token
+                   vocabulary (the QKV, attention, merge, O, gate|up and down launches at the
+                   workload's shapes)
+      ctx_project  the context append (W_c GEMM, RMSNorm, grouped K/V GEMM) of the step, or
+                   of --rows rows per sequence (a prefill)
+      sampling     dflash_sample + dflash_verify_sample at V = 151936, 16 sequences of B = 16
+                   (draft and target logits both larger than L2), tiny drafter otherwise
+    Prints the per-call CUDA-event time of each iteration's median."""
+    import torch
+    from block_diffusion_speculative_project_gb300.drafter import Drafter
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    case = args.profile_case
+    w = di.WORKLOADS[args.workload]
+    if args.nb:
+        w = w.with_(nb=args.nb)
+    if case == "sampling":
+        w = di.TINY.with_(V=151936, B=16, nb=16)
+    elif case == "draft_block":
+        w = w.with_(N=args.layers or 1, V=4096, L=1)
+    elif args.layers:
+        w = w.with_(N=args.layers)
+    weights = {}
+    for name, shp in di.weight_shapes(w).items():
+        t = torch.randn(shp, device=dev, generator=g) * 0.02
+        if name.rsplit(".", 1)[-1].startswith("g_"):
+            t += 1.0
+        weights[name] = t.to(torch.bfloat16)
+    i32 = lambda x: torch.tensor(np.asarray(x, np.int32), device=dev)
+    ctx = di.context_lengths(w).astype(np.int32)
+    rows = max(w.B, args.rows)
+    Cmax = int(ctx.max()) + max(w.B, rows)
+    dr = Drafter(w, weights, w.nb, Cmax, rows)
+    dr.kcache.normal_(generator=g)
+    dr.vcache.normal_(generator=g)
+    if case == "sampling":
+        nr = w.nb * (w.B - 1)
+        U = torch.randn(w.nb, w.B - 1, w.V, device=dev, generator=g) * 2
+        Z = torch.randn(w.nb, w.B, w.V, device=dev, generator=g) * 2
+        cand = torch.zeros(w.nb, w.B - 1, dtype=torch.int32, device=dev)
+        lse = torch.zeros(w.nb, w.B - 1, device=dev)
+        tau = torch.zeros(w.nb, dtype=torch.int32, device=dev)
+        tok = torch.zeros_like(tau)
+        calls = {"sample": lambda: dr.sample(nr, U, 1.0, 99, cand, lse),
+                 "verify_sample": lambda: dr.verify_sample(w.nb, U, lse, cand, Z, 1.0, 99, tau, tok)}
+    elif case == "ctx_project":
+        tp = di.tau_prev(w).astype(np.int32) if rows == w.B else np.full(w.nb, rows, np.int32)
+        hv = torch.randn(w.nb, rows, w.L * w.Dt, device=dev, generator=g).to(torch.bfloat16)
+        base = i32(np.zeros(w.nb) if rows > w.B else ctx - tp)
+        ctx_len = base.clone()
+        ncommit = i32(tp)
+        calls = {"ctx_project": lambda: (ctx_len.copy_(base), dr.ctx_project(w.nb, rows, hv, ncommit, ctx_len))}
+    else:
+        block = i32(di.block_ids(w, di.anchors(w)))
+        hidden = torch.randn(w.nb, w.B, w.D, device=dev, generator=g).to(torch.bfloat16)
+        tid = torch.empty(w.nb, w.B - 1, w.k_top, dtype=torch.int32, device=dev)
+        tv = torch.empty(w.nb, w.B - 1, w.k_top, dtype=torch.float32, device=dev)
+        ctx_t = i32(ctx)
+        if case == "lm_head":
+            calls = {"lm_head_topk": lambda: dr.lm_head_topk(w.nb, hidden, w.k_top, tid, tv)}
+        else:
+            calls = {"draft_block": lambda: dr.draft_block(w.nb, block, ctx_t, hidden,
+                                                           max_ctx_hint=int(ctx.max()))}
+    for f in calls.values():
+        f()
+    torch.cuda.synchronize()
+    if dr.status() != 0:
+        raise RuntimeError("device status reports an error")
+    for name, f in calls.items():
+        ts = []
+        for _ in range(args.iters):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            f()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        print(f"{case}: {w.name} nb={w.nb} N={w.N} {name}: median {np.median(ts) * 1e3:.1f} us, "
+              f"min {np.min(ts) * 1e3:.1f} us over {args.iters} calls (host launch time included)")
+    if dr.status() != 0:
+        raise RuntimeError("device status reports an error")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -557,7 +733,19 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="time only --workload (by default the default workload's run also times the "
+                         "batch-64 ragged workload)")
+    ap.add_argument("--profile-case", choices=["lm_head", "draft_block", "ctx_project", "sampling"],
+                    help="run one small kernel case for an ncu capture instead of the benchmark")
+    ap.add_argument("--layers", type=int, default=0, help="drafter layers of a --profile-case")
+    ap.add_argument("--nb", type=int, default=0, help="sequences of a --profile-case (0: the workload's)")
+    ap.add_argument("--rows", type=int, default=0, help="rows per sequence of --profile-case ctx_project")
+    ap.add_argument("--iters", type=int, default=3, help="timed calls of a --profile-case")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
