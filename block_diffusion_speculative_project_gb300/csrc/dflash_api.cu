@@ -837,9 +837,14 @@ int lm_head_impl(dflash_handle_t h, int nb, const void *hidden, int k, int32_t *
     p.smp_stream = 0;
     p.smp_seed = seed;
   }
+  // the per-range partial lists in the workspace hold num_sms ranges: check the plan
+  // before the launch writes them
+  int tpc = 0, ranges = 0;
+  topk_range_plan((c.V + kBNTopk - 1) / kBNTopk, (Ml + p.tile_rows - 1) / p.tile_rows, h->num_sms, &tpc,
+                  &ranges);
+  if (ranges > h->num_sms) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "top-k ranges exceed the workspace plan");
   DF_TRY(run_gemm(h, p, kBNTopk, s));
-  const int ranges = p.items / p.m_tiles;
-  if (ranges > h->num_sms) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "top-k ranges exceed the plan");
+  if (p.items / p.m_tiles != ranges) return fail(DFLASH_ERR_CUDA, "LM-head range plan mismatch");
   if (out_ids)
     DF_CUDA(launch_topk_merge(p.part_vals, p.part_ids, Ml, k, k, (long long)Ml * k, ranges, k, out_ids,
                               out_vals, s));
@@ -905,12 +910,12 @@ int dflash_lm_head_topk_noalloc(dflash_handle_t h, int nb, const void *hidden, i
   const int R = c.B - 1;
   const int S = 128 / R;
   const int Ml = nb * R;
-  // Same work split as the LM-head launch: vocabulary ranges x row tiles.
+  // The LM-head launch's own work split (vocabulary ranges x row tiles), from the planner
+  // the launch uses, so the size check below holds for what the kernel writes.
   const int m_tiles = (Ml + S * R - 1) / (S * R);
   const int n_tiles = (c.V + kBNTopk - 1) / kBNTopk;
-  const int ranges0 = std::max(1, h->num_sms / m_tiles);
-  const int tpc = (n_tiles + ranges0 - 1) / ranges0;
-  const int ranges = (n_tiles + tpc - 1) / tpc;
+  int tpc = 0, ranges = 0;
+  topk_range_plan(n_tiles, m_tiles, h->num_sms, &tpc, &ranges);
   const size_t list_bytes = (size_t)ranges * Ml * k * sizeof(float);
   const size_t need = 256 + 2 * list_bytes;
   if (need > kNoallocScratchBytes)
@@ -946,7 +951,10 @@ int dflash_lm_head_topk_noalloc(dflash_handle_t h, int nb, const void *hidden, i
   p.part_vals = reinterpret_cast<float *>(scratch + 256);
   p.part_ids = reinterpret_cast<int *>(scratch + 256 + list_bytes);
   DF_CUDA(gemm_launch(p, kBNTopk, h->num_sms, s));
-  if (p.items / p.m_tiles != ranges) return fail(DFLASH_ERR_CUDA, "LM-head range plan mismatch");
+  // gemm_launch planned with topk_range_plan on the same (n_tiles, m_tiles, num_sms), so the
+  // ranges it launched are the ones checked above
+  if (p.items / p.m_tiles != ranges || p.m_tiles != m_tiles)
+    return fail(DFLASH_ERR_CUDA, "LM-head range plan mismatch");
   DF_CUDA(launch_topk_merge(p.part_vals, p.part_ids, Ml, k, k, (long long)Ml * k, ranges, k, out_ids,
                             out_vals, s));
   return DFLASH_OK;

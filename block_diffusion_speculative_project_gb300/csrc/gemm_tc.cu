@@ -882,6 +882,13 @@ int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN) {
   return m_tiles * n_tiles * groups;
 }
 
+void topk_range_plan(int n_tiles, int m_tiles, int num_sms, int *tiles_per_cta, int *ranges) {
+  const int ranges0 = std::max(1, num_sms / std::max(1, m_tiles));
+  const int tpc = (n_tiles + ranges0 - 1) / ranges0;
+  *tiles_per_cta = std::max(1, tpc);
+  *ranges = (n_tiles + *tiles_per_cta - 1) / *tiles_per_cta;
+}
+
 // Chooses the cluster split S: the largest S <= 8 such that every tile's cluster of
 // S CTAs is resident at once (cluster_cap[S] = clusters of that size the device
 // holds concurrently; 0 = unknown, then tiles * S <= num_sms) and every split keeps
@@ -959,9 +966,8 @@ static cudaError_t plan_and_launch(GemmParams &p, int num_sms, cudaStream_t s) {
   if (EPI == EPI_TOPK) {
     p.splits = 1;
     p.kt_per_split = p.kt_total;
-    const int ranges0 = std::max(1, num_sms / p.m_tiles);
-    p.tiles_per_cta = (p.n_tiles + ranges0 - 1) / ranges0;
-    const int ranges = (p.n_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
+    int ranges = 0;
+    topk_range_plan(p.n_tiles, p.m_tiles, num_sms, &p.tiles_per_cta, &ranges);
     grid = ranges * p.m_tiles;
     p.items = grid;
   } else {

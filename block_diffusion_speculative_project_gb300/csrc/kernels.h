@@ -160,6 +160,11 @@ void gemm_plan(int M, int tile_rows, int N, int K, int groups, int dual, int BN,
                int epi, const int *cluster_cap, int *splits, int *kt_per_split, int *items, int *grid,
                int *csplit);
 int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN);
+// Vocabulary ranges of the LM head's top-k GEMM: the n_tiles column tiles are cut into
+// *ranges contiguous ranges of *tiles_per_cta tiles, one CTA per (range, row tile), with
+// ranges <= max(1, num_sms / m_tiles). The launch and every buffer sized per range use
+// this one plan.
+void topk_range_plan(int n_tiles, int m_tiles, int num_sms, int *tiles_per_cta, int *ranges);
 
 // ---------------------------------------------------------------- small kernels
 

@@ -267,7 +267,8 @@ DFLASH_API int dflash_lm_head_topk(dflash_handle_t h, int nb, const void *hidden
  *   any shape whose lists need more is rejected with DFLASH_ERR_UNSUPPORTED_SHAPE.
  *   out_status: int32 device word or NULL. When given, device-side errors are
  *   OR-ed into it (value 1: a bounded wait ran out; value 2: a bounds check
- *   failed); the caller clears it. When NULL they are not reported.
+ *   failed); the caller clears it. When NULL they are not reported, and out_ids /
+ *   out_vals are undefined after such an error (they may hold another call's lists).
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call before
  *   any stream capture. The call allocates nothing. All calls share the one array,
