@@ -18,10 +18,19 @@ the model's. The end-to-end comparison therefore requires |g - o| <= 0.1 (1 + |o
 (sqrt(2) x 0.056 with 25% margin), a mean error <= 0.015 (1.5 x the model's largest
 mean) and >= 93% of the elements within the stated tolerance.
 
+End-to-end ids: the GPU's logits drift from the oracle's by eps = max_v |z_gpu - z_oracle|
+per row (the hidden difference seen through W_lm; 0.056-0.091 measured, up to 0.074 in
+the storage model), above the stated delta = 1e-2 max(1, |v|) ~ 0.05 at the top of the
+vocabulary. So: the GPU's top-k is checked exactly against the fp64 logits of its own
+hidden rows (delta 2e-3); every top-k decision whose oracle margin exceeds 2 eps + 2e-3
+must be the oracle's; and the draft ids (top-1) must equal the oracle's wherever the
+oracle's margin exceeds the stated delta.
+
 Context caches are seeded random values for the sampled sequences (the same bf16 bits
 on both sides) and device-generated values for the others; the step then appends the
 previous round's committed rows through ctx_project, drafts, runs the LM head with
-top-k (and the selector), and accepts against a seeded target row.
+top-k (and the selector), and accepts against a seeded target row. The paged workloads
+run the same step through the bench's seeded shuffled block table.
 """
 import numpy as np
 import pytest
@@ -37,6 +46,10 @@ HIDDEN_ATOL = 0.1
 HIDDEN_RTOL = 0.1
 HIDDEN_MEAN = 0.015
 STATED_FRACTION = 0.93
+# End-to-end logit drift bound: the bf16 storage model's logits of the sampled sequences
+# deviate from the exact oracle's by up to 0.053 (Qwen3-4B shape) and 0.074 (Qwen3-8B
+# shape) at any vocabulary entry; twice the larger.
+LOGIT_DRIFT = 0.15
 
 _W = {}
 
@@ -52,6 +65,25 @@ def weights_for(w):
         bits = di.make_weights(w)
         _W[key] = (bits, orc.widen_all(bits))
     return _W[key]
+
+
+def seq_rows(pool, n, i, table):
+    """Cache rows [Hkv, Cmax, hd] of sequence i in layer n: a view of the contiguous
+    cache, or the sequence's pages gathered through the block table (a copy)."""
+    if table is None:
+        return pool[n, i]
+    pages = pool[n, torch.as_tensor(table[i], dtype=torch.long, device=pool.device)]  # [pps, Hkv, 64, hd]
+    return pages.permute(1, 0, 2, 3).reshape(pool.shape[2], -1, pool.shape[4])
+
+
+def set_seq_rows(pool, n, i, table, rows):
+    """Write rows [Hkv, Cmax, hd] of sequence i in layer n (through the table when paged)."""
+    if table is None:
+        pool[n, i].copy_(rows)
+        return
+    pr = pool.shape[3]
+    for q, pg in enumerate(table[i]):
+        pool[n, int(pg)].copy_(rows[:, q * pr:(q + 1) * pr])
 
 
 def run_case(w, sample):
@@ -71,9 +103,16 @@ def run_case(w, sample):
         fb, fy = di.relay_tokens(w)
     base = ctx - tp
     Cmax = int(ctx.max()) + B
+    if w.paged:
+        Cmax = -(-Cmax // di.PAGE_ROWS) * di.PAGE_ROWS
     dev = {n: drafter.to_device_bf16(v) for n, v in bits.items()}
-    dr = drafter.Drafter(w, dev, nb, Cmax, B)
+    pps = Cmax // di.PAGE_ROWS
+    dr = drafter.Drafter(w, dev, nb, Cmax, B, num_pages=nb * pps if w.paged else 0)
     i32 = lambda x: torch.tensor(np.asarray(x, np.int32), device="cuda")
+    table = None
+    if w.paged:  # the bench's seeded shuffled pages
+        table = di.block_table(nb, Cmax, 0)
+        dr.set_block_table(i32(table))
     g = torch.Generator(device="cuda")
     g.manual_seed(5)
     dr.kcache.normal_(generator=g)
@@ -83,8 +122,8 @@ def run_case(w, sample):
         for n in range(w.N):
             kb = di.normal_bf16(f"kc{i}_{n}", (w.Hkv, Cmax, w.hd), 1.0)
             vb = di.normal_bf16(f"vc{i}_{n}", (w.Hkv, Cmax, w.hd), 1.0)
-            dr.kcache[n, i].copy_(drafter.to_device_bf16(kb))
-            dr.vcache[n, i].copy_(drafter.to_device_bf16(vb))
+            set_seq_rows(dr.kcache, n, i, table, drafter.to_device_bf16(kb))
+            set_seq_rows(dr.vcache, n, i, table, drafter.to_device_bf16(vb))
             cache.K[n][si][:] = orc.widen(kb)
             cache.V[n][si][:] = orc.widen(vb)
     hv = di.verifier_rows(w, B, name="hv_full")
@@ -110,12 +149,12 @@ def run_case(w, sample):
                                    relay_y=None if fy is None else fy[s])
     assert np.array_equal(new_len, ctx[s])
     ohid = orc.draft_block(w, W, ids[s], new_len, cache, x0r)
-    K, V = dr.kcache, dr.vcache
     for si, i in enumerate(sample):
         lo, hi = int(base[i]), int(ctx[i])
         for n in range(w.N):
-            assert_close(K[n, i, :, lo:hi].float().cpu().numpy(), cache.K[n][si][:, lo:hi], f"K_c seq {i}")
-            assert_close(V[n, i, :, lo:hi].float().cpu().numpy(), cache.V[n][si][:, lo:hi], f"V_c seq {i}")
+            gK, gV = seq_rows(dr.kcache, n, i, table), seq_rows(dr.vcache, n, i, table)
+            assert_close(gK[:, lo:hi].float().cpu().numpy(), cache.K[n][si][:, lo:hi], f"K_c seq {i}")
+            assert_close(gV[:, lo:hi].float().cpu().numpy(), cache.V[n][si][:, lo:hi], f"V_c seq {i}")
         if relay:
             assert_close(x0[i].float().cpu().numpy(), x0r[si], f"x0_relay seq {i}")
         gh = hid[i].float().cpu().numpy().astype(np.float64)
@@ -130,8 +169,53 @@ def run_case(w, sample):
     odraft, _ = orc.topk(ol, 1)
     odraft = odraft[..., 0]
 
-    # LM head at full vocabulary, stage-wise on seeded hidden rows both sides read
+    # End to end. The GPU's step carries its own hidden (bf16 storage, fp32 accumulation),
+    # bounded against the oracle's exact hidden above, so the two sides' logits differ per
+    # row by eps = max_v |z_gpu - z_oracle| (the hidden difference seen through W_lm).
+    #  (1) The LM head and top-k on the step's own hidden: the GPU's ids and values against
+    #      the fp64 logits of the GPU's hidden rows, margin rule with delta = 2e-3 (same
+    #      inputs on both sides, fp32 against fp64 accumulation).
+    #  (2) Against the oracle: every top-k decision whose oracle margin exceeds 2 eps + 2e-3
+    #      must be the oracle's (a drift of eps cannot reorder it); eps is bounded by
+    #      LOGIT_DRIFT. The draft ids (top-1) must equal the oracle's wherever the oracle's
+    #      margin exceeds the stated delta = 1e-2 max(1, |v|); with top-1 gaps distributed
+    #      as the spacing of the largest of V Gaussian logits (mean ~0.26 here), 70-95% of
+    #      the offsets have a margin above delta, and at least 60% is required.
     ns = len(sample)
+    s_ids, s_vals = tid[s].cpu().numpy(), tv[s].cpu().numpy()
+    gl = orc.lm_logits(W, f64(hid[s]))
+    und_self = check_topk(s_ids, s_vals, gl, k, "top-k on the step's own hidden", abs_delta=2e-3)
+    eps = np.abs(gl - ol).max(axis=-1)                      # [ns, B-1]
+    assert eps.max() <= LOGIT_DRIFT, f"end-to-end logit drift {eps.max():.4f} > {LOGIT_DRIFT}"
+    cols = np.arange(w.V)
+    und_e2e = 0
+    top1_fixed = np.zeros((ns, B - 1), bool)               # top-1 margin above 2 eps + 2e-3
+    top1_stated = np.zeros((ns, B - 1), bool)              # top-1 margin above the stated delta
+    for si in range(ns):
+        for t in range(B - 1):
+            order = np.lexsort((cols, -ol[si, t]))[:k + 1]
+            v = ol[si, t, order]
+            thr = 2 * eps[si, t] + 2e-3
+            top1_stated[si, t] = v[0] - v[1] > 1e-2 * max(1.0, abs(v[0]))
+            for j in range(k):
+                if (j == 0 or v[j - 1] - v[j] > thr) and v[j] - v[j + 1] > thr:
+                    assert s_ids[si, t, j] == order[j], (f"end-to-end top-k seq {sample[si]} offset {t + 1} "
+                                                         f"pos {j}: {s_ids[si, t, j]} vs {order[j]}")
+                    top1_fixed[si, t] |= j == 0
+                else:
+                    und_e2e += 1
+    agree_stated = (s_ids[..., 0] == odraft)[top1_stated].mean() if top1_stated.any() else 1.0
+    # the draft itself (top-1): the GPU's id equals the oracle's wherever the oracle's margin
+    # exceeds the stated delta (every sampled workload meets this although eps can exceed
+    # delta: a top-1 gap is rarely within the drift)
+    assert agree_stated == 1.0, f"end-to-end draft ids differ above the stated margin: {agree_stated:.3f}"
+    assert top1_stated.mean() >= 0.6, f"only {top1_stated.mean():.3f} of the top-1 margins exceed delta"
+    print(f"{w.name}: logit drift eps max {eps.max():.4f} mean {eps.mean():.4f}; top-1 above the stated "
+          f"delta {top1_stated.mean():.3f} (GPU equal there {agree_stated:.3f}), above 2 eps "
+          f"{top1_fixed.mean():.3f}; top-k positions within the drift {und_e2e}/{ns * (B - 1) * k}; "
+          f"own-hidden top-k under 2e-3: {und_self}")
+
+    # LM head at full vocabulary, stage-wise on seeded hidden rows both sides read
     hs_bits = di.normal_bf16(f"hidden_stage_{w.name}", (ns, B, w.D), 1.0)
     sid = torch.empty(ns, B - 1, k, dtype=torch.int32, device="cuda")
     sv = torch.empty(ns, B - 1, k, dtype=torch.float32, device="cuda")
@@ -172,6 +256,10 @@ def run_case(w, sample):
     gd = gdraft.cpu().numpy()
     same = np.array([(gd[j, :min(int(ot[j]), B - 1)] == odraft[j, :min(int(ot[j]), B - 1)]).all()
                      for j in range(ns)])
+    # a sequence whose examined prefix is decided at every offset must have drafted the
+    # oracle's tokens there (checked above), so it takes part in the comparison
+    decided_prefix = np.array([top1_fixed[j, :min(int(ot[j]), B - 1)].all() for j in range(ns)])
+    assert same[decided_prefix].all(), f"drafts equal on the examined prefix: {same}, decided {decided_prefix}"
     assert np.array_equal(tau.cpu().numpy()[same], ot[same]) and np.array_equal(bonus.cpu().numpy()[same], ob[same])
     # the accept stage at this shape on the oracle's draft, which both sides read: exact
     tau2 = i32(np.zeros(ns))
@@ -179,7 +267,8 @@ def run_case(w, sample):
     dr.accept(ns, i32(odraft), i32(target), tau2, bonus2)
     assert np.array_equal(tau2.cpu().numpy(), ot) and np.array_equal(bonus2.cpu().numpy(), ob)
     print(f"{w.name}: sample {sample}: {und} of {ns * (B - 1) * k} stage top-k positions under the margin; "
-          f"{int(same.sum())}/{ns} drafts equal to the oracle's on the examined prefix")
+          f"{int(same.sum())}/{ns} drafts equal to the oracle's on the examined prefix "
+          f"({int(decided_prefix.sum())} decided there)")
 
 
 def test_fullsize_qwen3_4b_b16_nb1():
@@ -193,6 +282,17 @@ def test_fullsize_qwen3_8b_b16_nb8():
 def test_fullsize_qwen3_8b_b8_ragged_nb64():
     ctx = di.context_lengths(di.SWEEP_NB64)
     run_case(di.SWEEP_NB64, [int(np.argmin(ctx)), int(np.argmax(ctx))])
+
+
+def test_fullsize_paged_qwen3_8b_b16_nb8():
+    """The 8-sequence workload with the caches as page pools behind the bench's seeded
+    shuffled block table ([DFlash] 四、推理流程, the engineering note on reusing projected K/V)."""
+    run_case(di.PAGED_KV, [0, 5])
+
+
+def test_fullsize_paged_b8_ragged_nb64():
+    ctx = di.context_lengths(di.PAGED_KV_NB64)
+    run_case(di.PAGED_KV_NB64, [int(np.argmin(ctx)), int(np.argmax(ctx))])
 
 
 def test_fullsize_relay_dflash2_nb32():

@@ -490,3 +490,58 @@ def test_bounded_wait_times_out_and_context_survives():
     assert dr2.status() == dflash.DFLASH_OK
     want = orc.draft_block(w, W, di.block_ids(w, [3]), [0], orc.KVCache(w.N, 1, w.Hkv, 80, w.hd))
     assert_close(f64(out), want, "hidden after a timed-out call")
+
+
+# ----------------------------------------------------------------------------- shared K/V projection
+
+def test_shared_context_and_block_kv_projection():
+    """The shared-projection variant ([DFlash] 二、块扩散草稿: the attention equations write
+    W^K_c, W^V_c for the context and W^K_b, W^V_b for the block; reading c4 keeps them
+    separate and obtains the shared form by aliasing): every layer's Wk_c / Wv_c pointers
+    are the k_b / v_b row blocks of the same layer's fused W_qkv. The oracle runs with the
+    same aliased matrices; a whole step (prefill, append, draft, LM head) matches it."""
+    _, drafter = lib()
+    w = MEDIUM
+    bits = di.make_weights(w)
+    qd, kd = w.Hq * w.hd, w.Hkv * w.hd
+    for n in range(w.N):
+        qkv = bits[f"layer{n}.W_qkv"]
+        bits[f"layer{n}.Wk_c"] = qkv[qd:qd + kd]
+        bits[f"layer{n}.Wv_c"] = qkv[qd + kd:qd + 2 * kd]
+    dev = {k: drafter.to_device_bf16(v) for k, v in bits.items() if ".Wk_c" not in k and ".Wv_c" not in k}
+    for n in range(w.N):  # views into W_qkv: the library reads the same memory for both
+        qkv = dev[f"layer{n}.W_qkv"]
+        dev[f"layer{n}.Wk_c"] = qkv[qd:qd + kd]
+        dev[f"layer{n}.Wv_c"] = qkv[qd + kd:qd + 2 * kd]
+        assert dev[f"layer{n}.Wk_c"].data_ptr() == qkv.data_ptr() + qd * w.D * 2
+    Cmax, C = 96, 70
+    dr = drafter.Drafter(w, dev, w.nb, Cmax, C)
+    W = orc.widen_all(bits)
+    nb = w.nb
+    hv_pre = di.verifier_rows(w, C, name="hv_prefill_shared")
+    tp = np.minimum(di.tau_prev(w), w.B).astype(np.int32)
+    ctx = i32(np.zeros(nb, np.int32))
+    dr.ctx_project(nb, C, bf16(hv_pre), i32(C - tp), ctx)
+    cache = orc.KVCache(w.N, nb, w.Hkv, Cmax, w.hd)
+    lens, _ = orc.ctx_project(w, W, orc.widen(hv_pre), C - tp, np.zeros(nb), cache)
+    hv = di.verifier_rows(w, w.B, name="hv_step_shared")
+    dr.ctx_project(nb, w.B, bf16(hv), i32(tp), ctx)
+    ids = di.block_ids(w, di.anchors(w))
+    out = torch.empty(nb, w.B, w.D, dtype=torch.bfloat16, device="cuda")
+    dr.draft_block(nb, i32(ids), ctx, out, max_ctx_hint=C)
+    k = w.k_top
+    tid = torch.empty(nb, w.B - 1, k, dtype=torch.int32, device="cuda")
+    tv = torch.empty(nb, w.B - 1, k, dtype=torch.float32, device="cuda")
+    tl = torch.empty(nb, w.B - 1, w.V, dtype=torch.float32, device="cuda")
+    dr.lm_head_topk(nb, out, k, tid, tv, tl)
+    assert dr.status() == 0
+    o = orc.draft_step(w, W, orc.widen(hv), tp, lens, cache, ids, np.zeros((nb, w.B), np.int32))
+    assert np.array_equal(ctx.cpu().numpy(), o["ctx_len"])
+    gk = f64(dr.kcache)
+    for n in range(w.N):  # the appended context rows use the shared (block) projection
+        for i in range(nb):
+            assert_close(gk[n, i, :, :int(o["ctx_len"][i])], cache.K[n][i][:, :int(o["ctx_len"][i])],
+                         f"K_c layer {n} seq {i}")
+    assert_close(f64(out), o["hidden"], "hidden (shared projection)")
+    assert_close(tl.cpu().numpy(), o["logits"], "logits (shared projection)")
+    check_topk(tid.cpu().numpy(), tv.cpu().numpy(), o["logits"], k, "top-k (shared projection)")
