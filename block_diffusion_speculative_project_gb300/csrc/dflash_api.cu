@@ -840,8 +840,9 @@ int lm_head_impl(dflash_handle_t h, int nb, const void *hidden, int k, int32_t *
   // the per-range partial lists in the workspace hold num_sms ranges: check the plan
   // before the launch writes them
   int tpc = 0, ranges = 0;
-  topk_range_plan((c.V + kBNTopk - 1) / kBNTopk, (Ml + p.tile_rows - 1) / p.tile_rows, h->num_sms, &tpc,
-                  &ranges);
+  const int ms = gemm_mstack(EPI_TOPK, kBNTopk, Ml, p.tile_rows, c.V, 1, 1, 0, h->num_sms);
+  topk_range_plan((c.V + kBNTopk - 1) / kBNTopk, (Ml + ms * p.tile_rows - 1) / (ms * p.tile_rows), h->num_sms,
+                  &tpc, &ranges);
   if (ranges > h->num_sms) return fail(DFLASH_ERR_UNSUPPORTED_SHAPE, "top-k ranges exceed the workspace plan");
   DF_TRY(run_gemm(h, p, kBNTopk, s));
   if (p.items / p.m_tiles != ranges) return fail(DFLASH_ERR_CUDA, "LM-head range plan mismatch");
@@ -912,7 +913,8 @@ int dflash_lm_head_topk_noalloc(dflash_handle_t h, int nb, const void *hidden, i
   const int Ml = nb * R;
   // The LM-head launch's own work split (vocabulary ranges x row tiles), from the planner
   // the launch uses, so the size check below holds for what the kernel writes.
-  const int m_tiles = (Ml + S * R - 1) / (S * R);
+  const int ms = gemm_mstack(EPI_TOPK, kBNTopk, Ml, S * R, c.V, 1, 1, 0, h->num_sms);
+  const int m_tiles = (Ml + ms * S * R - 1) / (ms * S * R);
   const int n_tiles = (c.V + kBNTopk - 1) / kBNTopk;
   int tpc = 0, ranges = 0;
   topk_range_plan(n_tiles, m_tiles, h->num_sms, &tpc, &ranges);

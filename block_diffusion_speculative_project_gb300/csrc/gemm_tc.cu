@@ -18,6 +18,7 @@
 //     memory, in rank order (deterministic), and runs the epilogue on it.
 //   * weights are streamed with an L2 evict-first policy, activations evict-last.
 #include <algorithm>
+#include <cmath>
 #include <cfloat>
 #include <climits>
 
@@ -42,15 +43,23 @@ __host__ __device__ constexpr int gemm_slabs() {
   return (BN == 128 && EPI != EPI_SWIGLU && EPI != EPI_DUAL_F32 && EPI != EPI_TOPK) ? 2 : 1;
 }
 
-template <int BN, int SL>
+// MS: 128-row blocks per tile (M-stacking). With MS = 2 a tile is 256 rows: each weight
+// tile in shared memory feeds two M = 128 MMAs into two accumulators, which doubles the
+// FLOPs per operand byte an SM takes in when there are enough tiles to fill the GPU.
+template <int BN, int SL, int MS = 1>
 struct TileCfg {
   static constexpr int A_SLAB = BM * BK * 2;
   static constexpr int B_SLAB = BN * BK * 2;
-  static constexpr int A_BYTES = SL * A_SLAB;
+  static constexpr int A_BLOCK = SL * A_SLAB;  // one 128-row block of A in a stage
+  static constexpr int A_BYTES = MS * A_BLOCK;
   static constexpr int B_BYTES = SL * B_SLAB;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = (200 * 1024 / STAGE) > 8 ? 8 : (200 * 1024 / STAGE);
-  static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;  // power of two >= 2*BN
+  static constexpr int ACC = MS * BN;  // TMEM columns of one accumulator set
+  // Two accumulator sets (the epilogue of one tile runs under the MMAs of the next) when
+  // they fit in the 512 TMEM columns, else one.
+  static constexpr int NBUF = 2 * ACC <= 512 ? 2 : 1;
+  static constexpr int TMEM_COLS = (NBUF * ACC <= 256) ? 256 : 512;  // power of two >= the sets
   // Cluster split-K reuses the pipeline smem: the staged partial tile (BM rows of
   // RED_STRIDE floats) followed by the reduced row slice (at most BM / 2 rows). The
   // pipeline region is the larger of the stage ring and that; barriers follow it.
@@ -65,9 +74,16 @@ struct TileCfg {
 // 32 threads of a warp hit distinct banks).
 constexpr size_t kTopkStashBytes = 128 * 33 * sizeof(float);
 
-template <int BN, int EPI>
+// Slabs per stage: as the unstacked tile (an M-stacked 128-wide tile takes two 32 KB A
+// copies and one 32 KB B copy per 96 KB stage, two stages in flight).
+template <int BN, int EPI, int MS>
+__host__ __device__ constexpr int gemm_slabs_ms() {
+  return gemm_slabs<BN, EPI>();
+}
+
+template <int BN, int EPI, int MS = 1>
 constexpr size_t gemm_smem_bytes() {
-  return TileCfg<BN, gemm_slabs<BN, EPI>()>::SMEM + (EPI == EPI_TOPK ? kTopkStashBytes : 0);
+  return TileCfg<BN, gemm_slabs_ms<BN, EPI, MS>(), MS>::SMEM + (EPI == EPI_TOPK ? kTopkStashBytes : 0);
 }
 
 struct Item {
@@ -106,12 +122,16 @@ __device__ __forceinline__ Item item_at(const GemmParams &p, int j) {
     return r;
   }
   it = blockIdx.x + j * gridDim.x;
-  r.m = it % p.m_tiles;
-  it /= p.m_tiles;
-  r.n = it % p.n_tiles;
-  it /= p.n_tiles;
-  r.g = it % p.groups;
-  r.s = it / p.groups;
+  {
+    const int per_group = p.rast_gm * p.n_tiles * p.groups;
+    const int grp = it / per_group, rem = it - grp * per_group;
+    const int gm = min(p.rast_gm, p.m_tiles - grp * p.rast_gm);  // the last group may be short
+    r.m = grp * p.rast_gm + rem % gm;
+    const int ng = rem / gm;
+    r.n = ng % p.n_tiles;
+    r.g = ng / p.n_tiles;
+    r.s = 0;
+  }
   return r;
 }
 
@@ -514,10 +534,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
 
 // ------------------------------------------------------------------ kernel
 
-template <int BN, int EPI>
+template <int BN, int EPI, int MS>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
-  using C = TileCfg<BN, gemm_slabs<BN, EPI>()>;
-  static_assert(EPI == EPI_TOPK || C::RED_FITS, "cluster reduction buffers exceed the pipeline smem");
+  constexpr int SLABS = gemm_slabs_ms<BN, EPI, MS>();
+  using C = TileCfg<BN, SLABS, MS>;
+  static_assert(EPI == EPI_TOPK || MS > 1 || C::RED_FITS, "cluster reduction buffers exceed the pipeline smem");
+  static_assert(MS == 1 || EPI != EPI_DUAL_F32, "M-stacked tiles: no dual fp32 epilogue");
+  static_assert(C::NBUF * C::ACC <= 512, "accumulators exceed tensor memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -585,12 +608,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       };
       auto load_a = [&](const Cursor &c, int st) {
         uint8_t *a = sA + st * C::A_BYTES;
-        if (p.slabs == 2)  // A map {64, rows, K/64}: both slabs of the stage in one copy
-          tma_load_3d(a, &p.tmA, &full[st], 0, c.t.m * BM, c.kt * 2, pol_a);
-        else if (p.a_grouped)
-          tma_load_3d(a, &p.tmA, &full[st], c.kt * BK, 0, c.t.m * p.a_S, pol_a);
-        else
-          tma_load_3d(a, &p.tmA, &full[st], c.kt * BK, c.t.m * BM, 0, pol_a);
+#pragma unroll
+        for (int ms = 0; ms < MS; ++ms) {
+          const int row0 = c.t.m * (MS * BM) + ms * BM;
+          if (p.slabs == 2)  // A map {64, rows, K/64}: both slabs of the stage in one copy
+            tma_load_3d(a + ms * C::A_BLOCK, &p.tmA, &full[st], 0, row0, c.kt * 2, pol_a);
+          else if (p.a_grouped)
+            tma_load_3d(a + ms * C::A_BLOCK, &p.tmA, &full[st], c.kt * BK, 0, (c.t.m * MS + ms) * p.a_S, pol_a);
+          else
+            tma_load_3d(a + ms * C::A_BLOCK, &p.tmA, &full[st], c.kt * BK, row0, 0, pol_a);
+        }
       };
       auto load_b = [&](const Cursor &c, int st) {
         uint8_t *b = sB + st * C::B_BYTES;
@@ -654,14 +681,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       bool ok = true;
       for (int j = 0; j < nitems && ok; ++j) {
         const Item t = item_at(p, j);
-        const int buf = j & 1;
-        const uint32_t use = j >> 1;
+        const int buf = j % C::NBUF;
+        const uint32_t use = j / C::NBUF;
         if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, p.max_spin)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * BN;
+        const uint32_t d = tmem_base + buf * C::ACC;
         const int kt0 = t.s * p.kt_per_split;
         const int kt1 = min(p.kt_total, kt0 + p.kt_per_split);
         for (int kt = kt0; kt < kt1; ++kt, ++it) {
@@ -676,13 +703,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
           const uint64_t ad = a_desc0 + static_cast<uint64_t>((st * C::A_BYTES) >> 4);
           const uint64_t bd = b_desc0 + static_cast<uint64_t>((st * C::B_BYTES) >> 4);
 #pragma unroll
-          for (int sl = 0; sl < gemm_slabs<BN, EPI>(); ++sl) {
+          for (int sl = 0; sl < SLABS; ++sl) {
             if (sl >= p.slabs) break;
-            const uint64_t as = ad + static_cast<uint64_t>((sl * C::A_SLAB) >> 4);
             const uint64_t bs = bd + static_cast<uint64_t>((sl * C::B_SLAB) >> 4);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
-              tc_mma_bf16(d, as + 2 * k, bs + 2 * k, idesc, (kt > kt0 || sl > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+              for (int ms = 0; ms < MS; ++ms) {
+                const uint64_t as = ad + static_cast<uint64_t>((ms * C::A_BLOCK + sl * C::A_SLAB) >> 4);
+                tc_mma_bf16(d + ms * BN, as + 2 * k, bs + 2 * k, idesc, (kt > kt0 || sl > 0 || k > 0) ? 1u : 0u);
+              }
           }
           tc_commit(&empty[st]);
         }
@@ -700,22 +730,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     const int q = warp & 3;
     const int r = q * 32 + lane;
     float *stash = stash_base + r * 33;
-    TopkState tk;
-    if constexpr (EPI == EPI_TOPK) topk_init(tk);
+    TopkState tks[MS];
+    TopkState &tk = tks[0];
+    if constexpr (EPI == EPI_TOPK) {
+#pragma unroll
+      for (int ms = 0; ms < MS; ++ms) topk_init(tks[ms]);
+    }
     bool ok = true;
     for (int j = 0; j < nitems; ++j) {
       const Item t = item_at(p, j);
-      const int buf = j & 1;
-      const uint32_t use = j >> 1;
+      const int buf = j % C::NBUF;
+      const uint32_t use = j / C::NBUF;
       if (!mbar_wait(&acc_full[buf], use & 1, p.max_spin)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC;
       const int row = t.m * p.tile_rows + r;
       const bool row_ok = (r < p.tile_rows) && (row < p.M);
-      if (EPI != EPI_TOPK && p.csplit > 1) {
+      if (MS > 1) {
+        // 128-row block ms of the tile: rows (t.m * MS + ms) * tile_rows + r
+#pragma unroll
+        for (int ms = 0; ms < MS; ++ms) {
+          const int row_ms = (t.m * MS + ms) * p.tile_rows + r;
+          auto fetch = [&](int c, float (&v)[32]) { tmem_ld32(taddr + ms * BN + c * 32, v); };
+          epilogue_tile<BN, EPI>(p, t, row_ms, (r < p.tile_rows) && (row_ms < p.M), fetch, tks[ms], stash);
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+      } else if (EPI != EPI_TOPK && p.csplit > 1) {
         // Stage this CTA's partial tile, row r at red[r * RED_STRIDE], in the
         // pipeline smem (every TMA write has landed and every MMA has completed).
         float *red = reinterpret_cast<float *>(smem) + r * C::RED_STRIDE;
@@ -736,10 +780,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     }
     if (!ok) flag_status(p.status, kStatusTimeout);
     if constexpr (EPI == EPI_TOPK) {
+#pragma unroll
+      for (int ms = 0; ms < MS; ++ms) {
+      const TopkState &tk = tks[ms];
       if (ok && nitems > 0) {
         const int m = blockIdx.x % p.m_tiles;
         const int range = blockIdx.x / p.m_tiles;
-        const int row = m * p.tile_rows + r;
+        const int row = (m * MS + ms) * p.tile_rows + r;
         if (r < p.tile_rows && row < p.M) {
           if (p.smp_part) draw_store(p.smp_part + 2 * ((size_t)range * p.M + row), tk.dr);
           // order the members (value descending, ties to the lower id) by rank
@@ -764,6 +811,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
             }
           }
         }
+      }
       }
     }
   }
@@ -923,14 +971,14 @@ struct KernelSetup {
   int cluster_cap[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
 };
 
-template <int BN, int EPI>
+template <int BN, int EPI, int MS>
 static const KernelSetup &kernel_setup() {
   static const KernelSetup setup = [] {
     KernelSetup k;
-    constexpr size_t smem = gemm_smem_bytes<BN, EPI>();
-    k.err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr size_t smem = gemm_smem_bytes<BN, EPI, MS>();
+    k.err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, MS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
-    if (k.err != cudaSuccess || EPI == EPI_TOPK) return k;
+    if (k.err != cudaSuccess || EPI == EPI_TOPK || MS > 1) return k;
     for (int S = 2; S <= 8; ++S) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(S);
@@ -944,7 +992,7 @@ static const KernelSetup &kernel_setup() {
       cfg.attrs = &attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI>, &cfg) != cudaSuccess) {
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, EPI, MS>, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         n = 0;
       }
@@ -955,12 +1003,13 @@ static const KernelSetup &kernel_setup() {
   return setup;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int MS = 1>
 static cudaError_t plan_and_launch(GemmParams &p, int num_sms, cudaStream_t s) {
-  const KernelSetup &ks = kernel_setup<BN, EPI>();
+  const KernelSetup &ks = kernel_setup<BN, EPI, MS>();
   if (ks.err != cudaSuccess) return ks.err;
   if (p.slabs > gemm_slabs<BN, EPI>() || (p.slabs == 2 && (p.a_grouped || p.dual)))
     return cudaErrorInvalidValue;
+  if (MS > 1 && !p.a_grouped && p.tile_rows != BM) return cudaErrorInvalidValue;
   int grid;
   p.csplit = 1;
   if (EPI == EPI_TOPK) {
@@ -970,28 +1019,80 @@ static cudaError_t plan_and_launch(GemmParams &p, int num_sms, cudaStream_t s) {
     topk_range_plan(p.n_tiles, p.m_tiles, num_sms, &p.tiles_per_cta, &ranges);
     grid = ranges * p.m_tiles;
     p.items = grid;
+  } else if (MS > 1) {
+    // M-stacked tiles never split K (chosen only when the tiles fill the GPU)
+    p.splits = 1;
+    p.kt_per_split = p.kt_total;
+    p.items = p.m_tiles * p.n_tiles * p.groups;
+    grid = std::max(1, std::min(p.items, num_sms));
   } else {
     gemm_plan(p.M, p.tile_rows, p.N, p.K, p.groups, p.dual, BN, p.slabs, num_sms, p.epi, ks.cluster_cap,
               &p.splits, &p.kt_per_split, &p.items, &grid, &p.csplit);
   }
-  constexpr size_t smem = gemm_smem_bytes<BN, EPI>();
+  p.rast_gm = std::max(1, p.m_tiles);
+  if (EPI != EPI_TOPK && p.csplit == 1) {
+    // The tiles in flight at once (one per CTA) read A blocks of rast_gm m-tiles and the
+    // weight tiles of grid / rast_gm columns; each block is fetched from DRAM once per
+    // group and shared through L2. rast_gm = sqrt(grid * B tile / A tile) minimises the
+    // bytes one wave of tiles fetches.
+    const double a_tile = (double)MS * BM, b_tile = (double)BN;
+    const int gm = (int)std::lround(std::sqrt((double)grid * b_tile / a_tile));
+    p.rast_gm = std::max(1, std::min(p.m_tiles, gm));
+  }
+  constexpr size_t smem = gemm_smem_bytes<BN, EPI, MS>();
   if (p.csplit > 1)
-    return launch_pdl_cluster(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), smem, s, p.csplit,
+    return launch_pdl_cluster(gemm_tc_kernel<BN, EPI, MS>, dim3(grid), dim3(kGemmThreads), smem, s, p.csplit,
                               p);
-  return launch_pdl(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), smem, s, p);
+  return launch_pdl(gemm_tc_kernel<BN, EPI, MS>, dim3(grid), dim3(kGemmThreads), smem, s, p);
+}
+
+// 128-row blocks per tile (1 or 2) a launch takes. The stackable GEMMs (128-wide: W_c's
+// fp32 store and the K/V cache scatter; the 192-wide SwiGLU pair) stack when the CTA that
+// takes the most tiles (persistent rounds) then takes in fewer operand rows per k column
+// (A rows + B rows per tile times rounds): each stacked tile reads its weight tile once for
+// 256 rows instead of 128. The 128-wide ones hold two 96 KB stages when stacked, so they
+// also need a stacked tile for every SM. Measured and left out: the stacked QKV at 512 rows
+// (96 tiles on 96 SMs, 40 -> 43 us) and a stacked LM head (two 256-wide accumulators fill
+// the tensor memory, and its top-k epilogue, no longer under the next tile's MMAs, made the
+// 448-row LM head 0.44 -> 0.72 ms).
+int gemm_mstack(int epi, int BN, int M, int tile_rows, int N, int groups, int a_grouped, int dual, int num_sms) {
+  (void)tile_rows;
+  if (epi == EPI_TOPK) return 1;
+  const bool plain = BN == 128 && !dual && (epi == EPI_F32 || epi == EPI_KV);
+  const bool swiglu = BN == 192 && dual && epi == EPI_SWIGLU;
+  if (a_grouped || !(plain || swiglu) || M <= BM) return 1;
+  const long long cols = (long long)((N + (dual ? BN / 2 : BN) - 1) / (dual ? BN / 2 : BN)) * groups;
+  const long long t1 = (long long)((M + BM - 1) / BM) * cols, t2 = (long long)((M + 2 * BM - 1) / (2 * BM)) * cols;
+  const long long G = std::max(1, num_sms);
+  if (plain && t2 < G) return 1;
+  return ((t2 + G - 1) / G) * (2 * BM + BN) < ((t1 + G - 1) / G) * (BM + BN) ? 2 : 1;
+}
+
+static bool use_mstack(const GemmParams &p, int BN, int num_sms) {
+  return gemm_mstack(p.epi, BN, p.M, p.a_grouped ? p.tile_rows : BM, p.N, p.groups, p.a_grouped, p.dual,
+                     num_sms) == 2;
 }
 
 cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s) {
-  if (p.a_grouped == 0) p.tile_rows = BM;
-  p.m_tiles = (p.M + p.tile_rows - 1) / p.tile_rows;
+  const int ms = use_mstack(p, BN, num_sms) ? 2 : 1;
+  if (p.a_grouped == 0) p.tile_rows = BM;  // rows per 128-lane block; a tile has ms blocks
+  p.m_tiles = (p.M + ms * p.tile_rows - 1) / (ms * p.tile_rows);
   const int ncols = p.dual ? BN / 2 : BN;
   p.n_tiles = (p.N + ncols - 1) / ncols;
   if (p.slabs != 2) p.slabs = 1;
   p.kt_total = (p.K + BK * p.slabs - 1) / (BK * p.slabs);  // stages along K
-  // expect-tx bytes of one stage: the A box plus the B box(es), per slab (a slab past
-  // K is zero-filled by the copy and still counted)
+  // expect-tx bytes of one stage: the A box(es) plus the B box(es), per slab (a slab past
+  // K or rows past M are zero-filled by the copy and still counted)
   const uint32_t a_rows = p.a_grouped ? (uint32_t)p.tile_rows : (uint32_t)BM;
-  p.stage_tx_bytes = (uint32_t)p.slabs * (a_rows * BK * 2 + (uint32_t)BN * BK * 2);
+  p.stage_tx_bytes = (uint32_t)p.slabs * ((uint32_t)ms * a_rows * BK * 2 + (uint32_t)BN * BK * 2);
+  if (ms == 2) {
+    switch (BN * 16 + p.epi) {
+      case 128 * 16 + EPI_F32: return plan_and_launch<128, EPI_F32, 2>(p, num_sms, s);
+      case 128 * 16 + EPI_KV: return plan_and_launch<128, EPI_KV, 2>(p, num_sms, s);
+      case 192 * 16 + EPI_SWIGLU: return plan_and_launch<192, EPI_SWIGLU, 2>(p, num_sms, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (BN * 16 + p.epi) {
     case 128 * 16 + EPI_BF16: return plan_and_launch<128, EPI_BF16>(p, num_sms, s);
     case 128 * 16 + EPI_F32: return plan_and_launch<128, EPI_F32>(p, num_sms, s);

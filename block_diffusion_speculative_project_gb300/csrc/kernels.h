@@ -79,7 +79,7 @@ struct GemmParams {
   CUtensorMap tmA;
   CUtensorMap tmB[kMaxBMaps];
   int M;           // logical rows
-  int tile_rows;   // logical rows per m-tile (<= 128)
+  int tile_rows;   // logical rows per 128-lane block (<= 128); an m-tile holds MS blocks
   int a_grouped;   // 0: tile m loads rows [128m, 128m+128) of dim1; 1: groups [m*S, m*S+S)
   int a_S;         // groups per tile when a_grouped
   int N;           // output columns per group (per weight when dual)
@@ -87,6 +87,9 @@ struct GemmParams {
   int m_tiles, n_tiles, groups, dual, splits;
   int kt_total, kt_per_split;
   int items;       // m_tiles * n_tiles * groups * splits
+  int rast_gm;     // persistent tile order: groups of rast_gm m-tiles, m fastest inside a
+                   // group, then the column tile, then the weight group (rast_gm = m_tiles:
+                   // plain m-fastest order)
   uint32_t stage_tx_bytes;
   int epi;
   void *out;
@@ -165,6 +168,9 @@ int gemm_tiles(int M, int tile_rows, int N, int groups, int dual, int BN);
 // ranges <= max(1, num_sms / m_tiles). The launch and every buffer sized per range use
 // this one plan.
 void topk_range_plan(int n_tiles, int m_tiles, int num_sms, int *tiles_per_cta, int *ranges);
+// 128-row blocks per tile (1 or 2) gemm_launch takes for these launch parameters (tile_rows:
+// rows per 128-lane block); a launch's m_tiles = ceil(M / (blocks * tile_rows)).
+int gemm_mstack(int epi, int BN, int M, int tile_rows, int N, int groups, int a_grouped, int dual, int num_sms);
 
 // ---------------------------------------------------------------- small kernels
 

@@ -545,3 +545,47 @@ def test_shared_context_and_block_kv_projection():
     assert_close(f64(out), o["hidden"], "hidden (shared projection)")
     assert_close(tl.cpu().numpy(), o["logits"], "logits (shared projection)")
     check_topk(tid.cpu().numpy(), tv.cpu().numpy(), o["logits"], k, "top-k (shared projection)")
+
+
+# ----------------------------------------------------------------------------- stacked tiles
+
+def test_wide_batch_takes_stacked_tiles():
+    """320 sequences of the medium drafter (22,400 prefill rows, 5,120 block rows): the
+    context projection's W_c and K/V GEMMs (prefill and step) and the SwiGLU gate|up GEMM run
+    256-row M-stacked tiles, every GEMM visits its tiles in groups of row tiles, and the LM
+    head has 38 row tiles. Sequences are independent, so three of them (first, middle,
+    last) against the oracle fix the result: appended K/V rows, hidden, logits and top-k."""
+    w = MEDIUM.with_(name="medium_wide_batch_nb320", nb=320)
+    nb, B, k = w.nb, w.B, w.k_top
+    Cmax, C = 96, 70
+    dr, W, _ = make(w, Cmax, C)
+    sample = [0, nb // 2 - 3, nb - 1]
+    hv_pre = di.verifier_rows(w, C, name="hv_prefill_wide")
+    tp = np.minimum(di.tau_prev(w), B).astype(np.int32)
+    pre = (C - tp).astype(np.int32)
+    ctx = i32(np.zeros(nb, np.int32))
+    dr.ctx_project(nb, C, bf16(hv_pre), i32(pre), ctx)
+    hv = di.verifier_rows(w, B, name="hv_step_wide")
+    dr.ctx_project(nb, B, bf16(hv), i32(tp), ctx)
+    ids = di.block_ids(w, di.anchors(w))
+    out = torch.empty(nb, B, w.D, dtype=torch.bfloat16, device="cuda")
+    dr.draft_block(nb, i32(ids), ctx, out, max_ctx_hint=C)
+    tid = torch.empty(nb, B - 1, k, dtype=torch.int32, device="cuda")
+    tv = torch.empty(nb, B - 1, k, dtype=torch.float32, device="cuda")
+    tl = torch.empty(nb, B - 1, w.V, dtype=torch.float32, device="cuda")
+    dr.lm_head_topk(nb, out, k, tid, tv, tl)
+    assert dr.status() == 0
+    s = np.array(sample)
+    cache = orc.KVCache(w.N, len(sample), w.Hkv, Cmax, w.hd)
+    lens, _ = orc.ctx_project(w, W, orc.widen(hv_pre[s]), pre[s], np.zeros(len(sample)), cache)
+    o = orc.draft_step(w, W, orc.widen(hv[s]), tp[s], lens, cache, ids[s], np.zeros((len(sample), B), np.int32))
+    assert np.array_equal(ctx.cpu().numpy()[s], o["ctx_len"])
+    gk, gv = dr.kcache, dr.vcache
+    for si, i in enumerate(sample):
+        L = int(o["ctx_len"][si])
+        for n in range(w.N):
+            assert_close(f64(gk[n, i, :, :L]), cache.K[n][si][:, :L], f"K rows seq {i} layer {n}")
+            assert_close(f64(gv[n, i, :, :L]), cache.V[n][si][:, :L], f"V rows seq {i} layer {n}")
+    assert_close(f64(out[s]), o["hidden"], "hidden (stacked tiles)")
+    assert_close(tl[s].cpu().numpy(), o["logits"], "logits (stacked tiles)")
+    check_topk(tid[s].cpu().numpy(), tv[s].cpu().numpy(), o["logits"], k, "top-k (stacked tiles)")
