@@ -169,7 +169,9 @@ DFLASH_API int dflash_set_weights(dflash_handle_t h, const dflash_weights *w);
 DFLASH_API int dflash_set_block_table(dflash_handle_t h, const int32_t *table);
 
 /* Bytes of workspace every step call of this handle needs (sized for max_batch,
- * max_proj_rows and Cmax). The caller allocates it (256-byte aligned). */
+ * max_proj_rows and Cmax). The caller allocates it (256-byte aligned) and zero-fills it
+ * once before the first call: its first word is the device status word, which the
+ * kernels only OR into (dflash_status reads and clears it). */
 DFLASH_API int dflash_workspace_size(dflash_handle_t h, size_t *bytes);
 
 /* Synchronise `stream`, read and clear the device status word in `ws`.
