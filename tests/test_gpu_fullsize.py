@@ -14,9 +14,11 @@ from fp64 by max 0.044-0.072, max |err|/(1+|o|) 0.034-0.056, mean 0.0083-0.0098,
 96.0-98.5% of elements within the stated tolerance. The GPU adds an independent rounding
 noise of the same size (its pre-rounding values are fp32, not fp64, so some bf16 roundings
 land on the other side; RoPE angles in fp32), so its error is expected within sqrt(2) of
-the model's. The end-to-end comparison therefore requires |g - o| <= 0.1 (1 + |o|)
-(sqrt(2) x 0.056 with 25% margin), a mean error <= 0.015 (1.5 x the model's largest
-mean) and >= 93% of the elements within the stated tolerance.
+the model's. Measured, the GPU's hidden deviates as the model's does (max 0.044-0.076,
+mean 0.0082-0.0101, 95.9-98.6% within the stated tolerance on the seven workloads), so the
+end-to-end comparison requires |g - o| <= 0.08 (1 + |o|) (the model's largest 0.056 with
+40% margin), a mean error <= 0.0125 (1.25 x the model's largest mean) and >= 95% of the
+elements within the stated tolerance.
 
 End-to-end ids: the GPU's logits drift from the oracle's by eps = max_v |z_gpu - z_oracle|
 per row (the hidden difference seen through W_lm; 0.056-0.091 measured, up to 0.074 in
@@ -42,10 +44,10 @@ from oracle import dflash_oracle as orc
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-HIDDEN_ATOL = 0.1
-HIDDEN_RTOL = 0.1
-HIDDEN_MEAN = 0.015
-STATED_FRACTION = 0.93
+HIDDEN_ATOL = 0.08
+HIDDEN_RTOL = 0.08
+HIDDEN_MEAN = 0.0125
+STATED_FRACTION = 0.95
 # End-to-end logit drift bound: the bf16 storage model's logits of the sampled sequences
 # deviate from the exact oracle's by up to 0.053 (Qwen3-4B shape) and 0.074 (Qwen3-8B
 # shape) at any vocabulary entry; twice the larger.
