@@ -9,8 +9,13 @@
 //     epilogue; each epilogue warp owns the TMEM lane quarter (warp % 4).
 //   * an mbarrier ring of STAGES smem slots couples TMA and MMA; tcgen05.commit
 //     frees a slot when the MMAs that read it complete.
-//   * two TMEM accumulators (2*BN columns) let the epilogue of one work item run
-//     under the MMAs of the next; CTAs are persistent over work items.
+//   * two TMEM accumulator sets let the epilogue of one work item run under the MMAs
+//     of the next (one set when two do not fit the 512 columns); CTAs are persistent
+//     over work items, visited in groups of row tiles (rast_gm) so that the tiles of one
+//     wave share their A blocks and weight tiles through L2.
+//   * M-stacking (template MS = 2): a work item is two 128-row blocks; each weight tile in
+//     smem feeds two M = 128 MMAs into two accumulators (more FLOPs per operand byte an
+//     SM takes in), for launches with many row tiles (gemm_mstack).
 //   * split-K across a thread-block cluster: the S CTAs of a cluster each reduce a
 //     1/S slice of K for the same output tile, stage their fp32 partial in their own
 //     (now idle) pipeline smem, and after a hardware cluster barrier every CTA sums
