@@ -176,7 +176,7 @@ def max_over_ranks(values, device=None):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def measure_workload(args, w, weights, dev, world, steps, warmup, full=True):
+def measure_workload(w, weights, dev, world, steps, warmup, full=True):
     """Set up one workload on this GPU (caches, context prefill, step inputs), capture its
     step in a CUDA graph and time `steps` replays; with `full`, also the LM head inside the
     step, the end-to-end leg through host buffers and the prompt prefill. Returns the raw
@@ -469,12 +469,12 @@ def run_gpu(args, rank, world):
     bits = di.make_weights(w, 0)
     weights = {k: to_device_bf16(v, dev) for k, v in bits.items()}
     t_gen = time.time() - t0
-    m = measure_workload(args, w, weights, dev, world, args.steps, args.warmup, full=True)
+    m = measure_workload(w, weights, dev, world, args.steps, args.warmup, full=True)
     extra = {}
     if args.workload == DEFAULT_WORKLOAD and not args.no_extra_workloads:
         for name in EXTRA_WORKLOADS:
             torch.cuda.empty_cache()
-            m2 = measure_workload(args, di.WORKLOADS[name], weights, dev, world, max(args.steps, 100),
+            m2 = measure_workload(di.WORKLOADS[name], weights, dev, world, max(args.steps, 100),
                                   args.warmup, full=False)
             extra[name] = step_summary(m2, world)
             extra[name]["steps"] = max(args.steps, 100)
@@ -486,7 +486,7 @@ def run_gpu(args, rank, world):
     if rank != 0:
         return None
     hbm, tf_burst, tf_sus, src = load_peaks()
-    total_bytes, flops, wbytes, kvbytes = step_bytes_flops(w, ctx, tp)
+    total_bytes, flops, _, _ = step_bytes_flops(w, ctx, tp)
     lm_bytes = 2 * w.V * w.D + 2 * w.nb * (w.B - 1) * w.D + 8 * w.nb * (w.B - 1) * k
     if w.temperature > 0 and not w.flags & di.FLAG_SELECT:
         lm_bytes += 4 * w.nb * (w.B - 1) * w.V  # the fp32 logits the draw reads
