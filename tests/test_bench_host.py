@@ -57,3 +57,20 @@ def test_optional_weights_are_counted():
 def test_launches_per_default_step_match_the_launch_list():
     assert bench.kernels_per_step(di.QWEN3_8B) == 117 // 3
     assert bench.kernels_per_step(di.PAGED_KV) == bench.kernels_per_step(di.QWEN3_8B)
+
+
+def test_step_summary_of_a_measured_workload():
+    """The `workloads` entry of the bench line: blocks/s = sequences / step time and the
+    step's roofline fraction = max(bytes / HBM, FLOPs / sustained bf16) / step time."""
+    w = di.SWEEP_NB64
+    ctx = di.context_lengths(w).astype(np.int32)
+    tp = di.tau_prev(w).astype(np.int32)
+    m = dict(w=w, ctx=ctx, tp=tp, ms_step=2.5, clk=None, tau=np.full(w.nb, 3))
+    out = bench.step_summary(m, world=1)
+    assert abs(out["value"] - 64 / 2.5e-3) < 1e-6 * out["value"]
+    assert out["draft_tokens_per_s"] == round(out["value"] * 7, 1)
+    hbm, tf_burst, tf_sus, _ = bench.load_peaks()
+    total, flops, _, _ = bench.step_bytes_flops(w, ctx, tp)
+    roof = max(total / (hbm * 1e9), flops / ((tf_sus or tf_burst) * 1e12))
+    assert abs(out["step_roofline"]["frac"] - round(roof * 1e3 / 2.5, 4)) < 1e-9
+    assert out["config"]["nb_per_gpu"] == 64 and out["config"]["B"] == 8
