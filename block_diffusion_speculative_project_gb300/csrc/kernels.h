@@ -70,6 +70,7 @@ enum GemmEpi : int {
 };
 
 constexpr int kMaxBMaps = 12;
+constexpr int kMaxBlock = 16;  // largest block size B (dflash_create checks 2 <= B <= 16)
 constexpr int kTopkMax = 16;
 
 // Kernel parameters of the tcgen05 GEMM  D[M, N] = A[M, K] * B[N, K]^T.

@@ -135,18 +135,16 @@ __global__ void __launch_bounds__(256) relay_len_kernel(const uint16_t *h, int R
                                                         int *status) {
   griddep_wait();
   griddep_launch();
-  const int i = blockIdx.x;
+  const int i = blockIdx.x, j = blockIdx.y;  // sequence, block offset (one row per CTA)
   if (x0) {
     const int a = relay_a ? relay_a[i] : INT_MAX / 2;
-    for (int j = 0; j < B; ++j) {
-      const int k = j + a;
-      const bool take = relay_a && j >= 2 && j <= B - 1 - a && k < R && a >= 0;
-      uint4 *dst = reinterpret_cast<uint4 *>(x0 + ((size_t)i * B + j) * D);
-      const uint4 *src = take ? reinterpret_cast<const uint4 *>(h + ((size_t)i * R + k) * D) : nullptr;
-      for (int c = threadIdx.x; c < D / 8; c += 256) dst[c] = take ? src[c] : make_uint4(0, 0, 0, 0);
-    }
+    const int k = j + a;
+    const bool take = relay_a && j >= 2 && j <= B - 1 - a && k < R && a >= 0;
+    uint4 *dst = reinterpret_cast<uint4 *>(x0 + ((size_t)i * B + j) * D);
+    const uint4 *src = take ? reinterpret_cast<const uint4 *>(h + ((size_t)i * R + k) * D) : nullptr;
+    for (int c = threadIdx.x; c < D / 8; c += 256) dst[c] = take ? src[c] : make_uint4(0, 0, 0, 0);
   }
-  if (threadIdx.x == 0 && n_commit) {
+  if (j == 0 && threadIdx.x == 0 && n_commit) {
     const int nl = ctx_len[i] + n_commit[i];
     if (nl > Cmax || n_commit[i] < 0 || n_commit[i] > R) flag_status(status, kStatusCheck);
     ctx_len[i] = min(nl, Cmax);
@@ -157,8 +155,8 @@ cudaError_t launch_relay_and_len(const uint16_t *h, int nb, int R, int B, int D,
                                  const int *relay_a, const int *n_commit, int *ctx_len,
                                  uint16_t *x0_relay, int Cmax, int *status, cudaStream_t s) {
   if (nb <= 0) return cudaSuccess;
-  cudaError_t e = launch_pdl(relay_len_kernel, dim3(nb), dim3(256), 0, s, h, R, B, D, relay_a, n_commit,
-                             ctx_len, x0_relay, Cmax, status);
+  cudaError_t e = launch_pdl(relay_len_kernel, dim3(nb, x0_relay ? B : 1), dim3(256), 0, s, h, R, B, D, relay_a,
+                             n_commit, ctx_len, x0_relay, Cmax, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -541,22 +539,32 @@ __global__ void conv_apply_kernel(float *x, uint16_t *xb_out, const float *corr,
   const float b0 = bits_to_f32(base[ch]), b1 = bits_to_f32(base[D + ch]);
   float *xb = x + (size_t)i * B * D;
   uint16_t *ob = xb_out ? xb_out + (size_t)i * B * D : nullptr;
-  const float *cb = corr + (size_t)i * B * 2 * ng;
-  float prev = xb[(size_t)(B - 1) * D + ch];
-  for (int t = B - 1; t >= 0; --t) {
-    const float cur = prev;
-    prev = t > 0 ? xb[(size_t)(t - 1) * D + ch] : 0.f;
-    const float k0 = b0 + cb[(size_t)t * 2 * ng + ch / group];
-    const float k1 = b1 + cb[(size_t)t * 2 * ng + ng + ch / group];
-    const float y = k0 * cur + k1 * prev;
-    xb[(size_t)t * D + ch] = y;
-    if (ob) ob[(size_t)t * D + ch] = f32_to_bits(y);
+  const float *cb = corr + (size_t)i * B * 2 * ng + ch / group;
+  // every row of this channel and its two corrections are loaded before any is written
+  // (independent loads in flight together); x_{t-1} is the old row t-1, x_{-1} = 0
+  float xv[kMaxBlock], k0[kMaxBlock], k1[kMaxBlock];
+#pragma unroll
+  for (int t = 0; t < kMaxBlock; ++t) {
+    if (t < B) {
+      xv[t] = xb[(size_t)t * D + ch];
+      k0[t] = b0 + cb[(size_t)t * 2 * ng];
+      k1[t] = b1 + cb[(size_t)t * 2 * ng + ng];
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kMaxBlock; ++t) {
+    if (t < B) {
+      const float y = k0[t] * xv[t] + k1[t] * (t > 0 ? xv[t - 1] : 0.f);
+      xb[(size_t)t * D + ch] = y;
+      if (ob) ob[(size_t)t * D + ch] = f32_to_bits(y);
+    }
   }
 }
 
 cudaError_t launch_conv_apply(float *x, uint16_t *xb_out, const float *corr, const uint16_t *base, int M, int D,
                               int B, int group, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
+  if (B > kMaxBlock) return cudaErrorInvalidValue;
   dim3 grid(M / B, (D + 255) / 256);
   cudaError_t e = launch_pdl(conv_apply_kernel, grid, dim3(256), 0, s, x, xb_out, corr, base, D, B, group);
   if (e != cudaSuccess) return e;
@@ -605,28 +613,36 @@ __global__ void __launch_bounds__(256) select_table_kernel(const float *cand_val
                                                            float *table) {
   griddep_wait();
   griddep_launch();
-  extern __shared__ float gate[];  // [sel]
+  // shared memory: the gate (sel), then the A rows of the previous offset's candidates and
+  // the B rows of this offset's candidates, each row padded to sel + 1 floats so that the
+  // 16 candidate rows a warp reads at once fall in distinct banks
+  extern __shared__ float sm[];
   const int t = blockIdx.x + 1, i = blockIdx.y;
+  const int ld = sel + 1;
+  float *gate = sm;
+  float *As = sm + sel;
+  float *Bs = As + k * ld;
   const float *Gt = G + ((size_t)i * (B - 1) + (t - 1)) * sel;
-  for (int d = threadIdx.x; d < sel; d += blockDim.x) gate[d] = 1.0f / (1.0f + expf(-Gt[d]));
-  __syncthreads();
-  const int ai = threadIdx.x >> 4, b = threadIdx.x & 15;
-  if (b >= k || ai >= k || (t == 1 && ai > 0)) return;
   const int per = 1 + (B - 1) * k;
   const float *ABi = AB + (size_t)i * per * 2 * sel;
-  const int arow = t == 1 ? 0 : 1 + (t - 2) * k + ai;
-  const float4 *ar = reinterpret_cast<const float4 *>(ABi + (size_t)arow * 2 * sel);
-  const float4 *br = reinterpret_cast<const float4 *>(ABi + (size_t)(1 + (t - 1) * k + b) * 2 * sel + sel);
+  const int na = t == 1 ? 1 : k;  // offset 1 starts from the anchor (row 0)
+  for (int d = threadIdx.x; d < sel; d += blockDim.x) gate[d] = 1.0f / (1.0f + expf(-Gt[d]));
+  for (int e = threadIdx.x; e < na * sel; e += blockDim.x) {
+    const int a = e / sel, d = e - a * sel;
+    const int arow = t == 1 ? 0 : 1 + (t - 2) * k + a;
+    As[a * ld + d] = ABi[(size_t)arow * 2 * sel + d];
+  }
+  for (int e = threadIdx.x; e < k * sel; e += blockDim.x) {
+    const int b = e / sel, d = e - b * sel;
+    Bs[b * ld + d] = ABi[(size_t)(1 + (t - 1) * k + b) * 2 * sel + sel + d];
+  }
+  __syncthreads();
+  const int ai = threadIdx.x >> 4, b = threadIdx.x & 15;
+  if (b >= k || ai >= na) return;
+  const float *ar = As + ai * ld, *br = Bs + b * ld;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-  for (int q = 0; q < sel / 4; ++q) {
-    const float4 x = ar[q], y = br[q];
-    const float *g = gate + 4 * q;
-    acc[0] = fmaf(x.x * g[0], y.x, acc[0]);
-    acc[1] = fmaf(x.y * g[1], y.y, acc[1]);
-    acc[2] = fmaf(x.z * g[2], y.z, acc[2]);
-    acc[3] = fmaf(x.w * g[3], y.w, acc[3]);
-  }
+  for (int d = 0; d < sel; ++d) acc[d & 3] = fmaf(ar[d] * gate[d], br[d], acc[d & 3]);
   const size_t tr = (size_t)i * (B - 1) + (t - 1);
   table[(tr * k + ai) * k + b] = cand_vals[tr * k + b] + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
 }
@@ -661,8 +677,15 @@ cudaError_t launch_select_table(const float *cand_vals, const float *AB, const f
                                 int nb, int B, int k, int sel_dim, cudaStream_t s) {
   if (nb <= 0) return cudaSuccess;
   if (k > 16 || sel_dim % 4 || B < 2) return cudaErrorInvalidValue;
-  cudaError_t e = launch_pdl(select_table_kernel, dim3(B - 1, nb), dim3(256), (size_t)sel_dim * sizeof(float), s,
-                             cand_vals, AB, G, B, k, sel_dim, table);
+  const size_t smem = ((size_t)sel_dim + 2 * (size_t)k * (sel_dim + 1)) * sizeof(float);
+  static size_t opted = 48 * 1024;  // dynamic shared memory the kernel is configured for
+  if (smem > opted) {
+    cudaError_t a = cudaFuncSetAttribute(select_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (a != cudaSuccess) return a;
+    opted = smem;
+  }
+  cudaError_t e = launch_pdl(select_table_kernel, dim3(B - 1, nb), dim3(256), smem, s, cand_vals, AB, G, B, k,
+                             sel_dim, table);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -702,8 +725,15 @@ cudaError_t launch_select_walk(const int *cand_ids, const float *cand_vals, cons
                                cudaStream_t s) {
   if (nb <= 0) return cudaSuccess;
   if (k > 16 || sel_dim % 4 || B < 2) return cudaErrorInvalidValue;
-  cudaError_t e = launch_pdl(select_table_kernel, dim3(B - 1, nb), dim3(256), (size_t)sel_dim * sizeof(float), s,
-                             cand_vals, AB, G, B, k, sel_dim, table);
+  const size_t smem = ((size_t)sel_dim + 2 * (size_t)k * (sel_dim + 1)) * sizeof(float);
+  static size_t opted = 48 * 1024;  // dynamic shared memory the kernel is configured for
+  if (smem > opted) {
+    cudaError_t a = cudaFuncSetAttribute(select_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (a != cudaSuccess) return a;
+    opted = smem;
+  }
+  cudaError_t e = launch_pdl(select_table_kernel, dim3(B - 1, nb), dim3(256), smem, s, cand_vals, AB, G, B, k,
+                             sel_dim, table);
   if (e != cudaSuccess) return e;
   e = launch_pdl(select_walk_kernel, dim3(nb), dim3(256), (size_t)(B - 1) * k * (k + 1) * sizeof(float), s, cand_ids,
                  static_cast<const float *>(table), B, k, path);
