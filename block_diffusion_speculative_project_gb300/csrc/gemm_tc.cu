@@ -35,7 +35,18 @@ namespace df {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kGemmThreads = 192;
+// Epilogue warps per CTA: eight for the LM head's top-k (two per TMEM lane quarter, each
+// taking every other 32-column chunk of a tile: with one warp per SM sub-partition this
+// branchy, dependent code runs latency-bound), else four. Warps 0 and 1 are the TMA
+// producer and the MMA issuer.
+template <int EPI>
+__host__ __device__ constexpr int gemm_epi_warps() {
+  return EPI == EPI_TOPK ? 8 : 4;
+}
+template <int EPI>
+__host__ __device__ constexpr int gemm_threads() {
+  return 64 + 32 * gemm_epi_warps<EPI>();
+}
 // Bound of the teardown waits for this CTA's own TMA copies and MMAs, which finish
 // without help from any other thread; independent of the caller's max_spin.
 constexpr int kDrainSpin = 1 << 22;
@@ -70,14 +81,21 @@ struct TileCfg {
   // pipeline region is the larger of the stage ring and that; barriers follow it.
   static constexpr int RED_STRIDE = BN + 4;
   static constexpr size_t RED_BYTES = size_t(BM + BM / 2) * RED_STRIDE * 4;
-  static constexpr size_t PIPE = size_t(STAGES) * STAGE > RED_BYTES ? size_t(STAGES) * STAGE : RED_BYTES;
+  static constexpr bool SPLITS = BN <= 192 && MS == 1;  // top-k and M-stacked tiles never split K
+  static constexpr size_t PIPE =
+      (!SPLITS || size_t(STAGES) * STAGE > RED_BYTES) ? size_t(STAGES) * STAGE : RED_BYTES;
   static constexpr size_t SMEM = 1024 + PIPE + 256;
-  static constexpr bool RED_FITS = RED_BYTES <= PIPE;
+  static constexpr bool RED_FITS = !SPLITS || RED_BYTES <= PIPE;
 };
 
 // Top-k epilogue: a per-thread stash of one 32-value chunk (stride 33 floats, so the
-// 32 threads of a warp hit distinct banks).
-constexpr size_t kTopkStashBytes = 128 * 33 * sizeof(float);
+// 32 threads of a warp hit distinct banks), for each of the 256 epilogue threads.
+constexpr size_t kTopkStashBytes = 256 * 33 * sizeof(float);
+// Row stride (floats, odd: no bank conflicts) of the exchange through which the two
+// epilogue groups of the top-k GEMM see each other's members: group g's values at
+// [32 g, 32 g + 16) and ids at [32 g + 16, 32 g + 32), then the second group's draw
+// (m, s, best, x, id) at [64, 69).
+constexpr int kTopkXchg = 69;
 
 // Slabs per stage: as the unstacked tile (an M-stacked 128-wide tile takes two 32 KB A
 // copies and one 32 KB B copy per 96 KB stage, two stages in flight).
@@ -266,49 +284,41 @@ __device__ __forceinline__ void rope_pair(const GemmParams &p, int pos, int d0, 
   }
 }
 
-// Per-thread top-k state of the LM-head epilogue: an unsorted set of kTopkMax
-// (value, id) pairs in registers plus the position and value of its worst member,
-// which is the threshold a new value has to beat (value descending, ties to the
-// lower id). Replacing the worst member and rescanning for the new worst costs a
-// fixed, branch-free 2*kTopkMax steps, and the code stays small.
+// Per-thread top-k state of the LM-head epilogue: the kTopkMax best (value, id) pairs
+// seen so far, kept sorted in registers (v[0] ranks first: value descending, ties to the
+// lower id), so the last member is the threshold a new value has to beat. Fillers are
+// (-FLT_MAX, id_base + s) with distinct ids. Every step is written as compares and
+// selects: a taken branch costs a lone warp tens of cycles, and the epilogue runs one
+// or two warps per SM sub-partition.
 struct TopkState {
   float v[kTopkMax];
   int id[kTopkMax];
-  float worst_v;
-  int worst_id;
-  int worst_slot;
   DrawState dr;  // the draw at temperature T when sampling (smp_part set)
 };
 
-__device__ __forceinline__ void topk_init(TopkState &tk) {
+__device__ __forceinline__ void topk_init(TopkState &tk, int id_base) {
 #pragma unroll
   for (int s = 0; s < kTopkMax; ++s) {
     tk.v[s] = -FLT_MAX;
-    tk.id[s] = INT_MAX - s;  // distinct sentinels: the highest id is the worst
+    tk.id[s] = id_base + s;  // ascending ids: sorted
   }
-  tk.worst_v = -FLT_MAX;
-  tk.worst_id = INT_MAX;
-  tk.worst_slot = 0;
   draw_init(tk.dr);
 }
 
-__device__ __forceinline__ void topk_replace_worst(TopkState &tk, float v, int id) {
+// Insert (x, xi), which ranks before the last member: it goes to the first position it
+// ranks before, the members from there on move down one place and the last drops out.
+// The compares all read the old members, so they are independent of one another.
+__device__ __forceinline__ void topk_insert(TopkState &tk, float x, int xi) {
+  bool b[kTopkMax];
 #pragma unroll
-  for (int s = 0; s < kTopkMax; ++s)
-    if (s == tk.worst_slot) {
-      tk.v[s] = v;
-      tk.id[s] = id;
-    }
-  tk.worst_v = tk.v[0];
-  tk.worst_id = tk.id[0];
-  tk.worst_slot = 0;
+  for (int s = 0; s < kTopkMax; ++s) b[s] = topk_before(x, xi, tk.v[s], tk.id[s]);
 #pragma unroll
-  for (int s = 1; s < kTopkMax; ++s)
-    if (topk_before(tk.worst_v, tk.worst_id, tk.v[s], tk.id[s])) {
-      tk.worst_v = tk.v[s];
-      tk.worst_id = tk.id[s];
-      tk.worst_slot = s;
-    }
+  for (int s = kTopkMax - 1; s > 0; --s) {
+    tk.v[s] = b[s - 1] ? tk.v[s - 1] : (b[s] ? x : tk.v[s]);
+    tk.id[s] = b[s - 1] ? tk.id[s - 1] : (b[s] ? xi : tk.id[s]);
+  }
+  tk.v[0] = b[0] ? x : tk.v[0];
+  tk.id[0] = b[0] ? xi : tk.id[0];
 }
 
 // Runs the epilogue of one output tile. `fetch(c, v)` returns the 32 fp32 values of
@@ -508,7 +518,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
     }
   } else if constexpr (EPI == EPI_TOPK) {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = cpart; c < BN / 32; c += nparts) {
       float v[32];
       fetch(c, v);
       const int col0 = t.n * BN + c * 32;
@@ -518,7 +528,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
       uint32_t mask = 0;
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        mask |= static_cast<uint32_t>(i < nval && topk_before(v[i], col0 + i, tk.worst_v, tk.worst_id)) << i;
+        mask |= static_cast<uint32_t>((i < nval) & topk_before(v[i], col0 + i, tk.v[kTopkMax - 1], tk.id[kTopkMax - 1]))
+                << i;
       if (mask) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) stash[i] = v[i];
@@ -527,7 +538,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
           const int i = __ffs(mask) - 1;
           mask &= mask - 1;
           const float x = stash[i];
-          if (topk_before(x, col0 + i, tk.worst_v, tk.worst_id)) topk_replace_worst(tk, x, col0 + i);
+          if (topk_before(x, col0 + i, tk.v[kTopkMax - 1], tk.id[kTopkMax - 1])) topk_insert(tk, x, col0 + i);
         }
       }
       // the draw at temperature T (scales v in place, so it runs after the top-k)
@@ -540,11 +551,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
 // ------------------------------------------------------------------ kernel
 
 template <int BN, int EPI, int MS>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(gemm_threads<EPI>(), 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
   constexpr int SLABS = gemm_slabs_ms<BN, EPI, MS>();
   using C = TileCfg<BN, SLABS, MS>;
   static_assert(EPI == EPI_TOPK || MS > 1 || C::RED_FITS, "cluster reduction buffers exceed the pipeline smem");
   static_assert(MS == 1 || EPI != EPI_DUAL_F32, "M-stacked tiles: no dual fp32 epilogue");
+  static_assert(MS == 1 || EPI != EPI_TOPK, "M-stacked tiles: no top-k epilogue");
+  static_assert(EPI != EPI_TOPK || size_t(BM) * kTopkXchg * 4 <= C::PIPE, "top-k exchange exceeds the pipeline smem");
   static_assert(C::NBUF * C::ACC <= 512, "accumulators exceed tensor memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -570,7 +583,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 128);
+      mbar_init(&acc_empty[b], 32 * gemm_epi_warps<EPI>());
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -734,12 +747,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
     griddep_wait();
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    float *stash = stash_base + r * 33;
+    const int eg = (warp - 2) >> 2;  // epilogue group: 0, or 1 for the second top-k group
+    float *stash = stash_base + ((warp - 2) * 32 + lane) * 33;
     TopkState tks[MS];
     TopkState &tk = tks[0];
     if constexpr (EPI == EPI_TOPK) {
 #pragma unroll
-      for (int ms = 0; ms < MS; ++ms) topk_init(tks[ms]);
+      for (int ms = 0; ms < MS; ++ms) topk_init(tks[ms], INT_MAX - 2 * kTopkMax + 1 + eg * kTopkMax);
     }
     bool ok = true;
     for (int j = 0; j < nitems; ++j) {
@@ -778,45 +792,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
         }
       } else {
         auto fetch = [&](int c, float (&v)[32]) { tmem_ld32(taddr + c * 32, v); };
-        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, tk, stash);
+        constexpr int ng = gemm_epi_warps<EPI>() / 4;  // groups sharing a row's chunks
+        epilogue_tile<BN, EPI>(p, t, row, row_ok, fetch, tk, stash, ng > 1 ? eg : 0, ng);
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
       }
     }
     if (!ok) flag_status(p.status, kStatusTimeout);
     if constexpr (EPI == EPI_TOPK) {
+      // The two groups' sorted sets meet through the pipeline smem (every MMA has completed
+      // and every copy has landed once the last accumulator was ready). A member's rank in
+      // the union is its place in its own set plus the other set's members that rank before
+      // it; the members of rank < k are the CTA's partial, written straight to their
+      // places. The fillers' ids are distinct across the groups, so the ranks are too. The
+      // first group also merges the second group's draw. Every epilogue thread reaches the
+      // barrier.
+      float *xg = reinterpret_cast<float *>(smem) + r * kTopkXchg;
 #pragma unroll
-      for (int ms = 0; ms < MS; ++ms) {
-      const TopkState &tk = tks[ms];
-      if (ok && nitems > 0) {
-        const int m = blockIdx.x % p.m_tiles;
-        const int range = blockIdx.x / p.m_tiles;
-        const int row = (m * MS + ms) * p.tile_rows + r;
-        if (r < p.tile_rows && row < p.M) {
-          if (p.smp_part) draw_store(p.smp_part + 2 * ((size_t)range * p.M + row), tk.dr);
-          // order the members (value descending, ties to the lower id) by rank
-          float *pv = p.part_vals + ((size_t)range * p.M + row) * p.topk_k;
-          int *pi = p.part_ids + ((size_t)range * p.M + row) * p.topk_k;
-#pragma unroll 1
-          for (int a = 0; a < kTopkMax; ++a) {
-            float va = -FLT_MAX;
-            int ia = INT_MAX;
+      for (int s2 = 0; s2 < kTopkMax; ++s2) {
+        xg[eg * 32 + s2] = tk.v[s2];
+        xg[eg * 32 + kTopkMax + s2] = __int_as_float(tk.id[s2]);
+      }
+      if (eg == 1) {
+        xg[64] = tk.dr.m;
+        xg[65] = tk.dr.s;
+        xg[66] = tk.dr.best;
+        xg[67] = tk.dr.x;
+        xg[68] = __int_as_float(tk.dr.id);
+      }
+      named_bar_sync(2, 32 * gemm_epi_warps<EPI>());
+      const int m = blockIdx.x % p.m_tiles;
+      const int range = blockIdx.x / p.m_tiles;
+      const int row = m * p.tile_rows + r;
+      if (ok && nitems > 0 && r < p.tile_rows && row < p.M) {
+        const float *ov = xg + (1 - eg) * 32;
+        float w[kTopkMax];
+        int wi[kTopkMax];
 #pragma unroll
-            for (int s = 0; s < kTopkMax; ++s)
-              if (s == a) {
-                va = tk.v[s];
-                ia = tk.id[s];
-              }
-            int rank = 0;
+        for (int s2 = 0; s2 < kTopkMax; ++s2) {
+          w[s2] = ov[s2];
+          wi[s2] = __float_as_int(ov[kTopkMax + s2]);
+        }
+        float *pv = p.part_vals + ((size_t)range * p.M + row) * p.topk_k;
+        int *pi = p.part_ids + ((size_t)range * p.M + row) * p.topk_k;
 #pragma unroll
-            for (int s = 0; s < kTopkMax; ++s) rank += topk_before(tk.v[s], tk.id[s], va, ia) ? 1 : 0;
-            if (rank < p.topk_k) {
-              pv[rank] = va;
-              pi[rank] = ia;
-            }
+        for (int s2 = 0; s2 < kTopkMax; ++s2) {
+          int rank = s2;
+#pragma unroll
+          for (int t2 = 0; t2 < kTopkMax; ++t2) rank += topk_before(w[t2], wi[t2], tk.v[s2], tk.id[s2]) ? 1 : 0;
+          if (rank < p.topk_k) {
+            pv[rank] = tk.v[s2];
+            pi[rank] = tk.id[s2];
           }
         }
-      }
+        if (p.smp_part && eg == 0) {
+          DrawState o;
+          o.m = xg[64];
+          o.s = xg[65];
+          o.best = xg[66];
+          o.x = xg[67];
+          o.id = __float_as_int(xg[68]);
+          draw_merge(tk.dr, o);
+          draw_store(p.smp_part + 2 * ((size_t)range * p.M + row), tk.dr);
+        }
       }
     }
   }
@@ -987,7 +1025,7 @@ static const KernelSetup &kernel_setup() {
     for (int S = 2; S <= 8; ++S) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(S);
-      cfg.blockDim = dim3(kGemmThreads);
+      cfg.blockDim = dim3(gemm_threads<EPI>());
       cfg.dynamicSmemBytes = smem;
       cudaLaunchAttribute attr;
       attr.id = cudaLaunchAttributeClusterDimension;
@@ -1046,9 +1084,9 @@ static cudaError_t plan_and_launch(GemmParams &p, int num_sms, cudaStream_t s) {
   }
   constexpr size_t smem = gemm_smem_bytes<BN, EPI, MS>();
   if (p.csplit > 1)
-    return launch_pdl_cluster(gemm_tc_kernel<BN, EPI, MS>, dim3(grid), dim3(kGemmThreads), smem, s, p.csplit,
+    return launch_pdl_cluster(gemm_tc_kernel<BN, EPI, MS>, dim3(grid), dim3(gemm_threads<EPI>()), smem, s, p.csplit,
                               p);
-  return launch_pdl(gemm_tc_kernel<BN, EPI, MS>, dim3(grid), dim3(kGemmThreads), smem, s, p);
+  return launch_pdl(gemm_tc_kernel<BN, EPI, MS>, dim3(grid), dim3(gemm_threads<EPI>()), smem, s, p);
 }
 
 // 128-row blocks per tile (1 or 2) a launch takes. The stackable GEMMs (128-wide: W_c's
