@@ -239,15 +239,26 @@ __device__ __forceinline__ float deferred_rms(const GemmParams &p, int row) {
   float a[4] = {0.f, 0.f, 0.f, 0.f};
   int i = 0;
   if ((p.ss_n & 3) == 0 && aligned16(s)) {
-    for (; i < p.ss_n; i += 4) {
-      const float4 x = *reinterpret_cast<const float4 *>(s + i);
-      a[0] += x.x;
-      a[1] += x.y;
-      a[2] += x.z;
-      a[3] += x.w;
+    // eight float4 loads in flight at a time (one pass for ss_n <= 32), then the adds in
+    // the same order as one at a time; the loads past ss_n are zeros, and adding +0 to
+    // these non-negative sums changes nothing
+    constexpr int kV = 8;
+    for (; i < p.ss_n; i += 4 * kV) {
+      float4 x[kV];
+#pragma unroll
+      for (int k = 0; k < kV; ++k)
+        x[k] = i + 4 * k < p.ss_n ? *reinterpret_cast<const float4 *>(s + i + 4 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < kV; ++k) {
+        a[0] += x[k].x;
+        a[1] += x[k].y;
+        a[2] += x[k].z;
+        a[3] += x[k].w;
+      }
     }
+  } else {
+    for (; i < p.ss_n; ++i) a[i & 3] += s[i];
   }
-  for (; i < p.ss_n; ++i) a[i & 3] += s[i];
   return rsqrtf(((a[0] + a[1]) + (a[2] + a[3])) * p.inv_d + p.eps);
 }
 
@@ -401,12 +412,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t
     const int half = p.hd >> 1;
     int seq = 0, pos = 0;
     bool pos_ok = false;
-    const float rs = (p.ss_in && row_ok) ? deferred_rms(p, row) : 1.f;
-    if (row_ok) {
+    if (row_ok) {  // issued before the norm factor's loads: independent, so both are in flight
       seq = row / p.rows_per_seq;
       pos = p.ctx_len[seq] + row % p.rows_per_seq;
       pos_ok = pos >= 0 && pos < p.Cmax;
     }
+    const float rs = (p.ss_in && row_ok) ? deferred_rms(p, row) : 1.f;
 #pragma unroll 1
     for (int h0 = 0; h0 < BN; h0 += p.hd) {
       const int gcol = t.n * BN + h0;
