@@ -295,10 +295,26 @@ __global__ void accept_kernel(const int *draft, const int *target, int nb, int B
   if (i >= nb) return;
   const int *d = draft + (size_t)i * (B - 1);
   const int *t = target + (size_t)i * B;
+  // every load first (in flight together), then the longest matching prefix by compares
+  // and selects: a loop that loads as it compares pays one memory round trip per position
+  int dv[kMaxBlock], tv[kMaxBlock];
+#pragma unroll
+  for (int j = 0; j < kMaxBlock; ++j) {
+    dv[j] = j < B - 1 ? d[j] : 0;
+    tv[j] = j < B ? t[j] : 0;
+  }
   int n = 0;
-  while (n < B - 1 && d[n] == t[n]) ++n;
+  bool run = true;
+#pragma unroll
+  for (int j = 0; j < kMaxBlock - 1; ++j) {
+    run = run & (j < B - 1) & (dv[j] == tv[j]);
+    n += run ? 1 : 0;
+  }
+  int b = tv[0];
+#pragma unroll
+  for (int j = 1; j < kMaxBlock; ++j) b = j == n ? tv[j] : b;
   tau[i] = n + 1;
-  bonus[i] = t[n];
+  bonus[i] = b;
 }
 
 cudaError_t launch_accept(const int *draft, const int *target, int nb, int B, int *tau, int *bonus,
@@ -447,13 +463,23 @@ __global__ void __launch_bounds__(kHeadsThreads) topk_merge_heads_kernel(
     hi[t] = ids[(long long)t * part_stride + rowbase];
   }
   __syncthreads();
-  // (1) the k-th best head (when there are fewer than k lists every candidate survives)
-  if (t < parts && parts >= k) {
-    const float v = hv[t];
-    const int id = hi[t];
+  // (1) the k-th best head (when there are fewer than k lists every candidate survives).
+  // Ranks are counted by `sub` adjacent lanes per entry (each taking every sub-th entry),
+  // summed by shuffles: the counting loops are short and unrolled (a lone warp pays tens
+  // of cycles per taken branch).
+  const int sub1 = parts * 4 <= kHeadsThreads ? 4 : parts * 2 <= kHeadsThreads ? 2 : 1;
+  if (parts >= k) {
+    const int h = t / sub1, part = t % sub1;
+    const bool live = h < parts;
+    const float v = live ? hv[h] : 0.f;
+    const int id = live ? hi[h] : 0;
     int rank = 0;
-    for (int q = 0; q < parts; ++q) rank += topk_before(hv[q], hi[q], v, id) ? 1 : 0;
-    if (rank == k - 1) {
+    if (live) {
+#pragma unroll 8
+      for (int q = part; q < parts; q += sub1) rank += topk_before(hv[q], hi[q], v, id) ? 1 : 0;
+    }
+    for (int o = 1; o < sub1; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (live && part == 0 && rank == k - 1) {
       thr_v = v;
       thr_i = id;
     }
@@ -477,14 +503,21 @@ __global__ void __launch_bounds__(kHeadsThreads) topk_merge_heads_kernel(
     }
   }
   __syncthreads();
-  // (3) place the survivors by rank
+  // (3) place the survivors by rank (counted as in (1))
   const int ns = min(nsurv, kHeadsMaxSurv);
-  if (t < ns) {
-    const float v = sv[t];
-    const int id = si[t];
+  const int sub3 = ns * 4 <= kHeadsThreads ? 4 : ns * 2 <= kHeadsThreads ? 2 : 1;
+  {
+    const int h = t / sub3, part = t % sub3;
+    const bool live = h < ns;
+    const float v = live ? sv[h] : 0.f;
+    const int id = live ? si[h] : 0;
     int rank = 0;
-    for (int q = 0; q < ns; ++q) rank += topk_before(sv[q], si[q], v, id) ? 1 : 0;
-    if (rank < k) {
+    if (live) {
+#pragma unroll 8
+      for (int q = part; q < ns; q += sub3) rank += topk_before(sv[q], si[q], v, id) ? 1 : 0;
+    }
+    for (int o = 1; o < sub3; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (live && part == 0 && rank < k) {
       out_vals[(size_t)r * k + rank] = v;
       out_ids[(size_t)r * k + rank] = id;
     }
