@@ -290,10 +290,11 @@ def measure_workload(w, weights, dev, world, steps, warmup, full=True):
             dr.verify_sample(w.nb, draft_logits, draft_lse, draft_c, tgt_logits, w.temperature,
                              sample_seed, tau, bonus, stream=s)
             return
-        if select:
+        if select:  # the walk's path is the draft
             dr.select(w.nb, k, tid, tv, hidden, block, path, stream=s)
-        draft_c.copy_(draft)
-        dr.accept(w.nb, draft_c, target, tau, bonus, stream=s)
+            dr.accept(w.nb, path, target, tau, bonus, stream=s)
+        else:  # the first entry of each offset's top-k list is the draft
+            dr.accept_topk(w.nb, tid, k, target, tau, bonus, stream=s)
 
     with torch.cuda.stream(stream):
         step(stream)
@@ -301,7 +302,7 @@ def measure_workload(w, weights, dev, world, steps, warmup, full=True):
     if dr.status(stream) != 0:
         raise RuntimeError("device status reports an error after the first step")
     if not sampling:
-        trow = di.target_row_from_draft(draft_c.cpu().numpy(), w.V, seed)
+        trow = di.target_row_from_draft(draft.contiguous().cpu().numpy(), w.V, seed)
         target.copy_(i32(trow))
         # the host copy of the step's inputs carries the same target row, so the end-to-end
         # leg runs exactly the step the timed region runs

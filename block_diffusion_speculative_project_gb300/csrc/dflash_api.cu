@@ -1003,7 +1003,18 @@ int dflash_accept(dflash_handle_t h, int nb, const int32_t *draft, const int32_t
   if (nb < 0) return fail(DFLASH_ERR_INVALID_ARG, "nb < 0");
   if (nb == 0) return DFLASH_OK;
   if (!draft || !target || !out_tau || !out_bonus) return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor");
-  DF_CUDA(launch_accept(draft, target, nb, h->cfg.B, out_tau, out_bonus, stream));
+  DF_CUDA(launch_accept(draft, 1, target, nb, h->cfg.B, out_tau, out_bonus, stream));
+  return DFLASH_OK;
+}
+
+int dflash_accept_topk(dflash_handle_t h, int nb, const int32_t *topk_ids, int k, const int32_t *target,
+                       int32_t *out_tau, int32_t *out_bonus, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+  if (nb < 0) return fail(DFLASH_ERR_INVALID_ARG, "nb < 0");
+  if (k < 1 || k > kTopkMax) return fail(DFLASH_ERR_INVALID_ARG, "k=%d outside 1..%d", k, kTopkMax);
+  if (nb == 0) return DFLASH_OK;
+  if (!topk_ids || !target || !out_tau || !out_bonus) return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor");
+  DF_CUDA(launch_accept(topk_ids, k, target, nb, h->cfg.B, out_tau, out_bonus, stream));
   return DFLASH_OK;
 }
 

@@ -192,8 +192,9 @@ cudaError_t launch_film_cond(const uint16_t *h, const uint16_t *E, int nb, int R
                              uint16_t *cond, int *status, cudaStream_t s);
 cudaError_t launch_film_apply(const uint16_t *h, const float *bg, int nb, int R, int B, int D,
                               const int *relay_a, float eps, uint16_t *x0, cudaStream_t s);
-cudaError_t launch_accept(const int *draft, const int *target, int nb, int B, int *tau, int *bonus,
-                          cudaStream_t s);
+// draft position j of sequence i at draft[(i * (B - 1) + j) * draft_stride]
+cudaError_t launch_accept(const int *draft, int draft_stride, const int *target, int nb, int B, int *tau,
+                          int *bonus, cudaStream_t s);
 cudaError_t launch_topk_merge(const float *vals, const int *ids, int rows, int ncand_per_row,
                               long long row_stride, long long part_stride, int parts, int k,
                               int *out_ids, float *out_vals, cudaStream_t s);

@@ -287,20 +287,20 @@ cudaError_t launch_film_apply(const uint16_t *h, const float *bg, int nb, int R,
 }
 
 // ---------------------------------------------------------------- accept
-__global__ void accept_kernel(const int *draft, const int *target, int nb, int B, int *tau,
-                              int *bonus) {
+__global__ void accept_kernel(const int *draft, int draft_stride, const int *target, int nb, int B,
+                              int *tau, int *bonus) {
   griddep_wait();
   griddep_launch();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= nb) return;
-  const int *d = draft + (size_t)i * (B - 1);
+  const int *d = draft + (size_t)i * (B - 1) * draft_stride;
   const int *t = target + (size_t)i * B;
   // every load first (in flight together), then the longest matching prefix by compares
   // and selects: a loop that loads as it compares pays one memory round trip per position
   int dv[kMaxBlock], tv[kMaxBlock];
 #pragma unroll
   for (int j = 0; j < kMaxBlock; ++j) {
-    dv[j] = j < B - 1 ? d[j] : 0;
+    dv[j] = j < B - 1 ? d[(size_t)j * draft_stride] : 0;
     tv[j] = j < B ? t[j] : 0;
   }
   int n = 0;
@@ -317,11 +317,11 @@ __global__ void accept_kernel(const int *draft, const int *target, int nb, int B
   bonus[i] = b;
 }
 
-cudaError_t launch_accept(const int *draft, const int *target, int nb, int B, int *tau, int *bonus,
-                          cudaStream_t s) {
+cudaError_t launch_accept(const int *draft, int draft_stride, const int *target, int nb, int B, int *tau,
+                          int *bonus, cudaStream_t s) {
   if (nb <= 0) return cudaSuccess;
-  cudaError_t e = launch_pdl(accept_kernel, dim3((nb + 127) / 128), dim3(128), 0, s, draft, target, nb, B,
-                             tau, bonus);
+  cudaError_t e = launch_pdl(accept_kernel, dim3((nb + 127) / 128), dim3(128), 0, s, draft, draft_stride, target,
+                             nb, B, tau, bonus);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

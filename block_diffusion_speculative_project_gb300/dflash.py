@@ -82,6 +82,7 @@ def _load():
         "dflash_attention": (i, [p, i, i, p, p, p, p, i, p, p, sz, p]),
         "dflash_topk": (i, [p, i, i, p, i, p, p, p, sz, p]),
         "dflash_accept": (i, [p, i, p, p, p, p, p]),
+        "dflash_accept_topk": (i, [p, i, p, i, p, p, p, p]),
         "dflash_sample": (i, [p, i, p, ctypes.c_float, ctypes.c_uint64, i, p, p, p, p, sz, p]),
         "dflash_lm_head_sample": (i, [p, i, p, ctypes.c_float, ctypes.c_uint64, p, p, p, p, i, p, p, p,
                                       sz, p]),
@@ -108,7 +109,7 @@ EXPORTED = ("dflash_create", "dflash_destroy", "dflash_set_weights", "dflash_set
             "dflash_workspace_size",
             "dflash_status", "dflash_last_error", "dflash_ctx_project", "dflash_ctx_project_film",
             "dflash_draft_block",
-            "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_attention", "dflash_topk", "dflash_accept", "dflash_sample", "dflash_verify_sample",
+            "dflash_lm_head_topk", "dflash_lm_head_topk_noalloc", "dflash_attention", "dflash_topk", "dflash_accept", "dflash_accept_topk", "dflash_sample", "dflash_verify_sample",
             "dflash_lm_head_sample", "dflash_draw_gumbel", "dflash2_select_sample",
             "dflash_verify_sample_walk", "dflash_recall_at_k", "dflash2_conv",
             "dflash2_select")
@@ -213,6 +214,11 @@ def dflash_topk(h, rows, cols, logits, k, out_ids, out_vals, ws=None, stream=Non
 def dflash_accept(h, nb, draft, target, out_tau, out_bonus, stream=None) -> None:
     _check(LIB.dflash_accept(h, nb, _ptr(draft), _ptr(target), _ptr(out_tau), _ptr(out_bonus),
                              _stream(stream)))
+
+
+def dflash_accept_topk(h, nb, topk_ids, k, target, out_tau, out_bonus, stream=None) -> None:
+    _check(LIB.dflash_accept_topk(h, nb, _ptr(topk_ids), int(k), _ptr(target), _ptr(out_tau), _ptr(out_bonus),
+                                  _stream(stream)))
 
 
 def dflash_sample(h, rows, logits, temperature, seed, row0, out_ids, out_lse, out_logq, ws,

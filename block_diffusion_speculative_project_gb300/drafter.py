@@ -105,6 +105,9 @@ class Drafter:
     def accept(self, nb, draft, target, out_tau, out_bonus, stream=None):
         _d.dflash_accept(self.h, nb, draft, target, out_tau, out_bonus, stream)
 
+    def accept_topk(self, nb, topk_ids, k, target, out_tau, out_bonus, stream=None):
+        _d.dflash_accept_topk(self.h, nb, topk_ids, k, target, out_tau, out_bonus, stream)
+
     def sample(self, rows, logits, temperature, seed, out_ids, out_lse, out_logq=None, row0=0,
                stream=None):
         _d.dflash_sample(self.h, rows, logits, temperature, seed, row0, out_ids, out_lse, out_logq,

@@ -314,6 +314,17 @@ DFLASH_API int dflash_topk(dflash_handle_t h, int rows, int cols, const float *l
 DFLASH_API int dflash_accept(dflash_handle_t h, int nb, const int32_t *draft, const int32_t *target,
                   int32_t *out_tau, int32_t *out_bonus, dflash_stream_t stream);
 
+/* dflash_accept on the draft's top-k lists as dflash_lm_head_topk writes them: candidate
+ * c_j of sequence i is the first (best) entry of offset j's list, topk_ids[(i*(B-1) + j-1)*k]
+ * ([DFlash] dflash_cycle: the draft takes the argmax at every offset). No counterpart call
+ * on the pages: it reads the lists in place instead of a contiguous copy of their first
+ * column.
+ *   topk_ids int32 [nb, B-1, k], k 1..16; target, out_tau, out_bonus as dflash_accept.
+ * Errors: DFLASH_ERR_INVALID_ARG for a NULL tensor, nb < 0 or k outside 1..16. */
+DFLASH_API int dflash_accept_topk(dflash_handle_t h, int nb, const int32_t *topk_ids, int k,
+                  const int32_t *target, int32_t *out_tau, int32_t *out_bonus,
+                  dflash_stream_t stream);
+
 /* Draft sampling at temperature T > 0 ([DFlash2] 洞察一 and Results: sampling at T = 1;
  * each block offset draws independently from its own distribution, as the one-pass draft
  * predicts every position independently). Row r of `logits` draws

@@ -89,6 +89,27 @@ def test_accept_matches_oracle_exactly():
         assert (tt, bb) == (c["tau"], c["bonus"])
 
 
+@pytest.mark.parametrize("k", [1, 5, 16])
+def test_accept_topk_reads_the_first_entry_of_each_list(k):
+    # dflash_accept_topk on [nb, B-1, k] lists equals the oracle's accept of their first
+    # column; the other entries (set to match the target everywhere) must not be read
+    dr, _, _ = make(di.TINY, 80, 8)
+    B = di.TINY.B
+    rng = np.random.default_rng(10 + k)
+    n = 257
+    t = rng.integers(0, 3, (n, B)).astype(np.int32)
+    d = np.where(rng.random((n, B - 1)) < 0.8, t[:, :B - 1], rng.integers(0, 3, (n, B - 1))).astype(np.int32)
+    lists = np.repeat(t[:, :B - 1, None], k, axis=2).astype(np.int32)
+    lists[:, :, 0] = d
+    tau = torch.empty(n, dtype=torch.int32, device="cuda")
+    bonus = torch.empty(n, dtype=torch.int32, device="cuda")
+    dr.accept_topk(n, i32(lists), k, i32(t), tau, bonus)
+    ot, ob = orc.accept(d, t)
+    assert np.array_equal(tau.cpu().numpy(), ot)
+    assert np.array_equal(bonus.cpu().numpy(), ob)
+    assert (ot < B).any() and (ot == B).any()  # both a rejection and a full acceptance occur
+
+
 @pytest.mark.parametrize("rows,cols,k", [(7, 5000, 16), (1, 151936, 16), (3, 17, 16), (5, 300, 1)])
 def test_topk_exact_with_ties(rows, cols, k):
     dr, _, _ = make(di.TINY, 80, 8)
