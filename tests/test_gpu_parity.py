@@ -146,12 +146,54 @@ def test_lm_head_topk_stage(w):
     print(f"{w.name}: {und} top-k positions within 2e-3 of the next value")
     gi = ids.cpu().numpy().reshape(-1, k)
     gl = logits.cpu().numpy().reshape(-1, w.V)
+    assert np.array_equal(gi, own_logits_topk(gl, k)), "fused selection differs from the kernel's own logits"
     for r in range(gi.shape[0]):
         assert np.array_equal(gl[r, 5], gl[r, w.V - 2]), "duplicate rows must tie exactly"
         row = gi[r].tolist()
         for dup in (w.V - 2, w.V - 3):
             if dup in row:
                 assert 5 in row and row.index(5) < row.index(dup)
+
+
+def own_logits_topk(gl, k):
+    """Top-k of each row of the GPU's own fp32 logits: value descending, ties to the lower id."""
+    ids = np.zeros((gl.shape[0], k), np.int64)
+    for r in range(gl.shape[0]):
+        ids[r] = np.lexsort((np.arange(gl.shape[1]), -gl[r].astype(np.float64)))[:k]
+    return ids
+
+
+@pytest.mark.parametrize("V", [4096, 151936])
+def test_lm_head_topk_dense_ties_exact(V):
+    """W_lm rows drawn from seven distinct rows: every row's logits take seven values, so
+    the top-16 is decided by the lower-id rule across chunks, epilogue groups and
+    vocabulary ranges. The fused selection must equal, exactly, the top-k of the kernel's
+    own fp32 logits and the oracle's top-k of the fp64 logits (seven values far apart)."""
+    w = di.TINY.with_(name=f"tiny_ties_v{V}", V=V, nb=4)
+    bits = di.make_weights(w)
+    rng = np.random.default_rng(V)
+    pick = rng.integers(0, 7, V)
+    bits["W_lm"] = di.normal_bf16("wlm_ties", (7, w.D), 1.0)[pick].copy()
+    dr, W, _ = make(w, 64, w.B, bits=bits)
+    hid_bits = di.normal_bf16("hidden_ties", (w.nb, w.B, w.D), 1.0)
+    k = w.k_top
+    ids = torch.empty(w.nb, w.B - 1, k, dtype=torch.int32, device="cuda")
+    vals = torch.empty(w.nb, w.B - 1, k, dtype=torch.float32, device="cuda")
+    logits = torch.empty(w.nb, w.B - 1, w.V, dtype=torch.float32, device="cuda")
+    dr.lm_head_topk(w.nb, bf16(hid_bits), k, ids, vals, logits)
+    gi = ids.cpu().numpy().reshape(-1, k)
+    gv = vals.cpu().numpy().reshape(-1, k)
+    gl = logits.cpu().numpy().reshape(-1, V)
+    want = own_logits_topk(gl, k)
+    assert np.array_equal(gi, want)
+    assert np.array_equal(gv, np.take_along_axis(gl, want, 1))
+    ol = orc.lm_logits(W, orc.widen(hid_bits)).reshape(-1, V)
+    oi, _ = orc.topk(ol, k)
+    # rows whose seven values are all more than 1e-2 apart in fp64 (fp32 cannot reorder them)
+    gaps = np.array([np.diff(np.unique(r)).min() for r in ol])
+    far = gaps > 1e-2
+    assert far.mean() > 0.5
+    assert np.array_equal(gi[far], oi[far])
 
 
 @pytest.mark.parametrize("V,k", [(1000, 16), (1000, 5), (4096, 1)])
