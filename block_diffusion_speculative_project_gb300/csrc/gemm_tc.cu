@@ -3,10 +3,11 @@
 //   fp32 accumulation in TMEM, fused epilogues.
 //
 // Hardware mapping (sm_103a):
-//   * one CTA = 6 warps: warp 0 issues TMA tile loads (128B swizzle, K-major),
-//     warp 1 allocates TMEM and one thread issues tcgen05.mma (M=128, N=BN, K=16),
-//     warps 2..5 drain the fp32 accumulator with tcgen05.ld (32x32b) and run the
-//     epilogue; each epilogue warp owns the TMEM lane quarter (warp % 4).
+//   * one CTA = 6 warps (10 for the LM head's top-k): warp 0 issues TMA tile loads (128B
+//     swizzle, K-major), warp 1 allocates TMEM and one thread issues tcgen05.mma (M=128,
+//     N=BN, K=16), the other warps drain the fp32 accumulator with tcgen05.ld (32x32b)
+//     and run the epilogue; each epilogue warp reads the TMEM lane quarter (warp % 4), and
+//     the top-k's two groups of four split each tile's 32-column chunks.
 //   * an mbarrier ring of STAGES smem slots couples TMA and MMA; tcgen05.commit
 //     frees a slot when the MMAs that read it complete.
 //   * two TMEM accumulator sets let the epilogue of one work item run under the MMAs
@@ -336,8 +337,9 @@ __device__ __forceinline__ void topk_insert(TopkState &tk, float x, int xi) {
 // accumulator columns [32c, 32c+32) of this thread's row; it is called by every lane
 // (tcgen05.ld is warp-collective); only the stores depend on row validity.
 // cpart / nparts: this thread runs the row's 32-column chunks c with c % nparts == cpart
-// (nparts adjacent lanes share the row; nparts = 1 when one thread owns the whole row).
-// Every lane of the warp must call it (the RMS partial sums are combined by shuffles).
+// (nparts threads share the row: adjacent lanes in the split-K epilogue, whose residual
+// RMS partial sums are combined by shuffles, or the two epilogue groups of the top-k;
+// nparts = 1 when one thread owns the whole row). Every lane of the warp must call it.
 template <int BN, int EPI, class Fetch>
 __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const Item &t, int row,
                                               bool row_ok, Fetch &&fetch, TopkState &tk,
