@@ -113,6 +113,14 @@ int encode_slabs(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t K, uin
 constexpr int kBN = 128;       // tile width of the generic GEMMs
 constexpr int kBNTopk = 256;   // tile width of the LM head
 constexpr int kBNGateUp = 192; // gate|up GEMM: 96 gate + 96 up rows per tile (F/96 tiles)
+// Context projection of a large prefill: 256 x 256 tiles (two stacked 128-row blocks and
+// 256 weight rows per tile, twice the FLOPs per operand byte an SM takes in of the 256 x 128
+// tiles) once they give at least two waves.
+constexpr int kBNWide = 256;
+bool wide_tiles(int num_sms, int M, int N, int groups, int epi) {
+  const long long tiles = (long long)((M + 255) / 256) * ((N + kBNWide - 1) / kBNWide) * groups;
+  return tiles >= 2LL * num_sms && gemm_mstack(epi, kBNWide, M, 128, N, groups, 0, 0, num_sms) == 2;
+}
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -141,6 +149,9 @@ struct dflash_handle_s {
   std::vector<dflash_layer_weights> layers;
   CUtensorMap tm_Wc, tm_lm, tm_A, tm_B, tm_G, tm_f1, tm_f2;
   std::vector<CUtensorMap> tm_qkv, tm_kc, tm_vc, tm_o, tm_gate, tm_up, tm_down;
+  // 256-row boxes of the context projection's weights, for the wide tiles of large prefills
+  CUtensorMap tm_Wc_wide;
+  std::vector<CUtensorMap> tm_kc_wide, tm_vc_wide;
   std::vector<CUtensorMap> tm_c0, tm_c1;  // [layer*4 + which]
   float inv_freq[64];
   WsLayout ws;
@@ -453,6 +464,9 @@ int dflash_set_weights(dflash_handle_t h, const dflash_weights *w) {
   h->w.layers = h->layers.data();
   const int qkv_n = (c.Hq + 2 * c.Hkv) * c.hd;
   DF_TRY(encode_slabs(&h->tm_Wc, w->W_c, c.D, (uint64_t)c.L * c.Dt, kBN));
+  DF_TRY(encode_2d(&h->tm_Wc_wide, w->W_c, c.D, (uint64_t)c.L * c.Dt, (uint64_t)c.L * c.Dt, kBNWide));
+  h->tm_kc_wide.resize(c.N);
+  h->tm_vc_wide.resize(c.N);
   DF_TRY(encode_2d(&h->tm_lm, w->W_lm, c.V, c.D, c.D, kBNTopk));
   h->tm_qkv.resize(c.N);
   h->tm_kc.resize(c.N);
@@ -471,6 +485,8 @@ int dflash_set_weights(dflash_handle_t h, const dflash_weights *w) {
     DF_TRY(encode_slabs(&h->tm_qkv[n], L.W_qkv, qkv_n, c.D, kBN));
     DF_TRY(encode_slabs(&h->tm_kc[n], L.Wk_c, (uint64_t)c.Hkv * c.hd, c.D, kBN));
     DF_TRY(encode_slabs(&h->tm_vc[n], L.Wv_c, (uint64_t)c.Hkv * c.hd, c.D, kBN));
+    DF_TRY(encode_2d(&h->tm_kc_wide[n], L.Wk_c, (uint64_t)c.Hkv * c.hd, c.D, c.D, kBNWide));
+    DF_TRY(encode_2d(&h->tm_vc_wide[n], L.Wv_c, (uint64_t)c.Hkv * c.hd, c.D, c.D, kBNWide));
     DF_TRY(encode_slabs(&h->tm_o[n], L.W_o, c.D, (uint64_t)c.Hq * c.hd, kBN));
     DF_TRY(encode_2d(&h->tm_gate[n], L.W_gate, c.F, c.D, c.D, kBNGateUp / 2));
     DF_TRY(encode_2d(&h->tm_up[n], L.W_up, c.F, c.D, c.D, kBNGateUp / 2));
@@ -545,25 +561,38 @@ int ctx_project_impl(dflash_handle_t h, int nb, int R, const void *hv, const int
   uint16_t *hh = w.at<uint16_t>(h->ws.h);
   {  // pre = hv * W_c^T
     GemmParams p = base_params(h, w);
-    DF_TRY(encode_slabs(&p.tmA, hv, rows, (uint64_t)c.L * c.Dt, 128));
-    p.slabs = 2;
-    p.tmB[0] = h->tm_Wc;
+    const bool wide = wide_tiles(h->num_sms, rows, c.D, 1, EPI_F32);
+    if (wide) {
+      DF_TRY(encode_act(&p.tmA, hv, rows, (uint64_t)c.L * c.Dt));
+      p.slabs = 1;
+      p.tmB[0] = h->tm_Wc_wide;
+    } else {
+      DF_TRY(encode_slabs(&p.tmA, hv, rows, (uint64_t)c.L * c.Dt, 128));
+      p.slabs = 2;
+      p.tmB[0] = h->tm_Wc;
+    }
     p.M = rows;
     p.N = c.D;
     p.K = c.L * c.Dt;
     p.epi = EPI_F32;
     p.out = pre;
     p.ldo = c.D;
-    DF_TRY(run_gemm(h, p, kBN, s));
+    DF_TRY(run_gemm(h, p, wide ? kBNWide : kBN, s));
   }
   DF_CUDA(launch_rmsnorm(pre, rows, c.D, bf(h->w.g_ctx), c.eps, hh, s));
   {  // K_c / V_c of every layer, scattered into the caches (committed rows only)
     GemmParams p = base_params(h, w);
-    DF_TRY(encode_slabs(&p.tmA, hh, rows, c.D, 128));
-    p.slabs = 2;
+    const bool wide = wide_tiles(h->num_sms, rows, c.Hkv * c.hd, 2 * c.N, EPI_KV);
+    if (wide) {
+      DF_TRY(encode_act(&p.tmA, hh, rows, c.D));
+      p.slabs = 1;
+    } else {
+      DF_TRY(encode_slabs(&p.tmA, hh, rows, c.D, 128));
+      p.slabs = 2;
+    }
     for (int n = 0; n < c.N; ++n) {
-      p.tmB[2 * n] = h->tm_kc[n];
-      p.tmB[2 * n + 1] = h->tm_vc[n];
+      p.tmB[2 * n] = wide ? h->tm_kc_wide[n] : h->tm_kc[n];
+      p.tmB[2 * n + 1] = wide ? h->tm_vc_wide[n] : h->tm_vc[n];
     }
     p.groups = 2 * c.N;
     p.M = rows;
@@ -579,7 +608,7 @@ int ctx_project_impl(dflash_handle_t h, int nb, int R, const void *hv, const int
     p.Cmax = c.Cmax;
     p.max_batch = c.max_batch;
     set_paging(h, p);
-    DF_TRY(run_gemm(h, p, kBN, s));
+    DF_TRY(run_gemm(h, p, wide ? kBNWide : kBN, s));
   }
   const bool film = relay_b != nullptr;
   DF_CUDA(launch_relay_and_len(hh, nb, R, c.B, c.D, relay_a, n_commit, ctx_len,

@@ -1114,7 +1114,7 @@ static cudaError_t plan_and_launch(GemmParams &p, int num_sms, cudaStream_t s) {
 int gemm_mstack(int epi, int BN, int M, int tile_rows, int N, int groups, int a_grouped, int dual, int num_sms) {
   (void)tile_rows;
   if (epi == EPI_TOPK) return 1;
-  const bool plain = BN == 128 && !dual && (epi == EPI_F32 || epi == EPI_KV);
+  const bool plain = (BN == 128 || BN == 256) && !dual && (epi == EPI_F32 || epi == EPI_KV);
   const bool swiglu = BN == 192 && dual && epi == EPI_SWIGLU;
   if (a_grouped || !(plain || swiglu) || M <= BM) return 1;
   const long long cols = (long long)((N + (dual ? BN / 2 : BN) - 1) / (dual ? BN / 2 : BN)) * groups;
@@ -1145,6 +1145,8 @@ cudaError_t gemm_launch(GemmParams &p, int BN, int num_sms, cudaStream_t s) {
     switch (BN * 16 + p.epi) {
       case 128 * 16 + EPI_F32: return plan_and_launch<128, EPI_F32, 2>(p, num_sms, s);
       case 128 * 16 + EPI_KV: return plan_and_launch<128, EPI_KV, 2>(p, num_sms, s);
+      case 256 * 16 + EPI_F32: return plan_and_launch<256, EPI_F32, 2>(p, num_sms, s);
+      case 256 * 16 + EPI_KV: return plan_and_launch<256, EPI_KV, 2>(p, num_sms, s);
       case 192 * 16 + EPI_SWIGLU: return plan_and_launch<192, EPI_SWIGLU, 2>(p, num_sms, s);
       default: return cudaErrorInvalidValue;
     }

@@ -306,19 +306,21 @@ def test_fullsize_film_relay_nb32():
     run_case(di.FILM_RELAY, [int(np.argmin(a)), 3])  # the most relayed rows, and sequence 3
 
 
-def test_fullsize_prefill_qwen3_8b_2048_rows():
+@pytest.mark.parametrize("nb", [2, 3])
+def test_fullsize_prefill_qwen3_8b_2048_rows(nb):
     """The large-context path: dflash_ctx_project over 2048 prompt rows per sequence at the
-    Qwen3-8B shape (M = 4096 rows through the W_c and K/V GEMMs, 32 m-tiles), one sequence
-    from position 0 committing every row, one from position 100 committing 1500. The
-    oracle computes sampled rows one by one (rows are independent): h, then K_c / V_c of
-    every layer at those positions, compared at the stated tolerance; rows outside the
-    appended range stay untouched."""
+    Qwen3-8B shape (M = 4096 or 6144 rows through the W_c and K/V GEMMs), one sequence from
+    position 0 committing every row, one from position 100 committing 1500, a third from 37
+    committing 2000. At 4096 rows the K/V GEMM takes the wide 256 x 256 tiles and W_c the
+    256 x 128 ones; at 6144 rows both take the wide tiles. The oracle computes sampled rows
+    one by one (rows are independent): h, then K_c / V_c of every layer at those positions,
+    compared at the stated tolerance; rows outside the appended range stay untouched."""
     from block_diffusion_speculative_project_gb300 import drafter
-    w = di.QWEN3_8B.with_(nb=2)
+    w = di.QWEN3_8B.with_(nb=nb)
     bits, W = weights_for(w)
     R = 2048
-    start = np.array([0, 100], np.int32)
-    commit = np.array([R, 1500], np.int32)
+    start = np.array([0, 100, 37][:nb], np.int32)
+    commit = np.array([R, 1500, 2000][:nb], np.int32)
     Cmax = int((start + commit).max()) + w.B + 8
     dev = {n: drafter.to_device_bf16(v) for n, v in bits.items()}
     dr = drafter.Drafter(w, dev, w.nb, Cmax, R)
