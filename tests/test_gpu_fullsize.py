@@ -306,30 +306,31 @@ def test_fullsize_film_relay_nb32():
     run_case(di.FILM_RELAY, [int(np.argmin(a)), 3])  # the most relayed rows, and sequence 3
 
 
-@pytest.mark.parametrize("nb", [2, 3])
-def test_fullsize_prefill_qwen3_8b_2048_rows(nb):
-    """The large-context path: dflash_ctx_project over 2048 prompt rows per sequence at the
-    Qwen3-8B shape (M = 4096 or 6144 rows through the W_c and K/V GEMMs), one sequence from
-    position 0 committing every row, one from position 100 committing 1500, a third from 37
-    committing 2000. At 4096 rows the K/V GEMM takes the wide 256 x 256 tiles and W_c the
-    256 x 128 ones; at 6144 rows both take the wide tiles. The oracle computes sampled rows
-    one by one (rows are independent): h, then K_c / V_c of every layer at those positions,
-    compared at the stated tolerance; rows outside the appended range stay untouched."""
+@pytest.mark.parametrize("nb,R", [(2, 2048), (3, 2048), (5, 1500)])
+def test_fullsize_prefill_qwen3_8b_2048_rows(nb, R):
+    """The large-context path: dflash_ctx_project over R prompt rows per sequence at the
+    Qwen3-8B shape (M = 4096, 6144 or 7500 rows through the W_c and K/V GEMMs), sequences
+    starting at positions 0, 100, 37, 5, 250 and committing R, R - 548, R - 48, R / 2 and
+    R - 1 rows. At 4096 rows the K/V GEMM takes the wide 256 x 256 tiles and W_c the
+    256 x 128 ones; at 6144 rows both take the wide tiles, and at 7500 rows the last wide
+    row tile is ragged. The oracle computes sampled rows one by one (rows are independent):
+    h, then K_c / V_c of every layer at those positions, compared at the stated tolerance;
+    rows outside the appended range stay untouched."""
     from block_diffusion_speculative_project_gb300 import drafter
     w = di.QWEN3_8B.with_(nb=nb)
     bits, W = weights_for(w)
-    R = 2048
-    start = np.array([0, 100, 37][:nb], np.int32)
-    commit = np.array([R, 1500, 2000][:nb], np.int32)
+    start = np.array([0, 100, 37, 5, 250][:nb], np.int32)
+    commit = np.array([R, R - 548, R - 48, R // 2, R - 1][:nb], np.int32)
     Cmax = int((start + commit).max()) + w.B + 8
     dev = {n: drafter.to_device_bf16(v) for n, v in bits.items()}
     dr = drafter.Drafter(w, dev, w.nb, Cmax, R)
-    hv = di.verifier_rows(w, R, name="hv_prefill_2048")
+    hv = di.verifier_rows(w, R, name=f"hv_prefill_{R}")
     ctx = torch.tensor(start, device="cuda")
     dr.ctx_project(w.nb, R, drafter.to_device_bf16(hv), torch.tensor(commit, device="cuda"), ctx)
     assert dr.status() == 0
     assert np.array_equal(ctx.cpu().numpy(), start + commit)
-    rows = [0, 1, 63, 64, 127, 128, 129, 700, 1023, 1024, 1499, 1500, 2046, 2047]
+    rows = [r for r in (0, 1, 63, 64, 127, 128, 129, 700, 749, 750, 1023, 1024, 1451, 1452, 1499, 1500, 2046, 2047)
+            if r < R]
     K, V = dr.kcache, dr.vcache
     for i in range(w.nb):
         sel = [r for r in rows if r < commit[i]]
