@@ -652,19 +652,20 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   // The schedule (which CTAs share this pair) reads only ctx_len, written long before by
   // the context append: the attention triggers this launch after its own
   // griddepcontrol.wait, so every kernel before the attention has completed. It is
-  // computed before waiting for the attention; pairs written whole return right after the
-  // wait.
+  // computed before waiting for the attention; pairs written whole return at once.
   const int pair = blockIdx.x;
   const int i = pair / p.Hkv, g = pair % p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.Hq / p.Hkv;
   const int R = G * p.B;
   const int r = blockIdx.y * kMergeWarps + warp;
-  // Every CTA waits for the attention before it exits, also those with nothing to merge:
-  // this grid's completion (what the next launch's griddepcontrol.wait waits for) must
-  // imply the attention's, whose output o the next launch reads.
+  // This grid's completion (what the next launch's griddepcontrol.wait waits for) must imply
+  // the attention's, whose output o the next launch reads, even when no pair needs a merge:
+  // CTA (0, 0) always waits for the attention; other CTAs with nothing to merge leave at once
+  // (thousands of them waiting would hold the SMs' CTA slots).
+  const bool anchor = blockIdx.x == 0 && blockIdx.y == 0;
   if (r >= R) {
-    griddep_wait();
+    if (anchor) griddep_wait();
     return;
   }
   // total units and the units before this pair, in one pass over the sequences
@@ -684,8 +685,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const Attn
   const int U = attn_units(p, i);
   const long long A = before * p.Hkv + (long long)g * U;
   const int c0 = attn_cta_of(T, Ge, A), c1 = attn_cta_of(T, Ge, A + U - 1);
+  if (c0 == c1) {  // written whole by the attention kernel
+    if (anchor) griddep_wait();
+    return;
+  }
   griddep_wait();
-  if (c0 == c1) return;  // written whole by the attention kernel
   griddep_launch();
   const float sl2 = rsqrtf(static_cast<float>(HD)) * 1.4426950408889634f;
   {
