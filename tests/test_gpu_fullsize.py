@@ -306,8 +306,8 @@ def test_fullsize_film_relay_nb32():
     run_case(di.FILM_RELAY, [int(np.argmin(a)), 3])  # the most relayed rows, and sequence 3
 
 
-@pytest.mark.parametrize("nb,R", [(2, 2048), (3, 2048), (5, 1500)])
-def test_fullsize_prefill_qwen3_8b_2048_rows(nb, R):
+@pytest.mark.parametrize("nb,R,paged", [(2, 2048, False), (3, 2048, False), (5, 1500, False), (2, 2048, True)])
+def test_fullsize_prefill_qwen3_8b_2048_rows(nb, R, paged):
     """The large-context path: dflash_ctx_project over R prompt rows per sequence at the
     Qwen3-8B shape (M = 4096, 6144 or 7500 rows through the W_c and K/V GEMMs), sequences
     starting at positions 0, 100, 37, 5, 250 and committing R, R - 548, R - 48, R / 2 and
@@ -315,15 +315,20 @@ def test_fullsize_prefill_qwen3_8b_2048_rows(nb, R):
     256 x 128 ones; at 6144 rows both take the wide tiles, and at 7500 rows the last wide
     row tile is ragged. The oracle computes sampled rows one by one (rows are independent):
     h, then K_c / V_c of every layer at those positions, compared at the stated tolerance;
-    rows outside the appended range stay untouched."""
+    rows outside the appended range stay untouched. The paged case writes the same rows
+    through a shuffled block table of 64-row pages."""
     from block_diffusion_speculative_project_gb300 import drafter
     w = di.QWEN3_8B.with_(nb=nb)
     bits, W = weights_for(w)
     start = np.array([0, 100, 37, 5, 250][:nb], np.int32)
     commit = np.array([R, R - 548, R - 48, R // 2, R - 1][:nb], np.int32)
     Cmax = int((start + commit).max()) + w.B + 8
+    Cmax = (Cmax + 63) // 64 * 64
     dev = {n: drafter.to_device_bf16(v) for n, v in bits.items()}
-    dr = drafter.Drafter(w, dev, w.nb, Cmax, R)
+    table = di.block_table(nb, Cmax, 0) if paged else None
+    dr = drafter.Drafter(w, dev, w.nb, Cmax, R, num_pages=nb * (Cmax // 64) if paged else 0)
+    if paged:
+        dr.set_block_table(torch.tensor(table, device="cuda"))
     hv = di.verifier_rows(w, R, name=f"hv_prefill_{R}")
     ctx = torch.tensor(start, device="cuda")
     dr.ctx_project(w.nb, R, drafter.to_device_bf16(hv), torch.tensor(commit, device="cuda"), ctx)
@@ -335,17 +340,18 @@ def test_fullsize_prefill_qwen3_8b_2048_rows(nb, R):
     for i in range(w.nb):
         sel = [r for r in rows if r < commit[i]]
         h = orc.fuse_context(w, W, orc.widen(hv[i, sel]))
+        end = int(start[i] + commit[i])
         for n in range(w.N):
+            Kn, Vn = seq_rows(K, n, i, table), seq_rows(V, n, i, table)
             for j, r in enumerate(sel):
                 pos = int(start[i]) + r
                 k = (W[f"layer{n}.Wk_c"] @ h[j]).reshape(w.Hkv, w.hd)
                 v = (W[f"layer{n}.Wv_c"] @ h[j]).reshape(w.Hkv, w.hd)
                 ok = orc.rope(k[None], pos, w.rope_base)[0]
-                assert_close(K[n, i, :, pos].float().cpu().numpy(), ok, f"K_c seq {i} row {r} layer {n}")
-                assert_close(V[n, i, :, pos].float().cpu().numpy(), v, f"V_c seq {i} row {r} layer {n}")
-        end = int(start[i] + commit[i])
-        assert not K[:, i, :, end:].float().abs().sum().item(), "rows past the append"
-        assert not K[:, i, :, :int(start[i])].float().abs().sum().item(), "rows before the append"
+                assert_close(Kn[:, pos].float().cpu().numpy(), ok, f"K_c seq {i} row {r} layer {n}")
+                assert_close(Vn[:, pos].float().cpu().numpy(), v, f"V_c seq {i} row {r} layer {n}")
+            assert not Kn[:, end:].float().abs().sum().item(), "rows past the append"
+            assert not Kn[:, :int(start[i])].float().abs().sum().item(), "rows before the append"
 
 
 def test_fullsize_sampling_launch_shapes_qwen3_8b():
