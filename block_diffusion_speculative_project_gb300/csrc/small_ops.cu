@@ -692,17 +692,44 @@ __global__ void __launch_bounds__(256) select_walk_kernel(const int *cand_ids, c
   for (int e = threadIdx.x; e < n; e += blockDim.x) tab[e] = ti[e];
   for (int e = threadIdx.x; e < (B - 1) * k; e += blockDim.x) sid[e] = cand_ids[(size_t)i * (B - 1) * k + e];
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int ai = 0;
-    for (int t = 1; t < B; ++t) {
-      const float *row = tab + ((t - 1) * k + ai) * k;
-      const int *ids = sid + (t - 1) * k;
-      int best = 0;
-      for (int c = 1; c < k; ++c)
-        if (topk_before(row[c], ids[c], row[best], ids[best])) best = c;
-      path[(size_t)i * (B - 1) + (t - 1)] = ids[best];
-      ai = best;
+  // Warp 0 walks: lane c holds candidate c of the offset, and a butterfly of shuffles finds
+  // the first candidate by (score descending, id ascending), the one a scan over c keeping
+  // the best would find: the ids of one offset are distinct, so that order is strict. A NaN
+  // score would make the scan depend on its order; an offset holding one is scanned by
+  // lane 0 instead.
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int ai = 0;
+  for (int t = 1; t < B; ++t) {
+    const float *row = tab + ((t - 1) * k + ai) * k;
+    const int *ids = sid + (t - 1) * k;
+    const bool on = lane < k;
+    const float v = on ? row[lane] : -INFINITY;
+    const int id = on ? ids[lane] : INT_MAX;
+    int best;
+    if (__any_sync(0xffffffffu, on && isnan(v))) {
+      best = 0;
+      if (lane == 0)
+        for (int c = 1; c < k; ++c)
+          if (topk_before(row[c], ids[c], row[best], ids[best])) best = c;
+      best = __shfl_sync(0xffffffffu, best, 0);
+    } else {
+      float bv = v;
+      int bi = id, bs = lane;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+        const int s2 = __shfl_xor_sync(0xffffffffu, bs, o);
+        const bool take = topk_before(v2, i2, bv, bi);
+        bv = take ? v2 : bv;
+        bi = take ? i2 : bi;
+        bs = take ? s2 : bs;
+      }
+      best = bs;
     }
+    if (lane == 0) path[(size_t)i * (B - 1) + (t - 1)] = ids[best];
+    ai = best;
   }
 }
 
