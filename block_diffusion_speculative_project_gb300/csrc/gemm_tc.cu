@@ -756,7 +756,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1) gemm_tc_kernel(const _
       mbar_wait(mma_done, 0, kDrainSpin);
     }
   } else {
-    // ---------------- epilogue warps 2..5
+    // ---------------- epilogue warps 2..5 (2..9 for the top-k)
     griddep_wait();
     const int q = warp & 3;
     const int r = q * 32 + lane;
