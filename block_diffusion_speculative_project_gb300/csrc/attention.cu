@@ -127,14 +127,21 @@ struct AttnWalk {
   int stage;  // ring stages used before this unit's stage
 };
 
-__device__ __forceinline__ void walk_set_pair(AttnWalk &w, const AttnParams &p) {
+// Context rows of the first kCtxCache sequences, copied to shared memory with the schedule
+// (before griddepcontrol.wait), so the walks' pair changes read no global memory.
+constexpr int kCtxCache = 64;
+__device__ __forceinline__ int walk_ctx(const AttnParams &p, const int *sctx, int i) {
+  return i < kCtxCache ? sctx[i] : attn_ctx(p, i);
+}
+
+__device__ __forceinline__ void walk_set_pair(AttnWalk &w, const AttnParams &p, const int *sctx) {
   const int i = w.pair / p.Hkv;
-  w.L = attn_ctx(p, i) + p.B;
+  w.L = walk_ctx(p, sctx, i) + p.B;
   w.U = (w.L + kKeys - 1) / kKeys;
 }
 __device__ __forceinline__ bool walk_first(const AttnWalk &w) { return w.unit == w.seg_unit0; }
 __device__ __forceinline__ bool walk_last(const AttnWalk &w) { return w.left == 1 || w.unit == w.U - 1; }
-__device__ __forceinline__ void walk_next(AttnWalk &w, const AttnParams &p) {
+__device__ __forceinline__ void walk_next(AttnWalk &w, const AttnParams &p, const int *sctx) {
   // the next unit shares this unit's stage when this is its first slot and the
   // segment continues (then its keys follow directly)
   const bool share = w.slot == 0 && !walk_last(w);
@@ -146,7 +153,7 @@ __device__ __forceinline__ void walk_next(AttnWalk &w, const AttnParams &p) {
     w.unit = 0;
     w.seg_unit0 = 0;
     ++w.seg;
-    if (w.left > 0) walk_set_pair(w, p);
+    if (w.left > 0) walk_set_pair(w, p, sctx);
   }
 }
 
@@ -177,7 +184,9 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
   uint64_t *mma_done = ml_ready + 1;          // [2]: drain of the S and the PV issuer
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 2);
   int *sched = reinterpret_cast<int *>(tmem_slot + 1);  // [pair, unit, count]
-  static_assert((2 * kAttnStages + 2 + 2 + 4 + 4 + 2 + 4) * 8 + 4 + 12 <= C::OFF_ML - C::OFF_BAR,
+  int *sctx = reinterpret_cast<int *>(smem + C::OFF_BAR + 256);  // [kCtxCache] context rows
+  static_assert((2 * kAttnStages + 2 + 2 + 4 + 4 + 2 + 4) * 8 + 4 + 12 <= 256 &&
+                    256 + kCtxCache * 4 <= C::OFF_ML - C::OFF_BAR,
                 "barrier region overflows");
   float2 *ml1 = reinterpret_cast<float2 *>(smem + C::OFF_ML);
 
@@ -231,6 +240,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
   // computed while the QKV GEMM still runs; the q / k_b / v_b inputs are read after the
   // griddepcontrol.wait below.
   if (warp == Ro::PRODUCER) {
+    for (int i = lane; i < p.nb && i < kCtxCache; i += 32) sctx[i] = attn_ctx(p, i);
     // Schedule: total units, this CTA's range, and the pair/unit it starts at.
     const long long T = attn_units_before(p, p.nb, lane);
     const int Ge = T < p.grid ? static_cast<int>(T) : p.grid;
@@ -294,7 +304,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
   w0.left = nunits;
   w0.slot = 0;
   w0.stage = 0;
-  if (nunits > 0) walk_set_pair(w0, p);
+  if (nunits > 0) walk_set_pair(w0, p, sctx);
 
   if (warp == Ro::PRODUCER) {
     if (lane == 0 && nunits > 0 && !p.stall) {
@@ -356,7 +366,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
           }
           stages = w.stage + 1;
         }
-        walk_next(w, p);
+        walk_next(w, p, sctx);
       }
       if (!ok) flag_status(p.status, kStatusTimeout);
       // Every issued load must land before the CTA may exit (bounded).
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
         }
         tc_commit(&s_full[sb]);
         if (walk_last(ws)) tc_commit(q_empty);
-        walk_next(ws, p);
+        walk_next(ws, p, sctx);
       }
       if (!ok) flag_status(p.status, kStatusTimeout);
       // Every issued MMA must complete before TMEM is freed (bounded).
@@ -426,7 +436,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
                              (!start || kk > 0) ? 1u : 0u);
         tc_commit(&p_empty[pq]);
         if (wp.slot == 1 || walk_last(wp)) tc_commit(&kv_empty[st]);  // last unit of its stage
-        walk_next(wp, p);
+        walk_next(wp, p, sctx);
       }
       if (!ok) flag_status(p.status, kStatusTimeout);
       tc_commit(&mma_done[1]);
@@ -628,7 +638,7 @@ __global__ void __launch_bounds__(AttnRoles<NQ>::THREADS, 1)
           mbar_arrive(o_free);
         }
       }
-      walk_next(w, p);
+      walk_next(w, p, sctx);
     }
     if (!ok) flag_status(p.status, kStatusTimeout);
   }

@@ -660,14 +660,17 @@ __global__ void __launch_bounds__(256) select_table_kernel(const float *cand_val
   const float *ABi = AB + (size_t)i * per * 2 * sel;
   const int na = t == 1 ? 1 : k;  // offset 1 starts from the anchor (row 0)
   for (int d = threadIdx.x; d < sel; d += blockDim.x) gate[d] = 1.0f / (1.0f + expf(-Gt[d]));
-  for (int e = threadIdx.x; e < na * sel; e += blockDim.x) {
-    const int a = e / sel, d = e - a * sel;
-    const int arow = t == 1 ? 0 : 1 + (t - 2) * k + a;
-    As[a * ld + d] = ABi[(size_t)arow * 2 * sel + d];
-  }
   for (int e = threadIdx.x; e < k * sel; e += blockDim.x) {
     const int b = e / sel, d = e - b * sel;
     Bs[b * ld + d] = ABi[(size_t)(1 + (t - 1) * k + b) * 2 * sel + sel + d];
+  }
+  __syncthreads();
+  // the A rows are stored already multiplied by the gate (the same rounded products the
+  // dot products below would form), so the inner loop reads two operands, not three
+  for (int e = threadIdx.x; e < na * sel; e += blockDim.x) {
+    const int a = e / sel, d = e - a * sel;
+    const int arow = t == 1 ? 0 : 1 + (t - 2) * k + a;
+    As[a * ld + d] = ABi[(size_t)arow * 2 * sel + d] * gate[d];
   }
   __syncthreads();
   const int ai = threadIdx.x >> 4, b = threadIdx.x & 15;
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(256) select_table_kernel(const float *cand_val
   const float *ar = As + ai * ld, *br = Bs + b * ld;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-  for (int d = 0; d < sel; ++d) acc[d & 3] = fmaf(ar[d] * gate[d], br[d], acc[d & 3]);
+  for (int d = 0; d < sel; ++d) acc[d & 3] = fmaf(ar[d], br[d], acc[d & 3]);
   const size_t tr = (size_t)i * (B - 1) + (t - 1);
   table[(tr * k + ai) * k + b] = cand_vals[tr * k + b] + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
 }
