@@ -241,12 +241,16 @@ def measure_workload(w, weights, dev, world, steps, warmup, full=True):
     block = views["block"]
     hidden = torch.empty(w.nb, w.B, w.D, dtype=torch.bfloat16, device=dev)
     k = w.k_top
-    tid = torch.empty(w.nb, w.B - 1, k, dtype=torch.int32, device=dev)
+    # the step's results (tau, bonus, the top-k ids) in one device buffer, so the end-to-end
+    # leg reads them back with one copy
+    nt = w.nb * (w.B - 1) * k
+    out_dev = torch.zeros(nt + 2 * w.nb, dtype=torch.int32, device=dev)
+    tid = out_dev[:nt].view(w.nb, w.B - 1, k)
     tv = torch.empty(w.nb, w.B - 1, k, dtype=torch.float32, device=dev)
     path = torch.empty(w.nb, w.B - 1, dtype=torch.int32, device=dev)
     target = views["target"]
-    tau = i32(np.zeros(w.nb))
-    bonus = i32(np.zeros(w.nb))
+    tau = out_dev[nt:nt + w.nb]
+    bonus = out_dev[nt + w.nb:]
     select = bool(w.flags & di.FLAG_SELECT)
     draft = path if select else tid[..., 0]
     draft_c = torch.empty(w.nb, w.B - 1, dtype=torch.int32, device=dev)
@@ -376,9 +380,7 @@ def measure_workload(w, weights, dev, world, steps, warmup, full=True):
         # in, the step, the copy out; the rest is host-side launch and wake-up time.
         host_hv = hv_step.cpu().pin_memory()
         host_in = torch.from_numpy(host_in_np).pin_memory()
-        host_out = torch.empty(w.nb * (2 + (w.B - 1) * k), dtype=torch.int32).pin_memory()
-        out_dev = torch.empty_like(host_out, device=dev)
-        nt = w.nb * (w.B - 1) * k
+        host_out = torch.empty(out_dev.numel(), dtype=torch.int32).pin_memory()
         e2e_steps = 300
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(e2e_steps)]
         barrier()
@@ -393,9 +395,6 @@ def measure_workload(w, weights, dev, world, steps, warmup, full=True):
                 ev[1].record(stream)
                 graph.replay()
                 ev[2].record(stream)
-                out_dev[:w.nb].copy_(tau)
-                out_dev[w.nb:2 * w.nb].copy_(bonus)
-                out_dev[2 * w.nb:].copy_(tid.view(nt))
                 host_out.copy_(out_dev, non_blocking=True)
                 ev[3].record(stream)
                 stream.synchronize()
@@ -403,7 +402,7 @@ def measure_workload(w, weights, dev, world, steps, warmup, full=True):
         barrier()
         e2e_parts = np.array([[ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[2].elapsed_time(ev[3])]
                               for ev in evs]).mean(axis=0)
-        if not np.array_equal(host_out[:w.nb].numpy(), tau.cpu().numpy()):
+        if not np.array_equal(host_out[nt:nt + w.nb].numpy(), tau.cpu().numpy()):
             raise RuntimeError("the end-to-end leg's result differs from the device result")
         h2d = host_hv.numel() * 2 + host_in.numel() * 4
         d2h = host_out.numel() * 4
