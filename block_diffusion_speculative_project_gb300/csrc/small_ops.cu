@@ -49,17 +49,23 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float *xin, const in
   __shared__ float red[8];
   const int r = blockIdx.x;
   extern __shared__ float row[];  // D floats
+  int id = 0;
+  if (MODE == 1) {
+    id = ids[r];
+    if (id < 0 || id >= V) {
+      if (threadIdx.x == 0) flag_status(status, kStatusCheck);
+      id = 0;
+    }
+  }
   float ss = 0.f;
+  // unrolled so that a thread's loads of the row (4 at D = 4096) are in flight together;
+  // the squares are still summed in column order
+#pragma unroll 4
   for (int c = threadIdx.x * 4; c < D; c += 256 * 4) {
     float4 v;
     if (MODE == 0) {
       v = *reinterpret_cast<const float4 *>(xin + (size_t)r * D + c);
     } else {
-      int id = ids[r];
-      if (id < 0 || id >= V) {
-        if (c == threadIdx.x * 4 && threadIdx.x == 0) flag_status(status, kStatusCheck);
-        id = 0;
-      }
       const uint2 e = *reinterpret_cast<const uint2 *>(E + (size_t)id * D + c);
       v = make_float4(bits_to_f32(e.x & 0xFFFF), bits_to_f32(e.x >> 16), bits_to_f32(e.y & 0xFFFF),
                       bits_to_f32(e.y >> 16));
@@ -85,6 +91,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float *xin, const in
     if (j < skip) return;
     orow = (r / B) * rows_out_per_seq + (j - skip);
   }
+#pragma unroll 4
   for (int c = threadIdx.x * 4; c < D; c += 256 * 4) {
     const float4 v = *reinterpret_cast<const float4 *>(row + c);
     const uint2 gg = *reinterpret_cast<const uint2 *>(g + c);
